@@ -1,0 +1,129 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+This module holds no attention arithmetic: it only draws random tensors and
+names the workload shapes, so that the CUDA path and the CPU oracle can be fed
+identical values. Recipe:
+
+* ``torch.Generator('cpu').manual_seed(seed)``; ``randn`` in fp32, iid N(0,1);
+* bf16 inputs are the fp32 draws rounded to nearest-even by ``.to(bfloat16)``;
+* draw order: q, k, v; for decode: seqlens (uniform on [1, max_len] via
+  ``randint(1, max_len + 1)``), then q, k_cache, v_cache;
+* cache rows at or beyond ``seqlens[b]`` are set to NaN, so a kernel that
+  reads them produces NaN and fails parity;
+* workload ``c`` uses seed ``1000 + c``; sweep variants add ``10 * sub``.
+
+The shapes follow the synthetic stand-ins for the pages' workloads: a tiny
+fp32 GQA case, an MHA/GQA/MQA sweep, a LLaMA-3-8B-shaped prefill layer
+(BootstrapAI evolution log, collab-014 "Kernel 9 GQA": seq 2048, H_q=32,
+H_kv=8, d=128), a long-sequence case sized like the persistent-kernel entry's
+"seq=4096, h=16, b=4" example, and a decode step against a bf16 K/V cache
+(microLLM-rocm optimisation log, Experiments 064-065).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class PrefillShape:
+    name: str
+    B: int
+    H_q: int
+    H_kv: int
+    N_q: int
+    N_kv: int
+    d: int
+    causal: bool
+    dtype: torch.dtype
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOPs: 4*B*H_q*N_q*N_kv*d, halved when causal."""
+        f = 4.0 * self.B * self.H_q * self.N_q * self.N_kv * self.d
+        return f / 2 if self.causal else f
+
+
+@dataclass(frozen=True)
+class DecodeShape:
+    name: str
+    B: int
+    H_q: int
+    H_kv: int
+    max_len: int
+    d: int
+    dtype: torch.dtype
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+def sweep_shapes() -> list[PrefillShape]:
+    """MHA/GQA/MQA sweep: B=2, H_q=8, H_kv in {8,4,1}, N=1024, d=64, bf16."""
+    out = []
+    for sub, h_kv in enumerate((8, 4, 1)):
+        for causal in (False, True):
+            out.append(PrefillShape(f"sweep_hkv{h_kv}_{'causal' if causal else 'full'}",
+                                    2, 8, h_kv, 1024, 1024, 64, causal,
+                                    torch.bfloat16, 1001 + 10 * sub + int(causal)))
+    return out
+
+
+TINY = PrefillShape("tiny_gqa_fp32", 1, 4, 2, 128, 128, 64, False, torch.float32, 1000)
+LLAMA3_8B_LAYER = PrefillShape("llama3_8b_prefill_layer", 1, 32, 8, 2048, 2048, 128, True,
+                               torch.bfloat16, 1002)
+LONG_SEQ = PrefillShape("long_seq_persistent", 4, 16, 4, 4096, 4096, 64, True,
+                        torch.bfloat16, 1003)
+
+
+def decode_shapes() -> list[DecodeShape]:
+    """Decode against a bf16 cache: B in {1,8,64}, H_q=12, H_kv=2, d=128, max_len=2048."""
+    return [DecodeShape(f"decode_b{b}", b, 12, 2, 2048, 128, torch.bfloat16, 1004 + 10 * i)
+            for i, b in enumerate((1, 8, 64))]
+
+
+def prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, dtype=torch.bfloat16, seed=0):
+    """Return CPU tensors (q, k, v) in ``dtype``: q [B,H_q,N_q,d], k/v [B,H_kv,N_kv,d]."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn(B, H_q, N_q, d, generator=g, dtype=torch.float32).to(dtype)
+    k = torch.randn(B, H_kv, N_kv, d, generator=g, dtype=torch.float32).to(dtype)
+    v = torch.randn(B, H_kv, N_kv, d, generator=g, dtype=torch.float32).to(dtype)
+    return q, k, v
+
+
+def prefill_inputs_for(shape: PrefillShape):
+    return prefill_inputs(shape.B, shape.H_q, shape.H_kv, shape.N_q, shape.N_kv, shape.d,
+                          shape.dtype, shape.seed)
+
+
+def decode_inputs(B, H_q, H_kv, max_len, d, dtype=torch.bfloat16, seed=0, seqlens=None):
+    """Return CPU tensors (seqlens int32 [B], q [B,H_q,d], k_cache, v_cache [B,H_kv,max_len,d]).
+
+    Rows at or beyond seqlens[b] of both caches are NaN."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    drawn = torch.randint(1, max_len + 1, (B,), generator=g, dtype=torch.int64)
+    if seqlens is None:
+        seqlens = drawn
+    seqlens = torch.as_tensor(seqlens, dtype=torch.int64).clone()
+    q = torch.randn(B, H_q, d, generator=g, dtype=torch.float32).to(dtype)
+    kc = torch.randn(B, H_kv, max_len, d, generator=g, dtype=torch.float32).to(dtype)
+    vc = torch.randn(B, H_kv, max_len, d, generator=g, dtype=torch.float32).to(dtype)
+    pos = torch.arange(max_len).view(1, 1, max_len, 1)
+    dead = pos >= seqlens.view(B, 1, 1, 1)
+    kc = kc.masked_fill(dead, float("nan"))
+    vc = vc.masked_fill(dead, float("nan"))
+    return seqlens.to(torch.int32), q, kc, vc
+
+
+def decode_inputs_for(shape: DecodeShape):
+    return decode_inputs(shape.B, shape.H_q, shape.H_kv, shape.max_len, shape.d, shape.dtype,
+                         shape.seed)

@@ -1,0 +1,179 @@
+"""Float64 CPU oracle for grouped-query scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the
+benchmark's CPU-baseline / reference legs may import this package. The product
+library (``gqa_flash_attention_02_gb300``) never imports it, and this package
+imports nothing from the product.
+
+The arithmetic lives in ``gqa_oracle.c`` (plain C, float64, the definition of
+attention written out loop by loop). This module compiles that file with gcc
+and exposes it through ctypes, taking and returning numpy float64 arrays.
+Inputs in bf16 or fp32 are widened exactly to float64 by the caller (every
+bf16/fp32 value is representable in float64), so the oracle sees the very
+values the GPU path sees.
+
+What each function follows (page title and section):
+  * head mapping h_kv = h_q / (H_q / H_kv) -- BootstrapAI evolution log,
+    collab-014 "Kernel 9 GQA";
+  * softmax as max / exp / sum / weighted average, which the online form of
+    the tiled kernels equals -- BootstrapAI evolution log, collab-005
+    "Kernel 2 tiling";
+  * causal GQA without replicating K/V heads -- microLLM-rocm optimisation
+    log, Experiment 044;
+  * log-sum-exp merge of key-range partials -- microLLM-rocm optimisation
+    log, Experiments 282-284 (split-sequence cached attention).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libgqa_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP when available). Returns the .so path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c99", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_attend_row.argtypes = [_dp, _dp, _dp, ctypes.c_long,
+                                              ctypes.c_long, ctypes.c_double,
+                                              _dp, _dp]
+            lib.oracle_attend_row.restype = None
+            lib.oracle_prefill.argtypes = [_dp, _dp, _dp, _dp, _dp] + [ctypes.c_long] * 6 + [
+                ctypes.c_int, ctypes.c_double, ctypes.c_long, ctypes.c_long, ctypes.c_int]
+            lib.oracle_prefill.restype = ctypes.c_int
+            lib.oracle_decode.argtypes = [_dp, _dp, _dp, _ip, _dp, _dp] + [ctypes.c_long] * 5 + [
+                ctypes.c_double]
+            lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_lse_merge.argtypes = [_dp, _dp, ctypes.c_long, ctypes.c_long, _dp, _dp]
+            lib.oracle_lse_merge.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """Exact widening to a contiguous float64 numpy array (torch or numpy input)."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu")
+        import torch  # local: torch is only needed when a tensor is passed
+        a = a.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def attend_row(q_row, k_rows, v_rows, scale: float):
+    """Attention of one query row q[d] over all rows of k[n][d], v[n][d].
+
+    Returns (o[d], lse)."""
+    q_row, k_rows, v_rows = _f64(q_row), _f64(k_rows), _f64(v_rows)
+    n, d = k_rows.shape if k_rows.ndim == 2 else (0, q_row.shape[-1])
+    o = np.empty(d, dtype=np.float64)
+    lse = ctypes.c_double()
+    _load().oracle_attend_row(_ptr(q_row), _ptr(k_rows), _ptr(v_rows), n, d,
+                              float(scale), _ptr(o), ctypes.byref(lse))
+    return o, lse.value
+
+
+def prefill(q, k, v, causal: bool, scale: float, heads=None, n_threads: int = 1):
+    """Prefill attention. q:[B,H_q,N_q,d], k,v:[B,H_kv,N_kv,d] -> (o, lse).
+
+    ``heads`` optionally restricts the work to a contiguous range
+    (begin, end) of flattened b*H_q + h_q heads; the other heads of the
+    returned arrays are NaN."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H_q, N_q, d = q.shape
+    _, H_kv, N_kv, _ = k.shape
+    o = np.full(q.shape, np.nan)
+    lse = np.full(q.shape[:3], np.nan)
+    begin, end = (0, B * H_q) if heads is None else heads
+    rc = _load().oracle_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                B, H_q, H_kv, N_q, N_kv, d, int(bool(causal)),
+                                float(scale), begin, end, int(n_threads))
+    if rc != 0:
+        raise ValueError("oracle_prefill: H_q must be a positive multiple of H_kv")
+    return o, lse
+
+
+def prefill_rows(q, k, v, causal: bool, scale: float, rows):
+    """Prefill output for selected rows only.
+
+    ``rows`` is an iterable of (b, h_q, i). Returns (o[len(rows), d], lse[len(rows)])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H_q, N_q, d = q.shape
+    _, H_kv, N_kv, _ = k.shape
+    if H_q % H_kv:
+        raise ValueError("H_q must be a multiple of H_kv")
+    group = H_q // H_kv
+    rows = list(rows)
+    o = np.empty((len(rows), d))
+    lse = np.empty(len(rows))
+    for r, (b, h_q, i) in enumerate(rows):
+        n = N_kv if not causal else max(0, min(N_kv, i + (N_kv - N_q) + 1))
+        h_kv = h_q // group
+        o[r], lse[r] = attend_row(q[b, h_q, i], k[b, h_kv, :n], v[b, h_kv, :n], scale)
+    return o, lse
+
+
+def decode(q, k_cache, v_cache, seqlens, scale: float):
+    """Decode attention. q:[B,H_q,d], caches [B,H_kv,max_len,d], seqlens[B] -> (o, lse)."""
+    q, k_cache, v_cache = _f64(q), _f64(k_cache), _f64(v_cache)
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().cpu().numpy()
+    seqlens = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    B, H_q, d = q.shape
+    _, H_kv, max_len, _ = k_cache.shape
+    o = np.empty(q.shape)
+    lse = np.empty(q.shape[:2])
+    rc = _load().oracle_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                               seqlens.ctypes.data_as(_ip), _ptr(o), _ptr(lse),
+                               B, H_q, H_kv, max_len, d, float(scale))
+    if rc == -1:
+        raise ValueError("oracle_decode: H_q must be a positive multiple of H_kv")
+    if rc == -2:
+        raise ValueError("oracle_decode: seqlens outside [0, max_len]")
+    return o, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Merge partial results o_parts[S,d], lse_parts[S] -> (o[d], lse)."""
+    o_parts, lse_parts = _f64(o_parts), _f64(lse_parts)
+    S, d = o_parts.shape
+    o = np.empty(d)
+    lse = ctypes.c_double()
+    _load().oracle_lse_merge(_ptr(o_parts), _ptr(lse_parts), S, d, _ptr(o),
+                             ctypes.byref(lse))
+    return o, lse.value

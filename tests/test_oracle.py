@@ -1,0 +1,324 @@
+"""Pins for the float64 CPU oracle (no GPU).
+
+The oracle is the definition of attention written out; these tests tie it to
+things other than itself: hand-derived closed forms (tests/golden), invariants
+the mathematics fixes, special cases that reduce to a textbook formula, and a
+library routine (torch's scaled_dot_product_attention in float64 on the CPU).
+
+The second half plants plausible mistakes -- a wrong head mapping, a dropped
+term, a missing normalisation, a flipped sign, an off-by-one mask -- into a
+plain numpy restatement and checks that the pin suite rejects every one of
+them, so the pins are shown to have teeth.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_flash_attention_02_gb300.inputs import decode_inputs, prefill_inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _arr(x):
+    return np.array(x, dtype=np.float64)
+
+
+def _rand(B, H_q, H_kv, N_q, N_kv, d, seed):
+    q, k, v = prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, torch.float64, seed)
+    return q.numpy(), k.numpy(), v.numpy()
+
+
+# --------------------------------------------------------------------------
+# Pin checks. Each takes a prefill implementation
+#     impl(q, k, v, causal, scale) -> (o, lse)
+# and raises AssertionError when the implementation violates the pin.
+# --------------------------------------------------------------------------
+
+def pin_golden_closed_forms(impl):
+    """Hand-derived fixtures: weights such as [1/4, 3/4] and [1/8, 2/8, 5/8]."""
+    for name in ("two_keys_quarter_threequarter.json", "three_keys_scaled.json",
+                 "gqa_head_mapping.json", "bottom_right_causal.json"):
+        fx = _load(name)
+        for mode, exp in fx["expect"].items():
+            o, lse = impl(_arr(fx["q"]), _arr(fx["k"]), _arr(fx["v"]), mode == "causal",
+                          fx["scale"])
+            np.testing.assert_allclose(o, _arr(exp["o"]), rtol=0, atol=1e-12,
+                                       err_msg=f"{name}:{mode}")
+            np.testing.assert_allclose(lse, _arr(exp["lse"]), rtol=0, atol=1e-12,
+                                       err_msg=f"{name}:{mode} lse")
+
+
+def pin_gqa_equals_replicated_mha(impl):
+    """GQA == MHA on K/V with each head repeated group times (collab-014 mapping)."""
+    for (H_q, H_kv) in ((6, 2), (8, 1), (4, 4)):
+        q, k, v = _rand(2, H_q, H_kv, 9, 13, 8, seed=7 + H_q + H_kv)
+        g = H_q // H_kv
+        k_rep, v_rep = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+        for causal in (False, True):
+            o_gqa, _ = impl(q, k, v, causal, 0.3)
+            o_mha, _ = impl(q, k_rep, v_rep, causal, 0.3)
+            np.testing.assert_allclose(o_gqa, o_mha, rtol=0, atol=1e-14)
+
+
+def pin_identical_keys_give_mean(impl):
+    """All K rows equal -> uniform weights -> O = mean of the visible V rows."""
+    q, k, v = _rand(1, 2, 1, 6, 6, 4, seed=3)
+    k[:] = k[:, :, :1, :]
+    o, _ = impl(q, k, v, False, 0.7)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape),
+                               rtol=0, atol=1e-13)
+    o, _ = impl(q, k, v, True, 0.7)
+    csum = np.cumsum(v, axis=2) / np.arange(1, 7).reshape(1, 1, 6, 1)
+    np.testing.assert_allclose(o, np.broadcast_to(csum, o.shape), rtol=0, atol=1e-13)
+
+
+def pin_scale_zero_gives_mean(impl):
+    q, k, v = _rand(1, 2, 2, 5, 7, 4, seed=4)
+    o, lse = impl(q, k, v, False, 0.0)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape),
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, math.log(7), rtol=0, atol=1e-13)
+
+
+def pin_dominant_logit_selects_row(impl):
+    """One key aligned with q at a huge logit -> O equals that key's V row."""
+    q, k0, v = _rand(1, 1, 1, 3, 8, 4, seed=5)
+    for i, jstar in enumerate((2, 5, 7)):
+        # key j* scores 60 against row i; every other key scores below 1 in size
+        k = 0.05 * k0.copy()
+        q_hat = q[0, 0, i] / np.linalg.norm(q[0, 0, i])
+        k[0, 0, jstar] = 60.0 * q_hat
+        o, _ = impl(q_hat.reshape(1, 1, 1, 4), k, v, False, 1.0)
+        np.testing.assert_allclose(o[0, 0, 0], v[0, 0, jstar], rtol=0, atol=1e-12)
+
+
+def pin_single_key_returns_it(impl):
+    q, k, v = _rand(2, 4, 2, 3, 1, 8, seed=6)
+    o, lse = impl(q, k, v, False, 0.5)
+    want = np.repeat(v, 2, axis=1)  # every query row of head h_q sees K/V head h_q // 2
+    np.testing.assert_allclose(o, np.broadcast_to(want, o.shape), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.5 * np.einsum("bhid,bhd->bhi", q, np.repeat(k[:, :, 0], 2, axis=1)),
+                               rtol=0, atol=1e-13)
+
+
+def pin_causal_row_is_truncated_full(impl):
+    """Causal row i (N_q = N_kv) equals unmasked attention over keys [0, i]."""
+    q, k, v = _rand(1, 2, 1, 7, 7, 4, seed=8)
+    o_c, lse_c = impl(q, k, v, True, 0.4)
+    for i in range(7):
+        o_t, lse_t = impl(q[:, :, i:i + 1], k[:, :, :i + 1], v[:, :, :i + 1], False, 0.4)
+        np.testing.assert_allclose(o_c[:, :, i:i + 1], o_t, rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse_c[:, :, i:i + 1], lse_t, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(o_c[:, :, 0], np.repeat(v[:, :, 0], 2, axis=1), rtol=0, atol=1e-15)
+
+
+def pin_permutation_invariance(impl):
+    """Permuting K and V rows together leaves unmasked attention unchanged."""
+    q, k, v = _rand(1, 2, 2, 4, 9, 4, seed=9)
+    perm = np.random.default_rng(0).permutation(9)
+    o1, l1 = impl(q, k, v, False, 0.6)
+    o2, l2 = impl(q, k[:, :, perm], v[:, :, perm], False, 0.6)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+def pin_convex_hull(impl):
+    """Each output coordinate lies between the min and max of the visible V column."""
+    q, k, v = _rand(2, 4, 2, 6, 6, 4, seed=10)
+    for causal in (False, True):
+        o, _ = impl(q, k, v, causal, 2.0)
+        vr = np.repeat(v, 2, axis=1)
+        for i in range(6):
+            n = i + 1 if causal else 6
+            lo = vr[:, :, :n].min(axis=2)
+            hi = vr[:, :, :n].max(axis=2)
+            assert np.all(o[:, :, i] >= lo - 1e-12) and np.all(o[:, :, i] <= hi + 1e-12)
+
+
+def pin_library_sdpa(impl):
+    """Special case that reduces to torch's float64 CPU scaled_dot_product_attention."""
+    F = torch.nn.functional
+    for (H_q, H_kv, N_q, N_kv, causal) in ((4, 2, 11, 11, False), (4, 2, 11, 11, True),
+                                           (6, 1, 5, 12, False), (3, 3, 16, 16, True)):
+        q, k, v = _rand(2, H_q, H_kv, N_q, N_kv, 8, seed=11 + H_q + N_kv)
+        o, _ = impl(q, k, v, causal, 0.35)
+        ref = F.scaled_dot_product_attention(torch.from_numpy(q), torch.from_numpy(k),
+                                             torch.from_numpy(v), is_causal=causal,
+                                             scale=0.35, enable_gqa=True).numpy()
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+PINS = [pin_golden_closed_forms, pin_gqa_equals_replicated_mha, pin_identical_keys_give_mean,
+        pin_scale_zero_gives_mean, pin_dominant_logit_selects_row, pin_single_key_returns_it,
+        pin_causal_row_is_truncated_full, pin_permutation_invariance, pin_convex_hull,
+        pin_library_sdpa]
+
+
+def _oracle_impl(q, k, v, causal, scale):
+    return oracle.prefill(q, k, v, causal, scale)
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_prefill_pins(pin):
+    pin(_oracle_impl)
+
+
+# --------------------------------------------------------------------------
+# Decode, split merge and row-sampling pins (oracle only).
+# --------------------------------------------------------------------------
+
+def test_oracle_decode_golden():
+    fx = _load("decode_two_sequences.json")
+    kc = _arr([[[[float(x) for x in r] for r in h] for h in b] for b in fx["k_cache"]])
+    vc = _arr([[[[float(x) for x in r] for r in h] for h in b] for b in fx["v_cache"]])
+    o, lse = oracle.decode(_arr(fx["q"]), kc, vc, fx["seqlens"], fx["scale"])
+    np.testing.assert_allclose(o, _arr(fx["expect"]["o"]), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, _arr(fx["expect"]["lse"]), rtol=0, atol=1e-12)
+
+
+def test_oracle_decode_is_last_causal_prefill_row():
+    """Decode at length L equals the last row of causal prefill with N_q = N_kv = L."""
+    seqlens, q, kc, vc = decode_inputs(3, 6, 2, 40, 8, torch.float64, seed=12)
+    o, lse = oracle.decode(q, kc, vc, seqlens, 0.25)
+    assert np.isfinite(o).all()
+    for b in range(3):
+        L = int(seqlens[b])
+        qp = np.zeros((1, 6, L, 8))
+        qp[0, :, L - 1] = q[b].numpy()
+        op, lp = oracle.prefill(qp, kc[b:b + 1, :, :L].numpy(), vc[b:b + 1, :, :L].numpy(),
+                                True, 0.25)
+        np.testing.assert_allclose(o[b], op[0, :, L - 1], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[b], lp[0, :, L - 1], rtol=0, atol=1e-14)
+
+
+def test_oracle_decode_rejects_bad_seqlen():
+    seqlens, q, kc, vc = decode_inputs(2, 2, 1, 8, 4, torch.float64, seed=13)
+    with pytest.raises(ValueError):
+        oracle.decode(q, kc, vc, [3, 9], 1.0)
+
+
+def test_oracle_lse_merge_equals_unsplit():
+    """Merging key-range partials by log-sum-exp reproduces the unsplit result
+    (split-sequence cached attention, microLLM-rocm Experiments 282-284)."""
+    q, k, v = _rand(1, 1, 1, 3, 37, 8, seed=14)
+    o_full, lse_full = oracle.prefill(q, k, v, False, 0.5)
+    cuts = [0, 5, 6, 20, 37]
+    for i in range(3):
+        parts_o, parts_l = [], []
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            o_p, l_p = oracle.attend_row(q[0, 0, i], k[0, 0, a:b], v[0, 0, a:b], 0.5)
+            parts_o.append(o_p)
+            parts_l.append(l_p)
+        parts_o.append(np.zeros(8))  # an empty part carries no weight
+        parts_l.append(-np.inf)
+        o_m, l_m = oracle.lse_merge(np.stack(parts_o), np.array(parts_l))
+        np.testing.assert_allclose(o_m, o_full[0, 0, i], rtol=0, atol=1e-14)
+        assert abs(l_m - lse_full[0, 0, i]) < 1e-13
+
+
+def test_oracle_empty_row_and_empty_merge():
+    o, lse = oracle.attend_row(np.ones(4), np.zeros((0, 4)), np.zeros((0, 4)), 1.0)
+    assert np.all(o == 0) and lse == -np.inf
+    o, lse = oracle.lse_merge(np.ones((2, 4)), np.array([-np.inf, -np.inf]))
+    assert np.all(o == 0) and lse == -np.inf
+
+
+def test_oracle_prefill_rows_match_full():
+    q, k, v = _rand(2, 4, 2, 10, 14, 8, seed=15)
+    o, lse = oracle.prefill(q, k, v, True, 0.3)
+    rows = [(0, 0, 0), (1, 3, 9), (0, 2, 5), (1, 1, 3)]
+    o_r, l_r = oracle.prefill_rows(q, k, v, True, 0.3, rows)
+    for r, (b, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(o_r[r], o[b, h, i])
+        assert l_r[r] == lse[b, h, i]
+
+
+def test_oracle_head_subset_and_threads():
+    q, k, v = _rand(2, 4, 2, 10, 10, 8, seed=16)
+    o_all, _ = oracle.prefill(q, k, v, True, 0.3)
+    o_sub, _ = oracle.prefill(q, k, v, True, 0.3, heads=(2, 5), n_threads=2)
+    flat_all, flat_sub = o_all.reshape(8, 10, 8), o_sub.reshape(8, 10, 8)
+    np.testing.assert_array_equal(flat_sub[2:5], flat_all[2:5])
+    assert np.isnan(flat_sub[:2]).all() and np.isnan(flat_sub[5:]).all()
+
+
+def test_oracle_reads_bf16_exactly():
+    """bf16 inputs are widened exactly: the oracle on bf16 tensors equals the
+    oracle on the same values pre-converted to float64."""
+    q, k, v = prefill_inputs(1, 2, 1, 4, 4, 8, torch.bfloat16, seed=17)
+    o1, _ = oracle.prefill(q, k, v, False, 0.5)
+    o2, _ = oracle.prefill(q.double(), k.double(), v.double(), False, 0.5)
+    np.testing.assert_array_equal(o1, o2)
+
+
+def test_oracle_rejects_bad_head_ratio():
+    q, k, v = _rand(1, 3, 2, 2, 2, 4, seed=18)
+    with pytest.raises(ValueError):
+        oracle.prefill(q, k, v, False, 1.0)
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes: a numpy restatement with one error each must fail a pin.
+# --------------------------------------------------------------------------
+
+def _np_prefill(q, k, v, causal, scale, mutation=None):
+    B, H_q, N_q, d = q.shape
+    H_kv, N_kv = k.shape[1], k.shape[2]
+    g = H_q // H_kv
+    o = np.zeros(q.shape)
+    lse = np.zeros(q.shape[:3])
+    for b in range(B):
+        for h in range(H_q):
+            hk = h % H_kv if mutation == "head_modulo" else h // g
+            hv = (hk + 1) % H_kv if mutation == "value_head_shifted" else hk
+            for i in range(N_q):
+                off = 0 if mutation == "causal_top_left" else N_kv - N_q
+                n = min(N_kv, i + off + 1) if causal else N_kv
+                if mutation == "causal_strict" and causal:
+                    n = max(1, n - 1)
+                if mutation == "dropped_last_key" and n > 1:
+                    n -= 1
+                keys = k[b, hk, :n]
+                if mutation == "scores_key_reversed":
+                    keys = keys[::-1]
+                sc = 1.0 if mutation == "scale_ignored" else scale
+                s = sc * (keys @ q[b, h, i])
+                if mutation == "sign_flipped":
+                    s = -s
+                m = s.max()
+                p = np.exp(s - m)
+                l = p.sum()
+                o[b, h, i] = p @ v[b, hv, :n] / (1.0 if mutation == "unnormalised" else l)
+                lse[b, h, i] = (0.0 if mutation == "lse_without_max" else m) + math.log(l)
+    return o, lse
+
+
+MUTATIONS = ["head_modulo", "value_head_shifted", "causal_top_left", "causal_strict",
+             "dropped_last_key", "scores_key_reversed", "scale_ignored", "sign_flipped",
+             "unnormalised", "lse_without_max"]
+
+
+def test_pins_accept_unmutated_restatement():
+    for pin in PINS:
+        pin(lambda q, k, v, c, s: _np_prefill(q, k, v, c, s))
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS)
+def test_pins_reject_planted_mistake(mutation):
+    caught = []
+    for pin in PINS:
+        try:
+            pin(lambda q, k, v, c, s: _np_prefill(q, k, v, c, s, mutation))
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake '{mutation}'"
