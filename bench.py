@@ -1,0 +1,413 @@
+"""Benchmark of the GQA attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * prefill: the LLaMA-3-8B-shaped layer (B=1, H_q=32, H_kv=8, N=2048,
+    d=128, bf16, causal) through gqa_attn_fwd, and
+  * decode: one token per sequence against a bf16 K/V cache (B=64, H_q=12,
+    H_kv=2, d=128, max_len=2048, seqlens ~ U[1, 2048]) through
+    gqa_attn_decode (split-KV kernel + log-sum-exp combine).
+`value` is the prefill throughput in TFLOP/s (4*B*H_q*N_q*N_kv*d, halved for
+causal) over the prefill kernel's device time; the decode throughput in GB/s
+(valid cache rows once per K/V head, plus q, o and seqlens) is reported in
+the `decode` object. Inputs are rotated over enough copies that every step
+reads operands that are not in the 129 MB L2.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With --gpus N > 1 it runs under torch.distributed.run, one replica per GPU
+(no collective on the data path: the units are independent); rank 0 prints
+the single JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill TFLOP/s & decode KV-cache GB/s on 1 GB300, as fraction of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_src, name):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(name)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha") != source_sha(kernel_src):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling around the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = list(csv.reader(io.StringIO(self.out or "")))
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        top = max(sm)
+        loaded = [x for x in sm if x >= 0.5 * top] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from gqa_flash_attention_02_gb300 import inputs, ops
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    ops.load()
+    peaks, peak_src = load_peaks()
+
+    ps = inputs.LLAMA3_8B_LAYER
+    ds = inputs.decode_shapes()[-1]
+    # Rotate inputs so the operands of a step are evicted from L2 by the time
+    # they come round again.
+    q0, k0, v0 = inputs.prefill_inputs_for(ps)
+    sl0, dq0, kc0, vc0 = inputs.decode_inputs_for(ds)
+    step_in_bytes = (q0.numel() + k0.numel() + v0.numel()) * 2 + (kc0.numel() + vc0.numel()) * 2
+    copies = max(2, math.ceil(3 * L2_BYTES / step_in_bytes))
+    pre = [(q0.to(dev), k0.to(dev), v0.to(dev)) for _ in range(copies)]
+    dec = [(sl0.to(dev), dq0.to(dev), kc0.to(dev), vc0.to(dev)) for _ in range(copies)]
+    o_pre = torch.empty_like(pre[0][0])
+    o_dec = torch.empty_like(dec[0][1])
+    torch.cuda.synchronize()
+
+    pre_flops = ps.flops
+    n_valid = int(sl0.sum())
+    dec_bytes = (n_valid * ds.H_kv * ds.d * 2 * 2 + 2 * dq0.numel() * 2 + 4 * ds.B)
+
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        q, k, v = pre[i % copies]
+        sl, dq, kc, vc = dec[i % copies]
+        if ev is not None:
+            ev[0].record(stream)
+        ops.gqa_attn_fwd(q, k, v, o_pre, causal=True, scale=ps.scale, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ops.gqa_attn_decode(dq, kc, vc, sl, o_dec, scale=ds.scale, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                      else local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step(i, evs[i])
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t0
+    t_pre = [e[0].elapsed_time(e[1]) for e in evs]   # ms
+    t_dec = [e[1].elapsed_time(e[2]) for e in evs]
+    tot_pre, tot_dec = sum(t_pre), sum(t_dec)
+    gpu_err = ops.gqa_attn_get_device_error()
+    if gpu_err != 0:
+        raise RuntimeError(f"device error during the bench: {ops.status_string(gpu_err)}")
+
+    # ---- e2e through the public API with host buffers (pinned), copies timed
+    hq, hk, hv = (t.pin_memory() for t in (q0, k0, v0))
+    ho = torch.empty(o_pre.shape, dtype=o_pre.dtype).pin_memory()
+    hsl, hdq, hkc, hvc = (t.pin_memory() for t in (sl0, dq0, kc0, vc0))
+    hdo = torch.empty(o_dec.shape, dtype=o_dec.dtype).pin_memory()
+    dq_, dk_, dv_ = (torch.empty_like(t, device=dev) for t in (q0, k0, v0))
+    dsl_, ddq_, dkc_, dvc_ = (torch.empty_like(t, device=dev) for t in (sl0, dq0, kc0, vc0))
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step(evp):
+        evp[0].record(stream)
+        dq_.copy_(hq, non_blocking=True); dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        ops.gqa_attn_fwd(dq_, dk_, dv_, o_pre, causal=True, scale=ps.scale, stream=stream)
+        ho.copy_(o_pre, non_blocking=True)
+        evp[1].record(stream)
+        dsl_.copy_(hsl, non_blocking=True); ddq_.copy_(hdq, non_blocking=True)
+        dkc_.copy_(hkc, non_blocking=True); dvc_.copy_(hvc, non_blocking=True)
+        ops.gqa_attn_decode(ddq_, dkc_, dvc_, dsl_, o_dec, scale=ds.scale, stream=stream)
+        hdo.copy_(o_dec, non_blocking=True)
+        evp[2].record(stream)
+
+    for _ in range(2):
+        e2e_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize()
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        e2e_step(eev[i])
+    torch.cuda.synchronize()
+    e2e_pre = sum(e[0].elapsed_time(e[1]) for e in eev) / e2e_steps
+    e2e_dec = sum(e[1].elapsed_time(e[2]) for e in eev) / e2e_steps
+
+    # ---- max over ranks
+    vals = torch.tensor([tot_pre, tot_dec, wall, e2e_pre, e2e_dec], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    tot_pre, tot_dec, wall, e2e_pre, e2e_dec = vals.tolist()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    K = args.steps
+    pre_ms = tot_pre / K
+    dec_ms = tot_dec / K
+    value = world * K * pre_flops / (tot_pre * 1e-3) / 1e12
+    dec_gbs = world * K * dec_bytes / (tot_dec * 1e-3) / 1e9
+    pre_ach = pre_flops / (pre_ms * 1e-3) / 1e12
+    dec_ach = dec_bytes / (dec_ms * 1e-3) / 1e9
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    h2d_pre = (q0.numel() + k0.numel() + v0.numel()) * 2
+    d2h_pre = o_pre.numel() * 2
+    h2d_dec = sl0.numel() * 4 + (dq0.numel() + kc0.numel() + vc0.numel()) * 2
+    d2h_dec = o_dec.numel() * 2
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(pre_ms + dec_ms, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded iid N(0,1) q/k/v, bf16; decode seqlens ~ U[1,2048])",
+        "config": {
+            "workload": "llama3_8b_prefill_layer + decode_b64",
+            "prefill": {"B": ps.B, "H_q": ps.H_q, "H_kv": ps.H_kv, "N_q": ps.N_q,
+                        "N_kv": ps.N_kv, "d": ps.d, "causal": ps.causal},
+            "decode": {"B": ds.B, "H_q": ds.H_q, "H_kv": ds.H_kv, "max_len": ds.max_len,
+                       "d": ds.d, "sum_seqlens": n_valid},
+            "l2": f"inputs rotated over {copies} copies "
+                  f"({copies * step_in_bytes / 2**20:.0f} MiB > 129 MiB L2)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "prefill_tc_kernel<128>",
+            "achieved": round(pre_ach, 3),
+            "peak": tc_peak,
+            "unit": "TFLOP/s",
+            "frac": round(pre_ach / tc_peak, 4),
+            "peak_source": f"{peak_src} bf16_tflops (burst)",
+            "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
+                                        "prefill_tc_kernel<128>"),
+        },
+        "decode": {
+            "value": round(dec_gbs, 2),
+            "unit": "GB/s",
+            "ms": round(dec_ms, 6),
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "decode_splitkv_kernel + decode_combine_kernel",
+                "achieved": round(dec_ach, 2),
+                "peak": hbm_peak,
+                "unit": "GB/s",
+                "frac": round(dec_ach / hbm_peak, 4),
+                "peak_source": f"{peak_src} hbm_gbs",
+                "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
+                                            "decode_splitkv_kernel<128,128>"),
+            },
+            "e2e": {"value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},
+        },
+        "e2e": {"value": round(pre_flops / (e2e_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre},
+        "gpu_launches": 3 * K,
+        "wall_ms_per_step": round(wall * 1e3 / K, 6),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(ps)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# --------------------------------------------------------------------------- oracle
+
+def oracle_prefill_sample(ps, heads, threads):
+    """Times the float64 CPU oracle on `heads` (b, h_q) heads of the workload.
+    Returns (seconds, flops of that sample)."""
+    import oracle
+    from gqa_flash_attention_02_gb300 import inputs
+
+    q, k, v = inputs.prefill_inputs_for(ps)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.prefill(q, k, v, ps.causal, ps.scale, heads=(0, heads), n_threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, ps.flops * heads / (ps.B * ps.H_q)
+
+
+def cpu_baseline(ps):
+    cores = os.cpu_count() or 1
+    heads = min(ps.B * ps.H_q, max(2, cores))
+    dt, flops = oracle_prefill_sample(ps, heads, cores)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{heads} of {ps.B * ps.H_q} heads of the prefill layer "
+                      f"(all {ps.N_q} rows each), float64, OpenMP over heads, {dt:.2f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    from gqa_flash_attention_02_gb300 import inputs
+
+    ps = inputs.LLAMA3_8B_LAYER
+    cores = os.cpu_count() or 1
+    heads = max(1, min(ps.B * ps.H_q, cores))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(ps, 1, 1)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, flops = oracle_prefill_sample(ps, heads, cores)
+        times.append(dt)
+    tot = sum(times)
+    value = args.steps * flops / tot / 1e12
+    sample = (f"{heads} of {ps.B * ps.H_q} heads of the prefill layer per step, float64 "
+              f"oracle, OpenMP over heads")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(tot * 1e3 / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded iid N(0,1), bf16 values widened to float64)",
+        "config": {"workload": "llama3_8b_prefill_layer (head sample)",
+                   "prefill": {"B": ps.B, "H_q": ps.H_q, "H_kv": ps.H_kv, "N_q": ps.N_q,
+                               "N_kv": ps.N_kv, "d": ps.d, "causal": ps.causal}},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing leg (profiling runs)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,347 @@
+// C ABI of the library (declared in include/gqa_attn.h): argument
+// validation, the per-(device, stream) workspace, TMA tensor-map encoding and
+// dispatch to the kernels. No torch types cross this boundary.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gqa_attn.h"
+#include "gqa_internal.h"
+
+using namespace gqa;
+
+namespace {
+
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = e;
+  cudaGetLastError();  // clear the sticky-free error state for this thread
+  return GQA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ workspace
+
+struct WsKey {
+  int dev;
+  cudaStream_t stream;
+  bool operator<(const WsKey &o) const {
+    return dev != o.dev ? dev < o.dev : reinterpret_cast<uintptr_t>(stream) < reinterpret_cast<uintptr_t>(o.stream);
+  }
+};
+
+std::mutex g_ws_mutex;
+std::map<WsKey, Workspace> g_ws;
+std::map<int, int> g_num_sms;
+
+int device_sms(int dev) {
+  std::lock_guard<std::mutex> lk(g_ws_mutex);
+  auto it = g_num_sms.find(dev);
+  if (it != g_num_sms.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  g_num_sms[dev] = n;
+  return n;
+}
+
+// Returns the workspace of (current device, stream) with at least
+// `partials_bytes` of partials space; creates or grows it stream-ordered.
+int get_workspace(cudaStream_t stream, size_t partials_bytes, Workspace **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(g_ws_mutex);
+  Workspace &ws = g_ws[WsKey{dev, stream}];
+  if (ws.ctl == nullptr) {
+    void *p = nullptr;
+    e = cudaMallocAsync(&p, kCtlInts * sizeof(int), stream);
+    if (e != cudaSuccess) {
+      g_ws.erase(WsKey{dev, stream});
+      cudaGetLastError();
+      return GQA_ERR_OOM;
+    }
+    e = cudaMemsetAsync(p, 0, kCtlInts * sizeof(int), stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    ws.ctl = static_cast<int *>(p);
+  }
+  if (partials_bytes > ws.partials_bytes) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+      return GQA_ERR_OOM;  // cannot grow while capturing: warm up outside the capture first
+    if (ws.partials) cudaFreeAsync(ws.partials, stream);
+    ws.partials = nullptr;
+    ws.partials_bytes = 0;
+    void *p = nullptr;
+    // grow geometrically so a sweep of shapes does not reallocate each call
+    size_t want = partials_bytes < (1u << 20) ? (1u << 20) : partials_bytes + partials_bytes / 4;
+    e = cudaMallocAsync(&p, want, stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GQA_ERR_OOM;
+    }
+    ws.partials = static_cast<float *>(p);
+    ws.partials_bytes = want;
+  }
+  *out = &ws;
+  return GQA_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    cudaGetLastError();
+  });
+  return g_encode;
+}
+
+// bf16 tensor viewed as [planes][rows][d]; box = 64 columns x box_rows rows,
+// 128-byte swizzle, zero fill outside the tensor.
+bool encode_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long planes,
+                    int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ validation
+
+constexpr long long kMaxElems = (1ll << 31) - 1;
+
+int check_prefill_args(const void *q, const void *k, const void *v, const void *o, int B, int H_q,
+                       int H_kv, int N_q, int N_kv, int d, int causal, float scale) {
+  if (!q || !k || !v || !o) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GQA_ERR_INVALID_ARG;
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || N_q <= 0 || N_kv <= 0 || d <= 0) return GQA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (causal && N_q > N_kv) return GQA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H_q * N_q * d > kMaxElems ||
+      static_cast<long long>(B) * H_kv * N_kv * d > kMaxElems)
+    return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+int check_decode_args(const void *q, const void *kc, const void *vc, const int *seqlens,
+                      const void *o, int B, int H_q, int H_kv, int max_len, int d, float scale) {
+  if (!q || !kc || !vc || !seqlens || !o) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(o)) return GQA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seqlens) & 3u) != 0) return GQA_ERR_INVALID_ARG;
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_len <= 0 || d <= 0) return GQA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (max_len > (1 << 20)) return GQA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H_kv * max_len * d > kMaxElems ||
+      static_cast<long long>(B) * H_q * d > kMaxElems)
+    return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+bool d_supported_simt(int d) { return d == 32 || d == 64 || d == 96 || d == 128; }
+
+}  // namespace
+
+extern "C" {
+
+int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, int B, int H_q, int H_kv,
+                 int N_q, int N_kv, int d, int causal, float scale, cudaStream_t stream) {
+  int rc = check_prefill_args(q, k, v, o, B, H_q, H_kv, N_q, N_kv, d, causal, scale);
+  if (rc != GQA_OK) return rc;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  const PrefillPlan plan = make_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal);
+  Workspace *ws = nullptr;
+  rc = get_workspace(stream, 0, &ws);
+  if (rc != GQA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_3d(&tq, q, d, N_q, static_cast<long>(B) * H_q, kTileM) ||
+      !encode_bf16_3d(&tk, k, d, N_kv, static_cast<long>(B) * H_kv, kTileN) ||
+      !encode_bf16_3d(&tv, v, d, N_kv, static_cast<long>(B) * H_kv, kTileN))
+    return cuda_fail(cudaErrorInvalidValue);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e = launch_prefill_tc(tq, tk, tv, o, plan, d, scale, ws->ctl, device_sms(dev), stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o, int B, int H_q,
+                     int H_kv, int N_q, int N_kv, int d, int causal, float scale,
+                     cudaStream_t stream) {
+  int rc = check_prefill_args(q, k, v, o, B, H_q, H_kv, N_q, N_kv, d, causal, scale);
+  if (rc != GQA_OK) return rc;
+  if (!d_supported_simt(d)) return GQA_ERR_UNSUPPORTED;
+  Workspace *ws = nullptr;
+  rc = get_workspace(stream, 0, &ws);
+  if (rc != GQA_OK) return rc;
+  cudaError_t e = launch_attn_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                                  static_cast<const float *>(v), static_cast<float *>(o), B, H_q,
+                                  H_kv, N_q, N_kv, d, causal, scale, nullptr, N_kv,
+                                  ws->ctl + kCtlErr, stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_attn_decode_chunked(const void *q, const void *k_cache, const void *v_cache,
+                            const int *seqlens, void *o, int B, int H_q, int H_kv, int max_len,
+                            int d, float scale, int chunk_tokens, cudaStream_t stream) {
+  int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
+  if (rc != GQA_OK) return rc;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (chunk_tokens != 0 && chunk_tokens != 32 && chunk_tokens != 64 && chunk_tokens != 128 &&
+      chunk_tokens != 256)
+    return chunk_tokens % 32 == 0 && chunk_tokens >= 32 && chunk_tokens <= 256
+               ? GQA_ERR_UNSUPPORTED
+               : GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int chunk = chunk_tokens ? chunk_tokens : decode_default_chunk(B, H_kv, max_len, device_sms(dev));
+  Workspace *ws = nullptr;
+  rc = get_workspace(stream, decode_partials_bytes(B, H_q, max_len, d, chunk), &ws);
+  if (rc != GQA_OK) return rc;
+  CUtensorMap tk, tv;
+  if (!encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, chunk) ||
+      !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, chunk))
+    return cuda_fail(cudaErrorInvalidValue);
+  e = launch_decode_bf16(tk, tv, q, seqlens, o, ws->partials, B, H_q, H_kv, max_len, d, scale,
+                         chunk, ws->ctl + kCtlErr, stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int *seqlens,
+                    void *o, int B, int H_q, int H_kv, int max_len, int d, float scale,
+                    cudaStream_t stream) {
+  return gqa_attn_decode_chunked(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale,
+                                 0, stream);
+}
+
+int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
+                        const int *seqlens, void *o, int B, int H_q, int H_kv, int max_len, int d,
+                        float scale, cudaStream_t stream) {
+  int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
+  if (rc != GQA_OK) return rc;
+  if (!d_supported_simt(d)) return GQA_ERR_UNSUPPORTED;
+  Workspace *ws = nullptr;
+  rc = get_workspace(stream, 0, &ws);
+  if (rc != GQA_OK) return rc;
+  // decode = prefill form with one query row and per-sequence key counts
+  cudaError_t e = launch_attn_f32(static_cast<const float *>(q), static_cast<const float *>(k_cache),
+                                  static_cast<const float *>(v_cache), static_cast<float *>(o), B,
+                                  H_q, H_kv, 1, max_len, d, 0, scale, seqlens, max_len,
+                                  ws->ctl + kCtlErr, stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+const char *gqa_attn_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG: invalid argument (null/misaligned pointer, non-positive size, H_q not a multiple of H_kv, non-finite scale)";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: unsupported configuration (head dim, causal with N_q > N_kv, or size limit)";
+    case GQA_ERR_CUDA: {
+      thread_local char buf[160];
+      snprintf(buf, sizeof(buf), "GQA_ERR_CUDA: %s", cudaGetErrorName(g_last_cuda_error));
+      return buf;
+    }
+    case GQA_ERR_DEVICE_TIMEOUT: return "GQA_ERR_DEVICE_TIMEOUT: a bounded device-side wait ran out";
+    case GQA_ERR_OOM: return "GQA_ERR_OOM: workspace allocation failed (or would grow during stream capture)";
+    case GQA_ERR_BAD_SEQLEN: return "GQA_ERR_BAD_SEQLEN: a seqlens entry was outside [0, max_len]";
+    default: return "unknown gqa_status";
+  }
+}
+
+int gqa_attn_get_device_error(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int *ctl = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mutex);
+    auto it = g_ws.find(WsKey{dev, stream});
+    if (it == g_ws.end()) return GQA_OK;  // nothing ever ran on this stream
+    ctl = it->second.ctl;
+  }
+  int word = 0;
+  e = cudaMemcpyAsync(&word, ctl + kCtlErr, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctl + kCtlErr, 0, sizeof(int), stream);
+  if (e == cudaSuccess && (word & kErrTimeout)) {
+    // a pipeline that gave up may have left the work counter armed
+    e = cudaMemsetAsync(ctl + kCtlWork, 0, 2 * sizeof(int), stream);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word & kErrTimeout) return GQA_ERR_DEVICE_TIMEOUT;
+  if (word & kErrBadSeqlen) return GQA_ERR_BAD_SEQLEN;
+  return GQA_OK;
+}
+
+int gqa_attn_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv, int causal, int unit,
+                          int *out) {
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || N_q <= 0 || N_kv <= 0 || H_q % H_kv != 0) return -1;
+  if (causal && N_q > N_kv) return -1;
+  const PrefillPlan plan = make_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal);
+  if (out != nullptr && unit >= 0 && unit < plan.total_units) {
+    const Unit w = decode_unit(plan, unit);
+    out[0] = w.b;
+    out[1] = w.h_kv;
+    for (int t = 0; t < 2; ++t) {
+      out[2 + 3 * t] = w.t[t].h_q;
+      out[3 + 3 * t] = w.t[t].q_tile;
+      out[4 + 3 * t] = w.t[t].kv_blocks;
+    }
+  }
+  return plan.total_units;
+}
+
+int gqa_attn_selftest_wait_timeout(int timeout_us, cudaStream_t stream) {
+  if (timeout_us < 1 || timeout_us > 100000) return GQA_ERR_INVALID_ARG;
+  Workspace *ws = nullptr;
+  int rc = get_workspace(stream, 0, &ws);
+  if (rc != GQA_OK) return rc;
+  cudaError_t e = launch_wait_timeout_selftest(timeout_us, ws->ctl + kCtlErr, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return gqa_attn_get_device_error(stream);
+}
+
+void gqa_attn_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_ws_mutex);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto &kv : g_ws) {
+    cudaSetDevice(kv.first.dev);
+    cudaDeviceSynchronize();
+    if (kv.second.partials) cudaFree(kv.second.partials);
+    if (kv.second.ctl) cudaFree(kv.second.ctl);
+  }
+  g_ws.clear();
+  cudaSetDevice(cur);
+  cudaGetLastError();
+}
+
+}  // extern "C"

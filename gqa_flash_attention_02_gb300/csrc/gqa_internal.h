@@ -1,0 +1,138 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define GQA_HD __host__ __device__ __forceinline__
+#else
+#define GQA_HD inline
+#endif
+
+namespace gqa {
+
+// Bits of the device error word kept in each workspace.
+constexpr int kErrTimeout = 1 << 0;
+constexpr int kErrBadSeqlen = 1 << 1;
+
+constexpr int kTileM = 128;  // query rows per tile
+constexpr int kTileN = 128;  // key rows per K/V block
+
+// ------------------------------------------------------------------------
+// Persistent prefill schedule.
+//
+// A (b, h_kv) group owns g = H_q / H_kv query heads, each cut into
+// n_qt = ceil(N_q / 128) query tiles. Within a group the g * n_qt tiles are
+// listed heaviest first (q_tile descending -- later tiles see more keys
+// under the causal mask -- and head ascending within one q_tile) and paired
+// consecutively: a unit is two query tiles of the same group, so ONE stream
+// of K/V blocks feeds both. When g is even the two tiles share their q_tile
+// (identical causal extent). Units are numbered pair-rank-major across all
+// groups, so unit order is heavy-first globally; an atomic counter hands
+// them out (the persistent-kernel entry's global work queue, BootstrapAI
+// evolution log).
+// ------------------------------------------------------------------------
+struct PrefillPlan {
+  int B, H_q, H_kv, N_q, N_kv, causal;
+  int group;           // g
+  int n_qt, n_kt;      // query tiles per head, key blocks per head
+  int tiles_per_group; // g * n_qt
+  int pairs_per_group; // ceil(tiles_per_group / 2)
+  int total_units;     // B * H_kv * pairs_per_group
+  int kv_offset;       // N_kv - N_q (bottom-right causal alignment)
+};
+
+struct UnitTile {
+  int h_q, q_tile, kv_blocks;  // kv_blocks == 0 -> no tile
+};
+
+struct Unit {
+  int b, h_kv;
+  UnitTile t[2];
+};
+
+GQA_HD PrefillPlan make_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv, int causal) {
+  PrefillPlan p;
+  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_kv = N_kv; p.causal = causal ? 1 : 0;
+  p.group = H_q / H_kv;
+  p.n_qt = (N_q + kTileM - 1) / kTileM;
+  p.n_kt = (N_kv + kTileN - 1) / kTileN;
+  p.tiles_per_group = p.group * p.n_qt;
+  p.pairs_per_group = (p.tiles_per_group + 1) / 2;
+  p.total_units = B * H_kv * p.pairs_per_group;
+  p.kv_offset = N_kv - N_q;
+  return p;
+}
+
+// Number of key blocks query tile `qt` must visit.
+GQA_HD int kv_blocks_for_tile(const PrefillPlan &p, int qt) {
+  if (!p.causal) return p.n_kt;
+  int last_row = (qt + 1) * kTileM - 1;
+  if (last_row > p.N_q - 1) last_row = p.N_q - 1;
+  const int last_key = last_row + p.kv_offset;  // >= 0 because N_kv >= N_q
+  int nb = last_key / kTileN + 1;
+  return nb < p.n_kt ? nb : p.n_kt;
+}
+
+GQA_HD Unit decode_unit(const PrefillPlan &p, int u) {
+  Unit w;
+  const int groups = p.B * p.H_kv;
+  const int rank = u / groups;
+  const int bh = u - rank * groups;
+  w.b = bh / p.H_kv;
+  w.h_kv = bh - w.b * p.H_kv;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int f = 2 * rank + s;
+    if (f < p.tiles_per_group) {
+      const int qt = p.n_qt - 1 - f / p.group;
+      w.t[s].h_q = w.h_kv * p.group + (f % p.group);
+      w.t[s].q_tile = qt;
+      w.t[s].kv_blocks = kv_blocks_for_tile(p, qt);
+    } else {
+      w.t[s].h_q = -1;
+      w.t[s].q_tile = -1;
+      w.t[s].kv_blocks = 0;
+    }
+  }
+  return w;
+}
+
+// ------------------------------------------------------------------------
+// Workspace: per (device, stream). Layout of the control block (ints):
+//   [0] device error word   [1] work counter   [2] CTAs finished
+// ------------------------------------------------------------------------
+constexpr int kCtlErr = 0;
+constexpr int kCtlWork = 1;
+constexpr int kCtlDone = 2;
+constexpr int kCtlInts = 64;
+
+struct Workspace {
+  int *ctl = nullptr;        // kCtlInts ints, zeroed at creation
+  float *partials = nullptr; // split-KV decode partials
+  size_t partials_bytes = 0;
+};
+
+// Launchers (return a cudaError_t; arguments already validated).
+cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                              const CUtensorMap &tm_v, void *o, const PrefillPlan &plan, int d,
+                              float scale, int *ctl, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_attn_f32(const float *q, const float *k, const float *v, float *o, int B,
+                            int H_q, int H_kv, int N_q, int N_kv, int d, int causal, float scale,
+                            const int *seqlens, int kv_row_capacity, int *err_word,
+                            cudaStream_t stream);
+
+// Decode split-KV: `chunk` cache rows per split.
+size_t decode_partials_bytes(int B, int H_q, int max_len, int d, int chunk);
+int decode_default_chunk(int B, int H_kv, int max_len, int num_sms);
+cudaError_t launch_decode_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
+                               const int *seqlens, void *o, float *partials, int B, int H_q,
+                               int H_kv, int max_len, int d, float scale, int chunk,
+                               int *err_word, cudaStream_t stream);
+
+cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStream_t stream);
+
+}  // namespace gqa

@@ -1,0 +1,201 @@
+"""ctypes binding of libgqa_attn.so with the C ABI's names.
+
+Argument marshalling only: shapes and dtypes are checked, pointers and the
+current CUDA stream are passed through, and every step of the computation
+runs in the library's kernels. If the library cannot be loaded the call
+raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+GQA_OK = 0
+STATUS_NAMES = {
+    0: "GQA_OK",
+    1: "GQA_ERR_INVALID_ARG",
+    2: "GQA_ERR_UNSUPPORTED",
+    3: "GQA_ERR_CUDA",
+    4: "GQA_ERR_DEVICE_TIMEOUT",
+    5: "GQA_ERR_OOM",
+    6: "GQA_ERR_BAD_SEQLEN",
+}
+
+EXPORTED = [
+    "gqa_attn_fwd", "gqa_attn_fwd_f32", "gqa_attn_decode", "gqa_attn_decode_chunked",
+    "gqa_attn_decode_f32", "gqa_attn_status_string", "gqa_attn_get_device_error",
+    "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
+]
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libgqa_attn.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_missing else _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"libgqa_attn.so not found at {path}")
+            lib = ctypes.CDLL(path)
+            fwd = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp]
+            for name in ("gqa_attn_fwd", "gqa_attn_fwd_f32"):
+                getattr(lib, name).argtypes = fwd
+                getattr(lib, name).restype = _i
+            dec = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+            for name in ("gqa_attn_decode", "gqa_attn_decode_f32"):
+                getattr(lib, name).argtypes = dec
+                getattr(lib, name).restype = _i
+            lib.gqa_attn_decode_chunked.argtypes = dec[:-1] + [_i, _vp]
+            lib.gqa_attn_decode_chunked.restype = _i
+            lib.gqa_attn_status_string.argtypes = [_i]
+            lib.gqa_attn_status_string.restype = ctypes.c_char_p
+            lib.gqa_attn_get_device_error.argtypes = [_vp]
+            lib.gqa_attn_get_device_error.restype = _i
+            lib.gqa_attn_prefill_plan.argtypes = [_i] * 7 + [ctypes.POINTER(_i)]
+            lib.gqa_attn_prefill_plan.restype = _i
+            lib.gqa_attn_selftest_wait_timeout.argtypes = [_i, _vp]
+            lib.gqa_attn_selftest_wait_timeout.restype = _i
+            lib.gqa_attn_shutdown.argtypes = []
+            lib.gqa_attn_shutdown.restype = None
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().gqa_attn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != GQA_OK:
+        raise GqaError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str, ndim: int):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ---------------------------------------------------------------- prefill
+
+def gqa_attn_fwd(q, k, v, o=None, causal=False, scale=None, stream=None):
+    """bf16 prefill. q [B,H_q,N_q,d], k/v [B,H_kv,N_kv,d] -> o [B,H_q,N_q,d] (bf16)."""
+    return _fwd("gqa_attn_fwd", torch.bfloat16, q, k, v, o, causal, scale, stream)
+
+
+def gqa_attn_fwd_f32(q, k, v, o=None, causal=False, scale=None, stream=None):
+    """fp32 prefill with the same layouts."""
+    return _fwd("gqa_attn_fwd_f32", torch.float32, q, k, v, o, causal, scale, stream)
+
+
+def _fwd(name, dtype, q, k, v, o, causal, scale, stream):
+    B, H_q, N_q, d = q.shape
+    _, H_kv, N_kv, _ = k.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if scale is None:
+        scale = d ** -0.5
+    args = (_dev(q, dtype, "q", 4), _dev(k, dtype, "k", 4), _dev(v, dtype, "v", 4),
+            _dev(o, dtype, "o", 4))
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != d or \
+            tuple(o.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, k, v, o")
+    rc = getattr(load(), name)(*args, B, H_q, H_kv, N_q, N_kv, d, int(bool(causal)),
+                               float(scale), _stream(stream))
+    _check(rc, name)
+    return o
+
+
+# ---------------------------------------------------------------- decode
+
+def gqa_attn_decode(q, k_cache, v_cache, seqlens, o=None, scale=None, chunk_tokens=0,
+                    stream=None):
+    """bf16 decode. q [B,H_q,d], caches [B,H_kv,max_len,d], seqlens int32 [B] -> o [B,H_q,d]."""
+    return _decode("gqa_attn_decode_chunked", torch.bfloat16, q, k_cache, v_cache, seqlens, o,
+                   scale, chunk_tokens, stream)
+
+
+def gqa_attn_decode_f32(q, k_cache, v_cache, seqlens, o=None, scale=None, stream=None):
+    return _decode("gqa_attn_decode_f32", torch.float32, q, k_cache, v_cache, seqlens, o, scale,
+                   None, stream)
+
+
+def _decode(name, dtype, q, kc, vc, seqlens, o, scale, chunk, stream):
+    B, H_q, d = q.shape
+    _, H_kv, max_len, _ = kc.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if scale is None:
+        scale = d ** -0.5
+    if tuple(vc.shape) != tuple(kc.shape) or kc.shape[0] != B or kc.shape[3] != d or \
+            tuple(o.shape) != tuple(q.shape) or tuple(seqlens.shape) != (B,):
+        raise ValueError("shape mismatch between q, caches, seqlens, o")
+    args = [_dev(q, dtype, "q", 3), _dev(kc, dtype, "k_cache", 4), _dev(vc, dtype, "v_cache", 4),
+            _dev(seqlens, torch.int32, "seqlens", 1), _dev(o, dtype, "o", 3),
+            B, H_q, H_kv, max_len, d, float(scale)]
+    if chunk is not None:
+        args.append(int(chunk))
+    rc = getattr(load(), name)(*args, _stream(stream))
+    _check(rc, name)
+    return o
+
+
+# ---------------------------------------------------------------- misc
+
+def gqa_attn_get_device_error(stream=None) -> int:
+    return load().gqa_attn_get_device_error(_stream(stream))
+
+
+def gqa_attn_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal):
+    """Return the scheduler's unit list: [(b, h_kv, (h_q0, qt0, nb0), (h_q1, qt1, nb1)), ...]."""
+    lib = load()
+    n = lib.gqa_attn_prefill_plan(B, H_q, H_kv, N_q, N_kv, int(bool(causal)), -1, None)
+    if n < 0:
+        raise ValueError("invalid sizes")
+    out = (ctypes.c_int * 8)()
+    units = []
+    for u in range(n):
+        lib.gqa_attn_prefill_plan(B, H_q, H_kv, N_q, N_kv, int(bool(causal)), u, out)
+        units.append((out[0], out[1], (out[2], out[3], out[4]), (out[5], out[6], out[7])))
+    return units
+
+
+def gqa_attn_selftest_wait_timeout(timeout_us: int = 1000, stream=None) -> int:
+    return load().gqa_attn_selftest_wait_timeout(int(timeout_us), _stream(stream))
+
+
+def gqa_attn_shutdown():
+    load().gqa_attn_shutdown()

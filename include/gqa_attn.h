@@ -1,0 +1,170 @@
+/*
+ * gqa_attn.h -- C ABI of the GB300 (sm_103a) grouped-query attention library.
+ *
+ * Operation (both forms):  O = softmax(scale * Q K^T [+ causal mask]) V,
+ * where query head h_q reads K/V head h_kv = h_q / (H_q / H_kv). With
+ * H_kv == H_q this is multi-head attention, with H_kv == 1 multi-query
+ * attention, anything in between grouped-query attention.
+ *   - Head mapping and the MHA/GQA/MQA unification: BootstrapAI evolution log,
+ *     collab-014 "Kernel 9 GQA".
+ *   - Prefill is compute-bound, single-token decode against a K/V cache is
+ *     memory-bound: kaispace.site, the "prefill vs decode / chunked prefill"
+ *     note; cached GQA decode with per-row lengths and a bf16 cache:
+ *     microLLM-rocm optimisation log, Experiments 064-065.
+ *   - Split-sequence decode with a merge of partial results: microLLM-rocm
+ *     optimisation log, Experiments 282-284.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to contiguous row-major arrays
+ *     owned by the caller, at least 16-byte aligned. The library never frees,
+ *     retains or reallocates them.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream):
+ *     outputs are valid once the stream has synchronised.
+ *   - Precision: the unsuffixed entry points take bf16 inputs, accumulate in
+ *     fp32 on the tensor cores (prefill) or CUDA cores (decode), and write
+ *     bf16 output. The `_f32` siblings take and write fp32 with fp32 math
+ *     throughout (no TF32).
+ *   - Causal alignment is bottom-right: query row i sees key j iff
+ *     j <= i + (N_kv - N_q). With N_q == N_kv this is the ordinary lower
+ *     triangle. causal with N_q > N_kv is rejected (GQA_ERR_UNSUPPORTED).
+ *   - `scale` is used as given (typically 1/sqrt(d)); it must be finite.
+ *   - The library owns a small per-(device, stream) workspace (the scheduler
+ *     counters, the device error word and the split-KV partials). It grows
+ *     on demand with stream-ordered allocation and is released by
+ *     gqa_attn_shutdown(). Calls on DIFFERENT streams use different
+ *     workspaces and may run concurrently.
+ *   - Errors are returned as a gqa_status code before anything is launched;
+ *     nothing is launched when a call fails validation. Faults detected on
+ *     the device (a bounded wait that ran out, a seqlen outside
+ *     [0, max_len]) are recorded in the workspace's error word and reported
+ *     by gqa_attn_get_device_error(). No kernel traps or asserts.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gqa_status {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1,    /* dims <= 0, H_q % H_kv != 0, non-finite scale,
+                                   null or misaligned pointer */
+    GQA_ERR_UNSUPPORTED = 2,    /* d not in {64, 128}; causal with N_q > N_kv;
+                                   a size beyond the documented limits */
+    GQA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+    GQA_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out */
+    GQA_ERR_OOM = 5,            /* the workspace could not be grown */
+    GQA_ERR_BAD_SEQLEN = 6      /* the device saw seqlens[b] < 0 or > max_len */
+} gqa_status;
+
+/*
+ * Prefill attention, bf16 in / bf16 out, fp32 accumulation (tcgen05 tensor
+ * cores, TMEM accumulators, TMA-staged tiles, persistent tile scheduler).
+ *   q : [B][H_q][N_q][d]  bf16      k, v : [B][H_kv][N_kv][d]  bf16
+ *   o : [B][H_q][N_q][d]  bf16 (written)
+ *   d in {64, 128}; 1 <= B*H_q*N_q*d < 2^31 elements per tensor.
+ * Pages: BootstrapAI evolution log, collab-014 "Kernel 9 GQA" (semantics),
+ * and the persistent-kernel entry (atomic work counter over tiles).
+ */
+int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o,
+                 int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+                 int causal, float scale, cudaStream_t stream);
+
+/*
+ * Same operation in fp32: q, k, v, o are float arrays with the layouts of
+ * gqa_attn_fwd. SIMT FMA kernel (online softmax, warp-shuffle reductions);
+ * d in {32, 64, 96, 128}.
+ * Pages: BootstrapAI evolution log, collab-005 "Kernel 2 tiling" (online
+ * softmax over key tiles) and collab-014 "Kernel 9 GQA".
+ */
+int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o,
+                     int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+                     int causal, float scale, cudaStream_t stream);
+
+/*
+ * Single-token decode against a bf16 K/V cache, split-KV with a log-sum-exp
+ * combine; bf16 output, fp32 math.
+ *   q       : [B][H_q][d] bf16         o : [B][H_q][d] bf16 (written)
+ *   k_cache, v_cache : [B][H_kv][max_len][d] bf16; rows [0, seqlens[b]) are
+ *             valid, later rows are never read into the result
+ *   seqlens : [B] int32 on the device, each in [0, max_len]; a sequence of
+ *             length 0 yields O = 0. Out-of-range values make the call
+ *             record GQA_ERR_BAD_SEQLEN (read with gqa_attn_get_device_error)
+ *             and leave that sequence's output at 0.
+ *   d in {64, 128}; max_len <= 1 << 20.
+ * Pages: microLLM-rocm optimisation log, Experiments 064-065 (batched cached
+ * GQA decode, bf16 cache with fp32 accumulation) and 282-284 (split-sequence
+ * cached attention).
+ */
+int gqa_attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const int *seqlens, void *o,
+                    int B, int H_q, int H_kv, int max_len, int d,
+                    float scale, cudaStream_t stream);
+
+/*
+ * gqa_attn_decode with an explicit split size: each split covers
+ * `chunk_tokens` cache rows (a multiple of 32 in [32, 256]); 0 picks the
+ * library's default for the shape. The result is the same operation for
+ * every chunk size, up to fp32 rounding.
+ */
+int gqa_attn_decode_chunked(const void *q, const void *k_cache,
+                            const void *v_cache, const int *seqlens, void *o,
+                            int B, int H_q, int H_kv, int max_len, int d,
+                            float scale, int chunk_tokens, cudaStream_t stream);
+
+/*
+ * Decode in fp32 (q, caches and o are float arrays, layouts as
+ * gqa_attn_decode); d in {32, 64, 96, 128}.
+ */
+int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
+                        const int *seqlens, void *o,
+                        int B, int H_q, int H_kv, int max_len, int d,
+                        float scale, cudaStream_t stream);
+
+/* Human-readable text for a gqa_status (never NULL; static storage). For
+ * GQA_ERR_CUDA it includes the last CUDA error name seen by this thread. */
+const char *gqa_attn_status_string(int status);
+
+/*
+ * Synchronises `stream`, reads and clears the device error word of that
+ * stream's workspace on the current device, and returns GQA_OK,
+ * GQA_ERR_DEVICE_TIMEOUT or GQA_ERR_BAD_SEQLEN (timeout wins when both are
+ * set), or GQA_ERR_CUDA if the synchronisation itself failed.
+ */
+int gqa_attn_get_device_error(cudaStream_t stream);
+
+/*
+ * Work plan of the persistent prefill scheduler, for inspection and tests
+ * (host only, no CUDA call). A unit is the pair of 128-row query tiles that
+ * one CTA processes against one K/V stream. Units are handed out by an
+ * atomic counter in index order; units with more visible key blocks come
+ * first (heavy-first causal order).
+ * Returns the number of units, or -1 for invalid sizes. When `unit` is in
+ * range, writes out[0..7] = {b, h_kv, h_q0, q_tile0, kv_blocks0,
+ * h_q1, q_tile1, kv_blocks1}; the second tile has kv_blocks1 == 0 (and
+ * h_q1 = q_tile1 = -1) when the unit holds only one tile.
+ */
+int gqa_attn_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv,
+                          int causal, int unit, int *out);
+
+/*
+ * Failure-detection self-test: launches a kernel that waits on an mbarrier
+ * nobody arrives at, with a limit of `timeout_us` microseconds (1..100000),
+ * then returns the result of gqa_attn_get_device_error(stream), which is
+ * GQA_ERR_DEVICE_TIMEOUT when the bounded wait works. Nothing else runs in
+ * that kernel, so the context stays usable.
+ */
+int gqa_attn_selftest_wait_timeout(int timeout_us, cudaStream_t stream);
+
+/* Frees every library-owned workspace on every device (synchronising the
+ * streams they belong to first). Safe to call more than once. */
+void gqa_attn_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

@@ -1,0 +1,254 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances (fixed by the method's statement of the target):
+  * fp32 path: max abs error <= 2e-5;
+  * bf16 path (bf16 inputs, fp32 accumulation, bf16 output): max abs error
+    <= 2e-2 and mean abs error <= 2e-3.
+The oracle reads the very same bf16/fp32 values, widened exactly to float64.
+Small shapes are compared element by element; the full-size prefill layers
+are compared on every row of two heads plus 64 random rows of every head.
+Every output buffer starts as NaN, so a tile the scheduler never visited
+shows up as a non-finite value.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_flash_attention_02_gb300 import inputs, ops
+
+pytestmark = pytest.mark.gpu
+
+F32_MAX = 2e-5
+BF16_MAX = 2e-2
+BF16_MEAN = 2e-3
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+def _dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def _err(got, ref):
+    d = np.abs(got.astype(np.float64) - ref)
+    return float(d.max()), float(d.mean())
+
+
+def _check_bf16(got, ref, what):
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    mx, mean = _err(got, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN, f"{what}: max {mx:.3e} mean {mean:.3e}"
+    return mx, mean
+
+
+def _prefill_bf16(q, k, v, causal, scale):
+    qd, kd, vd = _dev(q, k, v)
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_fwd(qd, kd, vd, o, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    return o.float().cpu().numpy()
+
+
+# ------------------------------------------------------------------ fp32 path
+
+def test_tiny_gqa_fp32_matches_oracle():
+    s = inputs.TINY
+    q, k, v = inputs.prefill_inputs_for(s)
+    qd, kd, vd = _dev(q, k, v)
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_fwd_f32(qd, kd, vd, o, causal=s.causal, scale=s.scale)
+    ref, _ = oracle.prefill(q, k, v, s.causal, s.scale)
+    mx, _ = _err(o.cpu().numpy(), ref)
+    assert mx <= F32_MAX, mx
+
+
+@pytest.mark.parametrize("shape", [
+    (2, 8, 2, 77, 77, 32, True), (1, 4, 1, 200, 333, 96, False), (1, 6, 6, 130, 130, 128, True),
+    (2, 4, 2, 1, 45, 64, False), (1, 2, 1, 64, 300, 64, True)])
+def test_fp32_prefill_shapes(shape):
+    B, H_q, H_kv, N_q, N_kv, d, causal = shape
+    q, k, v = inputs.prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, torch.float32, seed=31 + d)
+    qd, kd, vd = _dev(q, k, v)
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_fwd_f32(qd, kd, vd, o, causal=causal, scale=d ** -0.5)
+    ref, _ = oracle.prefill(q, k, v, causal, d ** -0.5)
+    mx, _ = _err(o.cpu().numpy(), ref)
+    assert mx <= F32_MAX, mx
+
+
+def test_fp32_decode_matches_oracle():
+    seqlens, q, kc, vc = inputs.decode_inputs(8, 12, 2, 300, 128, torch.float32, seed=41,
+                                              seqlens=[0, 300, 1, 17, 128, 129, 250, 299])
+    qd, kd, vd, sd = _dev(q, kc, vc, seqlens)
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_decode_f32(qd, kd, vd, sd, o, scale=128 ** -0.5)
+    ref, _ = oracle.decode(q, kc, vc, seqlens, 128 ** -0.5)
+    mx, _ = _err(o.cpu().numpy(), ref)
+    assert mx <= F32_MAX, mx
+
+
+# ------------------------------------------------------------------ bf16 prefill
+
+SMALL_BF16 = [
+    # B, H_q, H_kv, N_q, N_kv, d, causal
+    (1, 4, 2, 128, 128, 64, False),
+    (1, 4, 2, 300, 300, 64, True),      # ragged tail, several tiles
+    (2, 6, 2, 200, 520, 128, True),     # N_q < N_kv bottom-right, odd group 3
+    (1, 8, 8, 384, 384, 128, True),     # MHA
+    (1, 8, 1, 256, 700, 64, False),     # MQA, ragged K/V
+    (2, 2, 1, 1, 129, 128, False),      # single query row
+    (1, 3, 3, 129, 129, 64, True),      # odd tile count: half-empty last unit
+    (1, 2, 2, 640, 640, 128, False),    # 5 K/V blocks through a 4-stage ring
+]
+
+
+@pytest.mark.parametrize("shape", SMALL_BF16)
+def test_bf16_prefill_small_shapes(shape):
+    B, H_q, H_kv, N_q, N_kv, d, causal = shape
+    q, k, v = inputs.prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, torch.bfloat16, seed=51 + N_q)
+    got = _prefill_bf16(q, k, v, causal, d ** -0.5)
+    ref, _ = oracle.prefill(q, k, v, causal, d ** -0.5, n_threads=THREADS)
+    _check_bf16(got, ref, str(shape))
+
+
+@pytest.mark.parametrize("shape", inputs.sweep_shapes(), ids=lambda s: s.name)
+def test_bf16_sweep_mha_gqa_mqa(shape):
+    q, k, v = inputs.prefill_inputs_for(shape)
+    got = _prefill_bf16(q, k, v, shape.causal, shape.scale)
+    ref, _ = oracle.prefill(q, k, v, shape.causal, shape.scale, n_threads=THREADS)
+    _check_bf16(got, ref, shape.name)
+
+
+def _sampled_rows_check(shape):
+    q, k, v = inputs.prefill_inputs_for(shape)
+    got = _prefill_bf16(q, k, v, shape.causal, shape.scale)
+    assert np.isfinite(got).all(), "a tile was never written"
+    B, H_q, N = shape.B, shape.H_q, shape.N_q
+    # every row of two heads: the first and the last (b, h_q)
+    for bh in (0, B * H_q - 1):
+        ref, _ = oracle.prefill(q, k, v, shape.causal, shape.scale, heads=(bh, bh + 1),
+                                n_threads=THREADS)
+        b, h = divmod(bh, H_q)
+        _check_bf16(got[b, h], ref[b, h], f"{shape.name} head {bh}")
+    # 64 random rows of every head
+    rng = np.random.default_rng(shape.seed)
+    rows = [(b, h, int(i)) for b in range(B) for h in range(H_q)
+            for i in rng.choice(N, 64, replace=False)]
+    ref, _ = oracle.prefill_rows(q, k, v, shape.causal, shape.scale, rows)
+    sel = np.stack([got[b, h, i] for (b, h, i) in rows])
+    _check_bf16(sel, ref, f"{shape.name} sampled rows")
+
+
+def test_bf16_llama3_8b_layer_sampled():
+    _sampled_rows_check(inputs.LLAMA3_8B_LAYER)
+
+
+def test_bf16_long_sequence_sampled():
+    _sampled_rows_check(inputs.LONG_SEQ)
+
+
+def test_bf16_prefill_deterministic():
+    s = inputs.LLAMA3_8B_LAYER
+    q, k, v = _dev(*inputs.prefill_inputs_for(s))
+    o1 = ops.gqa_attn_fwd(q, k, v, causal=True, scale=s.scale)
+    o2 = ops.gqa_attn_fwd(q, k, v, causal=True, scale=s.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+def test_bf16_prefill_repeated_launches_rearm_scheduler():
+    """The work counter re-arms itself: many back-to-back launches stay correct."""
+    q, k, v = inputs.prefill_inputs(1, 4, 2, 300, 300, 64, torch.bfloat16, seed=61)
+    qd, kd, vd = _dev(q, k, v)
+    ref, _ = oracle.prefill(q, k, v, True, 0.125)
+    outs = [ops.gqa_attn_fwd(qd, kd, vd, causal=True, scale=0.125) for _ in range(20)]
+    torch.cuda.synchronize()
+    for o in outs:
+        _check_bf16(o.float().cpu().numpy(), ref, "repeat")
+
+
+# ------------------------------------------------------------------ bf16 decode
+
+def _decode_run(seqlens, q, kc, vc, scale, chunk=0):
+    qd, kd, vd, sd = _dev(q, kc, vc, seqlens)
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_decode(qd, kd, vd, sd, o, scale=scale, chunk_tokens=chunk)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", inputs.decode_shapes(), ids=lambda s: s.name)
+def test_bf16_decode_matches_oracle(shape):
+    seqlens, q, kc, vc = inputs.decode_inputs_for(shape)
+    got = _decode_run(seqlens, q, kc, vc, shape.scale)
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, _ = oracle.decode(q, kc, vc, seqlens, shape.scale)
+    _check_bf16(got, ref, shape.name)
+
+
+@pytest.mark.parametrize("chunk", [32, 64, 128, 256])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_decode_split_invariance(chunk, d):
+    """Every split size gives the same operation (microLLM-rocm Exp 282-284)."""
+    seqlens, q, kc, vc = inputs.decode_inputs(5, 8, 2, 700, d, torch.bfloat16, seed=71 + d,
+                                              seqlens=[1, 700, 255, 256, 513])
+    ref, _ = oracle.decode(q, kc, vc, seqlens, d ** -0.5)
+    got = _decode_run(seqlens, q, kc, vc, d ** -0.5, chunk)
+    _check_bf16(got, ref, f"chunk {chunk} d {d}")
+
+
+def test_bf16_decode_edge_lengths():
+    seqlens, q, kc, vc = inputs.decode_inputs(4, 16, 1, 512, 128, torch.bfloat16, seed=81,
+                                              seqlens=[0, 512, 1, 2])
+    got = _decode_run(seqlens, q, kc, vc, 0.1)
+    assert np.all(got[0] == 0), "an empty sequence must give O = 0"
+    ref, _ = oracle.decode(q, kc, vc, seqlens, 0.1)
+    _check_bf16(got, ref, "edge lengths")
+    assert ops.gqa_attn_get_device_error() == 0
+
+
+def test_bf16_decode_bad_seqlen_is_reported():
+    seqlens, q, kc, vc = inputs.decode_inputs(2, 4, 2, 64, 64, torch.bfloat16, seed=82,
+                                              seqlens=[10, 64])
+    bad = torch.tensor([10, 65], dtype=torch.int32)  # 65 > max_len
+    got = _decode_run(bad, q, kc, vc, 0.125)
+    assert ops.gqa_attn_get_device_error() == 6      # GQA_ERR_BAD_SEQLEN
+    assert ops.gqa_attn_get_device_error() == 0      # reading clears it
+    # the valid sequence is still right, the invalid one is zero
+    assert np.all(got[1] == 0)
+    ref, _ = oracle.decode(q[:1], kc[:1], vc[:1], seqlens[:1], 0.125)
+    _check_bf16(got[:1], ref, "valid sequence next to an invalid one")
+
+
+def test_decode_equals_last_row_of_causal_prefill():
+    """Decode at length L == last row of causal prefill with N_q = N_kv = L."""
+    L, d = 333, 128
+    q, k, v = inputs.prefill_inputs(1, 12, 2, L, L, d, torch.bfloat16, seed=91)
+    pre = _prefill_bf16(q, k, v, True, d ** -0.5)
+    seqlens = torch.tensor([L], dtype=torch.int32)
+    dec = _decode_run(seqlens, q[:, :, L - 1].contiguous(), k, v, d ** -0.5)
+    mx, _ = _err(dec[0], pre[0, :, L - 1].astype(np.float64))
+    assert mx <= 2 * BF16_MAX
+
+
+def test_bf16_decode_deterministic():
+    s = inputs.decode_shapes()[-1]
+    seqlens, q, kc, vc = inputs.decode_inputs_for(s)
+    a = _decode_run(seqlens, q, kc, vc, s.scale)
+    b = _decode_run(seqlens, q, kc, vc, s.scale)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ failure detection
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    assert ops.gqa_attn_selftest_wait_timeout(2000) == 4  # GQA_ERR_DEVICE_TIMEOUT
+    assert ops.gqa_attn_get_device_error() == 0           # the word was cleared
+    # the context is still usable
+    q, k, v = inputs.prefill_inputs(1, 2, 1, 128, 128, 64, torch.bfloat16, seed=99)
+    got = _prefill_bf16(q, k, v, False, 0.125)
+    ref, _ = oracle.prefill(q, k, v, False, 0.125)
+    _check_bf16(got, ref, "after timeout")
