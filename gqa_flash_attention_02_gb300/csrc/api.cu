@@ -54,8 +54,10 @@ int device_sms(int dev) {
 }
 
 // Returns the workspace of (current device, stream) with at least
-// `partials_bytes` of partials space; creates or grows it stream-ordered.
-int get_workspace(cudaStream_t stream, size_t partials_bytes, Workspace **out) {
+// `partials_bytes` of partials space and `counters` zeroed decode counters;
+// creates or grows it stream-ordered.
+int get_workspace(cudaStream_t stream, size_t partials_bytes, Workspace **out,
+                  size_t counters = 0) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -90,6 +92,25 @@ int get_workspace(cudaStream_t stream, size_t partials_bytes, Workspace **out) {
     }
     ws.partials = static_cast<float *>(p);
     ws.partials_bytes = want;
+  }
+  if (counters > ws.counters_len) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+      return GQA_ERR_OOM;
+    if (ws.counters) cudaFreeAsync(ws.counters, stream);
+    ws.counters = nullptr;
+    ws.counters_len = 0;
+    void *p = nullptr;
+    const size_t want = counters < 4096 ? 4096 : counters + counters / 4;
+    e = cudaMallocAsync(&p, want * sizeof(int), stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GQA_ERR_OOM;
+    }
+    e = cudaMemsetAsync(p, 0, want * sizeof(int), stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    ws.counters = static_cast<int *>(p);
+    ws.counters_len = want;
   }
   *out = &ws;
   return GQA_OK;
@@ -212,24 +233,23 @@ int gqa_attn_decode_chunked(const void *q, const void *k_cache, const void *v_ca
   int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
   if (rc != GQA_OK) return rc;
   if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
-  if (chunk_tokens != 0 && chunk_tokens != 32 && chunk_tokens != 64 && chunk_tokens != 128 &&
-      chunk_tokens != 256)
-    return chunk_tokens % 32 == 0 && chunk_tokens >= 32 && chunk_tokens <= 256
-               ? GQA_ERR_UNSUPPORTED
-               : GQA_ERR_INVALID_ARG;
+  if (chunk_tokens != 0 &&
+      (chunk_tokens < 0 || chunk_tokens % kDecodeChunkUnit != 0 || chunk_tokens > kDecodeChunkMax))
+    return GQA_ERR_INVALID_ARG;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   const int chunk = chunk_tokens ? chunk_tokens : decode_default_chunk(B, H_kv, max_len, device_sms(dev));
   Workspace *ws = nullptr;
-  rc = get_workspace(stream, decode_partials_bytes(B, H_q, max_len, d, chunk), &ws);
+  rc = get_workspace(stream, decode_partials_bytes(B, H_q, max_len, d, chunk), &ws,
+                     static_cast<size_t>(B) * H_kv);
   if (rc != GQA_OK) return rc;
   CUtensorMap tk, tv;
-  if (!encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, chunk) ||
-      !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, chunk))
+  if (!encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit) ||
+      !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit))
     return cuda_fail(cudaErrorInvalidValue);
-  e = launch_decode_bf16(tk, tv, q, seqlens, o, ws->partials, B, H_q, H_kv, max_len, d, scale,
-                         chunk, ws->ctl + kCtlErr, stream);
+  e = launch_decode_bf16(tk, tv, q, seqlens, o, ws->partials, ws->counters, B, H_q, H_kv, max_len,
+                         d, scale, chunk, ws->ctl + kCtlErr, stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 
@@ -280,12 +300,15 @@ int gqa_attn_get_device_error(cudaStream_t stream) {
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  int *ctl = nullptr;
+  int *ctl = nullptr, *counters = nullptr;
+  size_t counters_len = 0;
   {
     std::lock_guard<std::mutex> lk(g_ws_mutex);
     auto it = g_ws.find(WsKey{dev, stream});
     if (it == g_ws.end()) return GQA_OK;  // nothing ever ran on this stream
     ctl = it->second.ctl;
+    counters = it->second.counters;
+    counters_len = it->second.counters_len;
   }
   int word = 0;
   e = cudaMemcpyAsync(&word, ctl + kCtlErr, sizeof(int), cudaMemcpyDeviceToHost, stream);
@@ -293,6 +316,8 @@ int gqa_attn_get_device_error(cudaStream_t stream) {
   if (e == cudaSuccess && (word & kErrTimeout)) {
     // a pipeline that gave up may have left the work counter armed
     e = cudaMemsetAsync(ctl + kCtlWork, 0, 2 * sizeof(int), stream);
+    if (e == cudaSuccess && counters != nullptr)
+      e = cudaMemsetAsync(counters, 0, counters_len * sizeof(int), stream);
   }
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -337,6 +362,7 @@ void gqa_attn_shutdown(void) {
     cudaSetDevice(kv.first.dev);
     cudaDeviceSynchronize();
     if (kv.second.partials) cudaFree(kv.second.partials);
+    if (kv.second.counters) cudaFree(kv.second.counters);
     if (kv.second.ctl) cudaFree(kv.second.ctl);
   }
   g_ws.clear();

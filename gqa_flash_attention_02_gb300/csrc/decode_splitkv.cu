@@ -1,27 +1,32 @@
-// Single-token GQA decode against a bf16 K/V cache: split-KV partials and a
-// log-sum-exp combine.
+// Single-token GQA decode against a bf16 K/V cache: split-KV with the
+// log-sum-exp merge done in the same kernel.
 //
-// The decode step reads every valid cache row once and does ~2 FLOPs per
-// byte, so it is bound by HBM bandwidth (kaispace.site, prefill-vs-decode
-// note). The cache is cut into fixed-size chunks ("splits", the
-// split-sequence cached attention of the microLLM-rocm optimisation log,
-// Experiments 282-284) so that B * H_kv * splits CTAs fill all SMs even at
-// small batch; ragged lengths balance themselves because splits past
-// seqlens[b] exit at once.
+// The decode step reads every valid cache row once and does about 3 FLOPs
+// per byte at the workload's group size, so it is bound by HBM bandwidth
+// (kaispace.site, prefill-vs-decode note). The cache of each (b, h_kv) is cut
+// into fixed-size splits (the split-sequence cached attention of the
+// microLLM-rocm optimisation log, Experiments 282-284) so that B * H_kv *
+// splits CTAs cover all SMs even at small batch; ragged lengths balance
+// themselves because splits past seqlens[b] exit at once.
 //
-// One CTA = one (b, h_kv, split). It serves ALL g = H_q / H_kv query heads
-// of the group from one read of its K and V chunk (no K/V replication,
-// microLLM-rocm Experiment 044 / BootstrapAI collab-014 "Kernel 9 GQA"):
-//   1. TMA copies the K chunk and the V chunk (128-byte swizzled panels of
-//      64 columns) into shared memory; V streams in while K is scored.
-//   2. Thread r scores cache row r against the g query vectors (fp32 FMA,
-//      q pre-scaled by scale*log2(e) and broadcast from shared memory).
-//   3. Per head: block max, p = 2^(s - m), block sum.
-//   4. O_partial[h][c] = sum_r p[h][r] V[r][c], with each thread owning a
-//      column pair over a slice of rows, then a shared-memory reduction.
-//   5. (m, l, O_partial) go to the workspace; a second kernel merges the
-//      splits of each (b, h_q):  M = max m_i, L = sum 2^(m_i - M) l_i,
-//      O = sum 2^(m_i - M) O_i / L.
+// One CTA = one (b, h_kv, split), 4 warps. It serves ALL g = H_q / H_kv
+// query heads of the group from a single read of its K/V rows (no K/V
+// replication: microLLM-rocm Experiment 044, BootstrapAI collab-014
+// "Kernel 9 GQA"):
+//   * TMA streams 64-row K and V sub-blocks (128-byte swizzled 64-column
+//     panels) through a multi-stage shared-memory ring, so loads for later
+//     sub-blocks are in flight while earlier ones are consumed.
+//   * Warp w takes rows [16w, 16w+16) of each sub-block. The group's query
+//     heads (padded to 16) times those rows is a dense contraction over d:
+//     S = Q K^T and O += P V run on mma.sync (bf16 in, fp32 accumulate) from
+//     ldmatrix fragments, which keeps the kernel's instruction count far
+//     below its memory time. Softmax (online, exp2 with the scale folded
+//     in) runs on the fragments in registers.
+//   * The 4 warps' (m, l, O) states merge in shared memory. A sequence that
+//     fits in one split writes its output directly; otherwise each split
+//     writes (m, l, O) to the workspace and the LAST split to finish
+//     (atomic counter per (b, h_kv), no waiting) merges them:
+//         M = max m_i,  L = sum 2^(m_i - M) l_i,  O = sum 2^(m_i - M) O_i / L.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -33,302 +38,373 @@ namespace gqa {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kMaxGroup = 8;  // query heads scored per pass over the K chunk
+constexpr int kSub = 64;     // cache rows per sub-block (16 per warp)
+constexpr int kHeads = 16;   // query heads per pass (mma M)
 
-// Byte offset of element (row, col) of a [rows][D] bf16 chunk stored as
-// D/64 panels of rows x 128 B with the TMA 128-byte swizzle (16-byte unit
-// index XOR row % 8).
-template <int C>
-__device__ __forceinline__ uint32_t swz_offset(int row, int col) {
-  const int panel = col >> 6;
-  const int byte_in_line = (col & 63) * 2;
-  const int unit = byte_in_line >> 4;
-  return static_cast<uint32_t>(panel * C * 128 + row * 128 + ((unit ^ (row & 7)) << 4) +
-                               (byte_in_line & 15));
+// Byte offset of (row, 16-byte unit u) inside a [rows][D] bf16 tile stored
+// as D/64 panels of `rows` x 128 B with the TMA 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int row, int u, int rows) {
+  return static_cast<uint32_t>((u >> 3) * rows * 128 + row * 128 + (((u & 7) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                          uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
-template <int D, int C>
+// D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int D, int NSTG>
 struct DecodeSmem {
-  static constexpr int kChunkBytes = C * D * 2;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kChunkBytes;
-  static constexpr int kOffQ = 2 * kChunkBytes;                   // float [kMaxGroup][D]
-  static constexpr int kOffP = kOffQ + kMaxGroup * D * 4;         // float [C][kMaxGroup]
-  static constexpr int kOffRed = kOffP + C * kMaxGroup * 4;       // float [4][kMaxGroup]
-  static constexpr int kRS = kThreads / (D / 2);                  // row slices in PV
-  static constexpr int kOffO = kOffRed + 4 * kMaxGroup * 4;       // float [kRS][kMaxGroup][D]
-  static constexpr int kOffBar = kOffO + kRS * kMaxGroup * D * 4; // 2 mbarriers
-  static constexpr int kBytes = kOffBar + 16;
-  static constexpr int kAlloc = kBytes + 1024;                    // room to align to 1 KB
+  static constexpr int kTile = kSub * D * 2;            // one K or V sub-block
+  static constexpr int kStage = 2 * kTile;               // K then V
+  static constexpr int kOffStage = 0;
+  static constexpr int kRingBytes = NSTG * kStage;
+  // merge area (reuses the ring once the sweep is done)
+  static constexpr int kMergeO = 4 * kHeads * D * 4;     // float [4 warps][16][D]
+  static constexpr int kMergeML = 4 * kHeads * 2 * 4;    // float [4][16][2]
+  static constexpr int kRegion = kRingBytes > kMergeO + kMergeML ? kRingBytes : kMergeO + kMergeML;
+  static constexpr int kOffBar = kRegion;                // NSTG mbarriers
+  static constexpr int kOffFlag = kOffBar + NSTG * 8;    // int: "this CTA merges"
+  static constexpr int kBytes = kOffFlag + 16;
+  static constexpr int kAlloc = kBytes + 1024;
 };
 
-template <int D, int C>
-__global__ void __launch_bounds__(kThreads) decode_splitkv_kernel(
-    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const __nv_bfloat16 *__restrict__ q, const int *__restrict__ seqlens,
-    float *__restrict__ part_o, float *__restrict__ part_ml, int H_q, int H_kv, int max_len,
-    int n_splits, float scale_log2, int *err_word) {
-  using L = DecodeSmem<D, C>;
-  constexpr int RPT = (C + kThreads - 1) / kThreads;  // score rows per thread
+struct DecodeParams {
+  const __nv_bfloat16 *q;
+  const int *seqlens;
+  __nv_bfloat16 *o;
+  float *part;     // [B][H_q][splits][D + 2]: O (unnormalised), m, l
+  int *counters;   // [B][H_kv], zero between launches
+  int *err_word;
+  int H_q, H_kv, max_len, n_splits, chunk;
+  float scale_log2;
+};
+
+template <int D, int NSTG>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                          const __grid_constant__ CUtensorMap tm_v,
+                                                          const DecodeParams prm) {
+  using L = DecodeSmem<D, NSTG>;
+  constexpr int NT = D / 8;  // n-tiles of O per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t s_k = smem_addr(smem + L::kOffK);
-  const uint32_t s_v = smem_addr(smem + L::kOffV);
-  float *qf = reinterpret_cast<float *>(smem + L::kOffQ);
-  float *ps = reinterpret_cast<float *>(smem + L::kOffP);
-  float *red = reinterpret_cast<float *>(smem + L::kOffRed);
-  float *ored = reinterpret_cast<float *>(smem + L::kOffO);
-  const uint32_t bar_k = smem_addr(smem + L::kOffBar);
-  const uint32_t bar_v = bar_k + 8;
+  const uint32_t s_base = smem_addr(smem);
+  const uint32_t bars = s_base + L::kOffBar;
+  volatile int *merge_flag = reinterpret_cast<volatile int *>(smem + L::kOffFlag);
 
   const int split = blockIdx.x, h_kv = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int group = H_q / H_kv;
+  const int group = prm.H_q / prm.H_kv;
 
-  const int len = seqlens[b];
-  if (len < 0 || len > max_len) {
-    if (tid == 0 && split == 0 && h_kv == 0) record_error(err_word, kErrBadSeqlen);
+  const int len = prm.seqlens[b];
+  if (len < 0 || len > prm.max_len) {
+    if (tid == 0 && split == 0 && h_kv == 0) record_error(prm.err_word, kErrBadSeqlen);
+    if (split == 0) {  // the sequence's output is defined as 0
+      for (int i = tid; i < group * D; i += kThreads)
+        prm.o[(static_cast<size_t>(b) * prm.H_q + h_kv * group) * D + i] = __float2bfloat16_rn(0.f);
+    }
     return;
   }
-  const int s0 = split * C;
-  if (s0 >= len) return;
-  const int n = min(C, len - s0);
-  const int kv_plane = b * H_kv + h_kv;
+  const int n_split_b = (len + prm.chunk - 1) / prm.chunk;
+  if (len == 0) {
+    if (split == 0)
+      for (int i = tid; i < group * D; i += kThreads)
+        prm.o[(static_cast<size_t>(b) * prm.H_q + h_kv * group) * D + i] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  if (split >= n_split_b) return;
+  const int r0 = split * prm.chunk;
+  const int n = min(prm.chunk, len - r0);  // rows of this split
+  const int nsub = (n + kSub - 1) / kSub;
+  const int plane = b * prm.H_kv + h_kv;
 
   if (tid == 0) {
-    mbar_init(bar_k, 1);
-    mbar_init(bar_v, 1);
+    for (int s = 0; s < NSTG; ++s) mbar_init(bars + 8 * s, 1);
     fence_barrier_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_k, L::kChunkBytes);
+  auto issue = [&](int i) {  // TMA for sub-block i into stage i % NSTG (thread 0)
+    const int st = i % NSTG;
+    const uint32_t dst = s_base + L::kOffStage + st * L::kStage;
+    mbar_arrive_expect_tx(bars + 8 * st, L::kStage);
 #pragma unroll
-    for (int p = 0; p < D / 64; ++p) tma_load_3d(s_k + p * C * 128, &tm_k, bar_k, p * 64, s0, kv_plane);
-    mbar_arrive_expect_tx(bar_v, L::kChunkBytes);
-#pragma unroll
-    for (int p = 0; p < D / 64; ++p) tma_load_3d(s_v + p * C * 128, &tm_v, bar_v, p * 64, s0, kv_plane);
-  }
+    for (int p = 0; p < D / 64; ++p) {
+      tma_load_3d(dst + p * kSub * 128, &tm_k, bars + 8 * st, p * 64, r0 + i * kSub, plane);
+      tma_load_3d(dst + L::kTile + p * kSub * 128, &tm_v, bars + 8 * st, p * 64, r0 + i * kSub,
+                  plane);
+    }
+  };
+  if (tid == 0)
+    for (int i = 0; i < NSTG && i < nsub; ++i) issue(i);
 
-  bool ok = mbar_wait(bar_k, 0, nullptr);
-  ok = mbar_wait(bar_v, 0, nullptr) && ok;  // both copies have landed before any exit
-  if (!__syncthreads_and(ok)) {             // CTA-uniform exit on a timeout
-    if (tid == 0) record_error(err_word, kErrTimeout);
-    return;
-  }
-
-  for (int hg = 0; hg < group; hg += kMaxGroup) {
-    const int G = min(kMaxGroup, group - hg);
+  bool ok = true;
+  // Each pass serves up to 16 query heads of the group.
+  for (int hg = 0; hg < group && ok; hg += kHeads) {
+    const int G = min(kHeads, group - hg);
     const int hq0 = h_kv * group + hg;
-    __syncthreads();  // previous pass done with qf / ps / ored
-    for (int i = tid; i < kMaxGroup * D; i += kThreads) {
-      const int h = i / D, c = i % D;
-      qf[i] = (h < G) ? __bfloat162float(q[(static_cast<size_t>(b) * H_q + hq0 + h) * D + c]) *
-                            scale_log2
-                      : 0.f;
-    }
-    __syncthreads();
-
-    // ---- scores: thread owns rows tid, tid + 128, ...
-    float s[RPT][kMaxGroup];
-#pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) {
-      const int r = tid + rr * kThreads;
-#pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) s[rr][h] = 0.f;
-      if (r < n) {
-#pragma unroll 2
-        for (int c8 = 0; c8 < D / 8; ++c8) {
-          const uint4 raw = *reinterpret_cast<const uint4 *>(smem + L::kOffK +
-                                                               swz_offset<C>(r, c8 * 8));
-          float kf[8];
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            kf[2 * e] = __uint_as_float(w[e] << 16);
-            kf[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-          }
-#pragma unroll
-          for (int h = 0; h < kMaxGroup; ++h) {
-            if (h < G) {
-              const float4 qa = *reinterpret_cast<const float4 *>(qf + h * D + c8 * 8);
-              const float4 qb = *reinterpret_cast<const float4 *>(qf + h * D + c8 * 8 + 4);
-              float a = s[rr][h];
-              a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
-              a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
-              a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
-              a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
-              s[rr][h] = a;
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) s[rr][h] = -INFINITY;
-      }
-    }
-
-    // ---- per-head max over the chunk
-    float mh[kMaxGroup];
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
-      float x = s[0][h];
-#pragma unroll
-      for (int rr = 1; rr < RPT; ++rr) x = fmaxf(x, s[rr][h]);
-      x = warp_max(x);
-      if (lane == 0) red[warp * kMaxGroup + h] = x;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h)
-      mh[h] = fmaxf(fmaxf(red[h], red[kMaxGroup + h]), fmaxf(red[2 * kMaxGroup + h], red[3 * kMaxGroup + h]));
-    __syncthreads();  // red reused for the sums
-
-    // ---- p = 2^(s - m), per-head sums
-    float lsum[kMaxGroup];
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) lsum[h] = 0.f;
-#pragma unroll
-    for (int rr = 0; rr < RPT; ++rr) {
-      const int r = tid + rr * kThreads;
-      if (r < C) {
-        float pv[kMaxGroup];
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
-          pv[h] = (r < n && h < G) ? ex2(s[rr][h] - mh[h]) : 0.f;
-          lsum[h] += pv[h];
-        }
-        float4 *dst = reinterpret_cast<float4 *>(ps + r * kMaxGroup);
-        dst[0] = make_float4(pv[0], pv[1], pv[2], pv[3]);
-        dst[1] = make_float4(pv[4], pv[5], pv[6], pv[7]);
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < kMaxGroup; ++h) {
-      const float x = warp_sum(lsum[h]);
-      if (lane == 0) red[warp * kMaxGroup + h] = x;
-    }
-    __syncthreads();
-
-    // ---- O_partial = P V : thread owns a column pair over a slice of rows
+    // Q fragments (A operand, 16 heads x D): thread holds rows lane/4 and
+    // lane/4 + 8, columns 2*(lane%4) + {0,1} and + 8, for each 16-wide k-step.
+    uint32_t qa[D / 16][4];
     {
-      constexpr int CP = D / 2;        // column pairs
-      constexpr int RS = kThreads / CP;  // row slices
-      constexpr int RPS = (C + RS - 1) / RS;
-      const int cp = tid % CP, slice = tid / CP;
-      const int r_begin = slice * RPS;
-      const int r_end = min(n, r_begin + RPS);
-      float acc[kMaxGroup][2];
+      const int r_lo = lane >> 2, r_hi = r_lo + 8, c = 2 * (lane & 3);
+      const uint32_t *qlo = reinterpret_cast<const uint32_t *>(
+          prm.q + (static_cast<size_t>(b) * prm.H_q + hq0 + r_lo) * D);
+      const uint32_t *qhi = reinterpret_cast<const uint32_t *>(
+          prm.q + (static_cast<size_t>(b) * prm.H_q + hq0 + r_hi) * D);
 #pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) acc[h][0] = acc[h][1] = 0.f;
-      for (int r = r_begin; r < r_end; ++r) {
-        const uint32_t w =
-            *reinterpret_cast<const uint32_t *>(smem + L::kOffV + swz_offset<C>(r, 2 * cp));
-        const float v0 = __uint_as_float(w << 16), v1 = __uint_as_float(w & 0xffff0000u);
-        const float4 pa = *reinterpret_cast<const float4 *>(ps + r * kMaxGroup);
-        const float4 pb = *reinterpret_cast<const float4 *>(ps + r * kMaxGroup + 4);
-        const float pr[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qa[ks][0] = r_lo < G ? __ldg(qlo + (ks * 16 + c) / 2) : 0u;
+        qa[ks][1] = r_hi < G ? __ldg(qhi + (ks * 16 + c) / 2) : 0u;
+        qa[ks][2] = r_lo < G ? __ldg(qlo + (ks * 16 + c + 8) / 2) : 0u;
+        qa[ks][3] = r_hi < G ? __ldg(qhi + (ks * 16 + c + 8) / 2) : 0u;
+      }
+    }
+    float acc[NT][4];
 #pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
-          acc[h][0] = fmaf(pr[h], v0, acc[h][0]);
-          acc[h][1] = fmaf(pr[h], v1, acc[h][1]);
+    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+
+    for (int i = 0; i < nsub; ++i) {
+      const int st = i % NSTG;
+      // fills of this stage before this one: per pass the ring restarts at
+      // stage 0 and stage st is filled ceil((nsub - st) / NSTG) times
+      const int fills = (hg / kHeads) * ((nsub - st + NSTG - 1) / NSTG) + i / NSTG;
+      const uint32_t phase = static_cast<uint32_t>(fills & 1);
+      if (!__syncthreads_and(mbar_wait(bars + 8 * st, phase, nullptr))) { ok = false; break; }
+      const uint32_t kt = s_base + L::kOffStage + st * L::kStage;
+      const uint32_t vt = kt + L::kTile;
+      const int rows_here = min(kSub, n - i * kSub);  // valid rows in this sub-block
+      const int wrow = warp * 16;                     // this warp's first row
+      if (rows_here < kSub) {
+        // rows past the sequence (other sequences' data or NaN padding) must
+        // not reach P.V: zero this warp's invalid V rows
+        for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+          const int r = wrow + idx / (D / 8), u = idx % (D / 8);
+          if (r >= rows_here)
+            *reinterpret_cast<uint4 *>(smem + (vt - s_base) + swz(r, u, kSub)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      // ---- S = Q K^T for this warp's 16 rows (two n-tiles of 8 keys)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        // lanes 0-7: keys 0-7 unit 2ks; 8-15: keys 0-7 unit 2ks+1;
+        // 16-23: keys 8-15 unit 2ks; 24-31: keys 8-15 unit 2ks+1
+        const int key = wrow + (lane & 7) + ((lane >> 4) << 3);
+        const int uo = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kt + swz(key, 2 * ks + uo, kSub), b0, b1, b2, b3);
+          mma_bf16(s0, qa[ks], b0, b1);
+          mma_bf16(s1, qa[ks], b2, b3);
         }
       }
+      // ---- online softmax on the fragments: rows (heads) lane/4 and lane/4+8
+      const int kc = wrow + 2 * (lane & 3);  // key of s?[0]; s?[1] is kc+1; s1 adds 8
+      const float sl2 = prm.scale_log2;
+      float x[8] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2,
+                    s0[2] * sl2, s0[3] * sl2, s1[2] * sl2, s1[3] * sl2};
+      const int keys[4] = {kc, kc + 1, kc + 8, kc + 9};
 #pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h) {
-        float2 *dst = reinterpret_cast<float2 *>(ored + (slice * kMaxGroup + h) * D + 2 * cp);
-        *dst = make_float2(acc[h][0], acc[h][1]);
+      for (int e = 0; e < 4; ++e) {
+        if (keys[e] >= rows_here) { x[e] = -INFINITY; x[4 + e] = -INFINITY; }
+      }
+      float mx_lo = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+      float mx_hi = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      // a warp whose 16 rows are all past the sequence sees mn = -inf: skip
+      const float a_lo = (mn_lo == -INFINITY) ? 1.f : ex2(m_lo - mn_lo);
+      const float a_hi = (mn_hi == -INFINITY) ? 1.f : ex2(m_hi - mn_hi);
+      float p[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        p[e] = (mn_lo == -INFINITY) ? 0.f : ex2(x[e] - mn_lo);
+        p[4 + e] = (mn_hi == -INFINITY) ? 0.f : ex2(x[4 + e] - mn_hi);
+      }
+      l_lo = l_lo * a_lo + ((p[0] + p[1]) + (p[2] + p[3]));
+      l_hi = l_hi * a_hi + ((p[4] + p[5]) + (p[6] + p[7]));
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        acc[t][0] *= a_lo; acc[t][1] *= a_lo;
+        acc[t][2] *= a_hi; acc[t][3] *= a_hi;
+      }
+      // P as the A operand (16 heads x 16 keys): keys 0-7 from n-tile 0, 8-15 from n-tile 1
+      const uint32_t pa[4] = {pack_bf16x2(p[0], p[1]), pack_bf16x2(p[4], p[5]),
+                              pack_bf16x2(p[2], p[3]), pack_bf16x2(p[6], p[7])};
+      // ---- O += P V (V rows = k, d = n): transposed ldmatrix of 8x8 blocks
+      {
+        // lanes 0-7: keys 0-7 unit u; 8-15: keys 8-15 unit u; 16-23: keys 0-7 unit u+1;
+        // 24-31: keys 8-15 unit u+1  -> {b0,b1} for d-tile u and {b0,b1} for u+1
+        const int key = wrow + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int uo = lane >> 4;
+#pragma unroll
+        for (int u = 0; u < NT; u += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vt + swz(key, u + uo, kSub), b0, b1, b2, b3);
+          mma_bf16(acc[u], pa, b0, b1);
+          mma_bf16(acc[u + 1], pa, b2, b3);
+        }
+      }
+      // all warps are done with this stage: refill it with sub-block i + NSTG
+      __syncthreads();
+      if (tid == 0 && i + NSTG < nsub) {
+        fence_proxy_async_smem();  // generic-proxy writes (V zeroing) before the TMA overwrite
+        issue(i + NSTG);
+      }
+    }
+    if (!ok) break;
+
+    // ---- merge the 4 warps' states in shared memory (the ring is idle now)
+    float *mo = reinterpret_cast<float *>(smem);                    // [4][16][D]
+    float *mml = reinterpret_cast<float *>(smem + L::kMergeO);      // [4][16][2]
+    {
+      const int r_lo = lane >> 2, r_hi = r_lo + 8;
+      // quad-reduce l across the 4 threads sharing a row
+      float ll = l_lo, lh = l_hi;
+      ll += __shfl_xor_sync(0xffffffffu, ll, 1);
+      ll += __shfl_xor_sync(0xffffffffu, ll, 2);
+      lh += __shfl_xor_sync(0xffffffffu, lh, 1);
+      lh += __shfl_xor_sync(0xffffffffu, lh, 2);
+      if ((lane & 3) == 0) {
+        mml[(warp * 16 + r_lo) * 2 + 0] = m_lo;
+        mml[(warp * 16 + r_lo) * 2 + 1] = ll;
+        mml[(warp * 16 + r_hi) * 2 + 0] = m_hi;
+        mml[(warp * 16 + r_hi) * 2 + 1] = lh;
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int col = t * 8 + 2 * (lane & 3);
+        *reinterpret_cast<float2 *>(mo + (warp * 16 + r_lo) * D + col) = make_float2(acc[t][0], acc[t][1]);
+        *reinterpret_cast<float2 *>(mo + (warp * 16 + r_hi) * D + col) = make_float2(acc[t][2], acc[t][3]);
       }
     }
     __syncthreads();
-
-    // ---- write (m, l, O_partial) for each head of this pass
-    for (int i = tid; i < G * D; i += kThreads) {
-      const int h = i / D, c = i % D;
-      float x = 0.f;
+    const bool single = (n_split_b == 1);
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      const int h = idx / D, c = idx % D;
+      float M = -INFINITY;
 #pragma unroll
-      for (int sl = 0; sl < L::kRS; ++sl) x += ored[(sl * kMaxGroup + h) * D + c];
-      const size_t slot = (static_cast<size_t>(b) * H_q + hq0 + h) * n_splits + split;
-      part_o[slot * D + c] = x;
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, mml[(w * 16 + h) * 2]);
+      float Lsum = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = mml[(w * 16 + h) * 2];
+        const float wgt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+        Lsum = fmaf(wgt, mml[(w * 16 + h) * 2 + 1], Lsum);
+        O = fmaf(wgt, mo[(w * 16 + h) * D + c], O);
+      }
+      const size_t row = static_cast<size_t>(b) * prm.H_q + hq0 + h;
+      if (single) {
+        prm.o[row * D + c] = __float2bfloat16_rn(O / Lsum);
+      } else {
+        float *dst = prm.part + (row * prm.n_splits + split) * (D + 2);
+        dst[c] = O;
+        if (c == 0) {
+          dst[D] = M;
+          dst[D + 1] = Lsum;
+        }
+      }
     }
-    if (tid < G) {
-      const int h = tid;
-      const size_t slot = (static_cast<size_t>(b) * H_q + hq0 + h) * n_splits + split;
-      const float l = red[h] + red[kMaxGroup + h] + red[2 * kMaxGroup + h] + red[3 * kMaxGroup + h];
-      part_ml[slot * 2 + 0] = mh[h];
-      part_ml[slot * 2 + 1] = l;
+    __syncthreads();  // merge area free again (next pass reloads the ring)
+    if (hg + kHeads < group) {
+      // another pass over the same rows: restart the ring
+      if (tid == 0)
+        for (int i = 0; i < NSTG && i < nsub; ++i) issue(i);
     }
   }
-}
-
-// One CTA of D threads per (b, h_q): merges the splits that saw keys.
-template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(
-    const float *__restrict__ part_o, const float *__restrict__ part_ml,
-    const int *__restrict__ seqlens, __nv_bfloat16 *__restrict__ o, int H_q, int max_len,
-    int n_splits, int chunk) {
-  const int bh = blockIdx.x;
-  const int b = bh / H_q;
-  const int c = threadIdx.x;
-  const int len = seqlens[b];
-  __nv_bfloat16 *dst = o + static_cast<size_t>(bh) * D + c;
-  if (len <= 0 || len > max_len) {  // empty or invalid sequence: O = 0
-    *dst = __float2bfloat16_rn(0.f);
+  if (!ok) {
+    if (tid == 0) record_error(prm.err_word, kErrTimeout);
     return;
   }
-  const int ns = (len + chunk - 1) / chunk;
-  const float *ml = part_ml + static_cast<size_t>(bh) * n_splits * 2;
-  const float *po = part_o + static_cast<size_t>(bh) * n_splits * D;
-  float M = -INFINITY;
-  for (int i = 0; i < ns; ++i) M = fmaxf(M, ml[2 * i]);
-  float acc = 0.f, Lsum = 0.f;
-  for (int i = 0; i < ns; ++i) {
-    const float w = ex2(ml[2 * i] - M);
-    Lsum = fmaf(w, ml[2 * i + 1], Lsum);
-    acc = fmaf(w, po[static_cast<size_t>(i) * D + c], acc);
+  if (n_split_b == 1) return;
+
+  // ---- the last split of (b, h_kv) to finish merges all of them
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    int *ctr = prm.counters + plane;
+    const int prev = atomicAdd(ctr, 1);
+    const bool last = (prev == n_split_b - 1);
+    if (last) atomicExch(ctr, 0);  // re-arm for the next launch
+    *merge_flag = last ? 1 : 0;
   }
-  *dst = __float2bfloat16_rn(acc / Lsum);
+  __syncthreads();
+  if (!*merge_flag) return;
+  __threadfence();
+  for (int idx = tid; idx < group * D; idx += kThreads) {
+    const int h = idx / D, c = idx % D;
+    const size_t row = static_cast<size_t>(b) * prm.H_q + h_kv * group + h;
+    const float *src = prm.part + row * prm.n_splits * (D + 2);
+    float M = -INFINITY;
+    for (int sp = 0; sp < n_split_b; ++sp) M = fmaxf(M, __ldcg(src + sp * (D + 2) + D));
+    float Lsum = 0.f, O = 0.f;
+    for (int sp = 0; sp < n_split_b; ++sp) {
+      const float *pp = src + sp * (D + 2);
+      const float wgt = ex2(__ldcg(pp + D) - M);
+      Lsum = fmaf(wgt, __ldcg(pp + D + 1), Lsum);
+      O = fmaf(wgt, __ldcg(pp + c), O);
+    }
+    prm.o[row * D + c] = __float2bfloat16_rn(O / Lsum);
+  }
 }
 
-template <int D, int C>
-cudaError_t launch_decode_dc(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
-                             const int *seqlens, void *o, float *partials, int B, int H_q,
-                             int H_kv, int max_len, float scale, int *err_word,
-                             cudaStream_t stream) {
-  using L = DecodeSmem<D, C>;
-  static bool configured = false;  // attribute is per device; harmless to repeat
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_splitkv_kernel<D, C>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  const int n_splits = (max_len + C - 1) / C;
-  float *part_o = partials;
-  float *part_ml = partials + static_cast<size_t>(B) * H_q * n_splits * D;
-  const float scale_log2 = scale * 1.4426950408889634f;
-  dim3 grid(n_splits, H_kv, B);
-  decode_splitkv_kernel<D, C><<<grid, kThreads, L::kAlloc, stream>>>(
-      tm_k, tm_v, static_cast<const __nv_bfloat16 *>(q), seqlens, part_o, part_ml, H_q, H_kv,
-      max_len, n_splits, scale_log2, err_word);
-  cudaError_t e = cudaGetLastError();
+template <int D, int NSTG>
+cudaError_t launch_decode_d(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
+                            const int *seqlens, void *o, float *partials, int *counters, int B,
+                            int H_q, int H_kv, int max_len, float scale, int chunk, int *err_word,
+                            cudaStream_t stream) {
+  using L = DecodeSmem<D, NSTG>;
+  static unsigned configured = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<B * H_q, D, 0, stream>>>(part_o, part_ml, seqlens,
-                                                      static_cast<__nv_bfloat16 *>(o), H_q,
-                                                      max_len, n_splits, C);
+  if (dev >= 32 || !(configured & (1u << dev))) {
+    e = cudaFuncSetAttribute(decode_kernel<D, NSTG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kAlloc);
+    if (e != cudaSuccess) return e;
+    if (dev < 32) configured |= 1u << dev;
+  }
+  DecodeParams prm;
+  prm.q = static_cast<const __nv_bfloat16 *>(q);
+  prm.seqlens = seqlens;
+  prm.o = static_cast<__nv_bfloat16 *>(o);
+  prm.part = partials;
+  prm.counters = counters;
+  prm.err_word = err_word;
+  prm.H_q = H_q;
+  prm.H_kv = H_kv;
+  prm.max_len = max_len;
+  prm.chunk = chunk;
+  prm.n_splits = (max_len + chunk - 1) / chunk;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  dim3 grid(prm.n_splits, H_kv, B);
+  decode_kernel<D, NSTG><<<grid, kThreads, L::kAlloc, stream>>>(tm_k, tm_v, prm);
   return cudaGetLastError();
 }
 
@@ -340,32 +416,26 @@ size_t decode_partials_bytes(int B, int H_q, int max_len, int d, int chunk) {
 }
 
 int decode_default_chunk(int B, int H_kv, int max_len, int num_sms) {
-  // Prefer long chunks (fewer partials to merge) as long as the grid still
-  // offers about two CTAs per SM.
-  for (int c : {128, 64}) {
+  // Longest split (fewest partials to merge) that still offers about four
+  // CTAs per SM when every sequence is full length.
+  for (int c : {512, 256, 128}) {
     const long ctas = static_cast<long>(B) * H_kv * ((max_len + c - 1) / c);
-    if (ctas >= 2L * num_sms) return c;
+    if (ctas >= 4L * num_sms) return c;
   }
-  return 32;
+  return 64;
 }
 
 cudaError_t launch_decode_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
-                               const int *seqlens, void *o, float *partials, int B, int H_q,
-                               int H_kv, int max_len, int d, float scale, int chunk,
+                               const int *seqlens, void *o, float *partials, int *counters, int B,
+                               int H_q, int H_kv, int max_len, int d, float scale, int chunk,
                                int *err_word, cudaStream_t stream) {
-#define GQA_DECODE_CASE(DD, CC)                                                              \
-  if (d == DD && chunk == CC)                                                                \
-    return launch_decode_dc<DD, CC>(tm_k, tm_v, q, seqlens, o, partials, B, H_q, H_kv,      \
-                                    max_len, scale, err_word, stream);
-  GQA_DECODE_CASE(64, 32)
-  GQA_DECODE_CASE(64, 64)
-  GQA_DECODE_CASE(64, 128)
-  GQA_DECODE_CASE(64, 256)
-  GQA_DECODE_CASE(128, 32)
-  GQA_DECODE_CASE(128, 64)
-  GQA_DECODE_CASE(128, 128)
-  GQA_DECODE_CASE(128, 256)
-#undef GQA_DECODE_CASE
+  if (chunk % kSub != 0 || chunk <= 0) return cudaErrorInvalidValue;
+  if (d == 64)
+    return launch_decode_d<64, 4>(tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q, H_kv,
+                                  max_len, scale, chunk, err_word, stream);
+  if (d == 128)
+    return launch_decode_d<128, 3>(tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q, H_kv,
+                                   max_len, scale, chunk, err_word, stream);
   return cudaErrorInvalidValue;
 }
 

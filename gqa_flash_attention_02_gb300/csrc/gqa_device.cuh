@@ -74,6 +74,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `hint_ns`
+// while the phase is incomplete, so waiting warps do not compete for issue
+// slots with the warps doing work on the same SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete. Returns false if
 // `abort_flag` (shared memory, set by another role that gave up) becomes
 // non-zero or the wait outlives `limit_ns`; the caller then records the
@@ -84,12 +100,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;  // sleep up to 1 ms
     if (abort_flag != nullptr && *abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// mbar_wait executed by a whole warp, with a warp-uniform result: the lanes
+// reconverge here and either all proceed or all take the failure path, so a
+// warp-collective instruction (elect.sync, tcgen05.ld/st) after it is safe
+// even when a wait gives up.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               const volatile int *abort_flag,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -161,6 +186,39 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Same MMAs with each 64-bit smem descriptor passed as two 32-bit words.
+// Only the low word (start address) changes between the K-steps of one
+// operand, so issuing an MMA costs one integer add per operand; a lean
+// issue loop matters because one thread issues every MMA of the CTA.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                         uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                         uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Low / high 32-bit words of sdesc_sw128 (same bit fields).
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
@@ -250,6 +308,19 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef GQA_R8
 #undef GQA_W8
 
+// ---------------------------------------------------------------- registers
+
+// Warpgroup-wide register re-allocation (all 4 warps of a warpgroup execute
+// the same instruction). N is a multiple of 8 in [24, 256].
+template <int N>
+__device__ __forceinline__ void regs_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- math
 
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero).
@@ -257,6 +328,80 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---- packed fp32 pairs (sm_100+ f32x2 instructions: one issue, two lanes)
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// a + b rounded toward -infinity.
+__device__ __forceinline__ float2 fadd2_rm(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rm.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// max of three (sm_100+ three-input max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Software 2^x for a pair, on the FMA pipe instead of the special-function
+// unit. Cody-Waite range reduction (Cody & Waite, "Software Manual for the
+// Elementary Functions", 1980): 2^x = 2^j * 2^f, j = floor(x), f in [0,1);
+// 2^f by a cubic with p(0) = 1, p(1) = 2 whose two free coefficients were
+// fitted for minimum maximum relative error (fit_exp2_poly.py beside this
+// file: 1.03e-4). j is obtained by adding 1.5 * 2^23 with rounding toward
+// -infinity (the sum's low mantissa bits then hold j) and is moved into the
+// exponent field with one shift-add. Inputs are clamped to >= -127; there
+// the result is below 2^-126, i.e. a negligible softmax weight.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  constexpr float kC1 = 0.69542414f, kC2 = 0.2263078f, kC3 = 0.07826809f;
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -127.0f);
+  x.y = fmaxf(x.y, -127.0f);
+  const float2 t = fadd2_rm(x, make_float2(kShift, kShift));
+  const float2 f = fsub2(x, fsub2(t, make_float2(kShift, kShift)));
+  float2 p = ffma2(f, make_float2(kC3, kC3), make_float2(kC2, kC2));
+  p = ffma2(p, f, make_float2(kC1, kC1));
+  p = ffma2(p, f, make_float2(1.0f, 1.0f));
+  // bits(t) << 23 == j << 23 (mod 2^32): the shift's high bits fall off
+  return make_float2(__uint_as_float((__float_as_uint(t.x) << 23) + __float_as_uint(p.x)),
+                     __uint_as_float((__float_as_uint(t.y) << 23) + __float_as_uint(p.y)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

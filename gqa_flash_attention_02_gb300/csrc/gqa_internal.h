@@ -113,6 +113,8 @@ struct Workspace {
   int *ctl = nullptr;        // kCtlInts ints, zeroed at creation
   float *partials = nullptr; // split-KV decode partials
   size_t partials_bytes = 0;
+  int *counters = nullptr;   // split-KV decode: splits finished per (b, h_kv); re-armed by the kernel
+  size_t counters_len = 0;
 };
 
 // Launchers (return a cudaError_t; arguments already validated).
@@ -125,12 +127,14 @@ cudaError_t launch_attn_f32(const float *q, const float *k, const float *v, floa
                             const int *seqlens, int kv_row_capacity, int *err_word,
                             cudaStream_t stream);
 
-// Decode split-KV: `chunk` cache rows per split.
+// Decode split-KV: `chunk` cache rows per split (the TMA box is 64 rows).
 size_t decode_partials_bytes(int B, int H_q, int max_len, int d, int chunk);
 int decode_default_chunk(int B, int H_kv, int max_len, int num_sms);
+constexpr int kDecodeChunkUnit = 64;   // split sizes are multiples of this
+constexpr int kDecodeChunkMax = 2048;
 cudaError_t launch_decode_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
-                               const int *seqlens, void *o, float *partials, int B, int H_q,
-                               int H_kv, int max_len, int d, float scale, int chunk,
+                               const int *seqlens, void *o, float *partials, int *counters, int B,
+                               int H_q, int H_kv, int max_len, int d, float scale, int chunk,
                                int *err_word, cudaStream_t stream);
 
 cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStream_t stream);

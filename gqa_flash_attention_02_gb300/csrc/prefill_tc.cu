@@ -16,6 +16,8 @@
 //       warps 4-7  softmax + epilogue for query tile 1
 //       warp  8    TMA producer: Q tiles and a ring of K/V blocks
 //       warp  9    tcgen05 MMA issuer (and tensor-memory owner)
+//       warps 10-11 idle (they complete the third warpgroup, which gives
+//                   its registers to the two softmax warpgroups)
 //   * Tensor memory (512 columns): S_t = Q_t K^T in columns [128t, 128t+128)
 //     as fp32; P_t (bf16, packed in pairs) overwrites the upper half of S_t;
 //     O_t accumulates in columns [256 + t*D, 256 + (t+1)*D).
@@ -40,17 +42,39 @@ namespace gqa {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // three warpgroups
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split (per thread). The block is launched with kLaunchRegs per
+// thread (65536 / 384 rounded down to a multiple of 8); setmaxnreg can only
+// move registers WITHIN that launch allocation, so the three warpgroups'
+// shares must sum to at most 3 * kLaunchRegs, or setmaxnreg.inc waits
+// forever. The producer/MMA warpgroup gives registers back so each softmax
+// thread can keep a full 128-column row of S in registers.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsLow = 104;
+constexpr int kRegsHigh = 200;
+static_assert(kRegsLow + 2 * kRegsHigh <= 3 * kLaunchRegs,
+              "register split exceeds the launch allocation: setmaxnreg.inc would never return");
+static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsLow >= 24 && kRegsHigh <= 256,
+              "setmaxnreg counts must be multiples of 8 in [24, 256]");
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows > 2^8
+#ifndef GQA_EMU_PAIRS
+#define GQA_EMU_PAIRS 0
+#endif
+// Of every 8 column pairs of a row, this many take the FMA-pipe 2^x and the
+// rest the special-function unit. On GB300 ex2 issues at 32 lanes/clock per
+// SM, so the softmax warp is bound by instruction issue rather than by the
+// special-function unit; the polynomial (about six issue slots per pair
+// instead of two) then only adds work, and the default is 0.
+constexpr int kEmuPairs = GQA_EMU_PAIRS;
 
 template <int D>
 struct TcLayout {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
   static constexpr int kPanelBytes = 128 * 128;   // 128 rows x 64 columns
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kStages = (D == 128) ? 5 : 8;  // K or V tiles in the ring
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
@@ -130,153 +154,207 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     record_error(err_word, kErrTimeout);
   };
 
+  if (warp >= 8) {
+  regs_dealloc<kRegsLow>();
+  // Both roles below run warp-uniform control flow on all 32 lanes (so the
+  // descriptor and index arithmetic lives in the uniform datapath); only the
+  // TMA / tcgen05 instructions themselves are issued by one elected lane.
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int it = 0, kv_it = 0, vc[2] = {0, 0};
-      while (true) {
-        const int u = atomicAdd(prm.ctl + kCtlWork, 1);
-        const int slot = it & 1;
-        if (!mbar_wait(bar(L::kSchedEmpty + slot), ((it >> 1) & 1) ^ 1, abort_flag)) { fail(); break; }
+    int it = 0, kv_it = 0, vc0 = 0, vc1 = 0;
+    bool ok = true;
+    while (ok) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(prm.ctl + kCtlWork, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      const int slot = it & 1;
+      if (!mbar_wait_warp(bar(L::kSchedEmpty + slot), ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+      __syncwarp();
+      if (lane == 0) {
         sched[slot] = u;
         mbar_arrive(bar(L::kSchedFull + slot));
-        ++it;
-        if (u >= plan.total_units) break;
-        const Unit w = decode_unit(plan, u);
-        const int nb = max(w.t[0].kv_blocks, w.t[1].kv_blocks);
-        bool ok = true;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (w.t[t].kv_blocks == 0) continue;
-          if (!mbar_wait(bar(L::kQEmpty + t), (vc[t] & 1) ^ 1, abort_flag)) { ok = false; break; }
-          ++vc[t];
+      }
+      ++it;
+      if (u >= plan.total_units) break;
+      const Unit w = decode_unit(plan, u);
+      const int nb = max(w.t[0].kv_blocks, w.t[1].kv_blocks);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const UnitTile tt = t ? w.t[1] : w.t[0];
+        int &vc = t ? vc1 : vc0;
+        if (!ok || tt.kv_blocks == 0) continue;
+        if (!mbar_wait_warp(bar(L::kQEmpty + t), (vc & 1) ^ 1, abort_flag)) { ok = false; continue; }
+        ++vc;
+        __syncwarp();
+        if (elect_one()) {
           const uint32_t dst = s_base + L::kOffQ + t * L::kTileBytes;
           mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
 #pragma unroll
           for (int p = 0; p < D / 64; ++p)
             tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64,
-                        w.t[t].q_tile * kTileM, w.b * plan.H_q + w.t[t].h_q);
+                        tt.q_tile * kTileM, w.b * plan.H_q + tt.h_q);
         }
-        const int kv_plane = w.b * plan.H_kv + w.h_kv;
-        for (int j = 0; j < nb && ok; ++j) {
-          for (int kind = 0; kind < 2; ++kind) {  // K_j then V_j
-            const int st = kv_it % L::kStages;
-            const uint32_t ph = (kv_it / L::kStages) & 1;
-            if (!mbar_wait(bar(L::kKVEmpty + st), ph ^ 1, abort_flag)) { ok = false; break; }
+        __syncwarp();
+      }
+      const int kv_plane = w.b * plan.H_kv + w.h_kv;
+      for (int j = 0; j < nb && ok; ++j) {
+#pragma unroll
+        for (int kind = 0; kind < 2; ++kind) {  // K_j then V_j
+          if (!ok) continue;
+          const int st = kv_it % L::kStages;
+          const uint32_t ph = (kv_it / L::kStages) & 1;
+          if (!mbar_wait_warp(bar(L::kKVEmpty + st), ph ^ 1, abort_flag)) { ok = false; continue; }
+          __syncwarp();
+          if (elect_one()) {
             const uint32_t dst = s_base + L::kOffKV + st * L::kTileBytes;
             mbar_arrive_expect_tx(bar(L::kKVFull + st), L::kTileBytes);
 #pragma unroll
             for (int p = 0; p < D / 64; ++p)
               tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
                           p * 64, j * kTileN, kv_plane);
-            ++kv_it;
           }
+          __syncwarp();
+          ++kv_it;
         }
-        if (!ok) { fail(); break; }
       }
     }
+    if (!ok && lane == 0) fail();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-      int it = 0, kv_it = 0, vc[2] = {0, 0};
-      uint32_t pcnt[2] = {0, 0};
-      bool ok = true;
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+    // Descriptor words: the high word (stride 1024 B, version, 128-byte
+    // swizzle) is shared by every operand; low words are base + constant.
+    constexpr uint32_t kDescHi = sdesc_hi_sw128(1024);
+    const uint32_t q_lo0 = sdesc_lo(s_base + L::kOffQ, 16);
+    const uint32_t kv_lo0 = sdesc_lo(s_base + L::kOffKV, 16);
+    const uint32_t v_lo0 = sdesc_lo(s_base + L::kOffKV, L::kPanelBytes);
+    int it = 0, kv_it = 0, vc0 = 0, vc1 = 0;
+    uint32_t pc0 = 0, pc1 = 0;
+    bool ok = true;
 
-      auto issue_qk = [&](int t, int st) {
-        const uint32_t qa = s_base + L::kOffQ + t * L::kTileBytes;
-        const uint32_t kb = s_base + L::kOffKV + st * L::kTileBytes;
+    auto issue_qk = [&](int t, int st) {
+      const uint32_t a_lo = q_lo0 + static_cast<uint32_t>(t * L::kTileBytes >> 4);
+      const uint32_t b_lo = kv_lo0 + static_cast<uint32_t>(st * L::kTileBytes >> 4);
+      const uint32_t d = tmem + 128u * t;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-          mma_ss(tmem + 128u * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 idesc_qk, kk > 0 ? 1u : 0u);
+          // K-step kk: panel kk/4 (64 columns each), 32 bytes per step inside it
+          const uint32_t off = static_cast<uint32_t>(((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4);
+          mma_ss_w(d, a_lo + off, kDescHi, b_lo + off, kDescHi, idesc_qk, kk > 0 ? 1u : 0u);
         }
-      };
-      auto issue_pv = [&](int t, int st, bool accumulate) {
-        const uint32_t vb = s_base + L::kOffKV + st * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts(tmem + 256u + D * t, tmem + 128u * t + 64u + kk * 8, sdesc_sw128(vb + kk * 2048, L::kPanelBytes, 1024),
-                 idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-      };
-      auto wait_kv = [&](int &st) -> bool {
-        st = kv_it % L::kStages;
-        const uint32_t ph = (kv_it / L::kStages) & 1;
-        ++kv_it;
-        return mbar_wait(bar(L::kKVFull + st), ph, abort_flag);
-      };
-      // PV for tile t over block jb (all checks on the caller's side).
-      auto do_pv = [&](int t, int jb, int st) -> bool {
-        if (jb == 0 && !mbar_wait(bar(L::kOEmpty + t), (vc[t] & 1) ^ 1, abort_flag)) return false;
-        if (!mbar_wait(bar(L::kPFull + t), pcnt[t] & 1, abort_flag)) return false;
-        ++pcnt[t];
-        tc_fence_after_sync();
-        issue_pv(t, st, jb > 0);
-        return true;
-      };
-
-      while (ok) {
-        const int slot = it & 1;
-        if (!mbar_wait(bar(L::kSchedFull + slot), (it >> 1) & 1, abort_flag)) { ok = false; break; }
-        const int u = sched[slot];
-        mbar_arrive(bar(L::kSchedEmpty + slot));
-        ++it;
-        if (u >= plan.total_units) break;
-        const Unit w = decode_unit(plan, u);
-        const int nbt[2] = {w.t[0].kv_blocks, w.t[1].kv_blocks};
-        const int nb = max(nbt[0], nbt[1]);
-        for (int t = 0; t < 2 && ok; ++t)
-          if (nbt[t] > 0 && !mbar_wait(bar(L::kQFull + t), vc[t] & 1, abort_flag)) ok = false;
-        if (!ok) break;
-        // block 0: S_t = Q_t K_0^T
-        int st_k, st_v;
-        if (!wait_kv(st_k)) { ok = false; break; }
-        tc_fence_after_sync();
-        for (int t = 0; t < 2; ++t) {
-          if (nbt[t] == 0) continue;
-          issue_qk(t, st_k);
-          tc_commit(bar(L::kSFull + t));
-          if (nbt[t] == 1) tc_commit(bar(L::kQEmpty + t));
-        }
-        // blocks 1..nb-1: O_t += P_t V_{j-1}, then S_t = Q_t K_j^T
-        for (int j = 1; j < nb && ok; ++j) {
-          tc_commit(bar(L::kKVEmpty + st_k));  // K_{j-1} no longer read after this point
-          if (!wait_kv(st_v) || !wait_kv(st_k)) { ok = false; break; }
-          tc_fence_after_sync();
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j - 1 < nbt[t]) {
-              if (!do_pv(t, j - 1, st_v)) { ok = false; break; }
-              if (j - 1 == nbt[t] - 1) tc_commit(bar(L::kOFull + t));
-            }
-            if (j < nbt[t]) {
-              issue_qk(t, st_k);
-              tc_commit(bar(L::kSFull + t));
-              if (j == nbt[t] - 1) tc_commit(bar(L::kQEmpty + t));
-            }
-          }
-          tc_commit(bar(L::kKVEmpty + st_v));
-        }
-        if (!ok) break;
-        // last block: O_t += P_t V_{nb-1}
-        tc_commit(bar(L::kKVEmpty + st_k));
-        if (!wait_kv(st_v)) { ok = false; break; }
-        tc_fence_after_sync();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (nbt[t] != nb) continue;
-          if (!do_pv(t, nb - 1, st_v)) { ok = false; break; }
-          tc_commit(bar(L::kOFull + t));
-        }
-        tc_commit(bar(L::kKVEmpty + st_v));
-        for (int t = 0; t < 2; ++t)
-          if (nbt[t] > 0) ++vc[t];
       }
-      if (!ok) fail();
-      // Drain: every tcgen05 operation issued above has completed.
-      tc_commit(bar(L::kDrain));
-      mbar_wait(bar(L::kDrain), 0, nullptr);
+      __syncwarp();
+    };
+    auto issue_pv = [&](int t, int st, bool accumulate) {
+      const uint32_t b_lo = v_lo0 + static_cast<uint32_t>(st * L::kTileBytes >> 4);
+      const uint32_t d = tmem + 256u + D * t;
+      const uint32_t a = tmem + 128u * t + 64u;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)  // 16 key rows (2048 B) per K-step
+          mma_ts_w(d, a + kk * 8, b_lo + kk * 128, kDescHi, idesc_pv,
+                   (accumulate || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    auto commit = [&](int b) {
+      if (elect_one()) tc_commit(bar(b));
+      __syncwarp();
+    };
+    auto wait_kv = [&](int &st) -> bool {
+      st = kv_it % L::kStages;
+      const uint32_t ph = (kv_it / L::kStages) & 1;
+      ++kv_it;
+      return mbar_wait_warp(bar(L::kKVFull + st), ph, abort_flag);
+    };
+    // PV for tile t over block jb (all checks on the caller's side).
+    auto do_pv = [&](int t, int jb, int st) -> bool {
+      const int vc = t ? vc1 : vc0;
+      uint32_t &pc = t ? pc1 : pc0;
+      if (jb == 0 && !mbar_wait_warp(bar(L::kOEmpty + t), (vc & 1) ^ 1, abort_flag)) return false;
+      if (!mbar_wait_warp(bar(L::kPFull + t), pc & 1, abort_flag)) return false;
+      ++pc;
+      __syncwarp();
+      tc_fence_after_sync();
+      issue_pv(t, st, jb > 0);
+      return true;
+    };
+
+    while (ok) {
+      const int slot = it & 1;
+      if (!mbar_wait_warp(bar(L::kSchedFull + slot), (it >> 1) & 1, abort_flag)) { ok = false; break; }
+      const int u = sched[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::kSchedEmpty + slot));
+      ++it;
+      if (u >= plan.total_units) break;
+      const Unit w = decode_unit(plan, u);
+      const int nbt0 = w.t[0].kv_blocks, nbt1 = w.t[1].kv_blocks;
+      const int nb = max(nbt0, nbt1);
+      if (nbt0 > 0 && !mbar_wait_warp(bar(L::kQFull + 0), vc0 & 1, abort_flag)) ok = false;
+      if (ok && nbt1 > 0 && !mbar_wait_warp(bar(L::kQFull + 1), vc1 & 1, abort_flag)) ok = false;
+      if (!ok) break;
+      // block 0: S_t = Q_t K_0^T
+      int st_k, st_v;
+      if (!wait_kv(st_k)) { ok = false; break; }
+      __syncwarp();
+      tc_fence_after_sync();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int nbt = t ? nbt1 : nbt0;
+        if (nbt == 0) continue;
+        issue_qk(t, st_k);
+        commit(L::kSFull + t);
+        if (nbt == 1) commit(L::kQEmpty + t);
+      }
+      // blocks 1..nb-1: O_t += P_t V_{j-1}, then S_t = Q_t K_j^T
+      for (int j = 1; j < nb && ok; ++j) {
+        commit(L::kKVEmpty + st_k);  // K_{j-1} no longer read after this point
+        if (!wait_kv(st_v) || !wait_kv(st_k)) { ok = false; break; }
+        __syncwarp();
+        tc_fence_after_sync();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nbt = t ? nbt1 : nbt0;
+          if (!ok) continue;
+          if (j - 1 < nbt) {
+            if (!do_pv(t, j - 1, st_v)) { ok = false; continue; }
+            if (j - 1 == nbt - 1) commit(L::kOFull + t);
+          }
+          if (j < nbt) {
+            issue_qk(t, st_k);
+            commit(L::kSFull + t);
+            if (j == nbt - 1) commit(L::kQEmpty + t);
+          }
+        }
+        commit(L::kKVEmpty + st_v);
+      }
+      if (!ok) break;
+      // last block: O_t += P_t V_{nb-1}
+      commit(L::kKVEmpty + st_k);
+      if (!wait_kv(st_v)) { ok = false; break; }
+      __syncwarp();
+      tc_fence_after_sync();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int nbt = t ? nbt1 : nbt0;
+        if (!ok || nbt != nb) continue;
+        if (!do_pv(t, nb - 1, st_v)) { ok = false; continue; }
+        commit(L::kOFull + t);
+      }
+      commit(L::kKVEmpty + st_v);
+      if (nbt0 > 0) ++vc0;
+      if (nbt1 > 0) ++vc1;
     }
+    if (!ok && lane == 0) fail();
+    // Drain: every tcgen05 operation issued above has completed.
+    commit(L::kDrain);
+    mbar_wait_warp(bar(L::kDrain), 0, nullptr);
+  }
   } else {
+    regs_alloc<kRegsHigh>();
     // ------------------------------------------------------------ softmax / epilogue
     const int t = warp >> 2;                       // query tile of this warpgroup
     const int row = (warp & 3) * 32 + lane;        // row in the tile == TMEM lane
@@ -290,23 +368,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     bool ok = true;
     while (ok) {
       const int slot = it & 1;
-      if (!mbar_wait(bar(L::kSchedFull + slot), (it >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(L::kSchedFull + slot), (it >> 1) & 1, abort_flag)) { ok = false; break; }
       const int u = sched[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kSchedEmpty + slot));
       ++it;
       if (u >= plan.total_units) break;
       const Unit w = decode_unit(plan, u);
-      const int nbt = w.t[t].kv_blocks;
+      const UnitTile mine = t ? w.t[1] : w.t[0];  // select, not a runtime index
+      const int nbt = mine.kv_blocks;
       if (nbt == 0) continue;
-      const int q_row = w.t[t].q_tile * kTileM + row;
+      const int q_row = mine.q_tile * kTileM + row;
       // last visible key of this row (inclusive)
       int lim = plan.N_kv - 1;
       if (plan.causal) lim = min(lim, q_row + plan.kv_offset);
       float m_ref = -INFINITY;  // reference maximum, log2-scaled units
       float l_sum = 0.f;
       for (int j = 0; j < nbt; ++j) {
-        if (!mbar_wait(bar(L::kSFull + t), scnt & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(bar(L::kSFull + t), scnt & 1, abort_flag)) { ok = false; break; }
         ++scnt;
         __syncwarp();  // tcgen05.ld/st below are warp-collective
         tc_fence_after_sync();
@@ -320,64 +399,98 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // P = 2^(S * scale*log2e - m) for pairs of columns with packed fp32
+        // ops, stored to tensor memory as bf16 pairs; returns the row sum.
+        // kEmuPairs of every 8 pairs use the FMA-pipe 2^x, the rest ex2.
+        auto make_p = [&](float m) -> float {
+          const float2 sl2v = make_float2(sl2, sl2);
+          const float2 negm = make_float2(-m, -m);
+          float2 lsum[4];  // four partial sums: no long dependency chain
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
-        }
-        const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-        // Raise the reference maximum only when it grows by more than 2^8
-        // (always on the first block, whose O is overwritten anyway).
-        float alpha = 1.f;
-        const bool raise = (j == 0) || (m_blk > m_ref + kRescaleThreshold);
-        if (raise) {
-          const float m_new = fmaxf(m_ref, m_blk);
-          alpha = (j == 0) ? 0.f : ex2(m_ref - m_new);
-          m_ref = m_new;
-        }
-        __syncwarp();
-        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          for (int i = 0; i < 4; ++i) lsum[i] = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t ov[32];
-            tmem_ld32_wait(tm_o + c0, ov);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tmem_st32(tm_o + c0, ov);
+            for (int c = 0; c < 32; ++c) {
+              const float2 x =
+                  ffma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2v, negm);
+              float2 p;
+              if ((c & 7) < kEmuPairs) {
+                p = exp2_poly2(x);
+              } else {
+                p.x = ex2(x.x);
+                p.y = ex2(x.y);
+              }
+              lsum[c & 3] = fadd2(lsum[c & 3], p);
+              pk[c] = pack_bf16x2(p.x, p.y);
+            }
+            tmem_st32(tm_p + h * 32u, pk);
           }
-        }
-        const float neg_m = -m_ref;
-        float ls0 = 0.f, ls1 = 0.f;
+          const float2 a = fadd2(lsum[0], lsum[1]), b = fadd2(lsum[2], lsum[3]);
+          return (a.x + b.x) + (a.y + b.y);
+        };
+        // row max: eight independent chains of three-input max
+        auto row_max = [&]() -> float {
+          float mx[8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+          for (int k = 0; k < 8; ++k) {
+            mx[k] = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2(fmaf(s[h * 64 + 2 * c], sl2, neg_m));
-            const float p1 = ex2(fmaf(s[h * 64 + 2 * c + 1], sl2, neg_m));
-            ls0 += p0;
-            ls1 += p1;
-            pk[c] = pack_bf16x2(p0, p1);
+            for (int c = 3; c < 15; c += 2) mx[k] = fmax3(mx[k], s[16 * k + c], s[16 * k + c + 1]);
+            mx[k] = fmaxf(mx[k], s[16 * k + 15]);
           }
-          tmem_st32(tm_p + h * 32u, pk);
+          return fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), mx[6]), mx[7]) *
+                 sl2;
+        };
+        float alpha = 1.f, row_sum;
+        bool raise;
+        if (j == 0) {
+          m_ref = row_max();  // first block: its O is overwritten, nothing to rescale
+          alpha = 0.f;
+          raise = false;
+          row_sum = make_p(m_ref);
+        } else {
+          // Speculate that the reference maximum still holds (it only moves
+          // when the row maximum grows by more than 2^8): the exponentials
+          // do not wait for the block maximum, which is computed alongside.
+          row_sum = make_p(m_ref);
+          const float m_blk = row_max();
+          raise = m_blk > m_ref + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, raise)) {
+            // rare: some row's maximum jumped; redo this warp's P with the
+            // raised maxima (rows that did not jump keep theirs, alpha = 1)
+            if (raise) {
+              alpha = ex2(m_ref - m_blk);
+              m_ref = m_blk;
+            }
+            row_sum = make_p(m_ref);
+            // O_t was last written by the PV of block j-1, which completed
+            // before S_t[j] was committed.
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t ov[32];
+              tmem_ld32_wait(tm_o + c0, ov);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+              tmem_st32(tm_o + c0, ov);
+            }
+          }
         }
         tmem_st_wait();
-        l_sum = l_sum * alpha + (ls0 + ls1);
+        l_sum = l_sum * alpha + row_sum;
         tc_fence_before_sync();
         mbar_arrive(bar(L::kPFull + t));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16 -> global
-      if (!mbar_wait(bar(L::kOFull + t), vc & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(L::kOFull + t), vc & 1, abort_flag)) { ok = false; break; }
       ++vc;
       __syncwarp();
       tc_fence_after_sync();
       const float inv_l = 1.f / l_sum;
       __nv_bfloat16 *dst =
-          prm.o + ((static_cast<size_t>(w.b) * plan.H_q + w.t[t].h_q) * plan.N_q + q_row) * D;
+          prm.o + ((static_cast<size_t>(w.b) * plan.H_q + mine.h_q) * plan.N_q + q_row) * D;
       const bool store = q_row < plan.N_q;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -428,11 +541,18 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 32 && !(configured & (1u << dev))) {
+  if (dev >= 32 || !(configured & (1u << dev))) {
+    // The register split is only safe if the compiled kernel is launched
+    // with at least kLaunchRegs registers per thread; refuse otherwise.
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, prefill_tc_kernel<D>);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs < kLaunchRegs || attr.maxThreadsPerBlock < kThreads)
+      return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAlloc);
     if (e != cudaSuccess) return e;
-    configured |= 1u << dev;
+    if (dev < 32) configured |= 1u << dev;
   }
   TcParams prm;
   prm.o = static_cast<__nv_bfloat16 *>(o);

@@ -106,9 +106,9 @@ int gqa_attn_decode(const void *q, const void *k_cache, const void *v_cache,
 
 /*
  * gqa_attn_decode with an explicit split size: each split covers
- * `chunk_tokens` cache rows (a multiple of 32 in [32, 256]); 0 picks the
+ * `chunk_tokens` cache rows (a multiple of 64 in [64, 2048]); 0 picks the
  * library's default for the shape. The result is the same operation for
- * every chunk size, up to fp32 rounding.
+ * every chunk size, up to fp32 rounding. Other values: GQA_ERR_INVALID_ARG.
  */
 int gqa_attn_decode_chunked(const void *q, const void *k_cache,
                             const void *v_cache, const int *seqlens, void *o,

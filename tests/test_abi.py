@@ -87,8 +87,9 @@ def test_decode_chunk_validation():
     f = ops.load().gqa_attn_decode_chunked
     base = (A, A, A, SEQ, A, 2, 12, 2, 2048, 128, 0.088)
     assert f(*base, 33, None) == 1
-    assert f(*base, 512, None) == 1
-    assert f(*base, 96, None) == 2   # multiple of 32 but no kernel for it
+    assert f(*base, 96, None) == 1    # not a multiple of the 64-row sub-block
+    assert f(*base, 4096, None) == 1  # above the largest split
+    assert f(*base, -64, None) == 1
 
 
 def test_selftest_rejects_bad_limit():
