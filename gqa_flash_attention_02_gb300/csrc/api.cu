@@ -152,6 +152,18 @@ bool encode_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long p
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+namespace gqa {
+// Shared with the other host-side translation units of the library.
+bool encode_tensor_map_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long planes,
+                               int box_rows) {
+  return encode_bf16_3d(map, base, d, rows, planes, box_rows);
+}
+}  // namespace gqa
+
+namespace {
+
 // ------------------------------------------------------------------ validation
 
 constexpr long long kMaxElems = (1ll << 31) - 1;

@@ -139,4 +139,9 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
 
 cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStream_t stream);
 
+// bf16 tensor viewed as [planes][rows][d] for TMA: boxes of 64 columns x
+// box_rows rows, 128-byte swizzle, zero fill outside. False on failure.
+bool encode_tensor_map_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long planes,
+                               int box_rows);
+
 }  // namespace gqa

@@ -30,6 +30,7 @@ EXPORTED = [
     "gqa_attn_fwd", "gqa_attn_fwd_f32", "gqa_attn_decode", "gqa_attn_decode_chunked",
     "gqa_attn_decode_f32", "gqa_attn_status_string", "gqa_attn_get_device_error",
     "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
+    "gqa_attn_decode_noalloc",
 ]
 
 
@@ -70,6 +71,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 getattr(lib, name).restype = _i
             lib.gqa_attn_decode_chunked.argtypes = dec[:-1] + [_i, _vp]
             lib.gqa_attn_decode_chunked.restype = _i
+            lib.gqa_attn_decode_noalloc.argtypes = dec
+            lib.gqa_attn_decode_noalloc.restype = _i
             lib.gqa_attn_status_string.argtypes = [_i]
             lib.gqa_attn_status_string.restype = ctypes.c_char_p
             lib.gqa_attn_get_device_error.argtypes = [_vp]
@@ -146,6 +149,13 @@ def gqa_attn_decode(q, k_cache, v_cache, seqlens, o=None, scale=None, chunk_toke
     """bf16 decode. q [B,H_q,d], caches [B,H_kv,max_len,d], seqlens int32 [B] -> o [B,H_q,d]."""
     return _decode("gqa_attn_decode_chunked", torch.bfloat16, q, k_cache, v_cache, seqlens, o,
                    scale, chunk_tokens, stream)
+
+
+def gqa_attn_decode_noalloc(q, k_cache, v_cache, seqlens, o, scale=None, stream=None):
+    """bf16 decode that allocates nothing (the library's fixed scratch array);
+    ``o`` must be given. See gqa_attn_decode_noalloc in include/gqa_attn.h."""
+    return _decode("gqa_attn_decode_noalloc", torch.bfloat16, q, k_cache, v_cache, seqlens, o,
+                   scale, None, stream)
 
 
 def gqa_attn_decode_f32(q, k_cache, v_cache, seqlens, o=None, scale=None, stream=None):

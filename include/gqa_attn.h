@@ -124,6 +124,36 @@ int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
                         int B, int H_q, int H_kv, int max_len, int d,
                         float scale, cudaStream_t stream);
 
+/*
+ * gqa_attn_decode for callers that must not allocate device memory. The
+ * pages describe no counterpart: this is a deployment variant of the same
+ * operation. gqa_attn_decode grows a per-stream workspace with
+ * cudaMallocAsync; a serving loop confined to a pre-reserved memory budget,
+ * a latency-critical path where an allocation may synchronise the device, or
+ * a process whose device memory belongs to another allocator cannot allow
+ * that. This entry point calls no allocation routine: its scratch (split
+ * partials and merge counters) is a fixed 4 MiB + 64 KiB array in the
+ * library's own device memory, present on every GPU that loads the library
+ * until the process exits.
+ *   - Arguments, layouts and results as gqa_attn_decode (same kernel), with
+ *     the split size chosen so the partials fit: B * H_q * ceil(max_len /
+ *     split) * (d + 2) * 4 bytes <= 4 MiB with splits of up to 2048 rows,
+ *     and B * H_kv <= 16384. Larger problems return GQA_ERR_UNSUPPORTED (use
+ *     gqa_attn_decode).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array and clears the parts that must start at
+ *     zero; calls that overlap on the GPU (different streams, or different
+ *     host threads) race on it and must be serialised by the caller.
+ *   - Sequences whose seqlens entry is outside [0, max_len] get O = 0; this
+ *     entry point does not report device-side errors.
+ */
+int gqa_attn_decode_noalloc(const void *q, const void *k_cache,
+                            const void *v_cache, const int *seqlens, void *o,
+                            int B, int H_q, int H_kv, int max_len, int d,
+                            float scale, cudaStream_t stream);
+
 /* Human-readable text for a gqa_status (never NULL; static storage). For
  * GQA_ERR_CUDA it includes the last CUDA error name seen by this thread. */
 const char *gqa_attn_status_string(int status);
