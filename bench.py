@@ -299,14 +299,14 @@ def run_ours(args):
             "ms": round(dec_ms, 6),
             "roofline": {
                 "bound": "hbm",
-                "kernel": "decode_kernel<128,3> (split-KV + in-kernel merge)",
+                "kernel": "decode_kernel<128,5> (persistent split-KV + in-kernel merge)",
                 "achieved": round(dec_ach, 2),
                 "peak": hbm_peak,
                 "unit": "GB/s",
                 "frac": round(dec_ach / hbm_peak, 4),
                 "peak_source": f"{peak_src} hbm_gbs",
                 "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
-                                            "decode_kernel<128,3>"),
+                                            "decode_kernel<128,5>"),
             },
             "e2e": {"value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},

@@ -245,23 +245,25 @@ int gqa_attn_decode_chunked(const void *q, const void *k_cache, const void *v_ca
   int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
   if (rc != GQA_OK) return rc;
   if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
   if (chunk_tokens != 0 &&
       (chunk_tokens < 0 || chunk_tokens % kDecodeChunkUnit != 0 || chunk_tokens > kDecodeChunkMax))
     return GQA_ERR_INVALID_ARG;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int chunk = chunk_tokens ? chunk_tokens : decode_default_chunk(B, H_kv, max_len, device_sms(dev));
+  const int grid = decode_grid(B, H_q, H_kv, max_len, d, device_sms(dev), chunk_tokens);
   Workspace *ws = nullptr;
-  rc = get_workspace(stream, decode_partials_bytes(B, H_q, max_len, d, chunk), &ws,
-                     static_cast<size_t>(B) * H_kv);
+  rc = get_workspace(stream, decode_partials_bytes(B, H_q, H_kv, d, grid), &ws,
+                     decode_planes(B, H_q, H_kv));
   if (rc != GQA_OK) return rc;
-  CUtensorMap tk, tv;
-  if (!encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit) ||
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
+      !encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit) ||
       !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit))
     return cuda_fail(cudaErrorInvalidValue);
-  e = launch_decode_bf16(tk, tv, q, seqlens, o, ws->partials, ws->counters, B, H_q, H_kv, max_len,
-                         d, scale, chunk, ws->ctl + kCtlErr, stream);
+  e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, ws->partials, ws->counters, B, H_q, H_kv,
+                         max_len, d, scale, grid, ws->ctl + kCtlErr, stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 

@@ -23,7 +23,7 @@ namespace {
 
 // Scratch layout (bytes): split partials | merge counters | error word.
 constexpr size_t kPartialsMax = 4u << 20;           // 4 MiB of fp32 partials
-constexpr size_t kCountersMax = 16384;              // (b, h_kv) pairs
+constexpr size_t kCountersMax = 16384;              // (b, h_kv, head group) planes
 constexpr size_t kCountersOff = kPartialsMax;
 constexpr size_t kErrOff = kCountersOff + kCountersMax * sizeof(int);
 constexpr size_t kScratchBytes = kErrOff + 256;
@@ -71,22 +71,24 @@ extern "C" int gqa_attn_decode_noalloc(const void *q, const void *k_cache, const
     return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
   if (max_len > (1 << 20) ||
       static_cast<long long>(B) * H_kv * max_len * d > (1ll << 31) - 1)
     return GQA_ERR_UNSUPPORTED;
 
-  // Start from the usual split size and lengthen the splits until their
-  // partials fit the fixed scratch (longer splits = fewer partials).
+  // The partials need one slot per CTA plus one per plane: shrink the grid
+  // until they fit the fixed scratch.
   int dev = 0, sms = 1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
-  int chunk = decode_default_chunk(B, H_kv, max_len, sms);
-  while (decode_partials_bytes(B, H_q, max_len, d, chunk) > kPartialsMax && chunk < kDecodeChunkMax)
-    chunk *= 2;
-  if (decode_partials_bytes(B, H_q, max_len, d, chunk) > kPartialsMax ||
-      static_cast<size_t>(B) * H_kv > kCountersMax)
+  const size_t planes = decode_planes(B, H_q, H_kv);
+  const size_t slot_bytes = decode_partials_bytes(B, H_q, H_kv, d, 1) / (planes + 1);
+  const size_t max_slots = kPartialsMax / slot_bytes;
+  if (planes >= max_slots || planes > kCountersMax)
     return GQA_ERR_UNSUPPORTED;  // beyond the fixed scratch: use gqa_attn_decode instead
+  int grid = decode_grid(B, H_q, H_kv, max_len, d, sms, 0);
+  if (static_cast<size_t>(grid) > max_slots - planes) grid = static_cast<int>(max_slots - planes);
 
   unsigned char *scratch = nullptr;
   e = scratch_for_current_device(&scratch);
@@ -95,17 +97,18 @@ extern "C" int gqa_attn_decode_noalloc(const void *q, const void *k_cache, const
   int *counters = reinterpret_cast<int *>(scratch + kCountersOff);
   int *err_word = reinterpret_cast<int *>(scratch + kErrOff);
   // the array keeps the previous call's contents: zero what must start at zero
-  e = cudaMemsetAsync(counters, 0, static_cast<size_t>(B) * H_kv * sizeof(int), stream);
+  e = cudaMemsetAsync(counters, 0, planes * sizeof(int), stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(err_word, 0, sizeof(int), stream);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
 
-  CUtensorMap tk, tv;
-  if (!encode_tensor_map_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv,
-                          kDecodeChunkUnit) ||
+  CUtensorMap tq, tk, tv;
+  if (!encode_tensor_map_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
+      !encode_tensor_map_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv,
+                                 kDecodeChunkUnit) ||
       !encode_tensor_map_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv,
-                          kDecodeChunkUnit))
+                                 kDecodeChunkUnit))
     return GQA_ERR_CUDA;
-  e = launch_decode_bf16(tk, tv, q, seqlens, o, partials, counters, B, H_q, H_kv, max_len, d, scale,
-                         chunk, err_word, stream);
+  e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, partials, counters, B, H_q, H_kv, max_len, d,
+                         scale, grid, err_word, stream);
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }

@@ -1,31 +1,34 @@
-// Single-token GQA decode against a bf16 K/V cache: split-KV with the
-// log-sum-exp merge done in the same kernel.
+// Single-token GQA decode against a bf16 K/V cache: a persistent,
+// row-balanced split-KV kernel with the log-sum-exp merge in the same launch.
 //
 // The decode step reads every valid cache row once and does about 3 FLOPs
 // per byte at the workload's group size, so it is bound by HBM bandwidth
-// (kaispace.site, prefill-vs-decode note). The cache of each (b, h_kv) is cut
-// into fixed-size splits (the split-sequence cached attention of the
-// microLLM-rocm optimisation log, Experiments 282-284) so that B * H_kv *
-// splits CTAs cover all SMs even at small batch; ragged lengths balance
-// themselves because splits past seqlens[b] exit at once.
+// (kaispace.site, prefill-vs-decode note). What keeps HBM busy is a steady
+// stream of bytes in flight on every SM. So the valid cache rows of all
+// sequences are cut into 64-row units -- (b, h_kv, head group, sub-block),
+// in that order -- and a persistent grid of a few CTAs per SM takes equal
+// contiguous ranges of units. Each CTA streams its range through a TMA ring
+// without stopping at sequence boundaries, so ragged lengths balance
+// themselves and every SM reads about the same number of bytes. A range that
+// covers part of a sequence produces a partial result: this is the
+// split-sequence cached attention of the microLLM-rocm optimisation log
+// (Experiments 282-284) with the splits chosen by row balance.
 //
-// One CTA = one (b, h_kv, split), 4 warps. It serves ALL g = H_q / H_kv
-// query heads of the group from a single read of its K/V rows (no K/V
-// replication: microLLM-rocm Experiment 044, BootstrapAI collab-014
-// "Kernel 9 GQA"):
-//   * TMA streams 64-row K and V sub-blocks (128-byte swizzled 64-column
-//     panels) through a multi-stage shared-memory ring, so loads for later
-//     sub-blocks are in flight while earlier ones are consumed.
-//   * Warp w takes rows [16w, 16w+16) of each sub-block. The group's query
+// A (b, h_kv, head group) "plane" serves up to 16 query heads of the group
+// from ONE read of its K/V rows (no K/V replication: microLLM-rocm Experiment
+// 044, BootstrapAI collab-014 "Kernel 9 GQA"). Per CTA:
+//   * warp 4 is the producer: it walks the same unit sequence and issues the
+//     TMA loads (K then V, 128-byte swizzled 64-column panels) into a ring of
+//     stages, refilling a stage once the four MMA warps have released it;
+//   * warps 0-3 take rows [16w, 16w+16) of each unit. The group's query
 //     heads (padded to 16) times those rows is a dense contraction over d:
 //     S = Q K^T and O += P V run on mma.sync (bf16 in, fp32 accumulate) from
-//     ldmatrix fragments, which keeps the kernel's instruction count far
-//     below its memory time. Softmax (online, exp2 with the scale folded
-//     in) runs on the fragments in registers.
-//   * The 4 warps' (m, l, O) states merge in shared memory. A sequence that
-//     fits in one split writes its output directly; otherwise each split
-//     writes (m, l, O) to the workspace and the LAST split to finish
-//     (atomic counter per (b, h_kv), no waiting) merges them:
+//     ldmatrix fragments, with an online softmax (exp2, scale folded in) on
+//     the register fragments;
+//   * at the end of a plane's run, the four warps' (m, l, O) merge through a
+//     small shared-memory tree; a run that covers the whole plane writes O,
+//     otherwise it writes a partial and the last run of the plane to finish
+//     (atomic counter, nobody waits) merges the partials:
 //         M = max m_i,  L = sum 2^(m_i - M) l_i,  O = sum 2^(m_i - M) O_i / L.
 #include <cuda_runtime.h>
 #include <math.h>
@@ -37,9 +40,20 @@ namespace gqa {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kSub = 64;     // cache rows per sub-block (16 per warp)
-constexpr int kHeads = 16;   // query heads per pass (mma M)
+constexpr int kMmaWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kEpilogueWarp = 5;
+constexpr int kThreads = 32 * (kMmaWarps + 2);
+constexpr int kSub = 64;     // cache rows per unit (16 per MMA warp)
+constexpr int kHeads = kDecodeHeads;  // query heads per plane (mma M)
+// Fewest units a CTA takes: fewer, longer runs (each run ends in a merge
+// step and a plane spans at most nsub / kMinUnits + 2 CTAs); no CTA range
+// is ever empty.
+constexpr int kMinUnits = 4;
+constexpr int kLenCache = 1024;  // sequence lengths kept in shared memory
+constexpr int kEpSlots = 2;      // run states queued for the epilogue warp
+constexpr int kEpPartial = 1, kEpStop = 2;
+constexpr int kCtasPerSm = 1;    // the balanced partition assumes one resident wave
 
 // Byte offset of (row, 16-byte unit u) inside a [rows][D] bf16 tile stored
 // as D/64 panels of `rows` x 128 B with the TMA 128-byte swizzle.
@@ -71,314 +85,728 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Barrier among the four MMA warps only (producer and epilogue keep going).
+__device__ __forceinline__ void mma_warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaWarps) : "memory");
+}
+
 template <int D, int NSTG>
 struct DecodeSmem {
-  static constexpr int kTile = kSub * D * 2;            // one K or V sub-block
-  static constexpr int kStage = 2 * kTile;               // K then V
-  static constexpr int kOffStage = 0;
+  static constexpr int kTile = kSub * D * 2;     // one K or V unit
+  static constexpr int kQTile = kHeads * D * 2;  // the plane's 16 query rows
+  static constexpr int kStage = 2 * kTile + kQTile;
   static constexpr int kRingBytes = NSTG * kStage;
-  // merge area (reuses the ring once the sweep is done)
-  static constexpr int kMergeO = 4 * kHeads * D * 4;     // float [4 warps][16][D]
-  static constexpr int kMergeML = 4 * kHeads * 2 * 4;    // float [4][16][2]
-  static constexpr int kRegion = kRingBytes > kMergeO + kMergeML ? kRingBytes : kMergeO + kMergeML;
-  static constexpr int kOffBar = kRegion;                // NSTG mbarriers
-  static constexpr int kOffFlag = kOffBar + NSTG * 8;    // int: "this CTA merges"
-  static constexpr int kBytes = kOffFlag + 16;
+  // A merged run state handed to the epilogue warp: O rows [16][kRow]
+  // (unnormalised), m[16], l[16].
+  static constexpr int kRow = D + 4;  // padded: fragment stores spread over banks
+  static constexpr int kStateFloats = kHeads * kRow + 2 * kHeads;
+  static constexpr int kStateBytes = kStateFloats * 4;
+  // At a run end the four MMA warps leave their (m, l, O) fragments in the
+  // stage of the run's last unit (released only afterwards): 4 warps x 32
+  // lanes x (D/8 * 4 accumulators + m_lo, m_hi, l_lo, l_hi).
+  static constexpr int kLaneFloats = D / 8 * 4 + 4;
+  static_assert(kMmaWarps * 32 * kLaneFloats * 4 <= kStage, "run-end slots");
+  static constexpr int kEpBytes = kStateBytes + 64;  // state + 16 ints of run metadata
+  static constexpr int kOffEp = kRingBytes;
+  static constexpr int kOffMeta = kOffEp + kEpSlots * kEpBytes;  // per stage: b, pib, s, len
+  static constexpr int kOffLen = kOffMeta + NSTG * 16;
+  static constexpr int kOffBar = kOffLen + kLenCache * 4;  // full, empty [NSTG]; ep_full, ep_empty
+  static constexpr int kOffInfo = kOffBar + (2 * NSTG + 2 * kEpSlots) * 8;
+  static constexpr int kBytes = kOffInfo + 32;
   static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kStage % 1024 == 0 && kEpBytes % 16 == 0 && kOffBar % 8 == 0, "alignment");
 };
 
 struct DecodeParams {
   const __nv_bfloat16 *q;
   const int *seqlens;
   __nv_bfloat16 *o;
-  float *part;     // [B][H_q][splits][D + 2]: O (unnormalised), m, l
-  int *counters;   // [B][H_kv], zero between launches
+  float *part;     // [(grid + planes)] slots of O [16][D] (unnormalised), m [16], l [16]
+  int *counters;   // [planes], zero between launches (the last merger re-arms it)
   int *err_word;
-  int H_q, H_kv, max_len, n_splits, chunk;
+  int B, H_q, H_kv, max_len, nhg;  // nhg = query-head groups of 16 per K/V head
   float scale_log2;
 };
 
-template <int D, int NSTG>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                          const __grid_constant__ CUtensorMap tm_v,
-                                                          const DecodeParams prm) {
-  using L = DecodeSmem<D, NSTG>;
-  constexpr int NT = D / 8;  // n-tiles of O per warp
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t s_base = smem_addr(smem);
-  const uint32_t bars = s_base + L::kOffBar;
-  volatile int *merge_flag = reinterpret_cast<volatile int *>(smem + L::kOffFlag);
+__device__ __forceinline__ int seq_len(const DecodeParams &prm, const int *s_len, int b) {
+  return b < kLenCache ? s_len[b] : __ldg(prm.seqlens + b);
+}
 
-  const int split = blockIdx.x, h_kv = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int group = prm.H_q / prm.H_kv;
+// Units of a sequence of length len for each of its planes (0 for a length
+// outside [1, max_len]).
+__device__ __forceinline__ int units_for(const DecodeParams &prm, int len) {
+  return (len <= 0 || len > prm.max_len) ? 0 : (len + kSub - 1) / kSub;
+}
 
-  const int len = prm.seqlens[b];
-  if (len < 0 || len > prm.max_len) {
-    if (tid == 0 && split == 0 && h_kv == 0) record_error(prm.err_word, kErrBadSeqlen);
-    if (split == 0) {  // the sequence's output is defined as 0
-      for (int i = tid; i < group * D; i += kThreads)
-        prm.o[(static_cast<size_t>(b) * prm.H_q + h_kv * group) * D + i] = __float2bfloat16_rn(0.f);
+// Position in the unit sequence: sequence b, plane pib inside it (h_kv-major,
+// then head group), unit s inside the plane (nsub units per plane).
+struct Pos {
+  int b, pib, s, nsub;
+};
+
+__device__ __forceinline__ void advance(const DecodeParams &prm, const int *s_len,
+                                        int planes_per_b, Pos &p) {
+  if (++p.s < p.nsub) return;
+  p.s = 0;
+  if (++p.pib < planes_per_b) return;
+  p.pib = 0;
+  do {
+    ++p.b;
+    p.nsub = (p.b < prm.B) ? units_for(prm, seq_len(prm, s_len, p.b)) : 1;  // past the end only at termination
+  } while (p.b < prm.B && p.nsub == 0);
+}
+
+// Balanced partition of U units over G CTAs: the first r = U % G CTAs take
+// q + 1 = U / G + 1 units, the others q.
+struct Split {
+  int q, r;
+};
+
+__device__ __forceinline__ int split_first(const Split &sp, int c) {
+  return c * sp.q + min(c, sp.r);
+}
+
+__device__ __forceinline__ int owner_of(int u, const Split &sp) {
+  const int t = sp.r * (sp.q + 1);
+  return u < t ? u / (sp.q + 1) : sp.r + (u - t) / sp.q;
+}
+
+// Merges another (m, l, acc) state into this one for one row: returns the
+// weights of the old and the new accumulator.
+__device__ __forceinline__ void merge_row(float &m, float &l, float m2, float l2, float &w1,
+                                          float &w2) {
+  const float M = fmaxf(m, m2);
+  w1 = (m == -INFINITY) ? 0.f : ex2(m - M);
+  w2 = (m2 == -INFINITY) ? 0.f : ex2(m2 - M);
+  l = fmaf(w1, l, w2 * l2);
+  m = M;
+}
+
+// Folds the parts j = 0, 1, ..., nparts - 1 of a plane, in that order, for
+// the (head, 4 columns) items it = t, t + nt, ... < Gh * D / 4 and writes O:
+//   M' = max(M, m_j),  L' = 2^(M-M') L + 2^(m_j-M') l_j,
+//   O' = 2^(M-M') O + 2^(m_j-M') O_j,  O = O' / L' at the end.
+// Part j lives in partial slot pbase + j * kSlot, except part jself, the
+// calling CTA's own state, which self(k, it, O, m, l) supplies for the k-th
+// item of a group. Every item's arithmetic is the same whichever CTA or
+// warp runs it, so the result does not depend on who merges. kBatch parts'
+// loads are in flight together.
+template <int D, int kItems, int kBatch, typename SelfFn>
+__device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int jself, SelfFn self,
+                                            int Gh, __nv_bfloat16 *o_plane, int t, int nt) {
+  constexpr int kQuads = D / 4;
+  constexpr int kSlot = kHeads * (D + 2);
+  const int items = Gh * kQuads;
+  for (int base = t; base < items; base += nt * kItems) {
+    float Mr[kItems], Lr[kItems];
+    float4 Ar[kItems];
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      Mr[k] = -INFINITY;
+      Lr[k] = 0.f;
+      Ar[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    return;
-  }
-  const int n_split_b = (len + prm.chunk - 1) / prm.chunk;
-  if (len == 0) {
-    if (split == 0)
-      for (int i = tid; i < group * D; i += kThreads)
-        prm.o[(static_cast<size_t>(b) * prm.H_q + h_kv * group) * D + i] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  if (split >= n_split_b) return;
-  const int r0 = split * prm.chunk;
-  const int n = min(prm.chunk, len - r0);  // rows of this split
-  const int nsub = (n + kSub - 1) / kSub;
-  const int plane = b * prm.H_kv + h_kv;
-
-  if (tid == 0) {
-    for (int s = 0; s < NSTG; ++s) mbar_init(bars + 8 * s, 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-  auto issue = [&](int i) {  // TMA for sub-block i into stage i % NSTG (thread 0)
-    const int st = i % NSTG;
-    const uint32_t dst = s_base + L::kOffStage + st * L::kStage;
-    mbar_arrive_expect_tx(bars + 8 * st, L::kStage);
+    for (int j0 = 0; j0 < nparts; j0 += kBatch) {
+      float4 v[kBatch][kItems];
+      float mj[kBatch][kItems], lj[kBatch][kItems];
 #pragma unroll
-    for (int p = 0; p < D / 64; ++p) {
-      tma_load_3d(dst + p * kSub * 128, &tm_k, bars + 8 * st, p * 64, r0 + i * kSub, plane);
-      tma_load_3d(dst + L::kTile + p * kSub * 128, &tm_v, bars + 8 * st, p * 64, r0 + i * kSub,
-                  plane);
-    }
-  };
-  if (tid == 0)
-    for (int i = 0; i < NSTG && i < nsub; ++i) issue(i);
-
-  bool ok = true;
-  // Each pass serves up to 16 query heads of the group.
-  for (int hg = 0; hg < group && ok; hg += kHeads) {
-    const int G = min(kHeads, group - hg);
-    const int hq0 = h_kv * group + hg;
-    // Q fragments (A operand, 16 heads x D): thread holds rows lane/4 and
-    // lane/4 + 8, columns 2*(lane%4) + {0,1} and + 8, for each 16-wide k-step.
-    uint32_t qa[D / 16][4];
-    {
-      const int r_lo = lane >> 2, r_hi = r_lo + 8, c = 2 * (lane & 3);
-      const uint32_t *qlo = reinterpret_cast<const uint32_t *>(
-          prm.q + (static_cast<size_t>(b) * prm.H_q + hq0 + r_lo) * D);
-      const uint32_t *qhi = reinterpret_cast<const uint32_t *>(
-          prm.q + (static_cast<size_t>(b) * prm.H_q + hq0 + r_hi) * D);
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const int j = j0 + jj;
+        const float *pp = pbase + static_cast<size_t>(j) * kSlot;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        qa[ks][0] = r_lo < G ? __ldg(qlo + (ks * 16 + c) / 2) : 0u;
-        qa[ks][1] = r_hi < G ? __ldg(qhi + (ks * 16 + c) / 2) : 0u;
-        qa[ks][2] = r_lo < G ? __ldg(qlo + (ks * 16 + c + 8) / 2) : 0u;
-        qa[ks][3] = r_hi < G ? __ldg(qhi + (ks * 16 + c + 8) / 2) : 0u;
-      }
-    }
-    float acc[NT][4];
-#pragma unroll
-    for (int i = 0; i < NT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-
-    for (int i = 0; i < nsub; ++i) {
-      const int st = i % NSTG;
-      // fills of this stage before this one: per pass the ring restarts at
-      // stage 0 and stage st is filled ceil((nsub - st) / NSTG) times
-      const int fills = (hg / kHeads) * ((nsub - st + NSTG - 1) / NSTG) + i / NSTG;
-      const uint32_t phase = static_cast<uint32_t>(fills & 1);
-      if (!__syncthreads_and(mbar_wait(bars + 8 * st, phase, nullptr))) { ok = false; break; }
-      const uint32_t kt = s_base + L::kOffStage + st * L::kStage;
-      const uint32_t vt = kt + L::kTile;
-      const int rows_here = min(kSub, n - i * kSub);  // valid rows in this sub-block
-      const int wrow = warp * 16;                     // this warp's first row
-      if (rows_here < kSub) {
-        // rows past the sequence (other sequences' data or NaN padding) must
-        // not reach P.V: zero this warp's invalid V rows
-        for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
-          const int r = wrow + idx / (D / 8), u = idx % (D / 8);
-          if (r >= rows_here)
-            *reinterpret_cast<uint4 *>(smem + (vt - s_base) + swz(r, u, kSub)) = make_uint4(0, 0, 0, 0);
-        }
-        __syncwarp();
-      }
-      // ---- S = Q K^T for this warp's 16 rows (two n-tiles of 8 keys)
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        // lanes 0-7: keys 0-7 unit 2ks; 8-15: keys 0-7 unit 2ks+1;
-        // 16-23: keys 8-15 unit 2ks; 24-31: keys 8-15 unit 2ks+1
-        const int key = wrow + (lane & 7) + ((lane >> 4) << 3);
-        const int uo = (lane >> 3) & 1;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kt + swz(key, 2 * ks + uo, kSub), b0, b1, b2, b3);
-          mma_bf16(s0, qa[ks], b0, b1);
-          mma_bf16(s1, qa[ks], b2, b3);
+        for (int k = 0; k < kItems; ++k) {
+          const int it = base + nt * k, h = it / kQuads;
+          const bool ok = j < nparts && it < items;
+          if (ok && j == jself) {
+            self(k, it, v[jj][k], mj[jj][k], lj[jj][k]);
+          } else if (ok) {
+            v[jj][k] = __ldcg(reinterpret_cast<const float4 *>(pp) + it);
+            mj[jj][k] = __ldcg(pp + kHeads * D + h);
+            lj[jj][k] = __ldcg(pp + kHeads * D + kHeads + h);
+          } else {
+            v[jj][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            mj[jj][k] = -INFINITY;
+            lj[jj][k] = 0.f;
+          }
         }
       }
-      // ---- online softmax on the fragments: rows (heads) lane/4 and lane/4+8
-      const int kc = wrow + 2 * (lane & 3);  // key of s?[0]; s?[1] is kc+1; s1 adds 8
-      const float sl2 = prm.scale_log2;
-      float x[8] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2,
-                    s0[2] * sl2, s0[3] * sl2, s1[2] * sl2, s1[3] * sl2};
-      const int keys[4] = {kc, kc + 1, kc + 8, kc + 9};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (keys[e] >= rows_here) { x[e] = -INFINITY; x[4 + e] = -INFINITY; }
-      }
-      float mx_lo = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-      float mx_hi = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-      // a warp whose 16 rows are all past the sequence sees mn = -inf: skip
-      const float a_lo = (mn_lo == -INFINITY) ? 1.f : ex2(m_lo - mn_lo);
-      const float a_hi = (mn_hi == -INFINITY) ? 1.f : ex2(m_hi - mn_hi);
-      float p[8];
+      for (int jj = 0; jj < kBatch; ++jj) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        p[e] = (mn_lo == -INFINITY) ? 0.f : ex2(x[e] - mn_lo);
-        p[4 + e] = (mn_hi == -INFINITY) ? 0.f : ex2(x[4 + e] - mn_hi);
-      }
-      l_lo = l_lo * a_lo + ((p[0] + p[1]) + (p[2] + p[3]));
-      l_hi = l_hi * a_hi + ((p[4] + p[5]) + (p[6] + p[7]));
-      m_lo = mn_lo;
-      m_hi = mn_hi;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        acc[t][0] *= a_lo; acc[t][1] *= a_lo;
-        acc[t][2] *= a_hi; acc[t][3] *= a_hi;
-      }
-      // P as the A operand (16 heads x 16 keys): keys 0-7 from n-tile 0, 8-15 from n-tile 1
-      const uint32_t pa[4] = {pack_bf16x2(p[0], p[1]), pack_bf16x2(p[4], p[5]),
-                              pack_bf16x2(p[2], p[3]), pack_bf16x2(p[6], p[7])};
-      // ---- O += P V (V rows = k, d = n): transposed ldmatrix of 8x8 blocks
-      {
-        // lanes 0-7: keys 0-7 unit u; 8-15: keys 8-15 unit u; 16-23: keys 0-7 unit u+1;
-        // 24-31: keys 8-15 unit u+1  -> {b0,b1} for d-tile u and {b0,b1} for u+1
-        const int key = wrow + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int uo = lane >> 4;
-#pragma unroll
-        for (int u = 0; u < NT; u += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vt + swz(key, u + uo, kSub), b0, b1, b2, b3);
-          mma_bf16(acc[u], pa, b0, b1);
-          mma_bf16(acc[u + 1], pa, b2, b3);
-        }
-      }
-      // all warps are done with this stage: refill it with sub-block i + NSTG
-      __syncthreads();
-      if (tid == 0 && i + NSTG < nsub) {
-        fence_proxy_async_smem();  // generic-proxy writes (V zeroing) before the TMA overwrite
-        issue(i + NSTG);
-      }
-    }
-    if (!ok) break;
-
-    // ---- merge the 4 warps' states in shared memory (the ring is idle now)
-    float *mo = reinterpret_cast<float *>(smem);                    // [4][16][D]
-    float *mml = reinterpret_cast<float *>(smem + L::kMergeO);      // [4][16][2]
-    {
-      const int r_lo = lane >> 2, r_hi = r_lo + 8;
-      // quad-reduce l across the 4 threads sharing a row
-      float ll = l_lo, lh = l_hi;
-      ll += __shfl_xor_sync(0xffffffffu, ll, 1);
-      ll += __shfl_xor_sync(0xffffffffu, ll, 2);
-      lh += __shfl_xor_sync(0xffffffffu, lh, 1);
-      lh += __shfl_xor_sync(0xffffffffu, lh, 2);
-      if ((lane & 3) == 0) {
-        mml[(warp * 16 + r_lo) * 2 + 0] = m_lo;
-        mml[(warp * 16 + r_lo) * 2 + 1] = ll;
-        mml[(warp * 16 + r_hi) * 2 + 0] = m_hi;
-        mml[(warp * 16 + r_hi) * 2 + 1] = lh;
-      }
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int col = t * 8 + 2 * (lane & 3);
-        *reinterpret_cast<float2 *>(mo + (warp * 16 + r_lo) * D + col) = make_float2(acc[t][0], acc[t][1]);
-        *reinterpret_cast<float2 *>(mo + (warp * 16 + r_hi) * D + col) = make_float2(acc[t][2], acc[t][3]);
-      }
-    }
-    __syncthreads();
-    const bool single = (n_split_b == 1);
-    for (int idx = tid; idx < G * D; idx += kThreads) {
-      const int h = idx / D, c = idx % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) M = fmaxf(M, mml[(w * 16 + h) * 2]);
-      float Lsum = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float mw = mml[(w * 16 + h) * 2];
-        const float wgt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-        Lsum = fmaf(wgt, mml[(w * 16 + h) * 2 + 1], Lsum);
-        O = fmaf(wgt, mo[(w * 16 + h) * D + c], O);
-      }
-      const size_t row = static_cast<size_t>(b) * prm.H_q + hq0 + h;
-      if (single) {
-        prm.o[row * D + c] = __float2bfloat16_rn(O / Lsum);
-      } else {
-        float *dst = prm.part + (row * prm.n_splits + split) * (D + 2);
-        dst[c] = O;
-        if (c == 0) {
-          dst[D] = M;
-          dst[D + 1] = Lsum;
+        for (int k = 0; k < kItems; ++k) {
+          float wa, wb;
+          merge_row(Mr[k], Lr[k], mj[jj][k], lj[jj][k], wa, wb);
+          Ar[k] = make_float4(fmaf(wa, Ar[k].x, wb * v[jj][k].x), fmaf(wa, Ar[k].y, wb * v[jj][k].y),
+                              fmaf(wa, Ar[k].z, wb * v[jj][k].z), fmaf(wa, Ar[k].w, wb * v[jj][k].w));
         }
       }
     }
-    __syncthreads();  // merge area free again (next pass reloads the ring)
-    if (hg + kHeads < group) {
-      // another pass over the same rows: restart the ring
-      if (tid == 0)
-        for (int i = 0; i < NSTG && i < nsub; ++i) issue(i);
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int it = base + nt * k;
+      if (it < items) {
+        const int h = it / kQuads, q4 = it % kQuads;
+        const float il = 1.f / Lr[k];
+        *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
+            make_uint2(pack_bf16x2(Ar[k].x * il, Ar[k].y * il), pack_bf16x2(Ar[k].z * il, Ar[k].w * il));
+      }
     }
-  }
-  if (!ok) {
-    if (tid == 0) record_error(prm.err_word, kErrTimeout);
-    return;
-  }
-  if (n_split_b == 1) return;
-
-  // ---- the last split of (b, h_kv) to finish merges all of them
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    int *ctr = prm.counters + plane;
-    const int prev = atomicAdd(ctr, 1);
-    const bool last = (prev == n_split_b - 1);
-    if (last) atomicExch(ctr, 0);  // re-arm for the next launch
-    *merge_flag = last ? 1 : 0;
-  }
-  __syncthreads();
-  if (!*merge_flag) return;
-  __threadfence();
-  for (int idx = tid; idx < group * D; idx += kThreads) {
-    const int h = idx / D, c = idx % D;
-    const size_t row = static_cast<size_t>(b) * prm.H_q + h_kv * group + h;
-    const float *src = prm.part + row * prm.n_splits * (D + 2);
-    float M = -INFINITY;
-    for (int sp = 0; sp < n_split_b; ++sp) M = fmaxf(M, __ldcg(src + sp * (D + 2) + D));
-    float Lsum = 0.f, O = 0.f;
-    for (int sp = 0; sp < n_split_b; ++sp) {
-      const float *pp = src + sp * (D + 2);
-      const float wgt = ex2(__ldcg(pp + D) - M);
-      Lsum = fmaf(wgt, __ldcg(pp + D + 1), Lsum);
-      O = fmaf(wgt, __ldcg(pp + c), O);
-    }
-    prm.o[row * D + c] = __float2bfloat16_rn(O / Lsum);
   }
 }
 
 template <int D, int NSTG>
-cudaError_t launch_decode_d(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
-                            const int *seqlens, void *o, float *partials, int *counters, int B,
-                            int H_q, int H_kv, int max_len, float scale, int chunk, int *err_word,
-                            cudaStream_t stream) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const DecodeParams prm) {
+  using L = DecodeSmem<D, NSTG>;
+  constexpr int NT = D / 8;                  // n-tiles of O per warp
+  constexpr int kSlot = kHeads * (D + 2);    // floats per partial slot
+  constexpr int kQuads = D / 4;              // float4 column groups per head
+  constexpr int kPer = kHeads * kQuads / (32 * kMmaWarps);  // merge items per MMA thread
+  constexpr int kEpPer = kHeads * kQuads / 32;              // merge items per epilogue lane
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_addr(smem);
+  const uint32_t full = s_base + L::kOffBar;
+  const uint32_t empty = full + 8 * NSTG;
+  const uint32_t ep_full = empty + 8 * NSTG;
+  const uint32_t ep_empty = ep_full + 8 * kEpSlots;
+  volatile int *info = reinterpret_cast<volatile int *>(smem + L::kOffInfo);
+  int *s_len = reinterpret_cast<int *>(smem + L::kOffLen);
+  int *stage_meta = reinterpret_cast<int *>(smem + L::kOffMeta);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  const int group = prm.H_q / prm.H_kv;
+  const int planes_per_b = prm.H_kv * prm.nhg;
+
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  // ---- warp 0: lengths (128 per pass, loads in flight together, the first
+  // kLenCache kept in shared memory), total units and this CTA's start
+  if (warp == 0) {
+    int U = 0;
+    int n_first[4], before_first[4];  // units and units before, sequences 32k + lane < 128
+    for (int b0 = 0; b0 < prm.B; b0 += 128) {
+      int len[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int b = b0 + 32 * k + lane;
+        len[k] = (b < prm.B) ? __ldg(prm.seqlens + b) : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int b = b0 + 32 * k + lane;
+        if (b < prm.B && b < kLenCache) s_len[b] = len[k];
+        if (b < prm.B && (len[k] < 0 || len[k] > prm.max_len) && c == 0)
+          record_error(prm.err_word, kErrBadSeqlen);
+        const int n = units_for(prm, len[k]);
+        const int x = n * planes_per_b;
+        int incl = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (b0 == 0) {
+          n_first[k] = n;
+          before_first[k] = U + incl - x;
+        }
+        U += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    __syncwarp();
+    // effective grid: every CTA takes at least kMinUnits units
+    const int G = max(1, min(static_cast<int>(gridDim.x), U / kMinUnits));
+    const Split sp{U / G, U % G};
+    const int u0 = (c < G) ? split_first(sp, c) : U;
+    // locate u0: the sequence whose units contain it, then the plane and unit
+    int sb = prm.B, spib = 0, ss = 0, snsub = 1;
+    auto found = [&](unsigned hit, int b0, int before, int n) {
+      const int src = __ffs(hit) - 1;
+      const int bef = __shfl_sync(0xffffffffu, before, src);
+      const int nn = __shfl_sync(0xffffffffu, n, src);
+      const int off = u0 - bef;
+      sb = b0 + src;
+      spib = off / nn;
+      ss = off % nn;
+      snsub = nn;
+    };
+    if (prm.B <= 128) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int b = 32 * k + lane, x = n_first[k] * planes_per_b;
+        const unsigned hit = __ballot_sync(
+            0xffffffffu, b < prm.B && x > 0 && u0 >= before_first[k] && u0 < before_first[k] + x);
+        if (hit && sb == prm.B) found(hit, 32 * k, before_first[k], n_first[k]);
+      }
+    } else {
+      int cum = 0;
+      for (int b0 = 0; b0 < prm.B && sb == prm.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int n = (b < prm.B) ? units_for(prm, seq_len(prm, s_len, b)) : 0;
+        const int x = n * planes_per_b;
+        int incl = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int before = cum + incl - x;  // units before sequence b
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, b < prm.B && x > 0 && u0 >= before && u0 < before + x);
+        if (hit) found(hit, b0, before, n);
+        cum += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    if (lane == 0) {
+      info[0] = U;
+      info[1] = sb;
+      info[2] = spib;
+      info[3] = ss;
+      info[5] = G;
+      info[6] = snsub;
+      for (int s = 0; s < NSTG; ++s) {
+        mbar_init(full + 8 * s, 1);
+        mbar_init(empty + 8 * s, kMmaWarps);
+      }
+      for (int e = 0; e < kEpSlots; ++e) {
+        mbar_init(ep_full + 8 * e, 1);
+        mbar_init(ep_empty + 8 * e, 1);
+      }
+      fence_barrier_init();
+    }
+  }
+  __syncthreads();
+  const int U = info[0];
+  const int G = info[5];
+  if (c >= G) return;
+  if (warp < kMmaWarps) {
+    // a sequence with no rows (or a rejected length) gets a zero output,
+    // written by CTA b % G
+    for (int b = c; b < prm.B; b += G) {
+      if (units_for(prm, seq_len(prm, s_len, b)) != 0) continue;
+      uint4 *ob = reinterpret_cast<uint4 *>(prm.o + static_cast<size_t>(b) * prm.H_q * D);
+      for (int idx = tid; idx < prm.H_q * D / 8; idx += 32 * kMmaWarps) ob[idx] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (U == 0) return;
+  const Split sp{U / G, U % G};
+  const int u0 = split_first(sp, c);
+  const int n_units = sp.q + (c < sp.r ? 1 : 0);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    // Walks the CTA's units; per unit it leaves (b, pib, s, len) in the
+    // stage's metadata and loads K, V and the plane's 16 query rows with one
+    // completion barrier.
+    if (lane == 0) {
+      Pos p{info[1], info[2], info[3], info[6]};
+      for (int i = 0; i < n_units; ++i) {
+        const int st = i % NSTG;
+        if (i >= NSTG && !mbar_wait(empty + 8 * st, ((i / NSTG) & 1) ^ 1, nullptr)) {
+          record_error(prm.err_word, kErrTimeout);
+          break;
+        }
+        int *meta = stage_meta + 4 * st;
+        meta[0] = p.b;
+        meta[1] = p.pib;
+        meta[2] = p.s;
+        meta[3] = seq_len(prm, s_len, p.b);
+        const int h_kv = p.pib / prm.nhg, hg = p.pib - h_kv * prm.nhg;
+        const int plane_kv = p.b * prm.H_kv + h_kv;
+        const uint32_t dst = s_base + st * L::kStage;
+        mbar_arrive_expect_tx(full + 8 * st, L::kStage);
+#pragma unroll
+        for (int q = 0; q < D / 64; ++q) {
+          tma_load_3d(dst + q * kSub * 128, &tm_k, full + 8 * st, q * 64, p.s * kSub, plane_kv);
+          tma_load_3d(dst + L::kTile + q * kSub * 128, &tm_v, full + 8 * st, q * 64, p.s * kSub,
+                      plane_kv);
+        }
+        // the plane's 16 query rows come with every unit (an L2 hit after the
+        // first), so the MMA warps keep no Q fragments across units
+        const int row = p.b * prm.H_q + h_kv * group + hg * kHeads;
+#pragma unroll
+        for (int q = 0; q < D / 64; ++q)
+          tma_load_3d(dst + 2 * L::kTile + q * kHeads * 128, &tm_q, full + 8 * st, q * 64, row, 0);
+        advance(prm, s_len, planes_per_b, p);
+      }
+    }
+    return;
+  }
+
+  if (warp == kEpilogueWarp) {
+    // ------------------------------------------------------------ epilogue
+    // Publishes the partial states of runs that end inside the CTA's range,
+    // so the MMA warps go on streaming meanwhile: the state goes to slot
+    // c + plane, then (fence) the plane's unit counter; the run that completes
+    // the count merges the plane's parts. A run whose count is already
+    // complete when it starts merges without publishing.
+    for (int k = 0;; ++k) {
+      const int e = k & 1;
+      if (!mbar_wait_warp(ep_full + 8 * e, (k >> 1) & 1, nullptr)) {
+        if (lane == 0) record_error(prm.err_word, kErrTimeout);
+        return;
+      }
+      float *so = reinterpret_cast<float *>(smem + L::kOffEp + e * L::kEpBytes);
+      float *sm = so + kHeads * L::kRow, *sl = sm + kHeads;
+      const volatile int *em = reinterpret_cast<const volatile int *>(so + L::kStateFloats);
+      if (em[0] == kEpStop) return;
+      const int b = em[1], hq0 = em[2], Gh = em[3], plane = em[4], c_first = em[5],
+                c_last = em[6], run_units = em[7], nsub = em[8];
+      int done = 0;
+      if (lane == 0) done = ld_acquire_gpu(prm.counters + plane);
+      bool last = __shfl_sync(0xffffffffu, done, 0) + run_units == nsub;
+      if (!last) {
+        float4 *dst = reinterpret_cast<float4 *>(prm.part + static_cast<size_t>(c + plane) * kSlot);
+#pragma unroll
+        for (int k2 = 0; k2 < kEpPer; ++k2) {
+          const int it = lane + 32 * k2;
+          dst[it] = *reinterpret_cast<const float4 *>(so + (it / kQuads) * L::kRow + 4 * (it % kQuads));
+        }
+        if (lane < kHeads) {
+          reinterpret_cast<float *>(dst)[kHeads * D + lane] = sm[lane];
+          reinterpret_cast<float *>(dst)[kHeads * D + kHeads + lane] = sl[lane];
+        }
+        fence_acq_rel_gpu();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(prm.counters + plane, run_units);
+        last = __shfl_sync(0xffffffffu, prev, 0) + run_units == nsub;
+      }
+      if (last) {
+        fence_acq_rel_gpu();
+        __syncwarp();
+        auto self = [&](int, int it, float4 &v, float &m, float &l) {
+          const int h = it / kQuads;
+          v = *reinterpret_cast<const float4 *>(so + h * L::kRow + 4 * (it % kQuads));
+          m = sm[h];
+          l = sl[h];
+        };
+        merge_parts<D, 2, 2>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+                             c_last - c_first + 1, c - c_first, self, Gh,
+                             prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D, lane, 32);
+        if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ep_empty + 8 * e);
+    }
+  }
+
+  // -------------------------------------------------------------- MMA warps
+  const float sl2 = prm.scale_log2;
+  const int wrow = warp * 16;  // this warp's first row in a unit
+  int seg_first_i = 0, seg_first_s = 0;
+  int ep_k = 0;  // run states handed to the epilogue warp so far
+  int counter_seen = 0, counter_seen2 = 0;  // the last run's looks at its plane counter
+  float acc[NT][4];
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+
+  for (int i = 0; i < n_units; ++i) {
+    const int st = i % NSTG;
+    if (!mbar_wait_warp(full + 8 * st, (i / NSTG) & 1, nullptr)) {
+      if (lane == 0) record_error(prm.err_word, kErrTimeout);
+      break;  // every MMA warp times out on the same phase
+    }
+    const int *meta = stage_meta + 4 * st;
+    const int b = meta[0], pib = meta[1], s = meta[2], len = meta[3];
+    const int nsub = (len + kSub - 1) / kSub;
+    const int h_kv = pib / prm.nhg, hg = pib - h_kv * prm.nhg;
+    const int Gh = min(kHeads, group - hg * kHeads);  // query heads in this plane
+    const int hq0 = h_kv * group + hg * kHeads;
+    const uint32_t kt = s_base + st * L::kStage;
+    const uint32_t vt = kt + L::kTile;
+    if (i == 0 || s == 0) {
+      // a new run
+      seg_first_i = i;
+      seg_first_s = s;
+      // The CTA's last run reads its plane's unit counter now; the value is
+      // used at the run's end (a fence then orders the reads it allows), so
+      // the load's latency hides behind the run's units.
+      if (warp == 0 && lane == 0 && i + (nsub - s) >= n_units)
+        counter_seen = ld_relaxed_gpu(prm.counters + b * planes_per_b + pib);
+      counter_seen2 = 0;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      m_lo = m_hi = -INFINITY;
+      l_lo = l_hi = 0.f;
+    }
+    if (warp == 0 && lane == 0 && i == n_units - 3 && i > seg_first_i && i + (nsub - s) >= n_units)
+      counter_seen2 = ld_relaxed_gpu(prm.counters + b * planes_per_b + pib);  // a later look
+    const int rows_here = min(kSub, len - s * kSub);  // valid rows in this unit
+    bool zeroed = false;
+    if (rows_here < kSub) {
+      // rows past the sequence (other sequences' data or NaN padding) must
+      // not reach P.V: zero this warp's invalid V rows
+      for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+        const int r = wrow + idx / (D / 8), u = idx % (D / 8);
+        if (r >= rows_here) {
+          *reinterpret_cast<uint4 *>(smem + (vt - s_base) + swz(r, u, kSub)) = make_uint4(0, 0, 0, 0);
+          zeroed = true;
+        }
+      }
+      __syncwarp();
+    }
+    // ---- S = Q K^T for this warp's 16 rows (two n-tiles of 8 keys)
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      // A (16 heads x 16 of D) from the stage's Q tile: ldmatrix lanes 0-15
+      // address rows 0-15 at a k-step's first 8 columns, lanes 16-31 the
+      // next 8; rows past the group are zero. B (K^T): lanes 0-7 keys 0-7
+      // unit 2ks; 8-15 keys 0-7 unit 2ks+1; 16-23 keys 8-15 unit 2ks;
+      // 24-31 keys 8-15 unit 2ks+1.
+      const uint32_t qt = kt + 2 * L::kTile;
+      const bool lo_ok = (lane >> 2) < Gh, hi_ok = (lane >> 2) + 8 < Gh;
+      const int key = wrow + (lane & 7) + ((lane >> 4) << 3);
+      const int uo = (lane >> 3) & 1;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t qa[4], b0, b1, b2, b3;
+        ldsm_x4(qt + swz(lane & 15, 2 * ks + (lane >> 4), kHeads), qa[0], qa[1], qa[2], qa[3]);
+        if (!lo_ok) qa[0] = qa[2] = 0u;
+        if (!hi_ok) qa[1] = qa[3] = 0u;
+        ldsm_x4(kt + swz(key, 2 * ks + uo, kSub), b0, b1, b2, b3);
+        mma_bf16(s0, qa, b0, b1);
+        mma_bf16(s1, qa, b2, b3);
+      }
+    }
+    // ---- online softmax on the fragments: rows (heads) lane/4 and lane/4+8
+    const int kc = wrow + 2 * (lane & 3);  // key of s?[0]; s?[1] is kc+1; s1 adds 8
+    float x[8] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2,
+                  s0[2] * sl2, s0[3] * sl2, s1[2] * sl2, s1[3] * sl2};
+    const int keys[4] = {kc, kc + 1, kc + 8, kc + 9};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (keys[e] >= rows_here) {
+        x[e] = -INFINITY;
+        x[4 + e] = -INFINITY;
+      }
+    }
+    float mx_lo = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    float mx_hi = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    // a warp whose 16 rows are all past the sequence sees mn = -inf: skip
+    const float a_lo = (mn_lo == -INFINITY) ? 1.f : ex2(m_lo - mn_lo);
+    const float a_hi = (mn_hi == -INFINITY) ? 1.f : ex2(m_hi - mn_hi);
+    float pr[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      pr[e] = (mn_lo == -INFINITY) ? 0.f : ex2(x[e] - mn_lo);
+      pr[4 + e] = (mn_hi == -INFINITY) ? 0.f : ex2(x[4 + e] - mn_hi);
+    }
+    l_lo = l_lo * a_lo + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    l_hi = l_hi * a_hi + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      acc[t][0] *= a_lo;
+      acc[t][1] *= a_lo;
+      acc[t][2] *= a_hi;
+      acc[t][3] *= a_hi;
+    }
+    // P as the A operand (16 heads x 16 keys): keys 0-7 from n-tile 0, 8-15 from n-tile 1
+    const uint32_t pa[4] = {pack_bf16x2(pr[0], pr[1]), pack_bf16x2(pr[4], pr[5]),
+                            pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[6], pr[7])};
+    // ---- O += P V (V rows = k, d = n): transposed ldmatrix of 8x8 blocks
+    {
+      // lanes 0-7: keys 0-7 unit u; 8-15: keys 8-15 unit u; 16-23: keys 0-7 unit u+1;
+      // 24-31: keys 8-15 unit u+1  -> {b0,b1} for d-tile u and {b0,b1} for u+1
+      const int key = wrow + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int uo = lane >> 4;
+#pragma unroll
+      for (int u = 0; u < NT; u += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vt + swz(key, u + uo, kSub), b0, b1, b2, b3);
+        mma_bf16(acc[u], pa, b0, b1);
+        mma_bf16(acc[u + 1], pa, b2, b3);
+      }
+    }
+
+    const bool final_run = (i == n_units - 1);
+    if (!final_run && s != nsub - 1) {
+      // release the stage to the producer (generic-proxy writes made visible
+      // to the TMA that will overwrite it)
+      if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + 8 * st);
+      continue;
+    }
+    // ---- the run ends here. Stage st stays held and serves as merge
+    // scratch; the other stages keep streaming the next units meanwhile.
+    const int plane_first = u0 + seg_first_i - seg_first_s;  // global unit of (plane, s = 0)
+    const int c_first = owner_of(plane_first, sp), c_last = owner_of(plane_first + nsub - 1, sp);
+    const bool split = c_first != c_last;
+    const int plane = b * planes_per_b + pib;
+    const int run_units = i - seg_first_i + 1;
+    const int e = ep_k & 1;
+    float *so = reinterpret_cast<float *>(smem + L::kOffEp + e * L::kEpBytes);  // epilogue slot
+    // full row sums of this warp: the four lanes of a quad hold different keys
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    if (warp == 0) {
+      if (split && !final_run && ep_k >= kEpSlots &&
+          !mbar_wait_warp(ep_empty + 8 * e, ((ep_k >> 1) & 1) ^ 1, nullptr) && lane == 0)
+        record_error(prm.err_word, kErrTimeout);
+      if (lane == 0 && split && final_run) {
+        // If every other run of the plane had counted in (their partials
+        // published before their count) when one of the early looks at the
+        // counter was made, this run is the last one and merges without
+        // publishing its own part.
+        const bool direct = max(counter_seen, counter_seen2) + run_units == nsub;
+        if (direct) fence_acq_rel_gpu();
+        info[4] = direct ? 1 : 0;
+      }
+    }
+    // each warp's (m, l, O) fragments to its own slot of the held stage
+    float *slots = reinterpret_cast<float *>(smem + st * L::kStage);
+    {
+      float *dst = slots + (warp * 32 + lane) * L::kLaneFloats;
+      mma_warps_sync();  // every warp is done reading stage st
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        *reinterpret_cast<float4 *>(dst + 4 * t) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+      *reinterpret_cast<float4 *>(dst + 4 * NT) = make_float4(m_lo, m_hi, l_lo, l_hi);
+      mma_warps_sync();
+    }
+    // merge the four warps' states for this thread's (head, 4 columns)
+    // items, warps in order: head h = 8 hi + r sits in the lanes 4 r + j,
+    // columns 8 t + 2 j + {0, 1} in accumulator t, components 2 hi + {0, 1}
+    float Mi[kPer], Li[kPer];
+    float4 Ai[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int it = tid + 32 * kMmaWarps * k, h = it / kQuads, q4 = it % kQuads;
+      const int hi = h >> 3, t = q4 >> 1, la = (h & 7) * 4 + (q4 & 1) * 2;
+      Mi[k] = -INFINITY;
+      Li[k] = 0.f;
+      Ai[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w) {
+        const float *sa = slots + (w * 32 + la) * L::kLaneFloats;
+        const float2 x = *reinterpret_cast<const float2 *>(sa + 4 * t + 2 * hi);
+        const float2 y = *reinterpret_cast<const float2 *>(sa + L::kLaneFloats + 4 * t + 2 * hi);
+        float wa, wb;
+        merge_row(Mi[k], Li[k], sa[4 * NT + hi], sa[4 * NT + 2 + hi], wa, wb);
+        Ai[k] = make_float4(fmaf(wa, Ai[k].x, wb * x.x), fmaf(wa, Ai[k].y, wb * x.y),
+                            fmaf(wa, Ai[k].z, wb * y.x), fmaf(wa, Ai[k].w, wb * y.y));
+      }
+    }
+    __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D;
+    if (!split) {
+      // this run is the whole plane: O = acc / l
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int it = tid + 32 * kMmaWarps * k, h = it / kQuads, q4 = it % kQuads;
+        if (h < Gh) {
+          const float il = 1.f / Li[k];
+          *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
+              make_uint2(pack_bf16x2(Ai[k].x * il, Ai[k].y * il), pack_bf16x2(Ai[k].z * il, Ai[k].w * il));
+        }
+      }
+    } else if (!final_run) {
+      // hand the state to the epilogue warp
+      float *sm = so + kHeads * L::kRow, *sl = sm + kHeads;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int it = tid + 32 * kMmaWarps * k, h = it / kQuads, q4 = it % kQuads;
+        *reinterpret_cast<float4 *>(so + h * L::kRow + 4 * q4) = Ai[k];
+        if (q4 == 0) {
+          sm[h] = Mi[k];
+          sl[h] = Li[k];
+        }
+      }
+      mma_warps_sync();
+      if (warp == 0 && lane == 0) {
+        int *em = reinterpret_cast<int *>(so + L::kStateFloats);
+        em[0] = kEpPartial;
+        em[1] = b;
+        em[2] = hq0;
+        em[3] = Gh;
+        em[4] = plane;
+        em[5] = c_first;
+        em[6] = c_last;
+        em[7] = run_units;
+        em[8] = nsub;
+        mbar_arrive(ep_full + 8 * e);
+      }
+      ++ep_k;
+    } else {
+      bool last = info[4] != 0;
+      if (!last) {
+        // publish the state to slot c + plane, then count the plane's units
+        // done: the run that completes the count merges (no CTA range is
+        // empty, so every owner takes part)
+        float *dst = prm.part + static_cast<size_t>(c + plane) * kSlot;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int it = tid + 32 * kMmaWarps * k, h = it / kQuads;
+          reinterpret_cast<float4 *>(dst)[it] = Ai[k];
+          if (it % kQuads == 0) {
+            dst[kHeads * D + h] = Mi[k];
+            dst[kHeads * D + kHeads + h] = Li[k];
+          }
+        }
+        fence_acq_rel_gpu();
+        mma_warps_sync();
+        if (tid == 0) {
+          const bool l0 = atomicAdd(prm.counters + plane, run_units) + run_units == nsub;
+          if (l0) fence_acq_rel_gpu();
+          info[4] = l0 ? 1 : 0;
+        }
+        mma_warps_sync();
+        last = info[4] != 0;
+      }
+      if (last) {
+        // ---- the plane's last run: merge the parts of CTAs c_first..c_last
+        // (CTA cs in slot cs + plane; this CTA's own part in registers)
+        fence_acq_rel_gpu();
+        auto self = [&](int k, int, float4 &v, float &m, float &l) {
+          v = Ai[k];
+          m = Mi[k];
+          l = Li[k];
+        };
+        merge_parts<D, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+                                c_last - c_first + 1, c - c_first, self, Gh, o_plane, tid,
+                                32 * kMmaWarps);
+        if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
+      }
+    }
+    // release the held stage (its generic-proxy writes ordered before the
+    // TMA that refills it)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + 8 * st);
+  }
+  // tell the epilogue warp that no more run states follow
+  if (warp == 0) {
+    const int e = ep_k & 1;
+    if (ep_k >= kEpSlots && !mbar_wait_warp(ep_empty + 8 * e, ((ep_k >> 1) & 1) ^ 1, nullptr)) {
+      if (lane == 0) record_error(prm.err_word, kErrTimeout);
+      return;
+    }
+    if (lane == 0) {
+      reinterpret_cast<int *>(smem + L::kOffEp + e * L::kEpBytes + L::kStateBytes)[0] = kEpStop;
+      mbar_arrive(ep_full + 8 * e);
+    }
+  }
+}
+
+template <int D, int NSTG>
+cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                            const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
+                            float *partials, int *counters, int B, int H_q, int H_kv, int max_len,
+                            float scale, int grid, int *err_word, cudaStream_t stream) {
   using L = DecodeSmem<D, NSTG>;
   static unsigned configured = 0;
   int dev = 0;
@@ -397,45 +825,62 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_k, const CUtensorMap &tm_v, co
   prm.part = partials;
   prm.counters = counters;
   prm.err_word = err_word;
+  prm.B = B;
   prm.H_q = H_q;
   prm.H_kv = H_kv;
   prm.max_len = max_len;
-  prm.chunk = chunk;
-  prm.n_splits = (max_len + chunk - 1) / chunk;
+  prm.nhg = decode_head_groups(H_q, H_kv);
   prm.scale_log2 = scale * 1.4426950408889634f;
-  dim3 grid(prm.n_splits, H_kv, B);
-  decode_kernel<D, NSTG><<<grid, kThreads, L::kAlloc, stream>>>(tm_k, tm_v, prm);
+  decode_kernel<D, NSTG><<<grid, kThreads, L::kAlloc, stream>>>(tm_q, tm_k, tm_v, prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t decode_partials_bytes(int B, int H_q, int max_len, int d, int chunk) {
-  const size_t n_splits = (static_cast<size_t>(max_len) + chunk - 1) / chunk;
-  return static_cast<size_t>(B) * H_q * n_splits * (static_cast<size_t>(d) + 2) * sizeof(float);
+int decode_head_groups(int H_q, int H_kv) { return (H_q / H_kv + kHeads - 1) / kHeads; }
+
+size_t decode_partials_bytes(int B, int H_q, int H_kv, int d, int grid) {
+  const size_t planes = static_cast<size_t>(B) * H_kv * decode_head_groups(H_q, H_kv);
+  return (static_cast<size_t>(grid) + planes) * kHeads * (static_cast<size_t>(d) + 2) * sizeof(float);
 }
 
-int decode_default_chunk(int B, int H_kv, int max_len, int num_sms) {
-  // Longest split (fewest partials to merge) that still offers about four
-  // CTAs per SM when every sequence is full length.
-  for (int c : {512, 256, 128}) {
-    const long ctas = static_cast<long>(B) * H_kv * ((max_len + c - 1) / c);
-    if (ctas >= 4L * num_sms) return c;
+size_t decode_planes(int B, int H_q, int H_kv) {
+  return static_cast<size_t>(B) * H_kv * decode_head_groups(H_q, H_kv);
+}
+
+bool decode_units_fit(int B, int H_q, int H_kv, int max_len) {
+  const long long units = static_cast<long long>(decode_planes(B, H_q, H_kv)) *
+                          ((static_cast<long long>(max_len) + kSub - 1) / kSub);
+  return units <= (1ll << 30);
+}
+
+int decode_grid(int B, int H_q, int H_kv, int max_len, int d, int num_sms, int chunk) {
+  (void)d;
+  // Rows of all planes if every sequence were full length; the real count is
+  // known on the device only, so this is an upper bound.
+  const long long rows = static_cast<long long>(decode_planes(B, H_q, H_kv)) * max_len;
+  long long g;
+  if (chunk > 0) {
+    g = (rows + chunk - 1) / chunk;
+  } else {
+    g = static_cast<long long>(num_sms) * kCtasPerSm;
   }
-  return 64;
+  if (g > 65535) g = 65535;
+  return g < 1 ? 1 : static_cast<int>(g);
 }
 
-cudaError_t launch_decode_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
-                               const int *seqlens, void *o, float *partials, int *counters, int B,
-                               int H_q, int H_kv, int max_len, int d, float scale, int chunk,
-                               int *err_word, cudaStream_t stream) {
-  if (chunk % kSub != 0 || chunk <= 0) return cudaErrorInvalidValue;
+cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                               const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
+                               float *partials, int *counters, int B, int H_q, int H_kv,
+                               int max_len, int d, float scale, int grid, int *err_word,
+                               cudaStream_t stream) {
+  if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
   if (d == 64)
-    return launch_decode_d<64, 4>(tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q, H_kv,
-                                  max_len, scale, chunk, err_word, stream);
+    return launch_decode_d<64, 8>(tm_q, tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q,
+                                  H_kv, max_len, scale, grid, err_word, stream);
   if (d == 128)
-    return launch_decode_d<128, 3>(tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q, H_kv,
-                                   max_len, scale, chunk, err_word, stream);
+    return launch_decode_d<128, 5>(tm_q, tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q,
+                                   H_kv, max_len, scale, grid, err_word, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -409,6 +409,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Acquire-release fence at GPU scope. Before a relaxed atomic it publishes
+// this thread's earlier writes to whoever observes the atomic; after a read
+// that observed such an atomic it makes those writes visible to later reads.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Relaxed load at GPU scope (not cached in L1): a value another CTA wrote
+// with an atomic; pair it with a fence before reading data it guards.
+__device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Load with acquire semantics at GPU scope: later reads see whatever the
+// writer published before its matching release (or fence + atomic).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void record_error(int *err_word, int bits) {
   if (err_word != nullptr) atomicOr(err_word, bits);
 }

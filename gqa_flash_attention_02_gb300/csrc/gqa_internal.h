@@ -127,15 +127,28 @@ cudaError_t launch_attn_f32(const float *q, const float *k, const float *v, floa
                             const int *seqlens, int kv_row_capacity, int *err_word,
                             cudaStream_t stream);
 
-// Decode split-KV: `chunk` cache rows per split (the TMA box is 64 rows).
-size_t decode_partials_bytes(int B, int H_q, int max_len, int d, int chunk);
-int decode_default_chunk(int B, int H_kv, int max_len, int num_sms);
-constexpr int kDecodeChunkUnit = 64;   // split sizes are multiples of this
-constexpr int kDecodeChunkMax = 2048;
-cudaError_t launch_decode_bf16(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const void *q,
-                               const int *seqlens, void *o, float *partials, int *counters, int B,
-                               int H_q, int H_kv, int max_len, int d, float scale, int chunk,
-                               int *err_word, cudaStream_t stream);
+// Decode: the valid cache rows are cut into 64-row units (one TMA box) and
+// balanced over a persistent grid; a CTA's run over part of a (b, h_kv,
+// head group) plane leaves a partial result merged in the same launch.
+constexpr int kDecodeChunkUnit = 64;    // rows per unit (the TMA box height)
+constexpr int kDecodeHeads = 16;        // query heads per plane (the Q box height)
+constexpr int kDecodeChunkMax = 2048;   // largest rows-per-CTA sizing hint
+int decode_head_groups(int H_q, int H_kv);                     // query heads per K/V head / 16, rounded up
+size_t decode_planes(int B, int H_q, int H_kv);                // merge counters needed
+size_t decode_partials_bytes(int B, int H_q, int H_kv, int d, int grid);
+// CTAs to launch: `chunk` > 0 sizes the grid as (upper bound of rows) / chunk;
+// 0 gives one wave of resident CTAs.
+int decode_grid(int B, int H_q, int H_kv, int max_len, int d, int num_sms, int chunk);
+// False when the unit count of the largest case would not fit the kernel's
+// 32-bit unit indices.
+bool decode_units_fit(int B, int H_q, int H_kv, int max_len);
+// tm_q views q as [1][B * H_q][d] with 16-row boxes; tm_k / tm_v view the
+// caches as [B * H_kv][max_len][d] with 64-row boxes.
+cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                               const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
+                               float *partials, int *counters, int B, int H_q, int H_kv,
+                               int max_len, int d, float scale, int grid, int *err_word,
+                               cudaStream_t stream);
 
 cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStream_t stream);
 

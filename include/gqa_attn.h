@@ -85,8 +85,9 @@ int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o,
                      int causal, float scale, cudaStream_t stream);
 
 /*
- * Single-token decode against a bf16 K/V cache, split-KV with a log-sum-exp
- * combine; bf16 output, fp32 math.
+ * Single-token decode against a bf16 K/V cache: persistent split-KV with the
+ * log-sum-exp merge of the splits in the same launch; bf16 output, fp32
+ * math.
  *   q       : [B][H_q][d] bf16         o : [B][H_q][d] bf16 (written)
  *   k_cache, v_cache : [B][H_kv][max_len][d] bf16; rows [0, seqlens[b]) are
  *             valid, later rows are never read into the result
@@ -105,10 +106,13 @@ int gqa_attn_decode(const void *q, const void *k_cache, const void *v_cache,
                     float scale, cudaStream_t stream);
 
 /*
- * gqa_attn_decode with an explicit split size: each split covers
- * `chunk_tokens` cache rows (a multiple of 64 in [64, 2048]); 0 picks the
- * library's default for the shape. The result is the same operation for
- * every chunk size, up to fp32 rounding. Other values: GQA_ERR_INVALID_ARG.
+ * gqa_attn_decode with an explicit work split. The valid cache rows are
+ * cut into 64-row units and balanced over a grid of CTAs; `chunk_tokens`
+ * (a multiple of 64 in [64, 2048]) sizes that grid as
+ * ceil(B * H_kv * ceil(g / 16) * max_len / chunk_tokens) CTAs, g = H_q / H_kv,
+ * so smaller values split each sequence into more partial results. 0 picks
+ * one wave of resident CTAs (the default). The result is the same operation
+ * for every value, up to fp32 rounding. Other values: GQA_ERR_INVALID_ARG.
  */
 int gqa_attn_decode_chunked(const void *q, const void *k_cache,
                             const void *v_cache, const int *seqlens, void *o,
@@ -136,10 +140,9 @@ int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
  * library's own device memory, present on every GPU that loads the library
  * until the process exits.
  *   - Arguments, layouts and results as gqa_attn_decode (same kernel), with
- *     the split size chosen so the partials fit: B * H_q * ceil(max_len /
- *     split) * (d + 2) * 4 bytes <= 4 MiB with splits of up to 2048 rows,
- *     and B * H_kv <= 16384. Larger problems return GQA_ERR_UNSUPPORTED (use
- *     gqa_attn_decode).
+ *     the grid trimmed so the partials fit: (grid + P) * 16 * (d + 2) * 4
+ *     bytes <= 4 MiB, where P = B * H_kv * ceil(H_q / H_kv / 16) <= 16384.
+ *     Larger problems return GQA_ERR_UNSUPPORTED (use gqa_attn_decode).
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.

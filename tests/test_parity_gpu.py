@@ -200,6 +200,37 @@ def test_bf16_decode_split_invariance(chunk, d):
     _check_bf16(got, ref, f"chunk {chunk} d {d}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_decode_plane_split_over_many_ctas(d):
+    """One long sequence cut into 64-row splits: each (K/V head, head group)
+    spreads over ~150 CTAs, so the log-sum-exp merge takes its parts in
+    several chunks. Also a 40-part case next to short sequences."""
+    seqlens, q, kc, vc = inputs.decode_inputs(1, 8, 1, 40000, d, torch.bfloat16, seed=95 + d,
+                                              seqlens=[40000])
+    ref, _ = oracle.decode(q, kc, vc, seqlens, d ** -0.5)
+    got = _decode_run(seqlens, q, kc, vc, d ** -0.5, 64)
+    assert ops.gqa_attn_get_device_error() == 0
+    _check_bf16(got, ref, f"one long sequence d {d}")
+    seqlens, q, kc, vc = inputs.decode_inputs(3, 20, 2, 10240, d, torch.bfloat16, seed=97 + d,
+                                              seqlens=[10240, 3, 9000])
+    ref, _ = oracle.decode(q, kc, vc, seqlens, d ** -0.5)
+    got = _decode_run(seqlens, q, kc, vc, d ** -0.5, 64)
+    _check_bf16(got, ref, f"long and short sequences d {d}")
+
+
+@pytest.mark.parametrize("B", [200, 1100])
+def test_bf16_decode_large_batch(B):
+    """More sequences than one warp pass of the start search (128) and than
+    the lengths kept in shared memory (1024); some sequences are empty."""
+    seqlens, q, kc, vc = inputs.decode_inputs(B, 4, 1, 96, 64, torch.bfloat16, seed=99 + B)
+    seqlens[::7] = 0
+    got = _decode_run(seqlens, q, kc, vc, 0.125)
+    assert ops.gqa_attn_get_device_error() == 0
+    assert np.all(got[::7] == 0)
+    ref, _ = oracle.decode(q, kc, vc, seqlens, 0.125)
+    _check_bf16(got, ref, f"B={B}")
+
+
 def test_bf16_decode_edge_lengths():
     seqlens, q, kc, vc = inputs.decode_inputs(4, 16, 1, 512, 128, torch.bfloat16, seed=81,
                                               seqlens=[0, 512, 1, 2])
