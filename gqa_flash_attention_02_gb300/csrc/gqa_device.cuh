@@ -106,6 +106,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // mbar_wait executed by a whole warp, with a warp-uniform result: the lanes
 // reconverge here and either all proceed or all take the failure path, so a
 // warp-collective instruction (elect.sync, tcgen05.ld/st) after it is safe
@@ -114,6 +127,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
                                                const volatile int *abort_flag,
                                                uint64_t limit_ns = kWaitLimitNs) {
   const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// mbar_wait_warp for waits on a pipeline's critical path whose phase is
+// expected within a few hundred cycles: polls without suspending first (a
+// suspended thread wakes up noticeably later than the phase completes),
+// then falls back to the bounded, suspending wait.
+__device__ __forceinline__ bool mbar_wait_warp_spin(uint32_t bar, uint32_t parity,
+                                                    const volatile int *abort_flag) {
+  bool ok = false;
+  for (int k = 0; k < 256 && !ok; ++k) ok = mbar_test_wait(bar, parity);
+  if (!ok) ok = mbar_wait(bar, parity, abort_flag);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -422,6 +447,13 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// 32-byte global store (one full sector); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *r) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 
 // Load with acquire semantics at GPU scope: later reads see whatever the

@@ -60,16 +60,6 @@ static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsLow >= 24 && kRegs
               "setmaxnreg counts must be multiples of 8 in [24, 256]");
 constexpr int kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows > 2^8
-#ifndef GQA_EMU_PAIRS
-#define GQA_EMU_PAIRS 0
-#endif
-// Of every 8 column pairs of a row, this many take the FMA-pipe 2^x and the
-// rest the special-function unit. On GB300 ex2 issues at 32 lanes/clock per
-// SM, so the softmax warp is bound by instruction issue rather than by the
-// special-function unit; the polynomial (about six issue slots per pair
-// instead of two) then only adds work, and the default is 0.
-constexpr int kEmuPairs = GQA_EMU_PAIRS;
-
 template <int D>
 struct TcLayout {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
@@ -79,10 +69,12 @@ struct TcLayout {
   static constexpr int kOffKV = 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   // barrier indices
+  // P arrives in two halves: kPFull for keys 0-63 of a block, kPFullB for 64-127
+  // (at D = 64 only kPFullB is used, for the whole block)
   static constexpr int kQFull = 0, kQEmpty = 2, kSFull = 4, kPFull = 6, kOFull = 8,
                        kOEmpty = 10, kSchedFull = 12, kSchedEmpty = 14, kDrain = 16,
-                       kKVFull = 17, kKVEmpty = 17 + kStages;
-  static constexpr int kNumBars = 17 + 2 * kStages;
+                       kPFullB = 17, kKVFull = 19, kKVEmpty = 19 + kStages;
+  static constexpr int kNumBars = 19 + 2 * kStages;
   static constexpr int kOffSched = kOffBar + kNumBars * 8;
   static constexpr int kOffTmem = kOffSched + 8;
   static constexpr int kOffAbort = kOffTmem + 4;
@@ -92,6 +84,7 @@ struct TcLayout {
 
 struct TcParams {
   __nv_bfloat16 *o;
+  int o_align32;  // o is 32-byte aligned (rows are then too: D * 2 bytes each)
   PrefillPlan plan;
   float scale_log2;
   int *ctl;
@@ -102,6 +95,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
   using L = TcLayout<D>;
+  // At D = 128 the P of a block is handed over in two halves, so the PV over
+  // the first 64 keys overlaps the exponentials of the other 64; at D = 64
+  // the PV is short and the extra hand-over costs more than it hides.
+  constexpr bool kSplitP = D == 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -122,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       mbar_init(bar(L::kQEmpty + t), 1);
       mbar_init(bar(L::kSFull + t), 1);
       mbar_init(bar(L::kPFull + t), 128);
+      mbar_init(bar(L::kPFullB + t), 128);
       mbar_init(bar(L::kOFull + t), 1);
       mbar_init(bar(L::kOEmpty + t), 128);
       mbar_init(bar(L::kSchedFull + t), 1);
@@ -247,15 +245,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       }
       __syncwarp();
     };
-    auto issue_pv = [&](int t, int st, bool accumulate) {
+    // O_t += P_t V over keys [64 half, 64 half + 64) of the block
+    auto issue_pv = [&](int t, int st, bool accumulate, int half) {
       const uint32_t b_lo = v_lo0 + static_cast<uint32_t>(st * L::kTileBytes >> 4);
       const uint32_t d = tmem + 256u + D * t;
       const uint32_t a = tmem + 128u * t + 64u;
       if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)  // 16 key rows (2048 B) per K-step
+        for (int k4 = 0; k4 < kTileN / 32; ++k4) {  // 16 key rows (2048 B) per K-step
+          const int kk = half * (kTileN / 32) + k4;
           mma_ts_w(d, a + kk * 8, b_lo + kk * 128, kDescHi, idesc_pv,
                    (accumulate || kk > 0) ? 1u : 0u);
+        }
       }
       __syncwarp();
     };
@@ -269,16 +270,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       ++kv_it;
       return mbar_wait_warp(bar(L::kKVFull + st), ph, abort_flag);
     };
-    // PV for tile t over block jb (all checks on the caller's side).
+    // PV for tile t over block jb (all checks on the caller's side): the
+    // first half of the keys as soon as their P is in tensor memory, the
+    // second half while nothing else waits.
     auto do_pv = [&](int t, int jb, int st) -> bool {
       const int vc = t ? vc1 : vc0;
       uint32_t &pc = t ? pc1 : pc0;
       if (jb == 0 && !mbar_wait_warp(bar(L::kOEmpty + t), (vc & 1) ^ 1, abort_flag)) return false;
-      if (!mbar_wait_warp(bar(L::kPFull + t), pc & 1, abort_flag)) return false;
+      if (kSplitP) {
+        if (!mbar_wait_warp(bar(L::kPFull + t), pc & 1, abort_flag)) return false;
+        tc_fence_after_sync();
+        issue_pv(t, st, jb > 0, 0);
+      }
+      if (!mbar_wait_warp(bar(L::kPFullB + t), pc & 1, abort_flag)) return false;
       ++pc;
-      __syncwarp();
       tc_fence_after_sync();
-      issue_pv(t, st, jb > 0);
+      if (!kSplitP) issue_pv(t, st, jb > 0, 0);
+      issue_pv(t, st, true, 1);
       return true;
     };
 
@@ -399,34 +407,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
         }
-        // P = 2^(S * scale*log2e - m) for pairs of columns with packed fp32
-        // ops, stored to tensor memory as bf16 pairs; returns the row sum.
-        // kEmuPairs of every 8 pairs use the FMA-pipe 2^x, the rest ex2.
-        auto make_p = [&](float m) -> float {
+        // P = 2^(S * scale*log2e - m) for the 64 columns of half h, with
+        // packed fp32 ops, stored to tensor memory as bf16 pairs; returns the
+        // half's row sum. (P of half 0 overwrites S columns 64-95, which are
+        // already in registers.)
+        auto make_half = [&](int h, float m) -> float {
           const float2 sl2v = make_float2(sl2, sl2);
           const float2 negm = make_float2(-m, -m);
           float2 lsum[4];  // four partial sums: no long dependency chain
 #pragma unroll
           for (int i = 0; i < 4; ++i) lsum[i] = make_float2(0.f, 0.f);
+          uint32_t pk[32];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float2 x =
-                  ffma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2v, negm);
-              float2 p;
-              if ((c & 7) < kEmuPairs) {
-                p = exp2_poly2(x);
-              } else {
-                p.x = ex2(x.x);
-                p.y = ex2(x.y);
-              }
-              lsum[c & 3] = fadd2(lsum[c & 3], p);
-              pk[c] = pack_bf16x2(p.x, p.y);
-            }
-            tmem_st32(tm_p + h * 32u, pk);
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = ffma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2v, negm);
+            float2 p;
+            p.x = ex2(x.x);
+            p.y = ex2(x.y);
+            lsum[c & 3] = fadd2(lsum[c & 3], p);
+            pk[c] = pack_bf16x2(p.x, p.y);
           }
+          tmem_st32(tm_p + h * 32u, pk);
           const float2 a = fadd2(lsum[0], lsum[1]), b = fadd2(lsum[2], lsum[3]);
           return (a.x + b.x) + (a.y + b.y);
         };
@@ -443,30 +444,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
           return fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), mx[6]), mx[7]) *
                  sl2;
         };
-        float alpha = 1.f, row_sum;
-        bool raise;
+        // halves computed before the row maximum is known: the first one
+        // when P is handed over in halves, else both
+        constexpr int kEarly = kSplitP ? 1 : 2;
+        float alpha = 1.f, sum = 0.f;
         if (j == 0) {
           m_ref = row_max();  // first block: its O is overwritten, nothing to rescale
           alpha = 0.f;
-          raise = false;
-          row_sum = make_p(m_ref);
+#pragma unroll
+          for (int h = 0; h < kEarly; ++h) sum += make_half(h, m_ref);
         } else {
           // Speculate that the reference maximum still holds (it only moves
           // when the row maximum grows by more than 2^8): the exponentials
-          // do not wait for the block maximum, which is computed alongside.
-          row_sum = make_p(m_ref);
+          // do not wait for the block maximum.
+#pragma unroll
+          for (int h = 0; h < kEarly; ++h) sum += make_half(h, m_ref);
           const float m_blk = row_max();
-          raise = m_blk > m_ref + kRescaleThreshold;
+          const bool raise = m_blk > m_ref + kRescaleThreshold;
           if (__any_sync(0xffffffffu, raise)) {
-            // rare: some row's maximum jumped; redo this warp's P with the
-            // raised maxima (rows that did not jump keep theirs, alpha = 1)
+            // rare: some row's maximum jumped; redo this warp's early halves
+            // with the raised maxima (rows that did not jump keep theirs,
+            // alpha = 1) and rescale O before any of this block's PV. O_t
+            // was last written by the PV of block j-1, which completed
+            // before S_t[j] was committed.
             if (raise) {
               alpha = ex2(m_ref - m_blk);
               m_ref = m_blk;
             }
-            row_sum = make_p(m_ref);
-            // O_t was last written by the PV of block j-1, which completed
-            // before S_t[j] was committed.
+            tmem_st_wait();
+            sum = 0.f;
+#pragma unroll
+            for (int h = 0; h < kEarly; ++h) sum += make_half(h, m_ref);
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
               uint32_t ov[32];
@@ -477,10 +485,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             }
           }
         }
+        if (kSplitP) {
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(bar(L::kPFull + t));  // PV over keys 0-63 may start
+          sum += make_half(1, m_ref);
+        }
         tmem_st_wait();
-        l_sum = l_sum * alpha + row_sum;
+        l_sum = l_sum * alpha + sum;
         tc_fence_before_sync();
-        mbar_arrive(bar(L::kPFull + t));
+        mbar_arrive(bar(L::kPFullB + t));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16 -> global
@@ -492,25 +506,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       __nv_bfloat16 *dst =
           prm.o + ((static_cast<size_t>(w.b) * plan.H_q + mine.h_q) * plan.N_q + q_row) * D;
       const bool store = q_row < plan.N_q;
+      // the whole row of O in one tensor-memory load; O_t is then free for
+      // the next unit's PV while the row is converted and stored
+      uint32_t ov[D];
+      __syncwarp();
+      if constexpr (D == 128)
+        tmem_ld128_wait(tm_o, ov);
+      else
+        tmem_ld64_wait(tm_o, ov);
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kOEmpty + t));
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ov[32];
-        __syncwarp();
-        tmem_ld32_wait(tm_o + c0, ov);
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          pk[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv_l,
-                              __uint_as_float(ov[2 * c + 1]) * inv_l);
+          pk[c] = pack_bf16x2(__uint_as_float(ov[c0 + 2 * c]) * inv_l,
+                              __uint_as_float(ov[c0 + 2 * c + 1]) * inv_l);
         if (store) {
-          uint4 *g = reinterpret_cast<uint4 *>(dst + c0);
+          // a lane writes its own row: whole 32-byte sectors when O allows
+          if (prm.o_align32) {
+            st_global_v8(dst + c0, pk);
+            st_global_v8(dst + c0 + 16, pk + 8);
+          } else {
+            uint4 *g = reinterpret_cast<uint4 *>(dst + c0);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            g[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            for (int v4 = 0; v4 < 4; ++v4)
+              g[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
         }
       }
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kOEmpty + t));
     }
     if (!ok) fail();
   }
@@ -556,6 +581,7 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
   }
   TcParams prm;
   prm.o = static_cast<__nv_bfloat16 *>(o);
+  prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   prm.plan = plan;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.ctl = ctl;

@@ -159,6 +159,24 @@ def test_bf16_prefill_deterministic():
     assert torch.equal(o1, o2)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_prefill_output_only_16_byte_aligned(d):
+    """O at a 16- but not 32-byte aligned address takes the 16-byte store
+    path and gives the same bits as an aligned O."""
+    q, k, v = inputs.prefill_inputs(1, 4, 2, 320, 320, d, torch.bfloat16, seed=77 + d)
+    qd, kd, vd = _dev(q, k, v)
+    o_al = ops.gqa_attn_fwd(qd, kd, vd, causal=True, scale=d ** -0.5)
+    flat = torch.full((qd.numel() + 8,), float("nan"), dtype=torch.bfloat16, device=qd.device)
+    o_off = flat[8:].view(qd.shape)  # 16 bytes past a 256-byte aligned allocation
+    assert o_off.data_ptr() % 32 == 16
+    ops.gqa_attn_fwd(qd, kd, vd, o_off, causal=True, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    assert torch.equal(o_al, o_off)
+    ref, _ = oracle.prefill(q, k, v, True, d ** -0.5)
+    _check_bf16(o_off.float().cpu().numpy(), ref, f"16-byte aligned O, d {d}")
+
+
 def test_bf16_prefill_repeated_launches_rearm_scheduler():
     """The work counter re-arms itself: many back-to-back launches stay correct."""
     q, k, v = inputs.prefill_inputs(1, 4, 2, 300, 300, 64, torch.bfloat16, seed=61)
