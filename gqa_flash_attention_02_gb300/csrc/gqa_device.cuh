@@ -106,19 +106,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
-// Non-blocking probe of a phase (never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // mbar_wait executed by a whole warp, with a warp-uniform result: the lanes
 // reconverge here and either all proceed or all take the failure path, so a
 // warp-collective instruction (elect.sync, tcgen05.ld/st) after it is safe
@@ -127,18 +114,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
                                                const volatile int *abort_flag,
                                                uint64_t limit_ns = kWaitLimitNs) {
   const bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// mbar_wait_warp for waits on a pipeline's critical path whose phase is
-// expected within a few hundred cycles: polls without suspending first (a
-// suspended thread wakes up noticeably later than the phase completes),
-// then falls back to the bounded, suspending wait.
-__device__ __forceinline__ bool mbar_wait_warp_spin(uint32_t bar, uint32_t parity,
-                                                    const volatile int *abort_flag) {
-  bool ok = false;
-  for (int k = 0; k < 256 && !ok; ++k) ok = mbar_test_wait(bar, parity);
-  if (!ok) ok = mbar_wait(bar, parity, abort_flag);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -377,56 +352,11 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   return d;
 }
 
-// a + b rounded toward -infinity.
-__device__ __forceinline__ float2 fadd2_rm(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rm.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-
-__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-
 // max of three (sm_100+ three-input max).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
-}
-
-// Software 2^x for a pair, on the FMA pipe instead of the special-function
-// unit. Cody-Waite range reduction (Cody & Waite, "Software Manual for the
-// Elementary Functions", 1980): 2^x = 2^j * 2^f, j = floor(x), f in [0,1);
-// 2^f by a cubic with p(0) = 1, p(1) = 2 whose two free coefficients were
-// fitted for minimum maximum relative error (fit_exp2_poly.py beside this
-// file: 1.03e-4). j is obtained by adding 1.5 * 2^23 with rounding toward
-// -infinity (the sum's low mantissa bits then hold j) and is moved into the
-// exponent field with one shift-add. Inputs are clamped to >= -127; there
-// the result is below 2^-126, i.e. a negligible softmax weight.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  constexpr float kC1 = 0.69542414f, kC2 = 0.2263078f, kC3 = 0.07826809f;
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -127.0f);
-  x.y = fmaxf(x.y, -127.0f);
-  const float2 t = fadd2_rm(x, make_float2(kShift, kShift));
-  const float2 f = fsub2(x, fsub2(t, make_float2(kShift, kShift)));
-  float2 p = ffma2(f, make_float2(kC3, kC3), make_float2(kC2, kC2));
-  p = ffma2(p, f, make_float2(kC1, kC1));
-  p = ffma2(p, f, make_float2(1.0f, 1.0f));
-  // bits(t) << 23 == j << 23 (mod 2^32): the shift's high bits fall off
-  return make_float2(__uint_as_float((__float_as_uint(t.x) << 23) + __float_as_uint(p.x)),
-                     __uint_as_float((__float_as_uint(t.y) << 23) + __float_as_uint(p.y)));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

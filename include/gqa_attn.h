@@ -95,7 +95,9 @@ int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o,
  *             length 0 yields O = 0. Out-of-range values make the call
  *             record GQA_ERR_BAD_SEQLEN (read with gqa_attn_get_device_error)
  *             and leave that sequence's output at 0.
- *   d in {64, 128}; max_len <= 1 << 20.
+ *   d in {64, 128}; max_len <= 1 << 20; at most 2^30 row units
+ *   (B * H_kv * ceil(H_q / H_kv / 16) * ceil(max_len / 64)), else
+ *   GQA_ERR_UNSUPPORTED.
  * Pages: microLLM-rocm optimisation log, Experiments 064-065 (batched cached
  * GQA decode, bf16 cache with fp32 accumulation) and 282-284 (split-sequence
  * cached attention).
