@@ -59,7 +59,10 @@ static_assert(kRegsLow + 2 * kRegsHigh <= 3 * kLaunchRegs,
 static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsLow >= 24 && kRegsHigh <= 256,
               "setmaxnreg counts must be multiples of 8 in [24, 256]");
 constexpr int kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows > 2^8
+constexpr float kRescaleThreshold = 8.0f;
+#ifndef GQA_EX2_BF16
+#define GQA_EX2_BF16 1
+#endif  // log2 units: rescale O when the max grows > 2^8
 template <int D>
 struct TcLayout {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
@@ -99,6 +102,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
   // the first 64 keys overlaps the exponentials of the other 64; at D = 64
   // the PV is short and the extra hand-over costs more than it hides.
   constexpr bool kSplitP = D == 128;
+  // At D = 128 the softmax bounds the block rate and P's exponentials run
+  // two per special-function instruction on bf16 pairs (the exponent rounded
+  // to bf16: the error against the float64 oracle grows from about 1.2e-4 to
+  // 1.7e-4 mean and 7.7e-3 to 9.3e-3 max, well inside the bf16 bounds); at
+  // D = 64 that measured slower, so fp32 ex2 stays.
+  constexpr bool kEx2Bf16 = D == 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -422,10 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
           for (int c = 0; c < 32; ++c) {
             const float2 x = ffma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2v, negm);
             float2 p;
-            p.x = ex2(x.x);
-            p.y = ex2(x.y);
+            if constexpr (kEx2Bf16) {
+              // two exponentials per special-function instruction, already
+              // in P's bf16 pair format; the exponent is rounded to bf16
+              pk[c] = ex2_bf16x2(pack_bf16x2(x.x, x.y));
+              p = make_float2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u));
+            } else {
+              p.x = ex2(x.x);
+              p.y = ex2(x.y);
+              pk[c] = pack_bf16x2(p.x, p.y);
+            }
             lsum[c & 3] = fadd2(lsum[c & 3], p);
-            pk[c] = pack_bf16x2(p.x, p.y);
           }
           tmem_st32(tm_p + h * 32u, pk);
           const float2 a = fadd2(lsum[0], lsum[1]), b = fadd2(lsum[2], lsum[3]);
