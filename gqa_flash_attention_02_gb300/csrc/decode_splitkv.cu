@@ -286,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  // Global reads (inputs, partials, counters) come after the previous grid
+  // of the stream has completed; the next grid may start setting up.
+  grid_dependency_wait();
+  grid_launch_dependents();
   // ---- warp 0: lengths (128 per pass, loads in flight together, the first
   // kLenCache kept in shared memory), total units and this CTA's start
   if (warp == 0) {
@@ -831,8 +835,8 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   prm.max_len = max_len;
   prm.nhg = decode_head_groups(H_q, H_kv);
   prm.scale_log2 = scale * 1.4426950408889634f;
-  decode_kernel<D, NSTG><<<grid, kThreads, L::kAlloc, stream>>>(tm_q, tm_k, tm_v, prm);
-  return cudaGetLastError();
+  return launch_programmatic(decode_kernel<D, NSTG>, grid, kThreads, L::kAlloc, stream, tm_q, tm_k,
+                             tm_v, prm);
 }
 
 }  // namespace

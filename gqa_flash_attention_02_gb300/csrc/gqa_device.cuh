@@ -117,6 +117,22 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may start while the previous grid of its stream is still
+// finishing: grid_dependency_wait() blocks until that grid has completed and
+// its writes are visible (it returns at once for a launch without such a
+// dependency), and must precede every global read of data that earlier work
+// in the stream may have written. grid_launch_dependents() lets the next
+// grid in the stream start its own set-up as SMs free up; it only ever runs
+// up to its own grid_dependency_wait() before this grid completes.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {

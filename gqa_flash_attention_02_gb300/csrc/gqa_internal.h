@@ -11,7 +11,35 @@
 #define GQA_HD inline
 #endif
 
+#ifdef __CUDACC__
+#include <cuda_runtime.h>
+
+#include <utility>
+#endif
+
 namespace gqa {
+
+#ifdef __CUDACC__
+// Launches `kernel` with programmatic stream serialisation: it may begin
+// while the previous grid of the stream is finishing. The kernels launched
+// this way call grid_dependency_wait() before reading anything earlier work
+// may have written, so stream order is kept.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                                cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#endif
 
 // Bits of the device error word kept in each workspace.
 constexpr int kErrTimeout = 1 << 0;

@@ -155,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // Everything above only set up this CTA. Global reads (inputs, the work
+  // counter) come after the previous grid of the stream has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   auto fail = [&]() {
     *abort_flag = 1;
@@ -602,8 +606,8 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.ctl = ctl;
   const int grid = min(num_sms, plan.total_units);
-  prefill_tc_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(tm_q, tm_k, tm_v, prm);
-  return cudaGetLastError();
+  return launch_programmatic(prefill_tc_kernel<D>, grid, kThreads, L::kAlloc, stream, tm_q, tm_k,
+                             tm_v, prm);
 }
 
 }  // namespace

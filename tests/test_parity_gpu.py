@@ -291,6 +291,35 @@ def test_bf16_decode_deterministic():
     assert np.array_equal(a, b)
 
 
+# ------------------------------------------------------------------ launch order
+
+def test_dependent_launches_back_to_back():
+    """Kernels may start while the previous grid of the stream finishes
+    (programmatic launch); one that reads the previous kernel's output, queued
+    right behind it with no synchronisation, must still see all of it."""
+    q, k, v = _dev(*inputs.prefill_inputs(1, 8, 2, 640, 640, 128, torch.bfloat16, seed=111))
+    o1 = ops.gqa_attn_fwd(q, k, v, causal=True, scale=0.09)
+    o2 = ops.gqa_attn_fwd(o1, k, v, causal=True, scale=0.09)   # reads o1 at once
+    torch.cuda.synchronize()
+    r1 = ops.gqa_attn_fwd(q, k, v, causal=True, scale=0.09)
+    torch.cuda.synchronize()
+    r2 = ops.gqa_attn_fwd(r1, k, v, causal=True, scale=0.09)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, r2)
+
+    seqlens, dq, kc, vc = _dev(*inputs.decode_inputs(16, 12, 2, 1024, 128, torch.bfloat16, seed=112))
+    a = dq * 1.0                                                  # a PyTorch kernel writes the query
+    d1 = ops.gqa_attn_decode(a, kc, vc, seqlens, scale=0.09)
+    d2 = ops.gqa_attn_decode(d1, kc, vc, seqlens, scale=0.09)     # reads d1 at once
+    torch.cuda.synchronize()
+    e1 = ops.gqa_attn_decode(dq, kc, vc, seqlens, scale=0.09)
+    torch.cuda.synchronize()
+    e2 = ops.gqa_attn_decode(e1, kc, vc, seqlens, scale=0.09)
+    torch.cuda.synchronize()
+    assert torch.equal(d1, e1) and torch.equal(d2, e2)
+    assert ops.gqa_attn_get_device_error() == 0
+
+
 # ------------------------------------------------------------------ failure detection
 
 def test_bounded_wait_reports_timeout_and_context_survives():
