@@ -101,11 +101,13 @@ struct DecodeSmem {
   static constexpr int kRow = D + 4;  // padded: fragment stores spread over banks
   static constexpr int kStateFloats = kHeads * kRow + 2 * kHeads;
   static constexpr int kStateBytes = kStateFloats * 4;
-  // At a run end the four MMA warps leave their (m, l, O) fragments in the
-  // stage of the run's last unit (released only afterwards): 4 warps x 32
-  // lanes x (D/8 * 4 accumulators + m_lo, m_hi, l_lo, l_hi).
+  // At a run end the four MMA warps merge their (m, l, O) fragments through
+  // two slots of 32 lanes x (D/8 * 4 accumulators + m_lo, m_hi, l_lo, l_hi)
+  // in the stage of the run's last unit (released only afterwards); the CTA's
+  // last run also keeps its merged state there, behind the slots.
   static constexpr int kLaneFloats = D / 8 * 4 + 4;
-  static_assert(kMmaWarps * 32 * kLaneFloats * 4 <= kStage, "run-end slots");
+  static constexpr int kTreeBytes = 2 * 32 * kLaneFloats * 4;
+  static_assert(kTreeBytes + kStateBytes <= kStage, "run-end scratch");
   static constexpr int kEpBytes = kStateBytes + 64;  // state + 16 ints of run metadata
   static constexpr int kOffEp = kRingBytes;
   static constexpr int kOffMeta = kOffEp + kEpSlots * kEpBytes;  // per stage: b, pib, s, len
@@ -507,6 +509,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   int seg_first_i = 0, seg_first_s = 0;
   int ep_k = 0;  // run states handed to the epilogue warp so far
   int counter_seen = 0, counter_seen2 = 0;  // the last run's looks at its plane counter
+  struct FinalRun {
+    int plane = -1, c_first, c_last, run_units, nsub, Gh;
+    __nv_bfloat16 *o_plane;
+    float *state;
+  } fin;
   float acc[NT][4];
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
 
@@ -652,145 +659,177 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int plane = b * planes_per_b + pib;
     const int run_units = i - seg_first_i + 1;
     const int e = ep_k & 1;
-    float *so = reinterpret_cast<float *>(smem + L::kOffEp + e * L::kEpBytes);  // epilogue slot
-    // full row sums of this warp: the four lanes of a quad hold different keys
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-    if (warp == 0) {
-      if (split && !final_run && ep_k >= kEpSlots &&
-          !mbar_wait_warp(ep_empty + 8 * e, ((ep_k >> 1) & 1) ^ 1, nullptr) && lane == 0)
-        record_error(prm.err_word, kErrTimeout);
-      if (lane == 0 && split && final_run) {
-        // If every other run of the plane had counted in (their partials
-        // published before their count) when one of the early looks at the
-        // counter was made, this run is the last one and merges without
-        // publishing its own part.
-        const bool direct = max(counter_seen, counter_seen2) + run_units == nsub;
-        if (direct) fence_acq_rel_gpu();
-        info[4] = direct ? 1 : 0;
-      }
-    }
-    // each warp's (m, l, O) fragments to its own slot of the held stage
-    float *slots = reinterpret_cast<float *>(smem + st * L::kStage);
-    {
-      float *dst = slots + (warp * 32 + lane) * L::kLaneFloats;
-      mma_warps_sync();  // every warp is done reading stage st
+    float *tree = reinterpret_cast<float *>(smem + st * L::kStage);
+    float *mine = tree + lane * L::kLaneFloats;
+    auto put = [&](int slot) {
+      float *dst = mine + slot * 32 * L::kLaneFloats;
 #pragma unroll
       for (int t = 0; t < NT; ++t)
         *reinterpret_cast<float4 *>(dst + 4 * t) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
       *reinterpret_cast<float4 *>(dst + 4 * NT) = make_float4(m_lo, m_hi, l_lo, l_hi);
-      mma_warps_sync();
-    }
-    // merge the four warps' states for this thread's (head, 4 columns)
-    // items, warps in order: head h = 8 hi + r sits in the lanes 4 r + j,
-    // columns 8 t + 2 j + {0, 1} in accumulator t, components 2 hi + {0, 1}
-    float Mi[kPer], Li[kPer];
-    float4 Ai[kPer];
+    };
+    auto take = [&](int slot) {
+      const float *src = mine + slot * 32 * L::kLaneFloats;
+      const float4 ml = *reinterpret_cast<const float4 *>(src + 4 * NT);
+      float w1l, w2l, w1h, w2h;
+      merge_row(m_lo, l_lo, ml.x, ml.z, w1l, w2l);
+      merge_row(m_hi, l_hi, ml.y, ml.w, w1h, w2h);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int it = tid + 32 * kMmaWarps * k, h = it / kQuads, q4 = it % kQuads;
-      const int hi = h >> 3, t = q4 >> 1, la = (h & 7) * 4 + (q4 & 1) * 2;
-      Mi[k] = -INFINITY;
-      Li[k] = 0.f;
-      Ai[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kMmaWarps; ++w) {
-        const float *sa = slots + (w * 32 + la) * L::kLaneFloats;
-        const float2 x = *reinterpret_cast<const float2 *>(sa + 4 * t + 2 * hi);
-        const float2 y = *reinterpret_cast<const float2 *>(sa + L::kLaneFloats + 4 * t + 2 * hi);
-        float wa, wb;
-        merge_row(Mi[k], Li[k], sa[4 * NT + hi], sa[4 * NT + 2 + hi], wa, wb);
-        Ai[k] = make_float4(fmaf(wa, Ai[k].x, wb * x.x), fmaf(wa, Ai[k].y, wb * x.y),
-                            fmaf(wa, Ai[k].z, wb * y.x), fmaf(wa, Ai[k].w, wb * y.y));
+      for (int t = 0; t < NT; ++t) {
+        const float4 a = *reinterpret_cast<const float4 *>(src + 4 * t);
+        acc[t][0] = fmaf(w1l, acc[t][0], w2l * a.x);
+        acc[t][1] = fmaf(w1l, acc[t][1], w2l * a.y);
+        acc[t][2] = fmaf(w1h, acc[t][2], w2h * a.z);
+        acc[t][3] = fmaf(w1h, acc[t][3], w2h * a.w);
       }
-    }
+    };
+    if (warp == 0 && split && !final_run && ep_k >= kEpSlots &&
+        !mbar_wait_warp(ep_empty + 8 * e, ((ep_k >> 1) & 1) ^ 1, nullptr) && lane == 0)
+      record_error(prm.err_word, kErrTimeout);
+    // merge the four warps (a lane with the same lane of another warp holds
+    // the same heads and columns): warps 2,3 -> 0,1, then warp 1 -> warp 0
+    mma_warps_sync();  // every warp is done reading stage st
+    if (warp >= 2) put(warp - 2);
+    mma_warps_sync();
+    if (warp < 2) take(warp);
+    mma_warps_sync();
+    if (warp == 1) put(0);
+    mma_warps_sync();
     __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D;
-    if (!split) {
-      // this run is the whole plane: O = acc / l
+    // where a split run's merged state goes: an epilogue slot, or (the CTA's
+    // last run) behind the tree slots in the held stage
+    float *state = final_run ? tree + L::kTreeBytes / 4
+                             : reinterpret_cast<float *>(smem + L::kOffEp + e * L::kEpBytes);
+    float *st_m = state + kHeads * L::kRow, *st_l = st_m + kHeads;
+    if (warp == 0) {
+      take(0);
+      // full row sums: the four lanes of a quad hold different keys
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+      const int r_lo = lane >> 2, r_hi = r_lo + 8, cc = 2 * (lane & 3);
+      if (!split) {
+        // this run is the whole plane: write O / l
+        const float il = 1.f / l_lo, ih = 1.f / l_hi;
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int it = tid + 32 * kMmaWarps * k, h = it / kQuads, q4 = it % kQuads;
-        if (h < Gh) {
-          const float il = 1.f / Li[k];
-          *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
-              make_uint2(pack_bf16x2(Ai[k].x * il, Ai[k].y * il), pack_bf16x2(Ai[k].z * il, Ai[k].w * il));
+        for (int t = 0; t < NT; ++t) {
+          if (r_lo < Gh)
+            *reinterpret_cast<uint32_t *>(o_plane + r_lo * D + t * 8 + cc) =
+                pack_bf16x2(acc[t][0] * il, acc[t][1] * il);
+          if (r_hi < Gh)
+            *reinterpret_cast<uint32_t *>(o_plane + r_hi * D + t * 8 + cc) =
+                pack_bf16x2(acc[t][2] * ih, acc[t][3] * ih);
         }
-      }
-    } else if (!final_run) {
-      // hand the state to the epilogue warp
-      float *sm = so + kHeads * L::kRow, *sl = sm + kHeads;
+      } else {
 #pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int it = tid + 32 * kMmaWarps * k, h = it / kQuads, q4 = it % kQuads;
-        *reinterpret_cast<float4 *>(so + h * L::kRow + 4 * q4) = Ai[k];
-        if (q4 == 0) {
-          sm[h] = Mi[k];
-          sl[h] = Li[k];
+        for (int t = 0; t < NT; ++t) {
+          *reinterpret_cast<float2 *>(state + r_lo * L::kRow + t * 8 + cc) = make_float2(acc[t][0], acc[t][1]);
+          *reinterpret_cast<float2 *>(state + r_hi * L::kRow + t * 8 + cc) = make_float2(acc[t][2], acc[t][3]);
         }
-      }
-      mma_warps_sync();
-      if (warp == 0 && lane == 0) {
-        int *em = reinterpret_cast<int *>(so + L::kStateFloats);
-        em[0] = kEpPartial;
-        em[1] = b;
-        em[2] = hq0;
-        em[3] = Gh;
-        em[4] = plane;
-        em[5] = c_first;
-        em[6] = c_last;
-        em[7] = run_units;
-        em[8] = nsub;
-        mbar_arrive(ep_full + 8 * e);
-      }
-      ++ep_k;
-    } else {
-      bool last = info[4] != 0;
-      if (!last) {
-        // publish the state to slot c + plane, then count the plane's units
-        // done: the run that completes the count merges (no CTA range is
-        // empty, so every owner takes part)
-        float *dst = prm.part + static_cast<size_t>(c + plane) * kSlot;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int it = tid + 32 * kMmaWarps * k, h = it / kQuads;
-          reinterpret_cast<float4 *>(dst)[it] = Ai[k];
-          if (it % kQuads == 0) {
-            dst[kHeads * D + h] = Mi[k];
-            dst[kHeads * D + kHeads + h] = Li[k];
+        if ((lane & 3) == 0) {
+          st_m[r_lo] = m_lo;
+          st_l[r_lo] = l_lo;
+          st_m[r_hi] = m_hi;
+          st_l[r_hi] = l_hi;
+        }
+        if (!final_run) {
+          // hand the state to the epilogue warp
+          __syncwarp();
+          if (lane == 0) {
+            int *em = reinterpret_cast<int *>(state + L::kStateFloats);
+            em[0] = kEpPartial;
+            em[1] = b;
+            em[2] = hq0;
+            em[3] = Gh;
+            em[4] = plane;
+            em[5] = c_first;
+            em[6] = c_last;
+            em[7] = run_units;
+            em[8] = nsub;
+            mbar_arrive(ep_full + 8 * e);
           }
+        } else if (lane == 0) {
+          // If every other run of the plane had counted in (their partials
+          // published before their count) when one of the early looks at the
+          // counter was made, this run is the last one and merges without
+          // publishing its own part.
+          const bool direct = max(counter_seen, counter_seen2) + run_units == nsub;
+          if (direct) fence_acq_rel_gpu();
+          info[4] = direct ? 1 : 0;
         }
-        fence_acq_rel_gpu();
-        mma_warps_sync();
-        if (tid == 0) {
-          const bool l0 = atomicAdd(prm.counters + plane, run_units) + run_units == nsub;
-          if (l0) fence_acq_rel_gpu();
-          info[4] = l0 ? 1 : 0;
-        }
-        mma_warps_sync();
-        last = info[4] != 0;
       }
-      if (last) {
-        // ---- the plane's last run: merge the parts of CTAs c_first..c_last
-        // (CTA cs in slot cs + plane; this CTA's own part in registers)
-        fence_acq_rel_gpu();
-        auto self = [&](int k, int, float4 &v, float &m, float &l) {
-          v = Ai[k];
-          m = Mi[k];
-          l = Li[k];
-        };
-        merge_parts<D, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
-                                c_last - c_first + 1, c - c_first, self, Gh, o_plane, tid,
-                                32 * kMmaWarps);
-        if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
-      }
+    }
+    if (split && !final_run) ++ep_k;
+    if (split && final_run) {
+      // the CTA's last run leaves the loop with its merged state in shared
+      // memory (the stage stays held); it is published and merged below,
+      // outside the loop, so the loop's registers stay low
+      fin.plane = plane;
+      fin.c_first = c_first;
+      fin.c_last = c_last;
+      fin.run_units = run_units;
+      fin.nsub = nsub;
+      fin.Gh = Gh;
+      fin.o_plane = o_plane;
+      fin.state = state;
+      break;
     }
     // release the held stage (its generic-proxy writes ordered before the
     // TMA that refills it)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + 8 * st);
+  }
+  if (fin.plane >= 0) {
+    // ---- the CTA's last run, part of a plane other CTAs share
+    const int plane = fin.plane, c_first = fin.c_first, c_last = fin.c_last;
+    const int run_units = fin.run_units, nsub = fin.nsub, Gh = fin.Gh;
+    __nv_bfloat16 *o_plane = fin.o_plane;
+    float *state = fin.state;
+    float *st_m = state + kHeads * L::kRow, *st_l = st_m + kHeads;
+    mma_warps_sync();  // the run's state is in shared memory
+    bool last = info[4] != 0;
+    if (!last) {
+      // publish the state to slot c + plane (coalesced, all MMA threads),
+      // then count the plane's units done: the run that completes the
+      // count merges (no CTA range is empty, so every owner takes part)
+      float *dst = prm.part + static_cast<size_t>(c + plane) * kSlot;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int it = tid + 32 * kMmaWarps * k;
+        reinterpret_cast<float4 *>(dst)[it] =
+            *reinterpret_cast<const float4 *>(state + (it / kQuads) * L::kRow + 4 * (it % kQuads));
+      }
+      if (tid < kHeads) {
+        dst[kHeads * D + tid] = st_m[tid];
+        dst[kHeads * D + kHeads + tid] = st_l[tid];
+      }
+      fence_acq_rel_gpu();
+      mma_warps_sync();
+      if (tid == 0) {
+        const bool l0 = atomicAdd(prm.counters + plane, run_units) + run_units == nsub;
+        if (l0) fence_acq_rel_gpu();
+        info[4] = l0 ? 1 : 0;
+      }
+      mma_warps_sync();
+      last = info[4] != 0;
+    }
+    if (last) {
+      // ---- the plane's last run: merge the parts of CTAs c_first..c_last
+      // (CTA cs in slot cs + plane; this CTA's own part in shared memory)
+      fence_acq_rel_gpu();
+      auto self = [&](int, int it, float4 &v, float &m, float &l) {
+        const int h = it / kQuads;
+        v = *reinterpret_cast<const float4 *>(state + h * L::kRow + 4 * (it % kQuads));
+        m = st_m[h];
+        l = st_l[h];
+      };
+      merge_parts<D, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, tid,
+                              32 * kMmaWarps);
+      if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
+    }
   }
   // tell the epilogue warp that no more run states follow
   if (warp == 0) {
