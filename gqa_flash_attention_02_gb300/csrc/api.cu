@@ -201,12 +201,45 @@ bool d_supported_simt(int d) { return d == 32 || d == 64 || d == 96 || d == 128;
 
 }  // namespace
 
+namespace {
+int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const int *seqlens,
+                void *o, float *lse, int B, int H_q, int H_kv, int max_len, int d, float scale,
+                int chunk_tokens, cudaStream_t stream) {
+  int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
+  if (rc != GQA_OK) return rc;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
+  if (chunk_tokens != 0 &&
+      (chunk_tokens < 0 || chunk_tokens % kDecodeChunkUnit != 0 || chunk_tokens > kDecodeChunkMax))
+    return GQA_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int grid = decode_grid(B, H_q, H_kv, max_len, d, device_sms(dev), chunk_tokens);
+  Workspace *ws = nullptr;
+  rc = get_workspace(stream, decode_partials_bytes(B, H_q, H_kv, d, grid), &ws,
+                     decode_planes(B, H_q, H_kv));
+  if (rc != GQA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
+      !encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit) ||
+      !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit))
+    return cuda_fail(cudaErrorInvalidValue);
+  e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, lse, ws->partials, ws->counters, B, H_q, H_kv,
+                         max_len, d, scale, grid, ws->ctl + kCtlErr, stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+}  // namespace
+
 extern "C" {
 
-int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, int B, int H_q, int H_kv,
-                 int N_q, int N_kv, int d, int causal, float scale, cudaStream_t stream) {
+int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H_q, int H_kv, int N_q, int N_kv, int d, int causal, float scale,
+                     cudaStream_t stream) {
   int rc = check_prefill_args(q, k, v, o, B, H_q, H_kv, N_q, N_kv, d, causal, scale);
   if (rc != GQA_OK) return rc;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
   const PrefillPlan plan = make_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal);
   Workspace *ws = nullptr;
@@ -219,8 +252,14 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, int B, in
     return cuda_fail(cudaErrorInvalidValue);
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e = launch_prefill_tc(tq, tk, tv, o, plan, d, scale, ws->ctl, device_sms(dev), stream);
+  cudaError_t e =
+      launch_prefill_tc(tq, tk, tv, o, lse, plan, d, scale, ws->ctl, device_sms(dev), stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, int B, int H_q, int H_kv,
+                 int N_q, int N_kv, int d, int causal, float scale, cudaStream_t stream) {
+  return gqa_attn_fwd_lse(q, k, v, o, nullptr, B, H_q, H_kv, N_q, N_kv, d, causal, scale, stream);
 }
 
 int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o, int B, int H_q,
@@ -242,36 +281,22 @@ int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o, int B
 int gqa_attn_decode_chunked(const void *q, const void *k_cache, const void *v_cache,
                             const int *seqlens, void *o, int B, int H_q, int H_kv, int max_len,
                             int d, float scale, int chunk_tokens, cudaStream_t stream) {
-  int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
-  if (rc != GQA_OK) return rc;
-  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
-  if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
-  if (chunk_tokens != 0 &&
-      (chunk_tokens < 0 || chunk_tokens % kDecodeChunkUnit != 0 || chunk_tokens > kDecodeChunkMax))
-    return GQA_ERR_INVALID_ARG;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  const int grid = decode_grid(B, H_q, H_kv, max_len, d, device_sms(dev), chunk_tokens);
-  Workspace *ws = nullptr;
-  rc = get_workspace(stream, decode_partials_bytes(B, H_q, H_kv, d, grid), &ws,
-                     decode_planes(B, H_q, H_kv));
-  if (rc != GQA_OK) return rc;
-  CUtensorMap tq, tk, tv;
-  if (!encode_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
-      !encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit) ||
-      !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit))
-    return cuda_fail(cudaErrorInvalidValue);
-  e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, ws->partials, ws->counters, B, H_q, H_kv,
-                         max_len, d, scale, grid, ws->ctl + kCtlErr, stream);
-  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+  return decode_bf16(q, k_cache, v_cache, seqlens, o, nullptr, B, H_q, H_kv, max_len, d, scale,
+                     chunk_tokens, stream);
 }
 
 int gqa_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int *seqlens,
                     void *o, int B, int H_q, int H_kv, int max_len, int d, float scale,
                     cudaStream_t stream) {
-  return gqa_attn_decode_chunked(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale,
-                                 0, stream);
+  return decode_bf16(q, k_cache, v_cache, seqlens, o, nullptr, B, H_q, H_kv, max_len, d, scale, 0,
+                     stream);
+}
+
+int gqa_attn_decode_lse(const void *q, const void *k_cache, const void *v_cache,
+                        const int *seqlens, void *o, float *lse, int B, int H_q, int H_kv,
+                        int max_len, int d, float scale, cudaStream_t stream) {
+  return decode_bf16(q, k_cache, v_cache, seqlens, o, lse, B, H_q, H_kv, max_len, d, scale, 0,
+                     stream);
 }
 
 int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,

@@ -108,7 +108,7 @@ extern "C" int gqa_attn_decode_noalloc(const void *q, const void *k_cache, const
       !encode_tensor_map_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv,
                                  kDecodeChunkUnit))
     return GQA_ERR_CUDA;
-  e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, partials, counters, B, H_q, H_kv, max_len, d,
+  e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, nullptr, partials, counters, B, H_q, H_kv, max_len, d,
                          scale, grid, err_word, stream);
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }

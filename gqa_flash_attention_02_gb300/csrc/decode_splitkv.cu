@@ -123,6 +123,7 @@ struct DecodeParams {
   const __nv_bfloat16 *q;
   const int *seqlens;
   __nv_bfloat16 *o;
+  float *lse;      // [B][H_q] natural-log sum of exp(scale q.k), or null
   float *part;     // [(grid + planes)] slots of O [16][D] (unnormalised), m [16], l [16]
   int *counters;   // [planes], zero between launches (the last merger re-arms it)
   int *err_word;
@@ -190,12 +191,14 @@ __device__ __forceinline__ void merge_row(float &m, float &l, float m2, float l2
 //   O' = 2^(M-M') O + 2^(m_j-M') O_j,  O = O' / L' at the end.
 // Part j lives in partial slot pbase + j * kSlot, except part jself, the
 // calling CTA's own state, which self(k, it, O, m, l) supplies for the k-th
-// item of a group. Every item's arithmetic is the same whichever CTA or
+// item of a group. lse_plane (if not null) receives each head's
+// log-sum-exp. Every item's arithmetic is the same whichever CTA or
 // warp runs it, so the result does not depend on who merges. kBatch parts'
 // loads are in flight together.
 template <int D, int kItems, int kBatch, typename SelfFn>
 __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int jself, SelfFn self,
-                                            int Gh, __nv_bfloat16 *o_plane, int t, int nt) {
+                                            int Gh, __nv_bfloat16 *o_plane, float *lse_plane,
+                                            int t, int nt) {
   constexpr int kQuads = D / 4;
   constexpr int kSlot = kHeads * (D + 2);
   const int items = Gh * kQuads;
@@ -251,6 +254,8 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
         const float il = 1.f / Lr[k];
         *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
             make_uint2(pack_bf16x2(Ar[k].x * il, Ar[k].y * il), pack_bf16x2(Ar[k].z * il, Ar[k].w * il));
+        // the head's log-sum-exp (M, L are in log2 units of scale * q.k)
+        if (lse_plane != nullptr && q4 == 0) lse_plane[h] = (Mr[k] + log2f(Lr[k])) * 0.6931471805599453f;
       }
     }
   }
@@ -398,6 +403,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (units_for(prm, seq_len(prm, s_len, b)) != 0) continue;
       uint4 *ob = reinterpret_cast<uint4 *>(prm.o + static_cast<size_t>(b) * prm.H_q * D);
       for (int idx = tid; idx < prm.H_q * D / 8; idx += 32 * kMmaWarps) ob[idx] = make_uint4(0, 0, 0, 0);
+      if (prm.lse != nullptr)
+        for (int h = tid; h < prm.H_q; h += 32 * kMmaWarps) prm.lse[static_cast<size_t>(b) * prm.H_q + h] = -INFINITY;
     }
   }
   if (U == 0) return;
@@ -495,7 +502,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         };
         merge_parts<D, 2, 2>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                              c_last - c_first + 1, c - c_first, self, Gh,
-                             prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D, lane, 32);
+                             prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D,
+                             prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0,
+                             lane, 32);
         if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
       }
       __syncwarp();
@@ -512,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   struct FinalRun {
     int plane = -1, c_first, c_last, run_units, nsub, Gh;
     __nv_bfloat16 *o_plane;
+    float *lse_plane;
     float *state;
   } fin;
   float acc[NT][4];
@@ -696,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (warp == 1) put(0);
     mma_warps_sync();
     __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D;
+    float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
     // where a split run's merged state goes: an epilogue slot, or (the CTA's
     // last run) behind the tree slots in the held stage
     float *state = final_run ? tree + L::kTreeBytes / 4
@@ -720,6 +731,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           if (r_hi < Gh)
             *reinterpret_cast<uint32_t *>(o_plane + r_hi * D + t * 8 + cc) =
                 pack_bf16x2(acc[t][2] * ih, acc[t][3] * ih);
+        }
+        if (lse_plane != nullptr && (lane & 3) == 0) {
+          // log-sum-exp per head (m, l in log2 units of scale * q.k)
+          if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
+          if (r_hi < Gh) lse_plane[r_hi] = (m_hi + log2f(l_hi)) * 0.6931471805599453f;
         }
       } else {
 #pragma unroll
@@ -772,6 +788,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       fin.nsub = nsub;
       fin.Gh = Gh;
       fin.o_plane = o_plane;
+      fin.lse_plane = lse_plane;
       fin.state = state;
       break;
     }
@@ -786,6 +803,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int plane = fin.plane, c_first = fin.c_first, c_last = fin.c_last;
     const int run_units = fin.run_units, nsub = fin.nsub, Gh = fin.Gh;
     __nv_bfloat16 *o_plane = fin.o_plane;
+    float *lse_plane = fin.lse_plane;
     float *state = fin.state;
     float *st_m = state + kHeads * L::kRow, *st_l = st_m + kHeads;
     mma_warps_sync();  // the run's state is in shared memory
@@ -826,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         l = st_l[h];
       };
       merge_parts<D, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
-                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, tid,
+                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
                               32 * kMmaWarps);
       if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
     }
@@ -848,8 +866,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 template <int D, int NSTG>
 cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
-                            float *partials, int *counters, int B, int H_q, int H_kv, int max_len,
-                            float scale, int grid, int *err_word, cudaStream_t stream) {
+                            float *lse, float *partials, int *counters, int B, int H_q, int H_kv,
+                            int max_len, float scale, int grid, int *err_word,
+                            cudaStream_t stream) {
   using L = DecodeSmem<D, NSTG>;
   static unsigned configured = 0;
   int dev = 0;
@@ -865,6 +884,7 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   prm.q = static_cast<const __nv_bfloat16 *>(q);
   prm.seqlens = seqlens;
   prm.o = static_cast<__nv_bfloat16 *>(o);
+  prm.lse = lse;
   prm.part = partials;
   prm.counters = counters;
   prm.err_word = err_word;
@@ -914,15 +934,15 @@ int decode_grid(int B, int H_q, int H_kv, int max_len, int d, int num_sms, int c
 
 cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
-                               float *partials, int *counters, int B, int H_q, int H_kv,
-                               int max_len, int d, float scale, int grid, int *err_word,
-                               cudaStream_t stream) {
+                               float *lse, float *partials, int *counters, int B, int H_q,
+                               int H_kv, int max_len, int d, float scale, int grid,
+                               int *err_word, cudaStream_t stream) {
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
   if (d == 64)
-    return launch_decode_d<64, 8>(tm_q, tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q,
+    return launch_decode_d<64, 8>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters, B, H_q,
                                   H_kv, max_len, scale, grid, err_word, stream);
   if (d == 128)
-    return launch_decode_d<128, 5>(tm_q, tm_k, tm_v, q, seqlens, o, partials, counters, B, H_q,
+    return launch_decode_d<128, 5>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters, B, H_q,
                                    H_kv, max_len, scale, grid, err_word, stream);
   return cudaErrorInvalidValue;
 }

@@ -146,9 +146,10 @@ struct Workspace {
 };
 
 // Launchers (return a cudaError_t; arguments already validated).
+// lse: optional per-row log-sum-exp output (null: not written).
 cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                              const CUtensorMap &tm_v, void *o, const PrefillPlan &plan, int d,
-                              float scale, int *ctl, int num_sms, cudaStream_t stream);
+                              const CUtensorMap &tm_v, void *o, float *lse, const PrefillPlan &plan,
+                              int d, float scale, int *ctl, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_attn_f32(const float *q, const float *k, const float *v, float *o, int B,
                             int H_q, int H_kv, int N_q, int N_kv, int d, int causal, float scale,
@@ -174,9 +175,9 @@ bool decode_units_fit(int B, int H_q, int H_kv, int max_len);
 // caches as [B * H_kv][max_len][d] with 64-row boxes.
 cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
-                               float *partials, int *counters, int B, int H_q, int H_kv,
-                               int max_len, int d, float scale, int grid, int *err_word,
-                               cudaStream_t stream);
+                               float *lse, float *partials, int *counters, int B, int H_q,
+                               int H_kv, int max_len, int d, float scale, int grid,
+                               int *err_word, cudaStream_t stream);
 
 cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStream_t stream);
 

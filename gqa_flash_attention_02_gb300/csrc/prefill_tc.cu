@@ -87,13 +87,16 @@ struct TcLayout {
 
 struct TcParams {
   __nv_bfloat16 *o;
+  float *lse;     // [B][H_q][N_q] natural-log sum of exp(scale q.k) per row, or null
   int o_align32;  // o is 32-byte aligned (rows are then too: D * 2 bytes each)
   PrefillPlan plan;
   float scale_log2;
   int *ctl;
 };
 
-template <int D>
+// kLse: also write each row's log-sum-exp (a separate instantiation, so the
+// plain kernel carries none of its code)
+template <int D, bool kLse>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
@@ -523,9 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       __syncwarp();
       tc_fence_after_sync();
       const float inv_l = 1.f / l_sum;
-      __nv_bfloat16 *dst =
-          prm.o + ((static_cast<size_t>(w.b) * plan.H_q + mine.h_q) * plan.N_q + q_row) * D;
+      const size_t o_row = (static_cast<size_t>(w.b) * plan.H_q + mine.h_q) * plan.N_q + q_row;
+      __nv_bfloat16 *dst = prm.o + o_row * D;
       const bool store = q_row < plan.N_q;
+      // log-sum-exp of the row in natural-log units: l is relative to
+      // 2^m_ref with m_ref in log2 units of scale * q.k
+      if (kLse && store) prm.lse[o_row] = (m_ref + log2f(l_sum)) * 0.6931471805599453f;
       // the whole row of O in one tensor-memory load; O_t is then free for
       // the next unit's PV while the row is converted and stored
       uint32_t ov[D];
@@ -577,10 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
   }
 }
 
-template <int D>
+template <int D, bool kLse>
 cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                     void *o, const PrefillPlan &plan, float scale, int *ctl, int num_sms,
-                     cudaStream_t stream) {
+                     void *o, float *lse, const PrefillPlan &plan, float scale, int *ctl,
+                     int num_sms, cudaStream_t stream) {
   using L = TcLayout<D>;
   static unsigned configured = 0;  // one bit per device ordinal
   int dev = 0;
@@ -590,33 +596,39 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
     // The register split is only safe if the compiled kernel is launched
     // with at least kLaunchRegs registers per thread; refuse otherwise.
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, prefill_tc_kernel<D>);
+    e = cudaFuncGetAttributes(&attr, prefill_tc_kernel<D, kLse>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs < kLaunchRegs || attr.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_tc_kernel<D, kLse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured |= 1u << dev;
   }
   TcParams prm;
   prm.o = static_cast<__nv_bfloat16 *>(o);
+  prm.lse = lse;
   prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   prm.plan = plan;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.ctl = ctl;
   const int grid = min(num_sms, plan.total_units);
-  return launch_programmatic(prefill_tc_kernel<D>, grid, kThreads, L::kAlloc, stream, tm_q, tm_k,
+  return launch_programmatic(prefill_tc_kernel<D, kLse>, grid, kThreads, L::kAlloc, stream, tm_q, tm_k,
                              tm_v, prm);
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                              const CUtensorMap &tm_v, void *o, const PrefillPlan &plan, int d,
-                              float scale, int *ctl, int num_sms, cudaStream_t stream) {
-  if (d == 64) return launch_d<64>(tm_q, tm_k, tm_v, o, plan, scale, ctl, num_sms, stream);
-  if (d == 128) return launch_d<128>(tm_q, tm_k, tm_v, o, plan, scale, ctl, num_sms, stream);
+                              const CUtensorMap &tm_v, void *o, float *lse, const PrefillPlan &plan,
+                              int d, float scale, int *ctl, int num_sms, cudaStream_t stream) {
+  const bool with_lse = lse != nullptr;
+  if (d == 64)
+    return with_lse ? launch_d<64, true>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream)
+                    : launch_d<64, false>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream);
+  if (d == 128)
+    return with_lse ? launch_d<128, true>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream)
+                    : launch_d<128, false>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

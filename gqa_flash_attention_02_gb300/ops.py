@@ -30,7 +30,7 @@ EXPORTED = [
     "gqa_attn_fwd", "gqa_attn_fwd_f32", "gqa_attn_decode", "gqa_attn_decode_chunked",
     "gqa_attn_decode_f32", "gqa_attn_status_string", "gqa_attn_get_device_error",
     "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
-    "gqa_attn_decode_noalloc",
+    "gqa_attn_decode_noalloc", "gqa_attn_fwd_lse", "gqa_attn_decode_lse",
 ]
 
 
@@ -73,6 +73,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.gqa_attn_decode_chunked.restype = _i
             lib.gqa_attn_decode_noalloc.argtypes = dec
             lib.gqa_attn_decode_noalloc.restype = _i
+            lib.gqa_attn_fwd_lse.argtypes = fwd[:4] + [_vp] + fwd[4:]
+            lib.gqa_attn_fwd_lse.restype = _i
+            lib.gqa_attn_decode_lse.argtypes = dec[:5] + [_vp] + dec[5:]
+            lib.gqa_attn_decode_lse.restype = _i
             lib.gqa_attn_status_string.argtypes = [_i]
             lib.gqa_attn_status_string.restype = ctypes.c_char_p
             lib.gqa_attn_get_device_error.argtypes = [_vp]
@@ -119,12 +123,24 @@ def gqa_attn_fwd(q, k, v, o=None, causal=False, scale=None, stream=None):
     return _fwd("gqa_attn_fwd", torch.bfloat16, q, k, v, o, causal, scale, stream)
 
 
+def gqa_attn_fwd_lse(q, k, v, o=None, lse=None, causal=False, scale=None, stream=None):
+    """bf16 prefill that also returns each row's log-sum-exp (fp32 [B,H_q,N_q]).
+    Returns (o, lse)."""
+    if lse is None:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if tuple(lse.shape) != tuple(q.shape[:3]):
+        raise ValueError("lse must be [B, H_q, N_q]")
+    o = _fwd("gqa_attn_fwd_lse", torch.bfloat16, q, k, v, o, causal, scale, stream,
+             lse=_dev(lse, torch.float32, "lse", 3))
+    return o, lse
+
+
 def gqa_attn_fwd_f32(q, k, v, o=None, causal=False, scale=None, stream=None):
     """fp32 prefill with the same layouts."""
     return _fwd("gqa_attn_fwd_f32", torch.float32, q, k, v, o, causal, scale, stream)
 
 
-def _fwd(name, dtype, q, k, v, o, causal, scale, stream):
+def _fwd(name, dtype, q, k, v, o, causal, scale, stream, lse=None):
     B, H_q, N_q, d = q.shape
     _, H_kv, N_kv, _ = k.shape
     if o is None:
@@ -136,6 +152,8 @@ def _fwd(name, dtype, q, k, v, o, causal, scale, stream):
     if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != d or \
             tuple(o.shape) != tuple(q.shape):
         raise ValueError("shape mismatch between q, k, v, o")
+    if lse is not None:
+        args = args + (lse,)
     rc = getattr(load(), name)(*args, B, H_q, H_kv, N_q, N_kv, d, int(bool(causal)),
                                float(scale), _stream(stream))
     _check(rc, name)
@@ -151,6 +169,18 @@ def gqa_attn_decode(q, k_cache, v_cache, seqlens, o=None, scale=None, chunk_toke
                    scale, chunk_tokens, stream)
 
 
+def gqa_attn_decode_lse(q, k_cache, v_cache, seqlens, o=None, lse=None, scale=None, stream=None):
+    """bf16 decode that also returns each head's log-sum-exp (fp32 [B,H_q],
+    -inf for an empty sequence). Returns (o, lse)."""
+    if lse is None:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    if tuple(lse.shape) != tuple(q.shape[:2]):
+        raise ValueError("lse must be [B, H_q]")
+    o = _decode("gqa_attn_decode_lse", torch.bfloat16, q, k_cache, v_cache, seqlens, o, scale,
+                None, stream, lse=_dev(lse, torch.float32, "lse", 2))
+    return o, lse
+
+
 def gqa_attn_decode_noalloc(q, k_cache, v_cache, seqlens, o, scale=None, stream=None):
     """bf16 decode that allocates nothing (the library's fixed scratch array);
     ``o`` must be given. See gqa_attn_decode_noalloc in include/gqa_attn.h."""
@@ -163,7 +193,7 @@ def gqa_attn_decode_f32(q, k_cache, v_cache, seqlens, o=None, scale=None, stream
                    None, stream)
 
 
-def _decode(name, dtype, q, kc, vc, seqlens, o, scale, chunk, stream):
+def _decode(name, dtype, q, kc, vc, seqlens, o, scale, chunk, stream, lse=None):
     B, H_q, d = q.shape
     _, H_kv, max_len, _ = kc.shape
     if o is None:
@@ -174,8 +204,10 @@ def _decode(name, dtype, q, kc, vc, seqlens, o, scale, chunk, stream):
             tuple(o.shape) != tuple(q.shape) or tuple(seqlens.shape) != (B,):
         raise ValueError("shape mismatch between q, caches, seqlens, o")
     args = [_dev(q, dtype, "q", 3), _dev(kc, dtype, "k_cache", 4), _dev(vc, dtype, "v_cache", 4),
-            _dev(seqlens, torch.int32, "seqlens", 1), _dev(o, dtype, "o", 3),
-            B, H_q, H_kv, max_len, d, float(scale)]
+            _dev(seqlens, torch.int32, "seqlens", 1), _dev(o, dtype, "o", 3)]
+    if lse is not None:
+        args.append(lse)
+    args += [B, H_q, H_kv, max_len, d, float(scale)]
     if chunk is not None:
         args.append(int(chunk))
     rc = getattr(load(), name)(*args, _stream(stream))

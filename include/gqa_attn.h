@@ -74,6 +74,20 @@ int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o,
                  int causal, float scale, cudaStream_t stream);
 
 /*
+ * gqa_attn_fwd that also returns each query row's log-sum-exp,
+ *   lse[b][h_q][i] = ln( sum_j exp(scale * q_i . k_j) )  over the visible keys,
+ * as fp32 [B][H_q][N_q] (device pointer, 4-byte aligned, caller-owned). It
+ * lets a caller merge this result with attention over other keys
+ * (O = sum_p exp(lse_p - M) O_p / sum_p exp(lse_p - M), M = max_p lse_p).
+ * All other arguments, layouts and errors as gqa_attn_fwd.
+ * Pages: microLLM-rocm optimisation log, Experiments 282-284 (split-sequence
+ * attention carries each part's (max, sum) to a log-sum-exp merge).
+ */
+int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+                     int causal, float scale, cudaStream_t stream);
+
+/*
  * Same operation in fp32: q, k, v, o are float arrays with the layouts of
  * gqa_attn_fwd. SIMT FMA kernel (online softmax, warp-shuffle reductions);
  * d in {32, 64, 96, 128}.
@@ -106,6 +120,18 @@ int gqa_attn_decode(const void *q, const void *k_cache, const void *v_cache,
                     const int *seqlens, void *o,
                     int B, int H_q, int H_kv, int max_len, int d,
                     float scale, cudaStream_t stream);
+
+/*
+ * gqa_attn_decode that also returns each query head's log-sum-exp,
+ *   lse[b][h_q] = ln( sum_{j < seqlens[b]} exp(scale * q . k_j) ),
+ * as fp32 [B][H_q] (device pointer, 4-byte aligned, caller-owned); -inf for
+ * a sequence with no rows. Other arguments as gqa_attn_decode.
+ * Pages: microLLM-rocm optimisation log, Experiments 282-284.
+ */
+int gqa_attn_decode_lse(const void *q, const void *k_cache, const void *v_cache,
+                        const int *seqlens, void *o, float *lse,
+                        int B, int H_q, int H_kv, int max_len, int d,
+                        float scale, cudaStream_t stream);
 
 /*
  * gqa_attn_decode with an explicit work split. The valid cache rows are

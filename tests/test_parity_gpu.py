@@ -291,6 +291,52 @@ def test_bf16_decode_deterministic():
     assert np.array_equal(a, b)
 
 
+# ------------------------------------------------------------------ log-sum-exp output
+
+# The lse is ln of a sum whose terms carry up to bf16 (2^-8) relative error
+# (P is formed from bf16 exponentials at d = 128), so |d lse| <= ~4e-3.
+LSE_MAX = 5e-3
+
+
+@pytest.mark.parametrize("d,causal,N", [(128, True, 640), (64, False, 384), (64, True, 1000)])
+def test_bf16_prefill_lse_matches_oracle(d, causal, N):
+    q, k, v = inputs.prefill_inputs(2, 8, 2, N, N, d, torch.bfloat16, seed=120 + d + N)
+    qd, kd, vd = _dev(q, k, v)
+    o, lse = ops.gqa_attn_fwd_lse(qd, kd, vd, causal=causal, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref_o, ref_lse = oracle.prefill(q, k, v, causal, d ** -0.5, n_threads=THREADS)
+    _check_bf16(o.float().cpu().numpy(), ref_o, "o with lse")
+    err = np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max()
+    assert err <= LSE_MAX, f"lse max err {err:.3e}"
+    # the plain entry point gives the same O
+    assert torch.equal(o, ops.gqa_attn_fwd(qd, kd, vd, causal=causal, scale=d ** -0.5))
+
+
+@pytest.mark.parametrize("case", ["mixed", "one_long"])
+def test_bf16_decode_lse_matches_oracle(case):
+    """Whole-plane runs, planes split over several CTAs (merged in-kernel)
+    and an empty sequence (lse = -inf)."""
+    if case == "mixed":
+        seqlens, q, kc, vc = inputs.decode_inputs(6, 24, 2, 1500, 128, torch.bfloat16, seed=130,
+                                                  seqlens=[1500, 0, 7, 900, 64, 1201])
+    else:
+        seqlens, q, kc, vc = inputs.decode_inputs(1, 8, 1, 20000, 64, torch.bfloat16, seed=131,
+                                                  seqlens=[20000])
+    qd, kd, vd, sd = _dev(q, kc, vc, seqlens)
+    o, lse = ops.gqa_attn_decode_lse(qd, kd, vd, sd, scale=0.09)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref_o, ref_lse = oracle.decode(q, kc, vc, seqlens, 0.09)
+    _check_bf16(o.float().cpu().numpy(), ref_o, f"decode with lse ({case})")
+    got = lse.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref_lse))
+    mask = np.isfinite(ref_lse)
+    assert np.abs(got[mask] - ref_lse[mask]).max() <= LSE_MAX
+    # the plain entry point gives the same O
+    assert torch.equal(o, ops.gqa_attn_decode(qd, kd, vd, sd, scale=0.09))
+
+
 # ------------------------------------------------------------------ launch order
 
 def test_dependent_launches_back_to_back():
