@@ -322,14 +322,14 @@ def run_ours(args):
         },
         "roofline": {
             "bound": "tensor",
-            "kernel": "prefill_tc_kernel<128>",
+            "kernel": "prefill_tc_kernel<128, 0> (no lse output)",
             "achieved": round(pre_ach, 3),
             "peak": tc_peak,
             "unit": "TFLOP/s",
             "frac": round(pre_ach / tc_peak, 4),
             "peak_source": f"{peak_src} bf16_tflops (burst)",
             "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
-                                        "prefill_tc_kernel<128>"),
+                                        "prefill_tc_kernel<128, 0>"),
         },
         "decode": {
             "value": round(dec_gbs, 2),
