@@ -25,11 +25,13 @@
 //     S = Q K^T and O += P V run on mma.sync (bf16 in, fp32 accumulate) from
 //     ldmatrix fragments, with an online softmax (exp2, scale folded in) on
 //     the register fragments;
-//   * at the end of a plane's run, the four warps' (m, l, O) merge through a
-//     small shared-memory tree; a run that covers the whole plane writes O,
-//     otherwise it writes a partial and the last run of the plane to finish
-//     (atomic counter, nobody waits) merges the partials:
+//   * at the end of a plane's run the four warps leave their (m, l, O) in
+//     shared memory and go on with the next unit; warp 5 (epilogue) merges
+//     them. A run that covers the whole plane writes O, otherwise it writes a
+//     partial and the last run of the plane to finish (atomic counter,
+//     nobody waits) merges the partials:
 //         M = max m_i,  L = sum 2^(m_i - M) l_i,  O = sum 2^(m_i - M) O_i / L.
+//     The CTA's last run is merged by the MMA warps themselves.
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -51,8 +53,7 @@ constexpr int kHeads = kDecodeHeads;  // query heads per plane (mma M)
 // is ever empty.
 constexpr int kMinUnits = 4;
 constexpr int kLenCache = 1024;  // sequence lengths kept in shared memory
-constexpr int kEpSlots = 2;      // run states queued for the epilogue warp
-constexpr int kEpPartial = 1, kEpStop = 2;
+constexpr int kEpRun = 1, kEpStop = 2;  // epilogue queue entry kinds
 constexpr int kCtasPerSm = 1;    // the balanced partition assumes one resident wave
 
 // Byte offset of (row, 16-byte unit u) inside a [rows][D] bf16 tile stored
@@ -96,27 +97,32 @@ struct DecodeSmem {
   static constexpr int kQTile = kHeads * D * 2;  // the plane's 16 query rows
   static constexpr int kStage = 2 * kTile + kQTile;
   static constexpr int kRingBytes = NSTG * kStage;
-  // A merged run state handed to the epilogue warp: O rows [16][kRow]
-  // (unnormalised), m[16], l[16].
+  // A merged run state: O rows [16][kRow] (unnormalised), m[16], l[16].
   static constexpr int kRow = D + 4;  // padded: fragment stores spread over banks
   static constexpr int kStateFloats = kHeads * kRow + 2 * kHeads;
   static constexpr int kStateBytes = kStateFloats * 4;
-  // At a run end the four MMA warps merge their (m, l, O) fragments through
-  // two slots of 32 lanes x (D/8 * 4 accumulators + m_lo, m_hi, l_lo, l_hi)
-  // in the stage of the run's last unit (released only afterwards); the CTA's
-  // last run also keeps its merged state there, behind the slots.
+  // At the end of the CTA's last run the four MMA warps merge their
+  // (m, l, O) fragments through two slots of 32 lanes x (D/8 * 4
+  // accumulators + m_lo, m_hi, l_lo, l_hi) in the stage of the run's last
+  // unit and keep the merged state there, behind the slots.
   static constexpr int kLaneFloats = D / 8 * 4 + 4;
   static constexpr int kTreeBytes = 2 * 32 * kLaneFloats * 4;
   static_assert(kTreeBytes + kStateBytes <= kStage, "run-end scratch");
-  static constexpr int kEpBytes = kStateBytes + 64;  // state + 16 ints of run metadata
-  static constexpr int kOffEp = kRingBytes;
-  static constexpr int kOffMeta = kOffEp + kEpSlots * kEpBytes;  // per stage: b, pib, s, len
+  // A run that ends before the CTA's last unit is finished by the epilogue
+  // warp: each MMA warp leaves its accumulator fragments in the K/V rows of
+  // the stage that only it reads (16 K and 16 V rows: 2 D bytes per lane)
+  // and its (m, l) in the stage's side buffer.
+  static_assert(32 * (D / 8) * 4 * 4 == 2 * (D / 64) * 16 * 128, "fragments fill the warp's rows");
+  static constexpr int kOffML = kRingBytes;                  // [NSTG][4 warps][32 lanes] float4
+  static constexpr int kOffEp = kOffML + NSTG * kMmaWarps * 32 * 16;  // epilogue's merged state
+  static constexpr int kOffQueue = kOffEp + kStateBytes;     // [NSTG] run entries of 16 ints
+  static constexpr int kOffMeta = kOffQueue + NSTG * 64;     // per stage: b, pib, s, len
   static constexpr int kOffLen = kOffMeta + NSTG * 16;
-  static constexpr int kOffBar = kOffLen + kLenCache * 4;  // full, empty [NSTG]; ep_full, ep_empty
-  static constexpr int kOffInfo = kOffBar + (2 * NSTG + 2 * kEpSlots) * 8;
+  static constexpr int kOffBar = kOffLen + kLenCache * 4;  // full, empty, ep_full [NSTG]
+  static constexpr int kOffInfo = kOffBar + 3 * NSTG * 8;
   static constexpr int kBytes = kOffInfo + 32;
   static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kStage % 1024 == 0 && kEpBytes % 16 == 0 && kOffBar % 8 == 0, "alignment");
+  static_assert(kStage % 1024 == 0 && kStateBytes % 16 == 0 && kOffBar % 8 == 0, "alignment");
 };
 
 struct DecodeParams {
@@ -277,8 +283,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t s_base = smem_addr(smem);
   const uint32_t full = s_base + L::kOffBar;
   const uint32_t empty = full + 8 * NSTG;
-  const uint32_t ep_full = empty + 8 * NSTG;
-  const uint32_t ep_empty = ep_full + 8 * kEpSlots;
+  const uint32_t ep_full = empty + 8 * NSTG;  // [NSTG]: a run queued for the epilogue warp
+  int *queue = reinterpret_cast<int *>(smem + L::kOffQueue);
+  float4 *side_ml = reinterpret_cast<float4 *>(smem + L::kOffML);
   volatile int *info = reinterpret_cast<volatile int *>(smem + L::kOffInfo);
   int *s_len = reinterpret_cast<int *>(smem + L::kOffLen);
   int *stage_meta = reinterpret_cast<int *>(smem + L::kOffMeta);
@@ -385,10 +392,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_init(full + 8 * s, 1);
         mbar_init(empty + 8 * s, kMmaWarps);
       }
-      for (int e = 0; e < kEpSlots; ++e) {
-        mbar_init(ep_full + 8 * e, 1);
-        mbar_init(ep_empty + 8 * e, 1);
-      }
+      for (int e = 0; e < NSTG; ++e) mbar_init(ep_full + 8 * e, kMmaWarps);
       fence_barrier_init();
     }
   }
@@ -454,25 +458,93 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == kEpilogueWarp) {
     // ------------------------------------------------------------ epilogue
-    // Publishes the partial states of runs that end inside the CTA's range,
-    // so the MMA warps go on streaming meanwhile: the state goes to slot
-    // c + plane, then (fence) the plane's unit counter; the run that completes
-    // the count merges the plane's parts. A run whose count is already
-    // complete when it starts merges without publishing.
+    // Finishes the runs that end before the CTA's last unit, so the MMA
+    // warps go on streaming meanwhile. Per queued run it folds the four MMA
+    // warps' (m, l, O) states, in warp order, from the run's last stage (then
+    // releases the stage), and either writes O (the run is the whole plane)
+    // or publishes a partial: the state goes to slot c + plane, then (fence)
+    // the plane's unit counter; the run that completes the count merges the
+    // plane's parts. A run whose count is already complete when it starts
+    // merges without publishing.
+    float *so = reinterpret_cast<float *>(smem + L::kOffEp);
+    float *sm = so + kHeads * L::kRow, *sl = sm + kHeads;
+    const int r_lo = lane >> 2, r_hi = r_lo + 8, cc = 2 * (lane & 3);
     for (int k = 0;; ++k) {
-      const int e = k & 1;
-      if (!mbar_wait_warp(ep_full + 8 * e, (k >> 1) & 1, nullptr)) {
+      const int qk = k % NSTG;
+      if (!mbar_wait_warp(ep_full + 8 * qk, (k / NSTG) & 1, nullptr)) {
         if (lane == 0) record_error(prm.err_word, kErrTimeout);
         return;
       }
-      float *so = reinterpret_cast<float *>(smem + L::kOffEp + e * L::kEpBytes);
-      float *sm = so + kHeads * L::kRow, *sl = sm + kHeads;
-      const volatile int *em = reinterpret_cast<const volatile int *>(so + L::kStateFloats);
-      if (em[0] == kEpStop) return;
-      const int b = em[1], hq0 = em[2], Gh = em[3], plane = em[4], c_first = em[5],
-                c_last = em[6], run_units = em[7], nsub = em[8];
+      const int *qe = queue + 16 * qk;
+      if (qe[0] == kEpStop) return;
+      const int b = qe[1], hq0 = qe[2], Gh = qe[3], plane = qe[4], c_first = qe[5],
+                c_last = qe[6], run_units = qe[7], nsub = qe[8], split = qe[9], st = qe[10];
+      // A first look at the plane's unit counter, its latency hidden behind
+      // the fold below (relaxed: a fence orders what it allows to be read).
       int done = 0;
-      if (lane == 0) done = ld_acquire_gpu(prm.counters + plane);
+      if (split && lane == 0) done = ld_relaxed_gpu(prm.counters + plane);
+      float A[NT][4];
+      float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) A[t][0] = A[t][1] = A[t][2] = A[t][3] = 0.f;
+      const float4 *frag = reinterpret_cast<const float4 *>(smem + st * L::kStage) + lane;
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w) {
+        const float4 ml = side_ml[(st * kMmaWarps + w) * 32 + lane];
+        float w1l, w2l, w1h, w2h;
+        merge_row(m_lo, l_lo, ml.x, ml.z, w1l, w2l);
+        merge_row(m_hi, l_hi, ml.y, ml.w, w1h, w2h);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float4 v = frag[(t >> 2) * kSub * 8 + w * 16 * 8 + (t & 3) * 32];
+          A[t][0] = fmaf(w1l, A[t][0], w2l * v.x);
+          A[t][1] = fmaf(w1l, A[t][1], w2l * v.y);
+          A[t][2] = fmaf(w1h, A[t][2], w2h * v.z);
+          A[t][3] = fmaf(w1h, A[t][3], w2h * v.w);
+        }
+      }
+      // the stage is free for the producer again
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cnt(empty + 8 * st, kMmaWarps);
+      // full row sums: the four lanes of a quad hold different keys
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+      __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D;
+      float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
+      if (!split) {
+        // the run is the whole plane: write O / l
+        const float il = 1.f / l_lo, ih = 1.f / l_hi;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (r_lo < Gh)
+            *reinterpret_cast<uint32_t *>(o_plane + r_lo * D + t * 8 + cc) =
+                pack_bf16x2(A[t][0] * il, A[t][1] * il);
+          if (r_hi < Gh)
+            *reinterpret_cast<uint32_t *>(o_plane + r_hi * D + t * 8 + cc) =
+                pack_bf16x2(A[t][2] * ih, A[t][3] * ih);
+        }
+        if (lse_plane != nullptr && (lane & 3) == 0) {
+          // log-sum-exp per head (m, l in log2 units of scale * q.k)
+          if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
+          if (r_hi < Gh) lse_plane[r_hi] = (m_hi + log2f(l_hi)) * 0.6931471805599453f;
+        }
+        continue;
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        *reinterpret_cast<float2 *>(so + r_lo * L::kRow + t * 8 + cc) = make_float2(A[t][0], A[t][1]);
+        *reinterpret_cast<float2 *>(so + r_hi * L::kRow + t * 8 + cc) = make_float2(A[t][2], A[t][3]);
+      }
+      if ((lane & 3) == 0) {
+        sm[r_lo] = m_lo;
+        sl[r_lo] = l_lo;
+        sm[r_hi] = m_hi;
+        sl[r_hi] = l_hi;
+      }
+      __syncwarp();
       bool last = __shfl_sync(0xffffffffu, done, 0) + run_units == nsub;
       if (!last) {
         float4 *dst = reinterpret_cast<float4 *>(prm.part + static_cast<size_t>(c + plane) * kSlot);
@@ -500,15 +572,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           m = sm[h];
           l = sl[h];
         };
-        merge_parts<D, 2, 2>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
-                             c_last - c_first + 1, c - c_first, self, Gh,
-                             prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D,
-                             prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0,
-                             lane, 32);
+        merge_parts<D, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+                             c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32);
         if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ep_empty + 8 * e);
+      __syncwarp();  // every lane is done with the state buffer
     }
   }
 
@@ -516,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const float sl2 = prm.scale_log2;
   const int wrow = warp * 16;  // this warp's first row in a unit
   int seg_first_i = 0, seg_first_s = 0;
-  int ep_k = 0;  // run states handed to the epilogue warp so far
+  int ep_k = 0;  // runs queued for the epilogue warp so far
   int counter_seen = 0, counter_seen2 = 0;  // the last run's looks at its plane counter
   struct FinalRun {
     int plane = -1, c_first, c_last, run_units, nsub, Gh;
@@ -661,14 +729,48 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (lane == 0) mbar_arrive(empty + 8 * st);
       continue;
     }
-    // ---- the run ends here. Stage st stays held and serves as merge
-    // scratch; the other stages keep streaming the next units meanwhile.
+    // ---- the run ends here; stage st stays held
     const int plane_first = u0 + seg_first_i - seg_first_s;  // global unit of (plane, s = 0)
     const int c_first = owner_of(plane_first, sp), c_last = owner_of(plane_first + nsub - 1, sp);
     const bool split = c_first != c_last;
     const int plane = b * planes_per_b + pib;
     const int run_units = i - seg_first_i + 1;
-    const int e = ep_k & 1;
+    if (!final_run) {
+      // Hand the run to the epilogue warp and go on streaming. The warp's
+      // fragments go to the K and V rows of the stage that only this warp
+      // reads (lane-contiguous float4 per n-tile: no bank conflicts), its
+      // (m, l) to the stage's side buffer; the epilogue warp releases the
+      // stage. The queue cannot overrun: every queued run holds a stage.
+      const int qk = ep_k % NSTG;
+      __syncwarp();  // the warp's reads of its rows are done
+      float4 *rows = reinterpret_cast<float4 *>(smem + st * L::kStage) + wrow * 8 + lane;
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        rows[(t >> 2) * kSub * 8 + (t & 3) * 32] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+      side_ml[(st * kMmaWarps + warp) * 32 + lane] = make_float4(m_lo, m_hi, l_lo, l_hi);
+      if (warp == 0 && lane == 0) {
+        int *qe = queue + 16 * qk;
+        qe[0] = kEpRun;
+        qe[1] = b;
+        qe[2] = hq0;
+        qe[3] = Gh;
+        qe[4] = plane;
+        qe[5] = c_first;
+        qe[6] = c_last;
+        qe[7] = run_units;
+        qe[8] = nsub;
+        qe[9] = split ? 1 : 0;
+        qe[10] = st;
+      }
+      fence_proxy_async_smem();  // before the TMA that refills the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ep_full + 8 * qk);
+      ++ep_k;
+      continue;
+    }
+    // The CTA's last run: the four warps merge their (m, l, O) fragments
+    // in the held stage (a lane with the same lane of another warp holds the
+    // same heads and columns): warps 2,3 -> 0,1, then warp 1 -> warp 0.
     float *tree = reinterpret_cast<float *>(smem + st * L::kStage);
     float *mine = tree + lane * L::kLaneFloats;
     auto put = [&](int slot) {
@@ -693,11 +795,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         acc[t][3] = fmaf(w1h, acc[t][3], w2h * a.w);
       }
     };
-    if (warp == 0 && split && !final_run && ep_k >= kEpSlots &&
-        !mbar_wait_warp(ep_empty + 8 * e, ((ep_k >> 1) & 1) ^ 1, nullptr) && lane == 0)
-      record_error(prm.err_word, kErrTimeout);
-    // merge the four warps (a lane with the same lane of another warp holds
-    // the same heads and columns): warps 2,3 -> 0,1, then warp 1 -> warp 0
     mma_warps_sync();  // every warp is done reading stage st
     if (warp >= 2) put(warp - 2);
     mma_warps_sync();
@@ -707,10 +804,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mma_warps_sync();
     __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D;
     float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
-    // where a split run's merged state goes: an epilogue slot, or (the CTA's
-    // last run) behind the tree slots in the held stage
-    float *state = final_run ? tree + L::kTreeBytes / 4
-                             : reinterpret_cast<float *>(smem + L::kOffEp + e * L::kEpBytes);
+    // a split run's merged state stays behind the tree slots in the stage
+    float *state = tree + L::kTreeBytes / 4;
     float *st_m = state + kHeads * L::kRow, *st_l = st_m + kHeads;
     if (warp == 0) {
       take(0);
@@ -749,23 +844,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           st_m[r_hi] = m_hi;
           st_l[r_hi] = l_hi;
         }
-        if (!final_run) {
-          // hand the state to the epilogue warp
-          __syncwarp();
-          if (lane == 0) {
-            int *em = reinterpret_cast<int *>(state + L::kStateFloats);
-            em[0] = kEpPartial;
-            em[1] = b;
-            em[2] = hq0;
-            em[3] = Gh;
-            em[4] = plane;
-            em[5] = c_first;
-            em[6] = c_last;
-            em[7] = run_units;
-            em[8] = nsub;
-            mbar_arrive(ep_full + 8 * e);
-          }
-        } else if (lane == 0) {
+        if (lane == 0) {
           // If every other run of the plane had counted in (their partials
           // published before their count) when one of the early looks at the
           // counter was made, this run is the last one and merges without
@@ -776,11 +855,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
       }
     }
-    if (split && !final_run) ++ep_k;
-    if (split && final_run) {
+    if (split) {
       // the CTA's last run leaves the loop with its merged state in shared
-      // memory (the stage stays held); it is published and merged below,
-      // outside the loop, so the loop's registers stay low
+      // memory; it is published and merged below, outside the loop, so the
+      // loop's registers stay low
       fin.plane = plane;
       fin.c_first = c_first;
       fin.c_last = c_last;
@@ -790,13 +868,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       fin.o_plane = o_plane;
       fin.lse_plane = lse_plane;
       fin.state = state;
-      break;
     }
-    // release the held stage (its generic-proxy writes ordered before the
-    // TMA that refills it)
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty + 8 * st);
+    break;
   }
   if (fin.plane >= 0) {
     // ---- the CTA's last run, part of a plane other CTAs share
@@ -849,18 +922,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
     }
   }
-  // tell the epilogue warp that no more run states follow
-  if (warp == 0) {
-    const int e = ep_k & 1;
-    if (ep_k >= kEpSlots && !mbar_wait_warp(ep_empty + 8 * e, ((ep_k >> 1) & 1) ^ 1, nullptr)) {
-      if (lane == 0) record_error(prm.err_word, kErrTimeout);
-      return;
-    }
-    if (lane == 0) {
-      reinterpret_cast<int *>(smem + L::kOffEp + e * L::kEpBytes + L::kStateBytes)[0] = kEpStop;
-      mbar_arrive(ep_full + 8 * e);
-    }
-  }
+  // tell the epilogue warp that no more runs follow (every queued run holds
+  // a stage, so the entry's previous use has been consumed)
+  const int qk = ep_k % NSTG;
+  if (warp == 0 && lane == 0) queue[16 * qk] = kEpStop;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(ep_full + 8 * qk);
 }
 
 template <int D, int NSTG>
