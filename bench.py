@@ -10,7 +10,9 @@ One step = one pass of the whole hot path over one batch of synthetic input:
 causal) over the prefill kernel's device time; the decode throughput in GB/s
 (valid cache rows once per K/V head, plus q, o and seqlens) is reported in
 the `decode` object. Inputs are rotated over enough copies that every step
-reads operands that are not in the 129 MB L2.
+reads operands that are not in the 129 MB L2. After the step, a ragged batch
+of eight prompts (LLaMA-3-8B heads, 256-4096 tokens) is timed through
+gqa_attn_fwd_varlen in a region of its own and reported in `varlen`.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With --gpus N > 1 it runs under torch.distributed.run, one replica per GPU
@@ -210,6 +212,31 @@ def run_ours(args):
         for i in range(rest):
             singles[i % copies].replay()
 
+    # The ragged batch (one call = the plan kernel + the prefill kernel) is
+    # timed in a region of its own after the step, over its own rotating
+    # copies.
+    vs = inputs.varlen_batch_shape()
+    vq0, vk0, vv0, vcq0, vck0 = inputs.varlen_inputs_for(vs)
+    var_bytes = (vq0.numel() + vk0.numel() + vv0.numel()) * 2
+    var_copies = max(2, math.ceil(3 * L2_BYTES / var_bytes))
+    var = [(vq0.to(dev), vk0.to(dev), vv0.to(dev), vcq0.to(dev), vck0.to(dev))
+           for _ in range(var_copies)]
+    o_var = torch.empty_like(var[0][0])
+
+    def call_var(i, s):
+        q, k, v, cq, ck = var[i % var_copies]
+        ops.gqa_attn_fwd_varlen(q, k, v, cq, ck, o_var, causal=True, scale=vs.scale, stream=s)
+
+    with torch.cuda.stream(cap):
+        for i in range(var_copies):
+            call_var(i, cap)
+    torch.cuda.synchronize()
+    var_chain = var_copies * max(1, 8 // var_copies)
+    chain_var = capture(call_var, 0, var_chain)
+    var_reps = max(1, math.ceil(min(max(K, 4), 40) / var_chain))
+    K_var = var_reps * var_chain
+    chain_var.replay()
+
     for _ in range(max(1, args.warmup // chain)):
         chain_pre.replay()
         chain_dec.replay()
@@ -234,6 +261,13 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
         wall = time.perf_counter() - t0
+        ev_var = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev_var[0].record(stream)
+        for _ in range(var_reps):
+            chain_var.replay()          # K_var ragged-batch calls
+        ev_var[1].record(stream)
+        torch.cuda.synchronize()
+    tot_var = ev_var[0].elapsed_time(ev_var[1])
     tot_pre = ev[0].elapsed_time(ev[1])   # ms
     tot_dec = ev[1].elapsed_time(ev[2])
     gpu_err = ops.gqa_attn_get_device_error(stream=cap)  # the graphs' error word
@@ -273,10 +307,11 @@ def run_ours(args):
     e2e_dec = sum(e[1].elapsed_time(e[2]) for e in eev) / e2e_steps
 
     # ---- max over ranks
-    vals = torch.tensor([tot_pre, tot_dec, wall, e2e_pre, e2e_dec], dtype=torch.float64, device=dev)
+    vals = torch.tensor([tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var], dtype=torch.float64,
+                        device=dev)
     if world > 1:
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    tot_pre, tot_dec, wall, e2e_pre, e2e_dec = vals.tolist()
+    tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var = vals.tolist()
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -348,6 +383,29 @@ def run_ours(args):
             },
             "e2e": {"value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},
+        },
+        "varlen": {
+            "value": round(world * K_var * vs.flops / (tot_var * 1e-3) / 1e12, 3),
+            "unit": "TFLOP/s",
+            "ms": round(tot_var / K_var, 6),
+            "calls": K_var,
+            "gpu_launches": 2 * K_var,  # the plan kernel + the prefill kernel per call
+            "config": {"workload": vs.name, "lens": list(vs.lens_q), "H_q": vs.H_q,
+                       "H_kv": vs.H_kv, "d": vs.d, "causal": vs.causal,
+                       "layout": "token-major [total][H][d], cu_seqlens on the device",
+                       "l2": f"inputs rotated over {var_copies} copies "
+                             f"({var_copies * var_bytes / 2**20:.0f} MiB)"},
+            "roofline": {
+                "bound": "tensor",
+                "kernel": "varlen_plan_kernel + prefill_varlen_kernel<128, 0> (per call)",
+                "achieved": round(vs.flops / (tot_var / K_var * 1e-3) / 1e12, 3),
+                "peak": tc_peak,
+                "unit": "TFLOP/s",
+                "frac": round(vs.flops / (tot_var / K_var * 1e-3) / 1e12 / tc_peak, 4),
+                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
+                                            "prefill_varlen_kernel<128, 0>"),
+            },
         },
         "e2e": {"value": round(pre_flops / (e2e_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre},

@@ -57,7 +57,7 @@ int device_sms(int dev) {
 // `partials_bytes` of partials space and `counters` zeroed decode counters;
 // creates or grows it stream-ordered.
 int get_workspace(cudaStream_t stream, size_t partials_bytes, Workspace **out,
-                  size_t counters = 0) {
+                  size_t counters = 0, size_t units = 0) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -112,6 +112,23 @@ int get_workspace(cudaStream_t stream, size_t partials_bytes, Workspace **out,
     ws.counters = static_cast<int *>(p);
     ws.counters_len = want;
   }
+  if (units > ws.units_len) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap != cudaStreamCaptureStatusNone)
+      return GQA_ERR_OOM;
+    if (ws.units) cudaFreeAsync(ws.units, stream);
+    ws.units = nullptr;
+    ws.units_len = 0;
+    void *p = nullptr;
+    const size_t want = units < 4096 ? 4096 : units + units / 4;
+    e = cudaMallocAsync(&p, want * sizeof(int4), stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GQA_ERR_OOM;
+    }
+    ws.units = static_cast<int4 *>(p);
+    ws.units_len = want;
+  }
   *out = &ws;
   return GQA_OK;
 }
@@ -152,10 +169,33 @@ bool encode_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long p
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor [tokens][heads][d] viewed for TMA as (column, head, token) with
+// boxes of 64 columns x 1 head x box_rows tokens: in shared memory such a box
+// is box_rows rows of 128 bytes, the layout of a [planes][rows][d] box.
+bool encode_bf16_thd(CUtensorMap *map, const void *base, int d, long heads, long tokens,
+                     int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(heads) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace gqa {
 // Shared with the other host-side translation units of the library.
+bool encode_tensor_map_bf16_thd(CUtensorMap *map, const void *base, int d, long heads,
+                                long tokens, int box_rows) {
+  return encode_bf16_thd(map, base, d, heads, tokens, box_rows);
+}
 bool encode_tensor_map_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long planes,
                                int box_rows) {
   return encode_bf16_3d(map, base, d, rows, planes, box_rows);
@@ -255,6 +295,64 @@ int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float
   cudaError_t e =
       launch_prefill_tc(tq, tk, tv, o, lse, plan, d, scale, ws->ctl, device_sms(dev), stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_attn_fwd_varlen_lse(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H_q,
+                            int H_kv, int total_q, int total_k, int d, int causal, float scale,
+                            cudaStream_t stream) {
+  if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GQA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) != 0)
+    return GQA_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
+  if (B <= 0 || H_q <= 0 || H_kv <= 0 || total_q < 0 || total_k < 0 || d <= 0)
+    return GQA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (B > kVarlenMaxB) return GQA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(total_q) * H_q * d > kMaxElems ||
+      static_cast<long long>(total_k) * H_kv * d > kMaxElems)
+    return GQA_ERR_UNSUPPORTED;
+  if (total_q == 0) return GQA_OK;  // no query rows: nothing to compute
+  if (total_k == 0) return GQA_ERR_INVALID_ARG;  // rows with no keys
+  const long long most = varlen_max_units(B, H_q, H_kv, total_q);
+  if (most > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
+  Workspace *ws = nullptr;
+  int rc = get_workspace(stream, 0, &ws, 0, static_cast<size_t>(most));
+  if (rc != GQA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_thd(&tq, q, d, H_q, total_q, kTileM) ||
+      !encode_bf16_thd(&tk, k, d, H_kv, total_k, kTileN) ||
+      !encode_bf16_thd(&tv, v, d, H_kv, total_k, kTileN))
+    return cuda_fail(cudaErrorInvalidValue);
+  VarlenArgs va;
+  va.cu_q = cu_seqlens_q;
+  va.cu_k = cu_seqlens_k;
+  va.units = ws->units;
+  va.B = B;
+  va.H_q = H_q;
+  va.H_kv = H_kv;
+  va.group = H_q / H_kv;
+  va.causal = causal ? 1 : 0;
+  va.total_q = total_q;
+  va.total_k = total_k;
+  cudaError_t e = launch_varlen_plan(va, ws->units, ws->ctl, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  e = launch_prefill_tc_varlen(tq, tk, tv, o, lse, va, d, scale, ws->ctl, device_sms(dev), stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H_q, int H_kv,
+                        int total_q, int total_k, int d, int causal, float scale,
+                        cudaStream_t stream) {
+  return gqa_attn_fwd_varlen_lse(q, k, v, o, nullptr, cu_seqlens_q, cu_seqlens_k, B, H_q, H_kv,
+                                 total_q, total_k, d, causal, scale, stream);
 }
 
 int gqa_attn_fwd(const void *q, const void *k, const void *v, void *o, int B, int H_q, int H_kv,

@@ -131,10 +131,12 @@ GQA_HD Unit decode_unit(const PrefillPlan &p, int u) {
 // ------------------------------------------------------------------------
 // Workspace: per (device, stream). Layout of the control block (ints):
 //   [0] device error word   [1] work counter   [2] CTAs finished
+//   [3] units listed by the ragged-batch plan kernel
 // ------------------------------------------------------------------------
 constexpr int kCtlErr = 0;
 constexpr int kCtlWork = 1;
 constexpr int kCtlDone = 2;
+constexpr int kCtlVarlenUnits = 3;
 constexpr int kCtlInts = 64;
 
 struct Workspace {
@@ -143,13 +145,62 @@ struct Workspace {
   size_t partials_bytes = 0;
   int *counters = nullptr;   // split-KV decode: splits finished per (b, h_kv); re-armed by the kernel
   size_t counters_len = 0;
+  int4 *units = nullptr;     // ragged-batch prefill: the plan kernel's unit list
+  size_t units_len = 0;
 };
+
+// ------------------------------------------------------------------------
+// Ragged-batch (varlen) prefill. B sequences packed token-major:
+// q / o [total_q][H_q][d] and k / v [total_k][H_kv][d]; sequence b owns the
+// query tokens [cu_q[b], cu_q[b+1]) and the key tokens [cu_k[b], cu_k[b+1]),
+// causal alignment bottom-right within each sequence. A one-block plan
+// kernel checks the offsets and lists the units -- (b, h_kv, pair of query
+// tiles), the tiles of each sequence paired heaviest first as in the dense
+// schedule -- sorted by key blocks, most first; the persistent kernel's
+// producer takes units from that list through the atomic counter.
+// ------------------------------------------------------------------------
+constexpr int kVarlenMaxB = 4096;       // sequences per call
+constexpr int kVarlenMaxBlocks = 4096;  // 128-row key blocks per sequence
+
+struct VarlenArgs {
+  const int *cu_q, *cu_k;  // device int32 [B + 1]
+  const int4 *units;       // the plan kernel's list: {b, h_kv, pair, key blocks}
+  int B, H_q, H_kv, group, causal, total_q, total_k;
+};
+
+// Units a call can list at most (workspace sizing): every sequence's query
+// tiles, paired, for each K/V head.
+GQA_HD long long varlen_max_units(int B, int H_q, int H_kv, long long total_q) {
+  const long long group = H_q / H_kv;
+  const long long tiles = total_q / kTileM + B;  // sum over b of ceil(len_q / 128)
+  return static_cast<long long>(H_kv) * ((group * tiles + B) / 2 + B);
+}
+
+// Key blocks query tile qt of a sequence (len_q, len_k) visits.
+GQA_HD int varlen_kv_blocks(int len_q, int len_k, int causal, int qt) {
+  const int n_kt = (len_k + kTileN - 1) / kTileN;
+  if (!causal) return n_kt;
+  int last_row = (qt + 1) * kTileM - 1;
+  if (last_row > len_q - 1) last_row = len_q - 1;
+  const int nb = (last_row + len_k - len_q) / kTileN + 1;  // len_k >= len_q: never negative
+  return nb < n_kt ? nb : n_kt;
+}
 
 // Launchers (return a cudaError_t; arguments already validated).
 // lse: optional per-row log-sum-exp output (null: not written).
 cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                               const CUtensorMap &tm_v, void *o, float *lse, const PrefillPlan &plan,
                               int d, float scale, int *ctl, int num_sms, cudaStream_t stream);
+
+// The varlen plan kernel (one block) writes the unit list to `units` and its
+// length to ctl[kCtlVarlenUnits]; bad offsets set kErrBadSeqlen in
+// ctl[kCtlErr] and the sequence is left out. The prefill kernel then reads
+// q, k, v through THD tensor maps: [total][H][d] with 128-token boxes.
+cudaError_t launch_varlen_plan(const VarlenArgs &va, int4 *units, int *ctl, cudaStream_t stream);
+cudaError_t launch_prefill_tc_varlen(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                     const CUtensorMap &tm_v, void *o, float *lse,
+                                     const VarlenArgs &va, int d, float scale, int *ctl,
+                                     int num_sms, cudaStream_t stream);
 
 cudaError_t launch_attn_f32(const float *q, const float *k, const float *v, float *o, int B,
                             int H_q, int H_kv, int N_q, int N_kv, int d, int causal, float scale,
@@ -185,5 +236,10 @@ cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStre
 // box_rows rows, 128-byte swizzle, zero fill outside. False on failure.
 bool encode_tensor_map_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long planes,
                                int box_rows);
+// bf16 tensor [tokens][heads][d] (token-major) for TMA: boxes of 64 columns
+// x 1 head x box_rows tokens, laid out in shared memory like a box_rows-row
+// tile of the [planes][rows][d] view. False on failure.
+bool encode_tensor_map_bf16_thd(CUtensorMap *map, const void *base, int d, long heads,
+                                long tokens, int box_rows);
 
 }  // namespace gqa

@@ -59,6 +59,11 @@ static_assert(kRegsLow + 2 * kRegsHigh <= 3 * kLaunchRegs,
 static_assert(kRegsLow % 8 == 0 && kRegsHigh % 8 == 0 && kRegsLow >= 24 && kRegsHigh <= 256,
               "setmaxnreg counts must be multiples of 8 in [24, 256]");
 constexpr int kTmemCols = 512;
+// A ragged-batch unit as the producer decodes it for the other roles:
+// b, h_kv, then (h_q, q_tile, key blocks) of tile 0 and of tile 1, then the
+// sequence's first query token, query length, first key token, key length.
+constexpr int kDescInts = 16;
+enum { kDB = 0, kDHkv, kDT0, kDT1 = kDT0 + 3, kDQ0 = kDT1 + 3, kDLenQ, kDK0, kDLenK };
 constexpr float kRescaleThreshold = 8.0f;
 #ifndef GQA_EX2_BF16
 #define GQA_EX2_BF16 1
@@ -81,25 +86,30 @@ struct TcLayout {
   static constexpr int kOffSched = kOffBar + kNumBars * 8;
   static constexpr int kOffTmem = kOffSched + 8;
   static constexpr int kOffAbort = kOffTmem + 4;
-  static constexpr int kBytes = kOffAbort + 4;
+  // ragged batches: the decoded unit of each schedule slot (kDescInts ints)
+  static constexpr int kOffDesc = (kOffAbort + 4 + 15) / 16 * 16;
+  static constexpr int kBytes = kOffDesc + 2 * kDescInts * 4;
   static constexpr int kAlloc = kBytes + 1024;
 };
 
 struct TcParams {
   __nv_bfloat16 *o;
-  float *lse;     // [B][H_q][N_q] natural-log sum of exp(scale q.k) per row, or null
+  float *lse;     // per row natural-log sum of exp(scale q.k), or null: [B][H_q][N_q]
+                  // (dense) or [H_q][total_q] (ragged batch)
   int o_align32;  // o is 32-byte aligned (rows are then too: D * 2 bytes each)
   PrefillPlan plan;
+  VarlenArgs va;  // ragged batches only
   float scale_log2;
   int *ctl;
 };
 
-// kLse: also write each row's log-sum-exp (a separate instantiation, so the
-// plain kernel carries none of its code)
-template <int D, bool kLse>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+// The kernel body. kLse: also write each row's log-sum-exp (a separate
+// instantiation, so the plain kernel carries none of its code). kVarlen: a
+// ragged batch packed token-major ([total][H][d]), its units taken from the
+// plan kernel's list; it is launched as its own kernel, prefill_varlen_kernel.
+template <int D, bool kLse, bool kVarlen>
+__device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                             const CUtensorMap &tm_v, const TcParams &prm) {
   using L = TcLayout<D>;
   // At D = 128 the P of a block is handed over in two halves, so the PV over
   // the first 64 keys overlaps the exponentials of the other 64; at D = 64
@@ -118,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
   const uint32_t bars = s_base + L::kOffBar;
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   volatile int *sched = reinterpret_cast<volatile int *>(smem + L::kOffSched);
+  volatile int *sdesc = reinterpret_cast<volatile int *>(smem + L::kOffDesc);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffTmem);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffAbort);
 
@@ -177,20 +188,68 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
     // ------------------------------------------------------------ producer
     int it = 0, kv_it = 0, vc0 = 0, vc1 = 0;
     bool ok = true;
+    // units to take: the dense plan's count, or the plan kernel's list length
+    // (written before this grid's dependency wait returned)
+    int total_units = plan.total_units;
+    if constexpr (kVarlen) total_units = __ldcg(prm.ctl + kCtlVarlenUnits);
     while (ok) {
       int u = 0;
       if (lane == 0) u = atomicAdd(prm.ctl + kCtlWork, 1);
       u = __shfl_sync(0xffffffffu, u, 0);
       const int slot = it & 1;
+      Unit w;
+      int q0 = 0, len_q = 0, k0 = 0, len_k = 0;
+      if (u < total_units) {
+        if constexpr (kVarlen) {
+          // the listed unit: sequence b, K/V head, pair of query tiles
+          const int4 un = __ldcg(prm.va.units + u);
+          const int g = prm.va.group;
+          w.b = un.x;
+          w.h_kv = un.y;
+          q0 = __ldg(prm.va.cu_q + w.b);
+          len_q = __ldg(prm.va.cu_q + w.b + 1) - q0;
+          k0 = __ldg(prm.va.cu_k + w.b);
+          len_k = __ldg(prm.va.cu_k + w.b + 1) - k0;
+          const int n_qt = (len_q + kTileM - 1) / kTileM;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int f = 2 * un.z + t;
+            if (f < g * n_qt) {
+              w.t[t].q_tile = n_qt - 1 - f / g;
+              w.t[t].h_q = w.h_kv * g + f % g;
+              w.t[t].kv_blocks = varlen_kv_blocks(len_q, len_k, prm.va.causal, w.t[t].q_tile);
+            } else {
+              w.t[t].q_tile = w.t[t].h_q = -1;
+              w.t[t].kv_blocks = 0;
+            }
+          }
+        } else {
+          w = decode_unit(plan, u);
+        }
+      }
       if (!mbar_wait_warp(bar(L::kSchedEmpty + slot), ((it >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
       __syncwarp();
       if (lane == 0) {
-        sched[slot] = u;
+        sched[slot] = u < total_units ? u : -1;  // -1: no more work
+        if constexpr (kVarlen) {
+          volatile int *dsc = sdesc + kDescInts * slot;
+          dsc[kDB] = w.b;
+          dsc[kDHkv] = w.h_kv;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            dsc[kDT0 + 3 * t] = w.t[t].h_q;
+            dsc[kDT0 + 3 * t + 1] = w.t[t].q_tile;
+            dsc[kDT0 + 3 * t + 2] = w.t[t].kv_blocks;
+          }
+          dsc[kDQ0] = q0;
+          dsc[kDLenQ] = len_q;
+          dsc[kDK0] = k0;
+          dsc[kDLenK] = len_k;
+        }
         mbar_arrive(bar(L::kSchedFull + slot));
       }
       ++it;
-      if (u >= plan.total_units) break;
-      const Unit w = decode_unit(plan, u);
+      if (u >= total_units) break;
       const int nb = max(w.t[0].kv_blocks, w.t[1].kv_blocks);
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -204,9 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
           const uint32_t dst = s_base + L::kOffQ + t * L::kTileBytes;
           mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTileBytes);
 #pragma unroll
-          for (int p = 0; p < D / 64; ++p)
-            tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64,
-                        tt.q_tile * kTileM, w.b * plan.H_q + tt.h_q);
+          for (int p = 0; p < D / 64; ++p) {
+            if constexpr (kVarlen)  // [total_q][H_q][d]: (column, head, token)
+              tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64, tt.h_q,
+                          q0 + tt.q_tile * kTileM);
+            else
+              tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64,
+                          tt.q_tile * kTileM, w.b * plan.H_q + tt.h_q);
+          }
         }
         __syncwarp();
       }
@@ -223,9 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
             const uint32_t dst = s_base + L::kOffKV + st * L::kTileBytes;
             mbar_arrive_expect_tx(bar(L::kKVFull + st), L::kTileBytes);
 #pragma unroll
-            for (int p = 0; p < D / 64; ++p)
-              tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
-                          p * 64, j * kTileN, kv_plane);
+            for (int p = 0; p < D / 64; ++p) {
+              if constexpr (kVarlen)  // [total_k][H_kv][d]: (column, head, token)
+                tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
+                            p * 64, w.h_kv, k0 + j * kTileN);
+              else
+                tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
+                            p * 64, j * kTileN, kv_plane);
+            }
           }
           __syncwarp();
           ++kv_it;
@@ -310,12 +379,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       const int slot = it & 1;
       if (!mbar_wait_warp(bar(L::kSchedFull + slot), (it >> 1) & 1, abort_flag)) { ok = false; break; }
       const int u = sched[slot];
+      int nbt0 = 0, nbt1 = 0;
+      if constexpr (kVarlen) {  // read before the slot is released
+        nbt0 = sdesc[kDescInts * slot + kDT0 + 2];
+        nbt1 = sdesc[kDescInts * slot + kDT1 + 2];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kSchedEmpty + slot));
       ++it;
-      if (u >= plan.total_units) break;
-      const Unit w = decode_unit(plan, u);
-      const int nbt0 = w.t[0].kv_blocks, nbt1 = w.t[1].kv_blocks;
+      if (u < 0) break;
+      if constexpr (!kVarlen) {
+        const Unit w = decode_unit(plan, u);
+        nbt0 = w.t[0].kv_blocks;
+        nbt1 = w.t[1].kv_blocks;
+      }
       const int nb = max(nbt0, nbt1);
       if (nbt0 > 0 && !mbar_wait_warp(bar(L::kQFull + 0), vc0 & 1, abort_flag)) ok = false;
       if (ok && nbt1 > 0 && !mbar_wait_warp(bar(L::kQFull + 1), vc1 & 1, abort_flag)) ok = false;
@@ -394,18 +471,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       const int slot = it & 1;
       if (!mbar_wait_warp(bar(L::kSchedFull + slot), (it >> 1) & 1, abort_flag)) { ok = false; break; }
       const int u = sched[slot];
+      // this warpgroup's tile: (b, h_q, q_tile, key blocks); the sequence's
+      // query and key lengths and (ragged batches) first query token
+      int b = 0, h_q = 0, q_tile = 0, nbt = 0, q0 = 0, len_q = plan.N_q, len_k = plan.N_kv;
+      if constexpr (kVarlen) {  // read before the slot is released
+        const volatile int *dsc = sdesc + kDescInts * slot;
+        b = dsc[kDB];
+        h_q = dsc[kDT0 + 3 * t];
+        q_tile = dsc[kDT0 + 3 * t + 1];
+        nbt = dsc[kDT0 + 3 * t + 2];
+        q0 = dsc[kDQ0];
+        len_q = dsc[kDLenQ];
+        len_k = dsc[kDLenK];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::kSchedEmpty + slot));
       ++it;
-      if (u >= plan.total_units) break;
-      const Unit w = decode_unit(plan, u);
-      const UnitTile mine = t ? w.t[1] : w.t[0];  // select, not a runtime index
-      const int nbt = mine.kv_blocks;
+      if (u < 0) break;
+      if constexpr (!kVarlen) {
+        const Unit w = decode_unit(plan, u);
+        const UnitTile mine = t ? w.t[1] : w.t[0];  // select, not a runtime index
+        b = w.b;
+        h_q = mine.h_q;
+        q_tile = mine.q_tile;
+        nbt = mine.kv_blocks;
+      }
       if (nbt == 0) continue;
-      const int q_row = mine.q_tile * kTileM + row;
-      // last visible key of this row (inclusive)
-      int lim = plan.N_kv - 1;
-      if (plan.causal) lim = min(lim, q_row + plan.kv_offset);
+      const int q_row = q_tile * kTileM + row;
+      // last visible key of this row (inclusive; bottom-right causal)
+      int lim = len_k - 1;
+      if (plan.causal) lim = min(lim, q_row + len_k - len_q);
       float m_ref = -INFINITY;  // reference maximum, log2-scaled units
       float l_sum = 0.f;
       for (int j = 0; j < nbt; ++j) {
@@ -526,12 +621,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
       __syncwarp();
       tc_fence_after_sync();
       const float inv_l = 1.f / l_sum;
-      const size_t o_row = (static_cast<size_t>(w.b) * plan.H_q + mine.h_q) * plan.N_q + q_row;
+      // O row: [B][H_q][N_q][D] dense, [total_q][H_q][D] ragged (rows past
+      // the sequence belong to the next one and are not stored)
+      size_t o_row, lse_at;
+      if constexpr (kVarlen) {
+        o_row = static_cast<size_t>(q0 + q_row) * plan.H_q + h_q;
+        lse_at = static_cast<size_t>(h_q) * prm.va.total_q + q0 + q_row;
+      } else {
+        o_row = (static_cast<size_t>(b) * plan.H_q + h_q) * plan.N_q + q_row;
+        lse_at = o_row;
+      }
       __nv_bfloat16 *dst = prm.o + o_row * D;
-      const bool store = q_row < plan.N_q;
+      const bool store = q_row < len_q;
       // log-sum-exp of the row in natural-log units: l is relative to
       // 2^m_ref with m_ref in log2 units of scale * q.k
-      if (kLse && store) prm.lse[o_row] = (m_ref + log2f(l_sum)) * 0.6931471805599453f;
+      if (kLse && store) prm.lse[lse_at] = (m_ref + log2f(l_sum)) * 0.6931471805599453f;
       // the whole row of O in one tensor-memory load; O_t is then free for
       // the next unit's PV while the row is converted and stored
       uint32_t ov[D];
@@ -583,10 +687,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
   }
 }
 
+// [B][H][N][d] batches of equal lengths
 template <int D, bool kLse>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+  prefill_body<D, kLse, false>(tm_q, tm_k, tm_v, prm);
+}
+
+// ragged batches packed token-major
+template <int D, bool kLse>
+__global__ void __launch_bounds__(kThreads, 1) prefill_varlen_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+  prefill_body<D, kLse, true>(tm_q, tm_k, tm_v, prm);
+}
+
+template <int D, bool kLse, bool kVarlen>
+constexpr auto prefill_entry() {
+  if constexpr (kVarlen)
+    return prefill_varlen_kernel<D, kLse>;
+  else
+    return prefill_tc_kernel<D, kLse>;
+}
+
+template <int D, bool kLse, bool kVarlen>
 cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                     void *o, float *lse, const PrefillPlan &plan, float scale, int *ctl,
-                     int num_sms, cudaStream_t stream) {
+                     void *o, float *lse, const PrefillPlan &plan, const VarlenArgs &va, int grid,
+                     float scale, int *ctl, cudaStream_t stream) {
   using L = TcLayout<D>;
   static unsigned configured = 0;  // one bit per device ordinal
   int dev = 0;
@@ -596,12 +724,12 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
     // The register split is only safe if the compiled kernel is launched
     // with at least kLaunchRegs registers per thread; refuse otherwise.
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, prefill_tc_kernel<D, kLse>);
+    e = cudaFuncGetAttributes(&attr, prefill_entry<D, kLse, kVarlen>());
     if (e != cudaSuccess) return e;
     if (attr.numRegs < kLaunchRegs || attr.maxThreadsPerBlock < kThreads)
       return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(prefill_tc_kernel<D, kLse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAlloc);
+    e = cudaFuncSetAttribute(prefill_entry<D, kLse, kVarlen>(),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured |= 1u << dev;
   }
@@ -610,11 +738,141 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
   prm.lse = lse;
   prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   prm.plan = plan;
+  prm.va = va;
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.ctl = ctl;
-  const int grid = min(num_sms, plan.total_units);
-  return launch_programmatic(prefill_tc_kernel<D, kLse>, grid, kThreads, L::kAlloc, stream, tm_q, tm_k,
-                             tm_v, prm);
+  return launch_programmatic(prefill_entry<D, kLse, kVarlen>(), grid, kThreads, L::kAlloc,
+                             stream, tm_q, tm_k, tm_v, prm);
+}
+
+template <bool kVarlen>
+cudaError_t launch_any(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                       void *o, float *lse, const PrefillPlan &plan, const VarlenArgs &va, int d,
+                       int grid, float scale, int *ctl, cudaStream_t stream) {
+  const bool with_lse = lse != nullptr;
+  if (d == 64)
+    return with_lse
+               ? launch_d<64, true, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream)
+               : launch_d<64, false, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream);
+  if (d == 128)
+    return with_lse
+               ? launch_d<128, true, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream)
+               : launch_d<128, false, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream);
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------ ragged-batch plan
+//
+// One block. Per sequence b: check the offsets, then count its units,
+// H_kv * ceil(g * n_qt / 2) (n_qt = ceil(len_q / 128)); number the units b by
+// b, and (h_kv fastest) the pairs of each sequence heaviest first. Then a
+// counting sort on each unit's key blocks (the larger of its two tiles')
+// lists them most first, so the atomic counter hands out the heaviest units
+// first across all sequences. The order inside one block count is not fixed;
+// which CTA computes a unit does not change its result.
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenArgs va, int4 *units,
+                                                                   int *ctl) {
+  __shared__ int s_pre[kVarlenMaxB + 1];          // units of sequences before b
+  __shared__ int s_bin[kVarlenMaxBlocks + 1];     // per key-block count, then its next slot
+  __shared__ int s_warp[kPlanThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the previous grid of the stream may still read the list or write the offsets
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int i = tid; i <= kVarlenMaxBlocks; i += kPlanThreads) s_bin[i] = 0;
+  // ---- units per sequence; a sequence with bad offsets gets none
+  constexpr int kPer = kVarlenMaxB / kPlanThreads;  // sequences per thread
+  int cnt[kPer];
+  int local = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int b = tid * kPer + k;
+    cnt[k] = 0;
+    if (b < va.B) {
+      const int q0 = __ldg(va.cu_q + b), q1 = __ldg(va.cu_q + b + 1);
+      const int k0 = __ldg(va.cu_k + b), k1 = __ldg(va.cu_k + b + 1);
+      const int len_q = q1 - q0, len_k = k1 - k0;
+      const bool ok = q0 >= 0 && q1 >= q0 && q1 <= va.total_q && k0 >= 0 && k1 >= k0 &&
+                      k1 <= va.total_k && (len_q == 0 || len_k > 0) &&
+                      (!va.causal || len_k >= len_q) &&
+                      (len_k + kTileN - 1) / kTileN <= kVarlenMaxBlocks;
+      if (!ok) {
+        record_error(ctl + kCtlErr, kErrBadSeqlen);
+      } else if (len_q > 0) {
+        const int n_qt = (len_q + kTileM - 1) / kTileM;
+        cnt[k] = va.H_kv * ((va.group * n_qt + 1) / 2);
+      }
+    }
+    local += cnt[k];
+  }
+  // ---- exclusive scan over sequences (thread-major, kPer each)
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int b = tid * kPer + k;
+    if (b < va.B) s_pre[b] = run;
+    run += cnt[k];
+  }
+  if (tid == 0) s_pre[va.B] = s_warp[kPlanThreads / 32 - 1];  // all units
+  __syncthreads();
+  const int total = s_pre[va.B];
+  // unit x -> (b, h_kv, pair, key blocks)
+  auto unit_at = [&](int x) -> int4 {
+    int lo = 0, hi = va.B - 1;  // last b with s_pre[b] <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pre[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo, r = x - s_pre[b];
+    const int q0 = __ldg(va.cu_q + b), len_q = __ldg(va.cu_q + b + 1) - q0;
+    const int len_k = __ldg(va.cu_k + b + 1) - __ldg(va.cu_k + b);
+    const int n_qt = (len_q + kTileM - 1) / kTileM;
+    const int pair = r / va.H_kv;
+    int nb = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int f = 2 * pair + t;
+      if (f < va.group * n_qt) nb = max(nb, varlen_kv_blocks(len_q, len_k, va.causal, n_qt - 1 - f / va.group));
+    }
+    return make_int4(b, r % va.H_kv, pair, nb);
+  };
+  // ---- counting sort on key blocks, most first
+  for (int x = tid; x < total; x += kPlanThreads) atomicAdd(&s_bin[unit_at(x).w], 1);
+  __syncthreads();
+  if (tid == 0) {
+    int at = 0;
+    for (int nb = kVarlenMaxBlocks; nb >= 0; --nb) {
+      const int c = s_bin[nb];
+      s_bin[nb] = at;
+      at += c;
+    }
+    ctl[kCtlVarlenUnits] = total;
+  }
+  __syncthreads();
+  for (int x = tid; x < total; x += kPlanThreads) {
+    const int4 un = unit_at(x);
+    units[atomicAdd(&s_bin[un.w], 1)] = un;
+  }
 }
 
 }  // namespace
@@ -622,14 +880,24 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
 cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                               const CUtensorMap &tm_v, void *o, float *lse, const PrefillPlan &plan,
                               int d, float scale, int *ctl, int num_sms, cudaStream_t stream) {
-  const bool with_lse = lse != nullptr;
-  if (d == 64)
-    return with_lse ? launch_d<64, true>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream)
-                    : launch_d<64, false>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream);
-  if (d == 128)
-    return with_lse ? launch_d<128, true>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream)
-                    : launch_d<128, false>(tm_q, tm_k, tm_v, o, lse, plan, scale, ctl, num_sms, stream);
-  return cudaErrorInvalidValue;
+  const VarlenArgs none = {};
+  return launch_any<false>(tm_q, tm_k, tm_v, o, lse, plan, none, d, min(num_sms, plan.total_units),
+                           scale, ctl, stream);
+}
+
+cudaError_t launch_varlen_plan(const VarlenArgs &va, int4 *units, int *ctl, cudaStream_t stream) {
+  return launch_programmatic(varlen_plan_kernel, 1, kPlanThreads, 0, stream, va, units, ctl);
+}
+
+cudaError_t launch_prefill_tc_varlen(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                     const CUtensorMap &tm_v, void *o, float *lse,
+                                     const VarlenArgs &va, int d, float scale, int *ctl,
+                                     int num_sms, cudaStream_t stream) {
+  // the schedule fields the kernel reads; the unit count comes from the plan kernel
+  PrefillPlan plan = make_prefill_plan(1, va.H_q, va.H_kv, 1, 1, va.causal);
+  const long long most = varlen_max_units(va.B, va.H_q, va.H_kv, va.total_q);
+  const int grid = static_cast<int>(most < num_sms ? (most < 1 ? 1 : most) : num_sms);
+  return launch_any<true>(tm_q, tm_k, tm_v, o, lse, plan, va, d, grid, scale, ctl, stream);
 }
 
 }  // namespace gqa

@@ -10,14 +10,19 @@ identical values. Recipe:
   ``randint(1, max_len + 1)``), then q, k_cache, v_cache;
 * cache rows at or beyond ``seqlens[b]`` are set to NaN, so a kernel that
   reads them produces NaN and fails parity;
-* workload ``c`` uses seed ``1000 + c``; sweep variants add ``10 * sub``.
+* workload ``c`` uses seed ``1000 + c``; sweep variants add ``10 * sub``;
+* ragged batches: lengths uniform on [lo, hi] via ``randint`` (their own
+  seed), offsets ``cu[0] = 0, cu[b+1] = cu[b] + len[b]``, then q, k, v
+  token-major ([total, H, d]) in that order.
 
 The shapes follow the synthetic stand-ins for the pages' workloads: a tiny
 fp32 GQA case, an MHA/GQA/MQA sweep, a LLaMA-3-8B-shaped prefill layer
 (BootstrapAI evolution log, collab-014 "Kernel 9 GQA": seq 2048, H_q=32,
 H_kv=8, d=128), a long-sequence case sized like the persistent-kernel entry's
 "seq=4096, h=16, b=4" example, and a decode step against a bf16 K/V cache
-(microLLM-rocm optimisation log, Experiments 064-065).
+(microLLM-rocm optimisation log, Experiments 064-065), and a ragged batch of
+prompts prefilled in one call (microLLM-rocm optimisation log, Experiment
+101) with the LLaMA-3-8B layer's heads.
 """
 from __future__ import annotations
 
@@ -85,6 +90,41 @@ LONG_SEQ = PrefillShape("long_seq_persistent", 4, 16, 4, 4096, 4096, 64, True,
                         torch.bfloat16, 1003)
 
 
+@dataclass(frozen=True)
+class VarlenShape:
+    name: str
+    lens_q: tuple
+    lens_k: tuple
+    H_q: int
+    H_kv: int
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOPs: sum over sequences of 4*H_q*len_q*len_k*d, halved when
+        causal (the dense layer's convention)."""
+        f = sum(4.0 * self.H_q * lq * lk * self.d for lq, lk in zip(self.lens_q, self.lens_k))
+        return f / 2 if self.causal else f
+
+
+def varlen_batch_shape() -> VarlenShape:
+    """Eight prompts of 256-4096 tokens (seeded), LLaMA-3-8B heads (32 / 8, d = 128),
+    causal self-attention (len_k = len_q)."""
+    lens = tuple(varlen_lengths(8, 256, 4096, seed=1005))
+    return VarlenShape("llama3_8b_varlen_batch8", lens, lens, 32, 8, 128, True, 1006)
+
+
+def varlen_inputs_for(shape: VarlenShape):
+    return varlen_inputs(list(shape.lens_q), list(shape.lens_k), shape.H_q, shape.H_kv, shape.d,
+                         torch.bfloat16, shape.seed)
+
+
 def decode_shapes() -> list[DecodeShape]:
     """Decode against a bf16 cache: B in {1,8,64}, H_q=12, H_kv=2, d=128, max_len=2048."""
     return [DecodeShape(f"decode_b{b}", b, 12, 2, 2048, 128, torch.bfloat16, 1004 + 10 * i)
@@ -103,6 +143,27 @@ def prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, dtype=torch.bfloat16, seed=0):
 def prefill_inputs_for(shape: PrefillShape):
     return prefill_inputs(shape.B, shape.H_q, shape.H_kv, shape.N_q, shape.N_kv, shape.d,
                           shape.dtype, shape.seed)
+
+
+def varlen_inputs(lens_q, lens_k, H_q, H_kv, d, dtype=torch.bfloat16, seed=0):
+    """Return CPU tensors (q [total_q,H_q,d], k, v [total_k,H_kv,d], cu_q, cu_k int32 [B+1])
+    for a ragged batch packed token-major; values N(0, 1) like prefill_inputs."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    cu_q = torch.zeros(len(lens_q) + 1, dtype=torch.int32)
+    cu_k = torch.zeros(len(lens_k) + 1, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(torch.tensor(lens_q, dtype=torch.int64), 0).to(torch.int32)
+    cu_k[1:] = torch.cumsum(torch.tensor(lens_k, dtype=torch.int64), 0).to(torch.int32)
+    total_q, total_k = int(cu_q[-1]), int(cu_k[-1])
+    q = torch.randn(total_q, H_q, d, generator=g, dtype=torch.float32).to(dtype)
+    k = torch.randn(total_k, H_kv, d, generator=g, dtype=torch.float32).to(dtype)
+    v = torch.randn(total_k, H_kv, d, generator=g, dtype=torch.float32).to(dtype)
+    return q, k, v, cu_q, cu_k
+
+
+def varlen_lengths(B, lo, hi, seed):
+    """B sequence lengths drawn uniformly from [lo, hi] (seeded)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).tolist()
 
 
 def decode_inputs(B, H_q, H_kv, max_len, d, dtype=torch.bfloat16, seed=0, seqlens=None):

@@ -31,6 +31,7 @@ EXPORTED = [
     "gqa_attn_decode_f32", "gqa_attn_status_string", "gqa_attn_get_device_error",
     "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
     "gqa_attn_decode_noalloc", "gqa_attn_fwd_lse", "gqa_attn_decode_lse",
+    "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse",
 ]
 
 
@@ -77,6 +78,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.gqa_attn_fwd_lse.restype = _i
             lib.gqa_attn_decode_lse.argtypes = dec[:5] + [_vp] + dec[5:]
             lib.gqa_attn_decode_lse.restype = _i
+            # q, k, v, o, cu_q, cu_k, B, H_q, H_kv, total_q, total_k, d, causal, scale, stream
+            var = [_vp] * 6 + [_i] * 7 + [_f, _vp]
+            lib.gqa_attn_fwd_varlen.argtypes = var
+            lib.gqa_attn_fwd_varlen.restype = _i
+            lib.gqa_attn_fwd_varlen_lse.argtypes = var[:4] + [_vp] + var[4:]
+            lib.gqa_attn_fwd_varlen_lse.restype = _i
             lib.gqa_attn_status_string.argtypes = [_i]
             lib.gqa_attn_status_string.restype = ctypes.c_char_p
             lib.gqa_attn_get_device_error.argtypes = [_vp]
@@ -156,6 +163,53 @@ def _fwd(name, dtype, q, k, v, o, causal, scale, stream, lse=None):
         args = args + (lse,)
     rc = getattr(load(), name)(*args, B, H_q, H_kv, N_q, N_kv, d, int(bool(causal)),
                                float(scale), _stream(stream))
+    _check(rc, name)
+    return o
+
+
+# ---------------------------------------------------------------- ragged batches
+
+def gqa_attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, o=None, causal=False, scale=None,
+                        stream=None):
+    """bf16 prefill over a ragged batch packed token-major.
+
+    q [total_q,H_q,d], k/v [total_k,H_kv,d], cu_seqlens_q/k int32 [B+1] on the
+    device (sequence b owns rows [cu[b], cu[b+1])) -> o [total_q,H_q,d] (bf16)."""
+    return _fwd_varlen("gqa_attn_fwd_varlen", q, k, v, cu_seqlens_q, cu_seqlens_k, o, causal,
+                       scale, stream)
+
+
+def gqa_attn_fwd_varlen_lse(q, k, v, cu_seqlens_q, cu_seqlens_k, o=None, lse=None, causal=False,
+                            scale=None, stream=None):
+    """gqa_attn_fwd_varlen that also returns each row's log-sum-exp, fp32
+    [H_q, total_q]. Returns (o, lse)."""
+    if lse is None:
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    if tuple(lse.shape) != (q.shape[1], q.shape[0]):
+        raise ValueError("lse must be [H_q, total_q]")
+    o = _fwd_varlen("gqa_attn_fwd_varlen_lse", q, k, v, cu_seqlens_q, cu_seqlens_k, o, causal,
+                    scale, stream, lse=_dev(lse, torch.float32, "lse", 2))
+    return o, lse
+
+
+def _fwd_varlen(name, q, k, v, cu_q, cu_k, o, causal, scale, stream, lse=None):
+    total_q, H_q, d = q.shape
+    total_k, H_kv, _ = k.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if scale is None:
+        scale = d ** -0.5
+    if tuple(v.shape) != tuple(k.shape) or k.shape[2] != d or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, k, v, o")
+    if cu_q.dim() != 1 or tuple(cu_k.shape) != tuple(cu_q.shape) or cu_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be [B + 1] with B >= 1")
+    args = [_dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
+            _dev(v, torch.bfloat16, "v", 3), _dev(o, torch.bfloat16, "o", 3)]
+    if lse is not None:
+        args.append(lse)
+    args += [_dev(cu_q, torch.int32, "cu_seqlens_q", 1), _dev(cu_k, torch.int32, "cu_seqlens_k", 1)]
+    rc = getattr(load(), name)(*args, cu_q.numel() - 1, H_q, H_kv, total_q, total_k, d,
+                               int(bool(causal)), float(scale), _stream(stream))
     _check(rc, name)
     return o
 

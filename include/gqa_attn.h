@@ -88,6 +88,45 @@ int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float
                      int causal, float scale, cudaStream_t stream);
 
 /*
+ * Ragged-batch ("varlen") prefill: B sequences of different lengths packed
+ * token-major, one call. bf16 in / bf16 out, fp32 accumulation, same kernel
+ * design as gqa_attn_fwd.
+ *   q : [total_q][H_q][d]  bf16     k, v : [total_k][H_kv][d]  bf16
+ *   o : [total_q][H_q][d]  bf16 (written for every token some sequence owns)
+ *   cu_seqlens_q, cu_seqlens_k : device int32 [B + 1], 4-byte aligned:
+ *       sequence b owns query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1])
+ *       and key tokens [cu_seqlens_k[b], cu_seqlens_k[b+1]).
+ *   Causal alignment is bottom-right inside each sequence: its query row i
+ *   sees its key j iff j <= i + (len_k - len_q).
+ *   d in {64, 128}; 1 <= B <= 4096; each of total_q*H_q*d, total_k*H_kv*d
+ *   below 2^31; at most 4096 blocks of 128 keys per sequence.
+ * The offsets live on the device, so the library checks them there: a
+ * sequence whose offsets are decreasing, outside [0, total], with keys
+ * missing (len_q > 0 with len_k == 0, or len_k < len_q when causal) or longer
+ * than the key limit is skipped (its o rows are left as they were) and
+ * GQA_ERR_BAD_SEQLEN is recorded (gqa_attn_get_device_error). total_q == 0
+ * returns GQA_OK without launching. Two kernels are launched: a one-block
+ * plan (lists the work units, heaviest first) and the prefill kernel.
+ * Pages: microLLM-rocm optimisation log, Experiment 101 (prompts batched
+ * into one prefill) and Experiment 062 (prefill into the cache);
+ * BootstrapAI evolution log, collab-014 "Kernel 9 GQA" (semantics).
+ */
+int gqa_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,
+                        const int *cu_seqlens_q, const int *cu_seqlens_k,
+                        int B, int H_q, int H_kv, int total_q, int total_k, int d,
+                        int causal, float scale, cudaStream_t stream);
+
+/*
+ * gqa_attn_fwd_varlen that also returns each query row's log-sum-exp as
+ * fp32 [H_q][total_q] (lse[h][t] for the token t of head h; device pointer,
+ * 4-byte aligned, caller-owned). Everything else as gqa_attn_fwd_varlen.
+ */
+int gqa_attn_fwd_varlen_lse(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int *cu_seqlens_q, const int *cu_seqlens_k,
+                            int B, int H_q, int H_kv, int total_q, int total_k, int d,
+                            int causal, float scale, cudaStream_t stream);
+
+/*
  * Same operation in fp32: q, k, v, o are float arrays with the layouts of
  * gqa_attn_fwd. SIMT FMA kernel (online softmax, warp-shuffle reductions);
  * d in {32, 64, 96, 128}.

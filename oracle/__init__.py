@@ -21,7 +21,9 @@ What each function follows (page title and section):
   * causal GQA without replicating K/V heads -- microLLM-rocm optimisation
     log, Experiment 044;
   * log-sum-exp merge of key-range partials -- microLLM-rocm optimisation
-    log, Experiments 282-284 (split-sequence cached attention).
+    log, Experiments 282-284 (split-sequence cached attention);
+  * a ragged batch as the list of its sequences, each attended on its own
+    -- microLLM-rocm optimisation log, Experiment 101.
 """
 from __future__ import annotations
 
@@ -145,6 +147,65 @@ def prefill_rows(q, k, v, causal: bool, scale: float, rows):
         n = N_kv if not causal else max(0, min(N_kv, i + (N_kv - N_q) + 1))
         h_kv = h_q // group
         o[r], lse[r] = attend_row(q[b, h_q, i], k[b, h_kv, :n], v[b, h_kv, :n], scale)
+    return o, lse
+
+
+def _offsets(cu) -> np.ndarray:
+    if hasattr(cu, "detach"):
+        cu = cu.detach().cpu().numpy()
+    return np.asarray(cu, dtype=np.int64).reshape(-1)
+
+
+def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float,
+                   n_threads: int = 1):
+    """Ragged-batch prefill. q:[total_q,H_q,d], k,v:[total_k,H_kv,d] (token-major).
+
+    Sequence b owns query rows [cu_q[b], cu_q[b+1]) and key rows
+    [cu_k[b], cu_k[b+1]) and is attended on its own, exactly as a batch of
+    one by ``prefill`` (bottom-right causal inside the sequence): the ragged
+    batch is the list of its sequences (microLLM-rocm optimisation log,
+    Experiment 101, prompts batched into one prefill).
+    Returns (o [total_q,H_q,d], lse [H_q,total_q]); rows no sequence owns are NaN."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cq, ck = _offsets(cu_seqlens_q), _offsets(cu_seqlens_k)
+    if cq.shape != ck.shape or cq.size < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be [B + 1]")
+    o = np.full(q.shape, np.nan)
+    lse = np.full((q.shape[1], q.shape[0]), np.nan)
+    for b in range(cq.size - 1):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0:
+            continue
+        # [len, H, d] -> [1, H, len, d]
+        qb = np.ascontiguousarray(q[q0:q1].transpose(1, 0, 2))[None]
+        kb = np.ascontiguousarray(k[k0:k1].transpose(1, 0, 2))[None]
+        vb = np.ascontiguousarray(v[k0:k1].transpose(1, 0, 2))[None]
+        ob, lb = prefill(qb, kb, vb, causal, scale, n_threads=n_threads)
+        o[q0:q1] = ob[0].transpose(1, 0, 2)
+        lse[:, q0:q1] = lb[0]
+    return o, lse
+
+
+def prefill_varlen_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale: float, rows):
+    """Ragged-batch prefill output for selected (token t, head h_q) rows only.
+
+    Returns (o[len(rows), d], lse[len(rows)])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cq, ck = _offsets(cu_seqlens_q), _offsets(cu_seqlens_k)
+    H_q, H_kv = q.shape[1], k.shape[1]
+    if H_q % H_kv:
+        raise ValueError("H_q must be a multiple of H_kv")
+    group = H_q // H_kv
+    rows = list(rows)
+    o = np.empty((len(rows), q.shape[2]))
+    lse = np.empty(len(rows))
+    for r, (t, h_q) in enumerate(rows):
+        b = int(np.searchsorted(cq, t, side="right")) - 1
+        i = t - int(cq[b])
+        len_q, k0, len_k = int(cq[b + 1] - cq[b]), int(ck[b]), int(ck[b + 1] - ck[b])
+        n = len_k if not causal else max(0, min(len_k, i + (len_k - len_q) + 1))
+        h_kv = h_q // group
+        o[r], lse[r] = attend_row(q[t, h_q], k[k0:k0 + n, h_kv], v[k0:k0 + n, h_kv], scale)
     return o, lse
 
 

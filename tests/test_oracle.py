@@ -19,7 +19,7 @@ import pytest
 import torch
 
 import oracle
-from gqa_flash_attention_02_gb300.inputs import decode_inputs, prefill_inputs
+from gqa_flash_attention_02_gb300.inputs import decode_inputs, prefill_inputs, varlen_inputs
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -250,6 +250,73 @@ def test_oracle_head_subset_and_threads():
     flat_all, flat_sub = o_all.reshape(8, 10, 8), o_sub.reshape(8, 10, 8)
     np.testing.assert_array_equal(flat_sub[2:5], flat_all[2:5])
     assert np.isnan(flat_sub[:2]).all() and np.isnan(flat_sub[5:]).all()
+
+
+# ------------------------------------------------------------------ ragged batches
+
+def _varlen_brute(q, k, v, cu_q, cu_k, causal, scale):
+    """Attention of every owned (token, head) row by the definition, written
+    out with Python loops over the sequence's visible keys."""
+    total_q, H_q, d = q.shape
+    H_kv = k.shape[1]
+    o = np.full(q.shape, np.nan)
+    lse = np.full((H_q, total_q), np.nan)
+    for b in range(len(cu_q) - 1):
+        len_q, len_k = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+        for i in range(len_q):
+            t = cu_q[b] + i
+            n = min(len_k, i + (len_k - len_q) + 1) if causal else len_k
+            for h in range(H_q):
+                hk = h // (H_q // H_kv)
+                logits = [scale * sum(q[t, h, c] * k[cu_k[b] + j, hk, c] for c in range(d))
+                          for j in range(n)]
+                m = max(logits)
+                w = [math.exp(x - m) for x in logits]
+                z = sum(w)
+                for c in range(d):
+                    o[t, h, c] = sum(w[j] * v[cu_k[b] + j, hk, c] for j in range(n)) / z
+                lse[h, t] = m + math.log(z)
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_oracle_varlen_brute_force(causal):
+    """A ragged batch -- lengths 1, 3, 0, 5 with 2, 3, 4, 7 keys (bottom-right
+    offsets 1, 0, -, 2) -- against the definition evaluated row by row."""
+    lens_q, lens_k = [1, 3, 0, 5], [2, 3, 4, 7]
+    q, k, v = (np.random.default_rng(21).standard_normal(s) for s in
+               ((9, 4, 3), (16, 2, 3), (16, 2, 3)))
+    cu_q, cu_k = np.cumsum([0] + lens_q), np.cumsum([0] + lens_k)
+    o, lse = oracle.prefill_varlen(q, k, v, cu_q, cu_k, causal, 0.7)
+    o_b, lse_b = _varlen_brute(q, k, v, cu_q, cu_k, causal, 0.7)
+    np.testing.assert_allclose(o, o_b, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_b, rtol=0, atol=1e-13)
+
+
+def test_oracle_varlen_equal_lengths_is_dense_batch():
+    """Equal lengths packed token-major give the dense batch, transposed."""
+    q, k, v = _rand(3, 4, 2, 6, 9, 8, seed=22)
+    o, lse = oracle.prefill(q, k, v, True, 0.4)
+    pack = lambda x: np.ascontiguousarray(x.transpose(0, 2, 1, 3).reshape(-1, x.shape[1], 8))
+    cu_q, cu_k = np.arange(4) * 6, np.arange(4) * 9
+    o_v, lse_v = oracle.prefill_varlen(pack(q), pack(k), pack(v), cu_q, cu_k, True, 0.4)
+    np.testing.assert_array_equal(o_v, pack(o))
+    np.testing.assert_array_equal(lse_v, lse.transpose(1, 0, 2).reshape(4, -1))
+
+
+def test_oracle_varlen_rows_and_unowned_rows():
+    """Selected rows equal the full result; rows past cu_q[B] stay NaN."""
+    q, k, v, cu_q, cu_k = (x.numpy() for x in
+                           varlen_inputs([4, 1, 7], [6, 1, 9], 6, 2, 8, torch.float64, seed=23))
+    q_pad = np.concatenate([q, np.ones((2, 6, 8))])  # two tokens no sequence owns
+    o, lse = oracle.prefill_varlen(q_pad, k, v, cu_q, cu_k, True, 0.3)
+    assert np.isnan(o[12:]).all() and np.isnan(lse[:, 12:]).all()
+    assert np.isfinite(o[:12]).all()
+    rows = [(0, 0), (4, 5), (11, 3), (7, 1)]
+    o_r, l_r = oracle.prefill_varlen_rows(q, k, v, cu_q, cu_k, True, 0.3, rows)
+    for r, (t, h) in enumerate(rows):
+        np.testing.assert_array_equal(o_r[r], o[t, h])
+        assert l_r[r] == lse[h, t]
 
 
 def test_oracle_reads_bf16_exactly():

@@ -368,6 +368,94 @@ def test_dependent_launches_back_to_back():
 
 # ------------------------------------------------------------------ failure detection
 
+# ------------------------------------------------------------------ ragged batches
+
+VARLEN_SMALL = [
+    # lens_q, lens_k (None: = lens_q), H_q, H_kv, d, causal
+    ([300, 1, 128, 129, 77], None, 8, 2, 128, True),   # ragged tails, a one-row sequence
+    ([64, 200, 1], [164, 500, 128], 12, 4, 64, True),  # prefill after a cached prefix, g = 3
+    ([500, 37], [20, 700], 4, 1, 128, False),          # MQA, fewer / more keys than queries
+    ([0, 130, 0, 5], [0, 130, 10, 5], 8, 8, 64, True), # MHA, empty sequences
+    ([1000, 257], None, 16, 2, 128, True),             # g = 8, several K/V blocks
+]
+
+
+def _varlen_run(q, k, v, cu_q, cu_k, causal, scale, o=None):
+    qd, kd, vd, cqd, ckd = _dev(q, k, v, cu_q, cu_k)
+    if o is None:
+        o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_fwd_varlen(qd, kd, vd, cqd, ckd, o, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("case", VARLEN_SMALL, ids=lambda c: "-".join(map(str, c[0])))
+def test_bf16_varlen_matches_oracle(case):
+    lens_q, lens_k, H_q, H_kv, d, causal = case
+    lens_k = lens_k or lens_q
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs(lens_q, lens_k, H_q, H_kv, d, torch.bfloat16,
+                                               seed=140 + sum(lens_q))
+    got = _varlen_run(q, k, v, cu_q, cu_k, causal, d ** -0.5)
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, _ = oracle.prefill_varlen(q, k, v, cu_q, cu_k, causal, d ** -0.5, n_threads=THREADS)
+    _check_bf16(got, ref, f"varlen {case}")
+
+
+def test_bf16_varlen_batch_sampled():
+    """The eight-prompt LLaMA-3-8B-headed batch: one whole sequence, the first
+    and last token of every sequence in every head, and 256 random rows."""
+    s = inputs.varlen_batch_shape()
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs_for(s)
+    got = _varlen_run(q, k, v, cu_q, cu_k, s.causal, s.scale)
+    assert ops.gqa_attn_get_device_error() == 0
+    assert np.isfinite(got).all(), "a tile was never written"
+    b = int(np.argmin(s.lens_q))  # the shortest sequence, every row of every head
+    q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+    ref, _ = oracle.prefill_varlen(q[q0:q1], k[k0:k1], v[k0:k1], [0, q1 - q0], [0, k1 - k0],
+                                   s.causal, s.scale, n_threads=THREADS)
+    _check_bf16(got[q0:q1], ref, "varlen batch, whole sequence")
+    rng = np.random.default_rng(s.seed)
+    ends = [int(t) for t in cu_q[:-1]] + [int(t) - 1 for t in cu_q[1:]]
+    rows = [(t, h) for t in ends for h in range(s.H_q)]
+    rows += [(int(t), int(h)) for t, h in zip(rng.integers(0, int(cu_q[-1]), 256),
+                                              rng.integers(0, s.H_q, 256))]
+    ref, _ = oracle.prefill_varlen_rows(q, k, v, cu_q, cu_k, s.causal, s.scale, rows)
+    _check_bf16(np.stack([got[t, h] for t, h in rows]), ref, "varlen batch, sampled rows")
+
+
+def test_bf16_varlen_lse_and_determinism():
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs([300, 1, 129], [400, 1, 129], 8, 2, 128,
+                                               torch.bfloat16, seed=150)
+    qd, kd, vd, cqd, ckd = _dev(q, k, v, cu_q, cu_k)
+    o, lse = ops.gqa_attn_fwd_varlen_lse(qd, kd, vd, cqd, ckd, causal=True, scale=0.09)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref_o, ref_lse = oracle.prefill_varlen(q, k, v, cu_q, cu_k, True, 0.09)
+    _check_bf16(o.float().cpu().numpy(), ref_o, "varlen with lse")
+    err = np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max()
+    assert err <= LSE_MAX, f"lse max err {err:.3e}"
+    o2 = ops.gqa_attn_fwd_varlen(qd, kd, vd, cqd, ckd, causal=True, scale=0.09)
+    o3 = ops.gqa_attn_fwd_varlen(qd, kd, vd, cqd, ckd, causal=True, scale=0.09)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(o2, o3)
+
+
+def test_bf16_varlen_bad_offsets_reported_and_skipped():
+    """Sequence 2 has fewer keys than queries under the causal mask: the device
+    records GQA_ERR_BAD_SEQLEN and leaves its rows alone; the others are right."""
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs([130, 50, 60], [130, 50, 40], 4, 2, 64,
+                                               torch.bfloat16, seed=151)
+    got = _varlen_run(q, k, v, cu_q, cu_k, True, 0.125)
+    assert ops.gqa_attn_get_device_error() == 6  # GQA_ERR_BAD_SEQLEN
+    assert np.isnan(got[180:]).all()
+    ref, _ = oracle.prefill_varlen(q[:180], k[:180], v[:180], cu_q[:3], cu_k[:3], True, 0.125)
+    _check_bf16(got[:180], ref, "valid sequences next to a bad one")
+    # the context is still usable
+    got = _varlen_run(q[:180], k[:180], v[:180], cu_q[:3], cu_k[:3], True, 0.125)
+    assert ops.gqa_attn_get_device_error() == 0
+    _check_bf16(got, ref, "after a bad call")
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     assert ops.gqa_attn_selftest_wait_timeout(2000) == 4  # GQA_ERR_DEVICE_TIMEOUT
     assert ops.gqa_attn_get_device_error() == 0           # the word was cleared
