@@ -197,20 +197,21 @@ def run_ours(args):
 
     # A chain graph holds `chain` back-to-back calls of one kernel over the
     # rotating copies (a multiple of `copies`, so replays continue the
-    # rotation); K = reps * chain + rest calls are timed per kernel.
+    # rotation); K = reps * chain + rest calls are timed per kernel, the rest
+    # as one more graph of `rest` back-to-back calls.
     K = args.steps
     chain = copies * max(1, 24 // copies)
     reps, rest = divmod(K, chain)
     chain_pre, chain_dec = capture(call_pre, 0, chain), capture(call_dec, 0, chain)
-    single_pre = [capture(call_pre, i, 1) for i in range(copies)]
-    single_dec = [capture(call_dec, i, 1) for i in range(copies)]
+    rest_pre = capture(call_pre, 0, rest) if rest else None
+    rest_dec = capture(call_dec, 0, rest) if rest else None
     torch.cuda.synchronize()
 
-    def run_kernel(chain_g, singles):
+    def run_kernel(chain_g, rest_g):
         for _ in range(reps):
             chain_g.replay()
-        for i in range(rest):
-            singles[i % copies].replay()
+        if rest_g is not None:
+            rest_g.replay()
 
     # The ragged batch (one call = the plan kernel + the prefill kernel) is
     # timed in a region of its own after the step, over its own rotating
@@ -237,12 +238,9 @@ def run_ours(args):
     K_var = var_reps * var_chain
     chain_var.replay()
 
-    for _ in range(max(1, args.warmup // chain)):
+    for _ in range(max(1, math.ceil(args.warmup / chain))):  # at least W calls of each
         chain_pre.replay()
         chain_dec.replay()
-    for i in range(args.warmup % chain):
-        single_pre[i % copies].replay()
-        single_dec[i % copies].replay()
     torch.cuda.synchronize()
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -253,9 +251,9 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         ev[0].record(stream)
-        run_kernel(chain_pre, single_pre)   # K prefill launches
+        run_kernel(chain_pre, rest_pre)     # K prefill launches
         ev[1].record(stream)
-        run_kernel(chain_dec, single_dec)   # K decode launches
+        run_kernel(chain_dec, rest_dec)     # K decode launches
         ev[2].record(stream)
         torch.cuda.synchronize()
         if world > 1:

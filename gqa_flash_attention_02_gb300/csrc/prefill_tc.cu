@@ -772,43 +772,11 @@ cudaError_t launch_any(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
 // which CTA computes a unit does not change its result.
 constexpr int kPlanThreads = 1024;
 
-__global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenArgs va, int4 *units,
-                                                                   int *ctl) {
-  __shared__ int s_pre[kVarlenMaxB + 1];          // units of sequences before b
-  __shared__ int s_bin[kVarlenMaxBlocks + 1];     // per key-block count, then its next slot
-  __shared__ int s_warp[kPlanThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the previous grid of the stream may still read the list or write the offsets
-  grid_dependency_wait();
-  grid_launch_dependents();
-  for (int i = tid; i <= kVarlenMaxBlocks; i += kPlanThreads) s_bin[i] = 0;
-  // ---- units per sequence; a sequence with bad offsets gets none
-  constexpr int kPer = kVarlenMaxB / kPlanThreads;  // sequences per thread
-  int cnt[kPer];
-  int local = 0;
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int b = tid * kPer + k;
-    cnt[k] = 0;
-    if (b < va.B) {
-      const int q0 = __ldg(va.cu_q + b), q1 = __ldg(va.cu_q + b + 1);
-      const int k0 = __ldg(va.cu_k + b), k1 = __ldg(va.cu_k + b + 1);
-      const int len_q = q1 - q0, len_k = k1 - k0;
-      const bool ok = q0 >= 0 && q1 >= q0 && q1 <= va.total_q && k0 >= 0 && k1 >= k0 &&
-                      k1 <= va.total_k && (len_q == 0 || len_k > 0) &&
-                      (!va.causal || len_k >= len_q) &&
-                      (len_k + kTileN - 1) / kTileN <= kVarlenMaxBlocks;
-      if (!ok) {
-        record_error(ctl + kCtlErr, kErrBadSeqlen);
-      } else if (len_q > 0) {
-        const int n_qt = (len_q + kTileM - 1) / kTileM;
-        cnt[k] = va.H_kv * ((va.group * n_qt + 1) / 2);
-      }
-    }
-    local += cnt[k];
-  }
-  // ---- exclusive scan over sequences (thread-major, kPer each)
-  int incl = local;
+// Exclusive prefix of one value per thread over the block (thread order);
+// `total` receives the block's sum. Every thread must call it.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *s_warp, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -826,16 +794,68 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenA
     s_warp[lane] = w;  // inclusive over warps
   }
   __syncthreads();
-  int run = incl - local + (warp > 0 ? s_warp[warp - 1] : 0);
-#pragma unroll
+  const int excl = incl - v + (warp > 0 ? s_warp[warp - 1] : 0);
+  total = s_warp[kPlanThreads / 32 - 1];
+  __syncthreads();  // s_warp may be reused
+  return excl;
+}
+
+// Dynamic shared memory of the plan kernel for B sequences.
+inline size_t plan_smem_bytes(int B) {
+  return (3 * static_cast<size_t>(B) + 1 + kVarlenMaxBlocks + 1) * sizeof(int);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenArgs va, int4 *units,
+                                                                   int *ctl) {
+  extern __shared__ int plan_smem[];
+  int *s_pre = plan_smem;            // [B + 1] units of the sequences before b
+  int *s_lq = s_pre + va.B + 1;      // [B] query length (0: no units)
+  int *s_lk = s_lq + va.B;           // [B] key length
+  int *s_bin = s_lk + va.B;          // [kVarlenMaxBlocks + 1] per key-block count
+  __shared__ int s_warp[kPlanThreads / 32];
+  __shared__ int s_max_nb;
+  const int tid = threadIdx.x;
+  // the previous grid of the stream may still read the list or write the offsets
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (tid == 0) s_max_nb = 0;
+  __syncthreads();
+  // ---- units per sequence (kPer consecutive sequences per thread); a
+  // sequence with bad offsets gets none
+  const int kPer = (va.B + kPlanThreads - 1) / kPlanThreads;
+  int local = 0;
   for (int k = 0; k < kPer; ++k) {
     const int b = tid * kPer + k;
-    if (b < va.B) s_pre[b] = run;
-    run += cnt[k];
+    if (b >= va.B) break;
+    const int q0 = __ldg(va.cu_q + b), q1 = __ldg(va.cu_q + b + 1);
+    const int k0 = __ldg(va.cu_k + b), k1 = __ldg(va.cu_k + b + 1);
+    const int len_q = q1 - q0, len_k = k1 - k0;
+    const int n_kt = (len_k + kTileN - 1) / kTileN;
+    const bool ok = q0 >= 0 && q1 >= q0 && q1 <= va.total_q && k0 >= 0 && k1 >= k0 &&
+                    k1 <= va.total_k && (len_q == 0 || len_k > 0) &&
+                    (!va.causal || len_k >= len_q) && n_kt <= kVarlenMaxBlocks;
+    if (!ok) record_error(ctl + kCtlErr, kErrBadSeqlen);
+    const int lq = ok ? len_q : 0;
+    s_lq[b] = lq;
+    s_lk[b] = len_k;
+    if (lq > 0) {
+      local += va.H_kv * ((va.group * ((lq + kTileM - 1) / kTileM) + 1) / 2);
+      atomicMax(&s_max_nb, n_kt);
+    }
   }
-  if (tid == 0) s_pre[va.B] = s_warp[kPlanThreads / 32 - 1];  // all units
+  int total = 0;
+  int run = block_exclusive_scan(local, s_warp, total);
+  for (int k = 0; k < kPer; ++k) {
+    const int b = tid * kPer + k;
+    if (b >= va.B) break;
+    s_pre[b] = run;
+    if (s_lq[b] > 0)
+      run += va.H_kv * ((va.group * ((s_lq[b] + kTileM - 1) / kTileM) + 1) / 2);
+  }
+  if (tid == 0) s_pre[va.B] = total;
+  const int max_nb = s_max_nb;
+  for (int i = tid; i <= max_nb; i += kPlanThreads) s_bin[i] = 0;
   __syncthreads();
-  const int total = s_pre[va.B];
   // unit x -> (b, h_kv, pair, key blocks)
   auto unit_at = [&](int x) -> int4 {
     int lo = 0, hi = va.B - 1;  // last b with s_pre[b] <= x
@@ -844,30 +864,39 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenA
       if (s_pre[mid] <= x) lo = mid; else hi = mid - 1;
     }
     const int b = lo, r = x - s_pre[b];
-    const int q0 = __ldg(va.cu_q + b), len_q = __ldg(va.cu_q + b + 1) - q0;
-    const int len_k = __ldg(va.cu_k + b + 1) - __ldg(va.cu_k + b);
+    const int len_q = s_lq[b], len_k = s_lk[b];
     const int n_qt = (len_q + kTileM - 1) / kTileM;
     const int pair = r / va.H_kv;
     int nb = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int f = 2 * pair + t;
-      if (f < va.group * n_qt) nb = max(nb, varlen_kv_blocks(len_q, len_k, va.causal, n_qt - 1 - f / va.group));
+      if (f < va.group * n_qt)
+        nb = max(nb, varlen_kv_blocks(len_q, len_k, va.causal, n_qt - 1 - f / va.group));
     }
     return make_int4(b, r % va.H_kv, pair, nb);
   };
   // ---- counting sort on key blocks, most first
   for (int x = tid; x < total; x += kPlanThreads) atomicAdd(&s_bin[unit_at(x).w], 1);
   __syncthreads();
-  if (tid == 0) {
-    int at = 0;
-    for (int nb = kVarlenMaxBlocks; nb >= 0; --nb) {
+  // each thread takes kb consecutive bins in descending block count
+  const int kb = (max_nb + 1 + kPlanThreads - 1) / kPlanThreads;
+  int mine = 0;
+  for (int i = 0; i < kb; ++i) {
+    const int nb = max_nb - (tid * kb + i);
+    if (nb >= 0) mine += s_bin[nb];
+  }
+  int dummy = 0;
+  int at = block_exclusive_scan(mine, s_warp, dummy);
+  for (int i = 0; i < kb; ++i) {
+    const int nb = max_nb - (tid * kb + i);
+    if (nb >= 0) {
       const int c = s_bin[nb];
       s_bin[nb] = at;
       at += c;
     }
-    ctl[kCtlVarlenUnits] = total;
   }
+  if (tid == 0) ctl[kCtlVarlenUnits] = total;
   __syncthreads();
   for (int x = tid; x < total; x += kPlanThreads) {
     const int4 un = unit_at(x);
@@ -886,7 +915,18 @@ cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
 }
 
 cudaError_t launch_varlen_plan(const VarlenArgs &va, int4 *units, int *ctl, cudaStream_t stream) {
-  return launch_programmatic(varlen_plan_kernel, 1, kPlanThreads, 0, stream, va, units, ctl);
+  const size_t smem = plan_smem_bytes(va.B);
+  static unsigned configured = 0;  // one bit per device ordinal
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 32 || !(configured & (1u << dev))) {
+    e = cudaFuncSetAttribute(varlen_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(plan_smem_bytes(kVarlenMaxB)));
+    if (e != cudaSuccess) return e;
+    if (dev < 32) configured |= 1u << dev;
+  }
+  return launch_programmatic(varlen_plan_kernel, 1, kPlanThreads, smem, stream, va, units, ctl);
 }
 
 cudaError_t launch_prefill_tc_varlen(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
