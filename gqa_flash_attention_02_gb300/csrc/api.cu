@@ -297,15 +297,16 @@ int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 
-int gqa_attn_fwd_varlen_lse(const void *q, const void *k, const void *v, void *o, float *lse,
-                            const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H_q,
-                            int H_kv, int total_q, int total_k, int d, int causal, float scale,
-                            cudaStream_t stream) {
-  if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k) return GQA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+// Ragged batch (cu_* given) or equal lengths uni_q / uni_k ([B][N][H][d],
+// cu_* null), packed token-major: the plan kernel, then the prefill kernel.
+int fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_q,
+               const int *cu_k, int uni_q, int uni_k, int B, int H_q, int H_kv, int total_q,
+               int total_k, int d, int causal, float scale, cudaStream_t stream) {
+  if (!q || !k || !v || !o) return GQA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GQA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 ||
-      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) != 0)
-    return GQA_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
   if (B <= 0 || H_q <= 0 || H_kv <= 0 || total_q < 0 || total_k < 0 || d <= 0)
     return GQA_ERR_INVALID_ARG;
@@ -329,8 +330,10 @@ int gqa_attn_fwd_varlen_lse(const void *q, const void *k, const void *v, void *o
       !encode_bf16_thd(&tv, v, d, H_kv, total_k, kTileN))
     return cuda_fail(cudaErrorInvalidValue);
   VarlenArgs va;
-  va.cu_q = cu_seqlens_q;
-  va.cu_k = cu_seqlens_k;
+  va.cu_q = cu_q;
+  va.cu_k = cu_k;
+  va.uni_q = uni_q;
+  va.uni_k = uni_k;
   va.units = ws->units;
   va.B = B;
   va.H_q = H_q;
@@ -345,6 +348,32 @@ int gqa_attn_fwd_varlen_lse(const void *q, const void *k, const void *v, void *o
   cudaGetDevice(&dev);
   e = launch_prefill_tc_varlen(tq, tk, tv, o, lse, va, d, scale, ws->ctl, device_sms(dev), stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+}  // namespace
+
+extern "C" {
+
+int gqa_attn_fwd_varlen_lse(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H_q,
+                            int H_kv, int total_q, int total_k, int d, int causal, float scale,
+                            cudaStream_t stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) return GQA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) != 0)
+    return GQA_ERR_INVALID_ARG;
+  return fwd_packed(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, 0, 0, B, H_q, H_kv, total_q,
+                    total_k, d, causal, scale, stream);
+}
+
+int gqa_attn_fwd_bshd(const void *q, const void *k, const void *v, void *o, int B, int H_q,
+                      int H_kv, int N_q, int N_kv, int d, int causal, float scale,
+                      cudaStream_t stream) {
+  if (B <= 0 || N_q <= 0 || N_kv <= 0) return GQA_ERR_INVALID_ARG;
+  if (causal && N_q > N_kv) return GQA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * N_q > INT32_MAX || static_cast<long long>(B) * N_kv > INT32_MAX)
+    return GQA_ERR_UNSUPPORTED;
+  return fwd_packed(q, k, v, o, nullptr, nullptr, nullptr, N_q, N_kv, B, H_q, H_kv, B * N_q,
+                    B * N_kv, d, causal, scale, stream);
 }
 
 int gqa_attn_fwd_varlen(const void *q, const void *k, const void *v, void *o,

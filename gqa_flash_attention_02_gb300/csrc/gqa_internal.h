@@ -163,10 +163,20 @@ constexpr int kVarlenMaxB = 4096;       // sequences per call
 constexpr int kVarlenMaxBlocks = 4096;  // 128-row key blocks per sequence
 
 struct VarlenArgs {
-  const int *cu_q, *cu_k;  // device int32 [B + 1]
+  const int *cu_q, *cu_k;  // device int32 [B + 1]; null: every sequence has uni_q / uni_k rows
   const int4 *units;       // the plan kernel's list: {b, h_kv, pair, key blocks}
   int B, H_q, H_kv, group, causal, total_q, total_k;
+  int uni_q, uni_k;        // the lengths when cu_q / cu_k are null ([B][N][H][d] batches)
 };
+
+// First row of sequence b: from the offsets, or b * n for equal lengths.
+GQA_HD int varlen_start(const int *cu, int n, int b) {
+#ifdef __CUDA_ARCH__
+  return cu ? __ldg(cu + b) : b * n;
+#else
+  return cu ? cu[b] : b * n;
+#endif
+}
 
 // Units a call can list at most (workspace sizing): every sequence's query
 // tiles, paired, for each K/V head.

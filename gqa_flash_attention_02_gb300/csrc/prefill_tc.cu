@@ -206,10 +206,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
           const int g = prm.va.group;
           w.b = un.x;
           w.h_kv = un.y;
-          q0 = __ldg(prm.va.cu_q + w.b);
-          len_q = __ldg(prm.va.cu_q + w.b + 1) - q0;
-          k0 = __ldg(prm.va.cu_k + w.b);
-          len_k = __ldg(prm.va.cu_k + w.b + 1) - k0;
+          q0 = varlen_start(prm.va.cu_q, prm.va.uni_q, w.b);
+          len_q = varlen_start(prm.va.cu_q, prm.va.uni_q, w.b + 1) - q0;
+          k0 = varlen_start(prm.va.cu_k, prm.va.uni_k, w.b);
+          len_k = varlen_start(prm.va.cu_k, prm.va.uni_k, w.b + 1) - k0;
           const int n_qt = (len_q + kTileM - 1) / kTileM;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
@@ -827,8 +827,8 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenA
   for (int k = 0; k < kPer; ++k) {
     const int b = tid * kPer + k;
     if (b >= va.B) break;
-    const int q0 = __ldg(va.cu_q + b), q1 = __ldg(va.cu_q + b + 1);
-    const int k0 = __ldg(va.cu_k + b), k1 = __ldg(va.cu_k + b + 1);
+    const int q0 = varlen_start(va.cu_q, va.uni_q, b), q1 = varlen_start(va.cu_q, va.uni_q, b + 1);
+    const int k0 = varlen_start(va.cu_k, va.uni_k, b), k1 = varlen_start(va.cu_k, va.uni_k, b + 1);
     const int len_q = q1 - q0, len_k = k1 - k0;
     const int n_kt = (len_k + kTileN - 1) / kTileN;
     const bool ok = q0 >= 0 && q1 >= q0 && q1 <= va.total_q && k0 >= 0 && k1 >= k0 &&

@@ -31,7 +31,7 @@ EXPORTED = [
     "gqa_attn_decode_f32", "gqa_attn_status_string", "gqa_attn_get_device_error",
     "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
     "gqa_attn_decode_noalloc", "gqa_attn_fwd_lse", "gqa_attn_decode_lse",
-    "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse",
+    "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse", "gqa_attn_fwd_bshd",
 ]
 
 
@@ -84,6 +84,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.gqa_attn_fwd_varlen.restype = _i
             lib.gqa_attn_fwd_varlen_lse.argtypes = var[:4] + [_vp] + var[4:]
             lib.gqa_attn_fwd_varlen_lse.restype = _i
+            lib.gqa_attn_fwd_bshd.argtypes = fwd
+            lib.gqa_attn_fwd_bshd.restype = _i
             lib.gqa_attn_status_string.argtypes = [_i]
             lib.gqa_attn_status_string.restype = ctypes.c_char_p
             lib.gqa_attn_get_device_error.argtypes = [_vp]
@@ -190,6 +192,25 @@ def gqa_attn_fwd_varlen_lse(q, k, v, cu_seqlens_q, cu_seqlens_k, o=None, lse=Non
     o = _fwd_varlen("gqa_attn_fwd_varlen_lse", q, k, v, cu_seqlens_q, cu_seqlens_k, o, causal,
                     scale, stream, lse=_dev(lse, torch.float32, "lse", 2))
     return o, lse
+
+
+def gqa_attn_fwd_bshd(q, k, v, o=None, causal=False, scale=None, stream=None):
+    """bf16 prefill, token-major batch: q [B,N_q,H_q,d], k/v [B,N_kv,H_kv,d] -> o [B,N_q,H_q,d]."""
+    B, N_q, H_q, d = q.shape
+    _, N_kv, H_kv, _ = k.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if scale is None:
+        scale = d ** -0.5
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != d or \
+            tuple(o.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch between q, k, v, o")
+    rc = load().gqa_attn_fwd_bshd(_dev(q, torch.bfloat16, "q", 4), _dev(k, torch.bfloat16, "k", 4),
+                                  _dev(v, torch.bfloat16, "v", 4), _dev(o, torch.bfloat16, "o", 4),
+                                  B, H_q, H_kv, N_q, N_kv, d, int(bool(causal)), float(scale),
+                                  _stream(stream))
+    _check(rc, "gqa_attn_fwd_bshd")
+    return o
 
 
 def _fwd_varlen(name, q, k, v, cu_q, cu_k, o, causal, scale, stream, lse=None):

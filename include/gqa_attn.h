@@ -127,6 +127,18 @@ int gqa_attn_fwd_varlen_lse(const void *q, const void *k, const void *v, void *o
                             int causal, float scale, cudaStream_t stream);
 
 /*
+ * gqa_attn_fwd for token-major batches: q, o are [B][N_q][H_q][d] and k, v
+ * [B][N_kv][H_kv][d] bf16 (the layout of a fused QKV projection's output).
+ * It is the ragged-batch path with every sequence of length N_q / N_kv (no
+ * offset arrays), so it launches the same two kernels as
+ * gqa_attn_fwd_varlen. B <= 4096; causal with N_q > N_kv is rejected
+ * (GQA_ERR_UNSUPPORTED); everything else as gqa_attn_fwd.
+ */
+int gqa_attn_fwd_bshd(const void *q, const void *k, const void *v, void *o,
+                      int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+                      int causal, float scale, cudaStream_t stream);
+
+/*
  * Same operation in fp32: q, k, v, o are float arrays with the layouts of
  * gqa_attn_fwd. SIMT FMA kernel (online softmax, warp-shuffle reductions);
  * d in {32, 64, 96, 128}.

@@ -83,6 +83,48 @@ def test_decode_validation(fn):
     assert call(L=(1 << 20) + 1) == 2
 
 
+@pytest.mark.parametrize("fn", ["gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse"])
+def test_varlen_validation(fn):
+    f = getattr(ops.load(), fn)
+    lse = fn.endswith("_lse")
+
+    def call(q=A, k=A, v=A, o=A, l=None, cq=SEQ, ck=SEQ, B=3, H_q=8, H_kv=2, tq=700, tk=900,
+             d=128, causal=1, scale=0.088):
+        head = (q, k, v, o) + ((l,) if lse else ())
+        return f(*head, cq, ck, B, H_q, H_kv, tq, tk, d, causal, scale, None)
+
+    assert call(cq=None) == 1
+    assert call(ck=ctypes.c_void_p(0x20002)) == 1   # offsets not 4-byte aligned
+    assert call(v=MIS) == 1
+    assert call(B=0) == 1
+    assert call(tq=-1) == 1
+    assert call(H_q=8, H_kv=3) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(d=96) == 2
+    assert call(B=4097) == 2                        # above the sequences-per-call limit
+    assert call(tq=1 << 22, H_q=1 << 10, H_kv=1 << 8) == 2
+    assert call(tq=0) == 0                          # no query rows: nothing launched
+    assert call(tk=0) == 1                          # query rows but no keys
+    if lse:
+        assert call(l=ctypes.c_void_p(0x30002)) == 1
+
+
+def test_bshd_validation():
+    f = ops.load().gqa_attn_fwd_bshd
+
+    def call(q=A, k=A, v=A, o=A, B=2, H_q=8, H_kv=2, N_q=300, N_kv=300, d=128, causal=1,
+             scale=0.088):
+        return f(q, k, v, o, B, H_q, H_kv, N_q, N_kv, d, causal, scale, None)
+
+    assert call(q=None) == 1
+    assert call(o=MIS) == 1
+    assert call(N_q=0) == 1
+    assert call(H_q=6, H_kv=4) == 1
+    assert call(causal=1, N_q=400, N_kv=300) == 2   # bottom-right mask undefined
+    assert call(d=32) == 2
+    assert call(B=5000, N_q=10, N_kv=10) == 2       # above the sequences-per-call limit
+
+
 def test_decode_chunk_validation():
     f = ops.load().gqa_attn_decode_chunked
     base = (A, A, A, SEQ, A, 2, 12, 2, 2048, 128, 0.088)

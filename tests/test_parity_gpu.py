@@ -456,6 +456,25 @@ def test_bf16_varlen_bad_offsets_reported_and_skipped():
     _check_bf16(got, ref, "after a bad call")
 
 
+@pytest.mark.parametrize("shape", [(2, 8, 2, 300, 300, 128, True), (3, 4, 1, 77, 500, 64, False),
+                                   (1, 6, 3, 129, 256, 128, True)])
+def test_bf16_bshd_matches_oracle_and_bhsd(shape):
+    """[B][N][H][d] batches: against the oracle, and bit for bit against the
+    [B][H][N][d] path on the same values (each row's arithmetic is the same)."""
+    B, H_q, H_kv, N_q, N_kv, d, causal = shape
+    q, k, v = inputs.prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, torch.bfloat16, seed=160 + N_q)
+    qd, kd, vd = _dev(q, k, v)
+    tok = lambda t: t.transpose(1, 2).contiguous()  # [B][H][N][d] -> [B][N][H][d]
+    o = torch.full_like(tok(qd), float("nan"))
+    ops.gqa_attn_fwd_bshd(tok(qd), tok(kd), tok(vd), o, causal=causal, scale=d ** -0.5)
+    o_bhsd = ops.gqa_attn_fwd(qd, kd, vd, causal=causal, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, _ = oracle.prefill(q, k, v, causal, d ** -0.5, n_threads=THREADS)
+    _check_bf16(o.transpose(1, 2).float().cpu().numpy(), ref, f"bshd {shape}")
+    assert torch.equal(o.transpose(1, 2), o_bhsd)
+
+
 def test_bounded_wait_reports_timeout_and_context_survives():
     assert ops.gqa_attn_selftest_wait_timeout(2000) == 4  # GQA_ERR_DEVICE_TIMEOUT
     assert ops.gqa_attn_get_device_error() == 0           # the word was cleared
