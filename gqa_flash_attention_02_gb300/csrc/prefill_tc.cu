@@ -32,6 +32,13 @@
 //     the running sum always use the same reference maximum.
 //   * Every wait is bounded: a stuck pipeline records kErrTimeout in the
 //     workspace error word and unwinds instead of hanging the GPU.
+//   * Ragged batches (prompts of different lengths packed token-major,
+//     [total][H][d], with per-sequence offsets; the pages' batched prompt
+//     prefill, microLLM-rocm optimisation log, Experiment 101) run the same
+//     body as prefill_varlen_kernel: a one-block plan kernel first lists the
+//     units heaviest first, the producer decodes each unit once and hands the
+//     other roles a descriptor, and the masks and stores follow each
+//     sequence's own lengths (bottom-right causal inside the sequence).
 #include <cuda_runtime.h>
 #include <math.h>
 

@@ -423,9 +423,37 @@ def test_bf16_varlen_batch_sampled():
     _check_bf16(np.stack([got[t, h] for t, h in rows]), ref, "varlen batch, sampled rows")
 
 
-def test_bf16_varlen_lse_and_determinism():
-    q, k, v, cu_q, cu_k = inputs.varlen_inputs([300, 1, 129], [400, 1, 129], 8, 2, 128,
-                                               torch.bfloat16, seed=150)
+def test_bf16_varlen_many_short_sequences():
+    """300 prompts of 0-200 tokens after cached prefixes of 0-64 keys: many
+    one-tile sequences in one unit list."""
+    lens_q = inputs.varlen_lengths(300, 0, 200, seed=152)
+    extra = inputs.varlen_lengths(300, 0, 64, seed=153)
+    lens_k = [lq + e if lq + e > 0 else 1 for lq, e in zip(lens_q, extra)]
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs(lens_q, lens_k, 8, 2, 64, torch.bfloat16, seed=154)
+    got = _varlen_run(q, k, v, cu_q, cu_k, True, 0.125)
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, _ = oracle.prefill_varlen(q, k, v, cu_q, cu_k, True, 0.125)
+    _check_bf16(got, ref, "300 short sequences")
+
+
+def test_bf16_varlen_most_sequences():
+    """4096 sequences (the per-call limit): one-token prompts over 1-3 keys,
+    plus a 300-token prompt in the middle."""
+    lens_q = [1] * 4096
+    lens_q[2000] = 300
+    lens_k = [1 + (b % 3) for b in range(4096)]
+    lens_k[2000] = 300
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs(lens_q, lens_k, 4, 1, 64, torch.bfloat16, seed=155)
+    got = _varlen_run(q, k, v, cu_q, cu_k, True, 0.125)
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, _ = oracle.prefill_varlen(q, k, v, cu_q, cu_k, True, 0.125)
+    _check_bf16(got, ref, "4096 sequences")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_varlen_lse_and_determinism(d):
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs([300, 1, 129], [400, 1, 129], 8, 2, d,
+                                               torch.bfloat16, seed=150 + d)
     qd, kd, vd, cqd, ckd = _dev(q, k, v, cu_q, cu_k)
     o, lse = ops.gqa_attn_fwd_varlen_lse(qd, kd, vd, cqd, ckd, causal=True, scale=0.09)
     torch.cuda.synchronize()
