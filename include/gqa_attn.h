@@ -25,18 +25,21 @@
  *     bf16 output. The `_f32` siblings take and write fp32 with fp32 math
  *     throughout (no TF32).
  *   - Causal alignment is bottom-right: query row i sees key j iff
- *     j <= i + (N_kv - N_q). With N_q == N_kv this is the ordinary lower
- *     triangle. causal with N_q > N_kv is rejected (GQA_ERR_UNSUPPORTED).
+ *     j <= i + (N_kv - N_q) (per sequence for ragged batches). With
+ *     N_q == N_kv this is the ordinary lower triangle. causal with
+ *     N_q > N_kv is rejected (GQA_ERR_UNSUPPORTED).
  *   - `scale` is used as given (typically 1/sqrt(d)); it must be finite.
  *   - The library owns a small per-(device, stream) workspace (the scheduler
- *     counters, the device error word and the split-KV partials). It grows
+ *     counters, the device error word, the split-KV partials and the
+ *     ragged-batch unit list). It grows
  *     on demand with stream-ordered allocation and is released by
  *     gqa_attn_shutdown(). Calls on DIFFERENT streams use different
  *     workspaces and may run concurrently.
  *   - Errors are returned as a gqa_status code before anything is launched;
  *     nothing is launched when a call fails validation. Faults detected on
  *     the device (a bounded wait that ran out, a seqlen outside
- *     [0, max_len]) are recorded in the workspace's error word and reported
+ *     [0, max_len], bad ragged-batch offsets) are recorded in the
+ *     workspace's error word and reported
  *     by gqa_attn_get_device_error(). No kernel traps or asserts.
  */
 #ifndef GQA_ATTN_H
