@@ -24,12 +24,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
-}
-
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
   asm volatile(
@@ -189,30 +183,12 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory");
 }
 
-// D(tmem) = A(smem) x B(smem) (+ D when accumulate != 0), kind::f16.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D(tmem) = A(tmem) x B(smem) (+ D when accumulate != 0), kind::f16.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Same MMAs with each 64-bit smem descriptor passed as two 32-bit words.
-// Only the low word (start address) changes between the K-steps of one
-// operand, so issuing an MMA costs one integer add per operand; a lean
-// issue loop matters because one thread issues every MMA of the CTA.
+// D(tmem) = A(smem) x B(smem) (+ D when accumulate != 0), kind::f16, and
+// (mma_ts_w) D = A(tmem) x B(smem). Each 64-bit smem descriptor is passed as
+// two 32-bit words: only the low word (start address) changes between the
+// K-steps of one operand, so issuing an MMA costs one integer add per
+// operand; a lean issue loop matters because one thread issues every MMA of
+// the CTA.
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -234,7 +210,12 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
       : "memory");
 }
 
-// Low / high 32-bit words of sdesc_sw128 (same bit fields).
+// Shared-memory matrix descriptor, 128-byte swizzle, as its low and high
+// 32-bit words. Bit fields of the 64-bit descriptor: [0,14) start address
+// >> 4; [16,30) leading-dimension byte offset >> 4; [32,46) stride-dimension
+// byte offset >> 4; [46,48) descriptor version (1); [61,64) layout (2 =
+// 128-byte swizzle). Atoms are 8 rows x 128 bytes and must start on a
+// 1024-byte boundary.
 __host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
@@ -251,19 +232,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle. Bit fields: [0,14)
-// start address >> 4; [16,30) leading-dimension byte offset >> 4; [32,46)
-// stride-dimension byte offset >> 4; [46,48) descriptor version (1);
-// [61,64) layout (2 = 128-byte swizzle). Atoms are 8 rows x 128 bytes and
-// must start on a 1024-byte boundary.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
-         (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
-         (2ull << 61);
 }
 
 // ---- tensor-memory loads and stores (32 lanes x 32-bit columns shape).
@@ -413,14 +381,6 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *r) {
   asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
                "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
-}
-
-// Load with acquire semantics at GPU scope: later reads see whatever the
-// writer published before its matching release (or fence + atomic).
-__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
 }
 
 __device__ __forceinline__ void record_error(int *err_word, int bits) {
