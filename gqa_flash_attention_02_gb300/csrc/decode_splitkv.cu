@@ -300,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  // While the previous grid finishes, warm L2 with the sequence lengths the
+  // prologue reads first (one prefetch per 128-byte line).
+  if (warp == 0)
+    for (int b = 32 * lane; b < prm.B; b += 32 * 32) prefetch_l2(prm.seqlens + b);
   // Global reads (inputs, partials, counters) come after the previous grid
   // of the stream has completed; the next grid may start setting up.
   grid_dependency_wait();

@@ -176,6 +176,26 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if constexpr (!kVarlen) {
+    // While the previous grid finishes, warm L2 with the first tiles of
+    // unit blockIdx.x: the counter hands out the first units about one per
+    // CTA, so together the CTAs cover the first wave's Q tiles and first K/V
+    // blocks, whichever CTA takes each unit.
+    if (warp == kProducerWarp && lane == 0 && static_cast<int>(blockIdx.x) < plan.total_units) {
+      const Unit w = decode_unit(plan, blockIdx.x);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (w.t[t].kv_blocks > 0)
+          for (int p = 0; p < D / 64; ++p)
+            tma_prefetch_l2_3d(&tm_q, p * 64, w.t[t].q_tile * kTileM, w.b * plan.H_q + w.t[t].h_q);
+      const int nb = min(2, max(w.t[0].kv_blocks, w.t[1].kv_blocks));
+      for (int j = 0; j < nb; ++j)
+        for (int p = 0; p < D / 64; ++p) {
+          tma_prefetch_l2_3d(&tm_k, p * 64, j * kTileN, w.b * plan.H_kv + w.h_kv);
+          tma_prefetch_l2_3d(&tm_v, p * 64, j * kTileN, w.b * plan.H_kv + w.h_kv);
+        }
+    }
+  }
   // Everything above only set up this CTA. Global reads (inputs, the work
   // counter) come after the previous grid of the stream has completed.
   grid_dependency_wait();
