@@ -140,6 +140,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, device, world):
+    """Elementwise maximum of per-rank timings over all ranks: the slowest
+    replica sets the job's time (all ranks must call it)."""
+    import torch
+    vals = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    return vals.tolist()
+
+
+def job_throughput(world, calls, units_per_call, total_ms, scale):
+    """Whole-job throughput with fixed work per replica (weak scaling): the
+    units all `world` ranks processed over the slowest rank's time, divided
+    by `scale` (1e12 for TFLOP/s, 1e9 for GB/s)."""
+    return world * calls * units_per_call / (total_ms * 1e-3) / scale
+
+
 # --------------------------------------------------------------------------- ours
 
 def run_ours(args):
@@ -312,11 +330,8 @@ def run_ours(args):
     e2e_dec = sum(e[1].elapsed_time(e[2]) for e in eev) / e2e_steps
 
     # ---- max over ranks
-    vals = torch.tensor([tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var], dtype=torch.float64,
-                        device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var = vals.tolist()
+    tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var = max_over_ranks(
+        [tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var], dev, world)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -325,8 +340,8 @@ def run_ours(args):
     K = args.steps
     pre_ms = tot_pre / K
     dec_ms = tot_dec / K
-    value = world * K * pre_flops / (tot_pre * 1e-3) / 1e12
-    dec_gbs = world * K * dec_bytes / (tot_dec * 1e-3) / 1e9
+    value = job_throughput(world, K, pre_flops, tot_pre, 1e12)
+    dec_gbs = job_throughput(world, K, dec_bytes, tot_dec, 1e9)
     pre_ach = pre_flops / (pre_ms * 1e-3) / 1e12
     dec_ach = dec_bytes / (dec_ms * 1e-3) / 1e9
     tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -390,7 +405,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},
         },
         "varlen": {
-            "value": round(world * K_var * vs.flops / (tot_var * 1e-3) / 1e12, 3),
+            "value": round(job_throughput(world, K_var, vs.flops, tot_var, 1e12), 3),
             "unit": "TFLOP/s",
             "ms": round(tot_var / K_var, 6),
             "calls": K_var,
