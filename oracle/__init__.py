@@ -23,7 +23,9 @@ What each function follows (page title and section):
   * log-sum-exp merge of key-range partials -- microLLM-rocm optimisation
     log, Experiments 282-284 (split-sequence cached attention);
   * a ragged batch as the list of its sequences, each attended on its own
-    -- microLLM-rocm optimisation log, Experiment 101.
+    -- microLLM-rocm optimisation log, Experiment 101;
+  * attention backward with the GQA head reduction of dK and dV (numpy,
+    float64) -- microLLM-rocm optimisation log, Experiments 051-057.
 """
 from __future__ import annotations
 
@@ -207,6 +209,52 @@ def prefill_varlen_rows(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, scale
         h_kv = h_q // group
         o[r], lse[r] = attend_row(q[t, h_q], k[k0:k0 + n, h_kv], v[k0:k0 + n, h_kv], scale)
     return o, lse
+
+
+def prefill_backward(q, k, v, do, causal: bool, scale: float):
+    """Gradients of prefill attention. q:[B,H_q,N_q,d], k,v:[B,H_kv,N_kv,d],
+    do = dL/dO:[B,H_q,N_q,d] -> (dq, dk, dv) in float64.
+
+    Row recompute, then the softmax backward, then the GQA head reduction
+    of dK and dV over the query heads of a group (microLLM-rocm optimisation
+    log, Experiments 051-057: causal GQA attention backward). Per (b, h_q),
+    with h_kv = h_q / (H_q / H_kv) and the bottom-right causal mask:
+        S = scale Q K^T (masked to -inf),  P = softmax(S),  O = P V
+        dV[h_kv] += P^T dO                dP = dO V^T
+        Delta_i = sum_d dO_i O_i          dS = P * (dP - Delta)
+        dQ = scale dS K                   dK[h_kv] += scale dS^T Q
+    A matrix product serves as a step; nothing else is fused or reordered.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H_q, N_q, d = q.shape
+    _, H_kv, N_kv, _ = k.shape
+    if H_kv <= 0 or H_q % H_kv:
+        raise ValueError("H_q must be a positive multiple of H_kv")
+    group = H_q // H_kv
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    rows = np.arange(N_q)[:, None]
+    keys = np.arange(N_kv)[None, :]
+    visible = keys <= rows + (N_kv - N_q) if causal else np.ones((N_q, N_kv), dtype=bool)
+    for b in range(B):
+        for h in range(H_q):
+            hk = h // group
+            s = scale * (q[b, h] @ k[b, hk].T)
+            s = np.where(visible, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            m = np.where(np.isfinite(m), m, 0.0)  # a row with no visible key
+            e = np.where(visible, np.exp(s - m), 0.0)
+            z = e.sum(axis=1, keepdims=True)
+            p = np.divide(e, z, out=np.zeros_like(e), where=z > 0)
+            o = p @ v[b, hk]
+            dv[b, hk] += p.T @ do[b, h]
+            dp = do[b, h] @ v[b, hk].T
+            delta = (do[b, h] * o).sum(axis=1, keepdims=True)
+            ds = p * (dp - delta)
+            dq[b, h] = scale * (ds @ k[b, hk])
+            dk[b, hk] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv
 
 
 def decode(q, k_cache, v_cache, seqlens, scale: float):

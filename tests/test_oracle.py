@@ -319,6 +319,111 @@ def test_oracle_varlen_rows_and_unowned_rows():
         assert l_r[r] == lse[h, t]
 
 
+# ------------------------------------------------------------------ backward
+
+def _sdpa_grads(q, k, v, do, causal, scale):
+    """Gradients from torch autograd through scaled_dot_product_attention in
+    float64 on the CPU (a library routine, with the bottom-right mask given
+    explicitly)."""
+    qt, kt, vt = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    n_q, n_kv = q.shape[2], k.shape[2]
+    mask = torch.ones(n_q, n_kv, dtype=torch.bool).tril(n_kv - n_q) if causal else None
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale,
+                                                         enable_gqa=True)
+    o.backward(torch.tensor(do))
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+def pin_backward_autograd(bwd):
+    """bwd(q, k, v, do, causal, scale) -> (dq, dk, dv) agrees with autograd."""
+    for (H_q, H_kv, N_q, N_kv), causal in [((4, 2, 5, 7), True), ((6, 1, 4, 4), False),
+                                           ((2, 2, 3, 9), True)]:
+        q, k, v = _rand(2, H_q, H_kv, N_q, N_kv, 6, seed=30 + N_kv)
+        do = np.random.default_rng(31 + N_q).standard_normal(q.shape)
+        got = bwd(q, k, v, do, causal, 0.6)
+        ref = _sdpa_grads(q, k, v, do, causal, 0.6)
+        for g, r, name in zip(got, ref, ("dq", "dk", "dv")):
+            np.testing.assert_allclose(g, r, rtol=0, atol=1e-12, err_msg=f"{name} causal={causal}")
+
+
+def test_oracle_backward_matches_autograd():
+    pin_backward_autograd(oracle.prefill_backward)
+
+
+def test_oracle_backward_finite_differences():
+    """Central differences of L = sum(O * dO), O from the forward oracle,
+    against the backward oracle: independent of the backward formula."""
+    q, k, v = _rand(1, 4, 2, 3, 5, 3, seed=32)
+    do = np.random.default_rng(33).standard_normal(q.shape)
+    dq, dk, dv = oracle.prefill_backward(q, k, v, do, True, 0.8)
+
+    def loss(q_, k_, v_):
+        return float((oracle.prefill(q_, k_, v_, True, 0.8)[0] * do).sum())
+
+    eps = 1e-6
+    for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args_p, args_m = [q.copy(), k.copy(), v.copy()], [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += eps
+            args_m[which][idx] -= eps
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=0, atol=1e-7)
+
+
+def test_oracle_backward_gqa_is_sum_over_replicated_heads():
+    """dK, dV of a K/V head are the sums over its query heads of the MHA
+    gradients with that head replicated; dQ is unchanged."""
+    q, k, v = _rand(1, 6, 2, 5, 5, 4, seed=34)
+    do = np.random.default_rng(35).standard_normal(q.shape)
+    dq, dk, dv = oracle.prefill_backward(q, k, v, do, True, 0.5)
+    k_r, v_r = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+    dq_m, dk_m, dv_m = oracle.prefill_backward(q, k_r, v_r, do, True, 0.5)
+    np.testing.assert_allclose(dq, dq_m, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk, dk_m.reshape(1, 2, 3, 5, 4).sum(axis=2), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, dv_m.reshape(1, 2, 3, 5, 4).sum(axis=2), rtol=0, atol=1e-13)
+
+
+def _bwd_restated(q, k, v, do, causal, scale, mutation=None):
+    """The backward restated in numpy, with an optional planted mistake."""
+    B, H_q, N_q, _ = q.shape
+    H_kv, N_kv = k.shape[1], k.shape[2]
+    g = H_q // H_kv
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    off = N_kv - N_q + (1 if mutation == "mask_off_by_one" else 0)
+    vis = (np.arange(N_kv)[None, :] <= np.arange(N_q)[:, None] + off) if causal else \
+        np.ones((N_q, N_kv), dtype=bool)
+    for b in range(B):
+        for h in range(H_q):
+            hk = h // g
+            # (planted) only the group's first query head reaches dK, dV
+            hk_acc = None if mutation == "first_head_only" and h % g else hk
+            s = np.where(vis, scale * q[b, h] @ k[b, hk].T, -np.inf)
+            e = np.exp(s - s.max(axis=1, keepdims=True))
+            p = e / e.sum(axis=1, keepdims=True)
+            o = p @ v[b, hk]
+            dp = do[b, h] @ v[b, hk].T
+            delta = 0.0 if mutation == "no_delta" else (do[b, h] * o).sum(axis=1, keepdims=True)
+            ds = p * (dp - delta)
+            dq[b, h] = (1.0 if mutation == "no_scale_dq" else scale) * (ds @ k[b, hk])
+            if hk_acc is not None:
+                # dV from P, or (planted) from the exponentials before normalising
+                dv[b, hk] += (e if mutation == "dv_unnormalised" else p).T @ do[b, h]
+                dk[b, hk] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv
+
+
+def test_backward_pin_accepts_unmutated_restatement():
+    pin_backward_autograd(_bwd_restated)
+
+
+@pytest.mark.parametrize("mutation", ["no_delta", "no_scale_dq", "first_head_only",
+                                      "mask_off_by_one", "dv_unnormalised"])
+def test_backward_pin_rejects_planted_mistake(mutation):
+    with pytest.raises(AssertionError):
+        pin_backward_autograd(lambda *a: _bwd_restated(*a, mutation=mutation))
+
+
 def test_oracle_reads_bf16_exactly():
     """bf16 inputs are widened exactly: the oracle on bf16 tensors equals the
     oracle on the same values pre-converted to float64."""
