@@ -67,3 +67,20 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     args = type("A", (), {"steps": 1, "warmup": 3, "gpus": 2, "impl": "reference",
                           "no_cpu_baseline": True})()
     assert bench.run_reference(args) is None  # other ranks exit without work
+
+
+def test_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """Recorded DRAM traffic is keyed by a hash of the kernel code without
+    comments and blank lines: documenting a kernel keeps its counters, any
+    code change voids them."""
+    base = "int f(int x) {\n  return x + 1;\n}\n"
+    variants = {
+        "a.cu": base,
+        "b.cu": "// what f does\n" + base.replace("{\n", "{  // add one\n") + "\n\n/* note\n*/\n",
+        "c.cu": base.replace("x + 1", "x + 2"),
+    }
+    for name, text in variants.items():
+        (tmp_path / name).write_text(text)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.source_sha("a.cu") == bench.source_sha("b.cu")
+    assert bench.source_sha("a.cu") != bench.source_sha("c.cu")
