@@ -53,15 +53,33 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_sha(rel):
-    """Hash of a kernel source with comments and blank lines removed, so an
-    edit of the comments alone leaves recorded counters valid."""
-    with open(os.path.join(ROOT, rel)) as f:
+def _code_text(path):
+    with open(path) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
-    code = "\n".join(ln for ln in lines if ln)
-    return hashlib.sha256(code.encode()).hexdigest()[:16]
+    return [ln for ln in lines if ln]
+
+
+def source_sha(rel):
+    """Hash of a kernel source and of the local headers it includes
+    (recursively, ``#include "..."`` next to the file), with comments and
+    blank lines removed, so an edit of the comments alone leaves recorded
+    counters valid while any code change, in the file or a header, voids
+    them."""
+    seen, parts, todo = set(), [], [os.path.join(ROOT, rel)]
+    while todo:
+        path = os.path.normpath(todo.pop(0))
+        if path in seen or not os.path.exists(path):
+            continue
+        seen.add(path)
+        lines = _code_text(path)
+        parts.append("\n".join(lines))
+        for ln in lines:
+            m = re.match(r'\s*#\s*include\s+"([^"]+)"', ln)
+            if m:
+                todo.append(os.path.join(os.path.dirname(path), m.group(1)))
+    return hashlib.sha256("\n\0".join(parts).encode()).hexdigest()[:16]
 
 
 def recorded_traffic(kernel_src, name):
@@ -160,6 +178,143 @@ def job_throughput(world, calls, units_per_call, total_ms, scale):
 
 # --------------------------------------------------------------------------- ours
 
+def decode_bytes(seqlens, shape):
+    """Algorithmic bytes of one decode call: every valid cache row once per
+    K/V head (K and V), plus q, o and seqlens."""
+    n_valid = int(seqlens.sum())
+    return (n_valid * shape.H_kv * shape.d * 2 * 2 + 2 * shape.B * shape.H_q * shape.d * 2
+            + 4 * shape.B)
+
+
+class GraphChain:
+    """`calls` back-to-back calls fn(i, stream) (i = 0, 1, ...) captured in one
+    CUDA graph on `stream`, so nothing on the host sits between the kernels;
+    the inputs are rotated by the callers over enough copies that a call's
+    operands are not in the L2 when they come round again."""
+
+    def __init__(self, torch, fn, calls, stream):
+        self.calls = calls
+        self.graph = None
+        if calls > 0:
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=stream):
+                for i in range(calls):
+                    fn(i, stream)
+
+    def replay(self):
+        if self.graph is not None:
+            self.graph.replay()
+
+
+def copies_for(bytes_per_call, cap_bytes=1 << 30):
+    """Copies of a call's inputs to rotate over: three L2 sizes' worth, at
+    least two, and no more than cap_bytes in all (then at least two)."""
+    n = max(2, math.ceil(3 * L2_BYTES / max(1, bytes_per_call)))
+    return max(2, min(n, cap_bytes // max(1, bytes_per_call)))
+
+
+def time_calls(torch, fn, copies, stream, reps=21, min_chain_us=300.0, est_us=None):
+    """Median device time of one call, in ms, over `reps` repetitions of a
+    graph of back-to-back calls over the rotating copies (CUDA events on the
+    launching stream around each replay). Returns (ms_per_call, calls_per_rep)."""
+    if est_us is None:
+        g = GraphChain(torch, fn, copies, stream)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        est_us = max(1e-3, e0.elapsed_time(e1) * 1e3 / copies)
+    chain = copies * max(1, math.ceil(min_chain_us / est_us / copies))
+    g = GraphChain(torch, fn, chain, stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev) / chain, chain
+
+
+def roofline_obj(bound, achieved, peak, unit, peak_src, kernel, traffic=None):
+    return {"bound": bound, "kernel": kernel, "achieved": round(achieved, 3), "peak": peak,
+            "unit": unit, "frac": round(achieved / peak, 4), "peak_source": peak_src,
+            "traffic": traffic}
+
+
+def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
+    """Per-workload throughput beside the headline step: the MHA/GQA/MQA sweep
+    (six variants), the long-sequence case and decode at B = 1, 8, 64. Each
+    is the median over 21 repetitions of a graph of back-to-back calls over
+    rotating input copies."""
+    out = {}
+
+    def prefill_block(shape):
+        q, k, v = inputs.prefill_inputs_for(shape)
+        nbytes = (q.numel() + k.numel() + v.numel()) * 2
+        copies = copies_for(nbytes)
+        bufs = [(q.to(dev), k.to(dev), v.to(dev)) for _ in range(copies)]
+        o = torch.empty_like(bufs[0][0])
+
+        def call(i, s):
+            a, b, c = bufs[i % copies]
+            ops.gqa_attn_fwd(a, b, c, o, causal=shape.causal, scale=shape.scale, stream=s)
+
+        for i in range(copies):
+            call(i, stream)
+        ms, chain = time_calls(torch, call, copies, stream)
+        assert ops.gqa_attn_get_device_error(stream=stream) == 0
+        del bufs, o
+        torch.cuda.empty_cache()
+        ach = shape.flops / (ms * 1e-3) / 1e12
+        return {"ms": round(ms, 6), "value": round(ach, 3), "unit": "TFLOP/s",
+                "shape": {"B": shape.B, "H_q": shape.H_q, "H_kv": shape.H_kv, "N": shape.N_q,
+                          "d": shape.d, "causal": shape.causal},
+                "calls_per_rep": chain, "reps": 21, "l2": f"{copies} rotating copies",
+                "roofline": roofline_obj("tensor", ach, tc_peak, "TFLOP/s",
+                                         f"{peak_src} bf16_tflops (burst)",
+                                         f"prefill_tc_kernel<{shape.d}, 0>")}
+
+    for shape in inputs.sweep_shapes():
+        out[shape.name] = prefill_block(shape)
+    out[inputs.LONG_SEQ.name] = prefill_block(inputs.LONG_SEQ)
+
+    for shape in inputs.decode_shapes():
+        sl, q, kc, vc = inputs.decode_inputs_for(shape)
+        in_bytes = (q.numel() + kc.numel() + vc.numel()) * 2
+        copies = copies_for(in_bytes)
+        bufs = [(sl.to(dev), q.to(dev), kc.to(dev), vc.to(dev)) for _ in range(copies)]
+        o = torch.empty_like(bufs[0][1])
+
+        def call(i, s):
+            a, b, c, d = bufs[i % copies]
+            ops.gqa_attn_decode(b, c, d, a, o, scale=shape.scale, stream=s)
+
+        for i in range(copies):
+            call(i, stream)
+        ms, chain = time_calls(torch, call, copies, stream)
+        assert ops.gqa_attn_get_device_error(stream=stream) == 0
+        nbytes = decode_bytes(sl, shape)
+        ach = nbytes / (ms * 1e-3) / 1e9
+        out[shape.name] = {
+            "ms": round(ms, 6), "value": round(ach, 2), "unit": "GB/s",
+            "shape": {"B": shape.B, "H_q": shape.H_q, "H_kv": shape.H_kv,
+                      "max_len": shape.max_len, "d": shape.d, "sum_seqlens": int(sl.sum())},
+            "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
+            "l2": f"{copies} rotating copies",
+            "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
+                                     "decode_kernel<128,5>")}
+        del bufs, o
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -173,6 +328,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     ops.load()
     peaks, peak_src = load_peaks()
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
 
     ps = inputs.LLAMA3_8B_LAYER
     ds = inputs.decode_shapes()[-1]
@@ -190,7 +347,7 @@ def run_ours(args):
 
     pre_flops = ps.flops
     n_valid = int(sl0.sum())
-    dec_bytes = (n_valid * ds.H_kv * ds.d * 2 * 2 + 2 * dq0.numel() * 2 + 4 * ds.B)
+    dec_bytes = decode_bytes(sl0, ds)
 
     stream = torch.cuda.current_stream()
 
@@ -213,30 +370,37 @@ def run_ours(args):
             call_dec(i, cap)
     torch.cuda.synchronize()
 
-    def capture(fn, first, count):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=cap):
-            for i in range(first, first + count):
-                fn(i, cap)
-        return g
-
     # A chain graph holds `chain` back-to-back calls of one kernel over the
     # rotating copies (a multiple of `copies`, so replays continue the
-    # rotation); K = reps * chain + rest calls are timed per kernel, the rest
-    # as one more graph of `rest` back-to-back calls.
+    # rotation); one repetition of the step is K prefill calls then K decode
+    # calls: reps * chain + rest calls per kernel, the rest as one more graph.
     K = args.steps
     chain = copies * max(1, 24 // copies)
-    reps, rest = divmod(K, chain)
-    chain_pre, chain_dec = capture(call_pre, 0, chain), capture(call_dec, 0, chain)
-    rest_pre = capture(call_pre, 0, rest) if rest else None
-    rest_dec = capture(call_dec, 0, rest) if rest else None
+    n_chain, rest = divmod(K, chain)
+    chain_pre, chain_dec = GraphChain(torch, call_pre, chain, cap), GraphChain(torch, call_dec, chain, cap)
+    rest_pre, rest_dec = GraphChain(torch, call_pre, rest, cap), GraphChain(torch, call_dec, rest, cap)
     torch.cuda.synchronize()
 
     def run_kernel(chain_g, rest_g):
-        for _ in range(reps):
+        for _ in range(n_chain):
             chain_g.replay()
-        if rest_g is not None:
-            rest_g.replay()
+        rest_g.replay()
+
+    for _ in range(max(1, math.ceil(args.warmup / chain))):  # at least W calls of each
+        chain_pre.replay()
+        chain_dec.replay()
+    torch.cuda.synchronize()
+    # Repetitions of the K-step region: at least 21, and enough to last about
+    # a second, so the median is robust and the clock sampler sees the load.
+    t0 = time.perf_counter()
+    run_kernel(chain_pre, rest_pre)
+    run_kernel(chain_dec, rest_dec)
+    torch.cuda.synchronize()
+    rep_s = max(1e-6, time.perf_counter() - t0)
+    reps = int(min(max(21, math.ceil(1.0 / rep_s)), 5001))
+    if args.reps:
+        reps = args.reps  # profiling runs: a fixed, small count
+    reps += 1 - reps % 2  # odd: the median is one repetition's time
 
     # The ragged batch (one call = the plan kernel + the prefill kernel) is
     # timed in a region of its own after the step, over its own rotating
@@ -257,42 +421,29 @@ def run_ours(args):
         for i in range(var_copies):
             call_var(i, cap)
     torch.cuda.synchronize()
-    var_chain = var_copies * max(1, 8 // var_copies)
-    chain_var = capture(call_var, 0, var_chain)
-    var_reps = max(1, math.ceil(min(max(K, 4), 40) / var_chain))
-    K_var = var_reps * var_chain
-    chain_var.replay()
 
-    for _ in range(max(1, math.ceil(args.warmup / chain))):  # at least W calls of each
-        chain_pre.replay()
-        chain_dec.replay()
-    torch.cuda.synchronize()
-
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
     with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                       else local) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        ev[0].record(stream)
-        run_kernel(chain_pre, rest_pre)     # K prefill launches
-        ev[1].record(stream)
-        run_kernel(chain_dec, rest_dec)     # K decode launches
-        ev[2].record(stream)
+        for e in ev:
+            e[0].record(stream)
+            run_kernel(chain_pre, rest_pre)     # K prefill launches
+            e[1].record(stream)
+            run_kernel(chain_dec, rest_dec)     # K decode launches
+            e[2].record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         wall = time.perf_counter() - t0
-        ev_var = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        ev_var[0].record(stream)
-        for _ in range(var_reps):
-            chain_var.replay()          # K_var ragged-batch calls
-        ev_var[1].record(stream)
-        torch.cuda.synchronize()
-    tot_var = ev_var[0].elapsed_time(ev_var[1])
-    tot_pre = ev[0].elapsed_time(ev[1])   # ms
-    tot_dec = ev[1].elapsed_time(ev[2])
+        var_ms, var_chain = time_calls(torch, call_var, var_copies, cap, min_chain_us=2000.0)
+        blocks = None if args.no_configs else config_blocks(
+            torch, ops, inputs, dev, cap, tc_peak, hbm_peak, peak_src)
+    tot_pre = statistics.median(e[0].elapsed_time(e[1]) for e in ev)   # ms for K calls
+    tot_dec = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     gpu_err = ops.gqa_attn_get_device_error(stream=cap)  # the graphs' error word
     if gpu_err != 0:
         raise RuntimeError(f"device error during the bench: {ops.status_string(gpu_err)}")
@@ -326,26 +477,23 @@ def run_ours(args):
     for i in range(e2e_steps):
         e2e_step(eev[i])
     torch.cuda.synchronize()
-    e2e_pre = sum(e[0].elapsed_time(e[1]) for e in eev) / e2e_steps
-    e2e_dec = sum(e[1].elapsed_time(e[2]) for e in eev) / e2e_steps
+    e2e_pre = statistics.median(e[0].elapsed_time(e[1]) for e in eev)
+    e2e_dec = statistics.median(e[1].elapsed_time(e[2]) for e in eev)
 
     # ---- max over ranks
-    tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var = max_over_ranks(
-        [tot_pre, tot_dec, wall, e2e_pre, e2e_dec, tot_var], dev, world)
+    tot_pre, tot_dec, wall, e2e_pre, e2e_dec, var_ms = max_over_ranks(
+        [tot_pre, tot_dec, wall, e2e_pre, e2e_dec, var_ms], dev, world)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return None
 
-    K = args.steps
     pre_ms = tot_pre / K
     dec_ms = tot_dec / K
     value = job_throughput(world, K, pre_flops, tot_pre, 1e12)
     dec_gbs = job_throughput(world, K, dec_bytes, tot_dec, 1e9)
     pre_ach = pre_flops / (pre_ms * 1e-3) / 1e12
     dec_ach = dec_bytes / (dec_ms * 1e-3) / 1e9
-    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     h2d_pre = (q0.numel() + k0.numel() + v0.numel()) * 2
     d2h_pre = o_pre.numel() * 2
     h2d_dec = sl0.numel() * 4 + (dq0.numel() + kc0.numel() + vc0.numel()) * 2
@@ -373,64 +521,52 @@ def run_ours(args):
             "l2": f"inputs rotated over {copies} copies "
                   f"({copies * step_in_bytes / 2**20:.0f} MiB > 129 MiB L2)",
             "launch": "CUDA graphs: chains of back-to-back calls of each kernel over the rotating copies",
+            "timing": f"median over {reps} repetitions of the K-step region "
+                      "(CUDA events around the K prefill and the K decode calls of each)",
             "parallelism": f"replicas x{world}",
         },
-        "roofline": {
-            "bound": "tensor",
-            "kernel": "prefill_tc_kernel<128, 0> (no lse output)",
-            "achieved": round(pre_ach, 3),
-            "peak": tc_peak,
-            "unit": "TFLOP/s",
-            "frac": round(pre_ach / tc_peak, 4),
-            "peak_source": f"{peak_src} bf16_tflops (burst)",
-            "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
-                                        "prefill_tc_kernel<128, 0>"),
-        },
+        "repetitions": reps,
+        "roofline": roofline_obj(
+            "tensor", pre_ach, tc_peak, "TFLOP/s", f"{peak_src} bf16_tflops (burst)",
+            "prefill_tc_kernel<128, 0> (no lse output)",
+            recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
+                             "prefill_tc_kernel<128, 0>")),
         "decode": {
             "value": round(dec_gbs, 2),
             "unit": "GB/s",
             "ms": round(dec_ms, 6),
-            "roofline": {
-                "bound": "hbm",
-                "kernel": "decode_kernel<128,5> (persistent split-KV + in-kernel merge)",
-                "achieved": round(dec_ach, 2),
-                "peak": hbm_peak,
-                "unit": "GB/s",
-                "frac": round(dec_ach / hbm_peak, 4),
-                "peak_source": f"{peak_src} hbm_gbs",
-                "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
-                                            "decode_kernel<128,5>"),
-            },
+            "roofline": roofline_obj(
+                "hbm", dec_ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
+                "decode_kernel<128,5> (persistent split-KV + in-kernel merge)",
+                recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
+                                 "decode_kernel<128,5>")),
             "e2e": {"value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},
         },
         "varlen": {
-            "value": round(job_throughput(world, K_var, vs.flops, tot_var, 1e12), 3),
+            "value": round(job_throughput(world, 1, vs.flops, var_ms, 1e12), 3),
             "unit": "TFLOP/s",
-            "ms": round(tot_var / K_var, 6),
-            "calls": K_var,
-            "gpu_launches": 2 * K_var,  # the plan kernel + the prefill kernel per call
+            "ms": round(var_ms, 6),
+            "calls_per_rep": var_chain,
+            "reps": 21,
+            "gpu_launches_per_call": 2,  # the plan kernel + the prefill kernel
             "config": {"workload": vs.name, "lens": list(vs.lens_q), "H_q": vs.H_q,
                        "H_kv": vs.H_kv, "d": vs.d, "causal": vs.causal,
                        "layout": "token-major [total][H][d], cu_seqlens on the device",
                        "l2": f"inputs rotated over {var_copies} copies "
                              f"({var_copies * var_bytes / 2**20:.0f} MiB)"},
-            "roofline": {
-                "bound": "tensor",
-                "kernel": "varlen_plan_kernel + prefill_varlen_kernel<128, 0> (per call)",
-                "achieved": round(vs.flops / (tot_var / K_var * 1e-3) / 1e12, 3),
-                "peak": tc_peak,
-                "unit": "TFLOP/s",
-                "frac": round(vs.flops / (tot_var / K_var * 1e-3) / 1e12 / tc_peak, 4),
-                "peak_source": f"{peak_src} bf16_tflops (burst)",
-                "traffic": recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
-                                            "prefill_varlen_kernel<128, 0>"),
-            },
+            "roofline": roofline_obj(
+                "tensor", vs.flops / (var_ms * 1e-3) / 1e12, tc_peak, "TFLOP/s",
+                f"{peak_src} bf16_tflops (burst)",
+                "varlen_plan_kernel + prefill_varlen_kernel<128, 0> (per call)",
+                recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
+                                 "prefill_varlen_kernel<128, 0>")),
         },
+        "configs": blocks,
         "e2e": {"value": round(pre_flops / (e2e_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre},
-        "gpu_launches": 2 * K,  # one prefill + one decode launch per step
-        "wall_ms_per_step": round(wall * 1e3 / K, 6),
+        "gpu_launches": 2 * K * reps,  # one prefill + one decode launch per step, per repetition
+        "wall_ms_per_step": round(wall * 1e3 / (K * reps), 6),
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
@@ -456,10 +592,12 @@ def oracle_prefill_sample(ps, heads, threads):
     return dt, ps.flops * heads / (ps.B * ps.H_q)
 
 
-def cpu_baseline(ps, min_seconds=10.0, max_passes=64):
+def cpu_baseline(ps, min_seconds=10.0, max_passes=64, single_seconds=5.0):
     """The oracle as it stands, timed on the host cores: whole passes over
-    the prefill layer (every head, every row) until at least `min_seconds`
-    of work, so the rate is not a sub-second sample."""
+    the prefill layer (every head, every row) with OpenMP over heads until at
+    least `min_seconds` of work; beside it, one thread on the first two heads
+    until at least `single_seconds` (the rate per FLOP of the whole layer,
+    since every head of the layer costs the same)."""
     import oracle
     from gqa_flash_attention_02_gb300 import inputs
 
@@ -473,10 +611,21 @@ def cpu_baseline(ps, min_seconds=10.0, max_passes=64):
         oracle.prefill(q, k, v, ps.causal, ps.scale, heads=(0, heads), n_threads=cores)
         dt += time.perf_counter() - t0
         passes += 1
+    one_heads, one_passes, one_dt = 2, 0, 0.0
+    while one_passes == 0 or one_dt < single_seconds:
+        t0 = time.perf_counter()
+        oracle.prefill(q, k, v, ps.causal, ps.scale, heads=(0, one_heads), n_threads=1)
+        one_dt += time.perf_counter() - t0
+        one_passes += 1
+    one_flops = one_passes * ps.flops * one_heads / heads
     return {"value": round(passes * ps.flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{passes} passes over the whole prefill layer ({heads} heads x "
-                      f"{ps.N_q} rows), float64, OpenMP over heads, {dt:.1f} s"}
+                      f"{ps.N_q} rows), float64, OpenMP over heads, {dt:.1f} s",
+            "single_thread": {
+                "value": round(one_flops / one_dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+                "sample": f"{one_passes} passes over heads 0-{one_heads - 1} of the prefill "
+                          f"layer, one thread, {one_dt:.1f} s"}}
 
 
 def run_reference(args):
@@ -530,6 +679,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing leg (profiling runs)")
+    ap.add_argument("--reps", type=int, default=0,
+                    help="repetitions of the K-step region (default: at least 21, about 1 s)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload blocks after the step (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -529,6 +529,7 @@ void gqa_attn_shutdown(void) {
     cudaDeviceSynchronize();
     if (kv.second.partials) cudaFree(kv.second.partials);
     if (kv.second.counters) cudaFree(kv.second.counters);
+    if (kv.second.units) cudaFree(kv.second.units);
     if (kv.second.ctl) cudaFree(kv.second.ctl);
   }
   g_ws.clear();

@@ -27,9 +27,10 @@
 //     swizzle the MMA descriptors expect.
 //   * Online softmax (BootstrapAI collab-005 "Kernel 2 tiling") in fp32
 //     registers with exp2 and the scale folded into the exponent. The
-//     running maximum is only raised when it grows by more than 2^8, so O is
-//     rescaled in tensor memory rarely; the result is unchanged because O and
-//     the running sum always use the same reference maximum.
+//     running maximum is only raised when it grows by more than 2^4 (2^8
+//     with fp32 exponentials), so O is rescaled in tensor memory rarely; the
+//     result is unchanged because O and the running sum always use the same
+//     reference maximum.
 //   * Every wait is bounded: a stuck pipeline records kErrTimeout in the
 //     workspace error word and unwinds instead of hanging the GPU.
 //   * Ragged batches (prompts of different lengths packed token-major,
@@ -71,10 +72,6 @@ constexpr int kTmemCols = 512;
 // sequence's first query token, query length, first key token, key length.
 constexpr int kDescInts = 16;
 enum { kDB = 0, kDHkv, kDT0, kDT1 = kDT0 + 3, kDQ0 = kDT1 + 3, kDLenQ, kDK0, kDLenK };
-constexpr float kRescaleThreshold = 8.0f;
-#ifndef GQA_EX2_BF16
-#define GQA_EX2_BF16 1
-#endif  // log2 units: rescale O when the max grows > 2^8
 template <int D>
 struct TcLayout {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
@@ -98,6 +95,24 @@ struct TcLayout {
   static constexpr int kBytes = kOffDesc + 2 * kDescInts * 4;
   static constexpr int kAlloc = kBytes + 1024;
 };
+
+// Extreme of a 128-column score row in eight independent chains of
+// three-input max: the maximum, or with kMin the minimum (as minus the
+// maximum of the negated values; the negation folds into the instruction).
+template <bool kMin>
+__device__ __forceinline__ float row_extreme(const float (&s)[128]) {
+  auto v = [&](int c) { return kMin ? -s[c] : s[c]; };
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    mx[k] = fmax3(v(16 * k), v(16 * k + 1), v(16 * k + 2));
+#pragma unroll
+    for (int c = 3; c < 15; c += 2) mx[k] = fmax3(mx[k], v(16 * k + c), v(16 * k + c + 1));
+    mx[k] = fmaxf(mx[k], v(16 * k + 15));
+  }
+  const float r = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), mx[6]), mx[7]);
+  return kMin ? -r : r;
+}
 
 struct TcParams {
   __nv_bfloat16 *o;
@@ -128,6 +143,14 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   // 1.7e-4 mean and 7.7e-3 to 9.3e-3 max, well inside the bf16 bounds); at
   // D = 64 that measured slower, so fp32 ex2 stays.
   constexpr bool kEx2Bf16 = D == 128;
+  // The running (reference) maximum is only raised, and O rescaled, when a
+  // row's maximum grows past it by more than this many log2 units; until
+  // then exponents up to this bound are allowed. The bf16 exponent input
+  // has an absolute rounding error of up to 2^-9 |x|, so there the bound is
+  // 2^4 (the error of the largest terms stays that of an exponent near 0);
+  // the fp32 path takes 2^8. On iid N(0,1) inputs either bound is crossed in
+  // about 0.1 % of (warp, key block) steps after the first block.
+  constexpr float kRescaleThreshold = kEx2Bf16 ? 4.0f : 8.0f;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -491,6 +514,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
     const uint32_t tm_p = tm_s + 64u;
     const uint32_t tm_o = tmem + lane_off + 256u + t * D;
     const float sl2 = prm.scale_log2;
+    // a masked score: whatever the sign of the scale, it scales to -inf
+    // (the host never passes a zero scale_log2)
+    const float s_masked = sl2 >= 0.f ? -INFINITY : INFINITY;
     int it = 0, vc = 0;
     uint32_t scnt = 0;
     bool ok = true;
@@ -543,7 +569,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
         const int kbase = j * kTileN;
         if (__any_sync(0xffffffffu, kbase + kTileN - 1 > lim)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? -INFINITY : s[c];
+          for (int c = 0; c < 128; ++c) s[c] = (kbase + c > lim) ? s_masked : s[c];
         }
         // P = 2^(S * scale*log2e - m) for the 64 columns of half h, with
         // packed fp32 ops, stored to tensor memory as bf16 pairs; returns the
@@ -576,18 +602,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
           const float2 a = fadd2(lsum[0], lsum[1]), b = fadd2(lsum[2], lsum[3]);
           return (a.x + b.x) + (a.y + b.y);
         };
-        // row max: eight independent chains of three-input max
+        // row maximum of s * scale * log2e: the maximum of s for a
+        // non-negative scale, its minimum for a negative one
         auto row_max = [&]() -> float {
-          float mx[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            mx[k] = fmax3(s[16 * k], s[16 * k + 1], s[16 * k + 2]);
-#pragma unroll
-            for (int c = 3; c < 15; c += 2) mx[k] = fmax3(mx[k], s[16 * k + c], s[16 * k + c + 1]);
-            mx[k] = fmaxf(mx[k], s[16 * k + 15]);
-          }
-          return fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), mx[6]), mx[7]) *
-                 sl2;
+          return (sl2 >= 0.f ? row_extreme<false>(s) : row_extreme<true>(s)) * sl2;
         };
         // halves computed before the row maximum is known: the first one
         // when P is handed over in halves, else both
@@ -600,7 +618,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
           for (int h = 0; h < kEarly; ++h) sum += make_half(h, m_ref);
         } else {
           // Speculate that the reference maximum still holds (it only moves
-          // when the row maximum grows by more than 2^8): the exponentials
+          // when the row maximum grows by more than the threshold): the exponentials
           // do not wait for the block maximum.
 #pragma unroll
           for (int h = 0; h < kEarly; ++h) sum += make_half(h, m_ref);
@@ -766,7 +784,13 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
   prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   prm.plan = plan;
   prm.va = va;
-  prm.scale_log2 = scale * 1.4426950408889634f;
+  // A zero scale (uniform weights over the visible keys) is taken as a
+  // tiny one of the same effect: the kernel scales masked scores (+-inf)
+  // by it, and inf * 0 would be NaN. Any |s| below 1e8 then gives an
+  // exponent within 2^-70 of zero, so every weight is exactly 1 in bf16.
+  float sl2 = scale * 1.4426950408889634f;
+  if (fabsf(sl2) < 1e-30f) sl2 = sl2 < 0.f ? -1e-30f : 1e-30f;
+  prm.scale_log2 = sl2;
   prm.ctl = ctl;
   return launch_programmatic(prefill_entry<D, kLse, kVarlen>(), grid, kThreads, L::kAlloc,
                              stream, tm_q, tm_k, tm_v, prm);

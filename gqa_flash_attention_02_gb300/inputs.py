@@ -188,3 +188,46 @@ def decode_inputs(B, H_q, H_kv, max_len, d, dtype=torch.bfloat16, seed=0, seqlen
 def decode_inputs_for(shape: DecodeShape):
     return decode_inputs(shape.B, shape.H_q, shape.H_kv, shape.max_len, shape.d, shape.dtype,
                          shape.seed)
+
+
+# ---------------------------------------------------------------------------
+# Structured variants for parity at wide logit spreads. Each starts from the
+# iid draws above and overwrites column 0 of q and k, so the score of key j,
+# q . k_j, gets one large, known component; the values stay bf16-exact
+# (they are rounded like every other input). They exercise the running-max
+# update of the online softmax, which iid N(0,1) inputs at scale 1/sqrt(d)
+# hardly ever reach after the first key block.
+
+def with_rising_logits(q, k, key_pos, step, q_level=8.0):
+    """Copies of q, k with q[..., 0] = q_level and k[..., 0] = step * key_pos,
+    so the score of every query row grows by q_level * step per key position.
+    ``key_pos`` holds each key row's position inside its sequence and
+    broadcasts against k[..., :1] (e.g. [1, 1, N, 1] for [B, H, N, d], or
+    [total, 1, 1] for token-major rows)."""
+    q = q.float().clone()
+    k = k.float().clone()
+    q[..., 0] = q_level
+    k[..., :1] = step * key_pos.to(torch.float32).expand_as(k[..., :1])
+    return q.to(torch.bfloat16), k.to(torch.bfloat16)
+
+
+def with_dominant_keys(q, k, key_mask, level=64.0):
+    """Copies of q, k with q[..., 0] = 2 + |q[..., 0]| (positive for every
+    query row) and k[..., 0] = level on the key rows where ``key_mask`` (a
+    bool tensor broadcasting against k[..., :1]) is set: each such key's score
+    exceeds the others' by about 2 * level."""
+    q = q.float().clone()
+    k = k.float().clone()
+    q[..., 0] = 2.0 + q[..., 0].abs()
+    col = k[..., :1]
+    k[..., :1] = torch.where(key_mask.expand_as(col), torch.full_like(col, level), col)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16)
+
+
+def token_positions(cu_seqlens, total):
+    """Position of each packed token inside its own sequence: int64 [total]."""
+    cu = [int(x) for x in cu_seqlens]
+    pos = torch.zeros(total, dtype=torch.int64)
+    for b in range(len(cu) - 1):
+        pos[cu[b]:cu[b + 1]] = torch.arange(cu[b + 1] - cu[b])
+    return pos

@@ -231,8 +231,12 @@ int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
  *   - Every call uses the same array and clears the parts that must start at
  *     zero; calls that overlap on the GPU (different streams, or different
  *     host threads) race on it and must be serialised by the caller.
- *   - Sequences whose seqlens entry is outside [0, max_len] get O = 0; this
- *     entry point does not report device-side errors.
+ *   - Sequences whose seqlens entry is outside [0, max_len] get O = 0. This
+ *     entry point does not report device-side errors: its error word lives
+ *     in the scratch array and is cleared on every call, and
+ *     gqa_attn_get_device_error() reads the per-stream workspaces of the
+ *     other entry points, not this array. A bounded wait that ran out here
+ *     (which leaves O incomplete) is therefore not reported either.
  */
 int gqa_attn_decode_noalloc(const void *q, const void *k_cache,
                             const void *v_cache, const int *seqlens, void *o,

@@ -84,3 +84,15 @@ def test_source_hash_ignores_comments_only(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.source_sha("a.cu") == bench.source_sha("b.cu")
     assert bench.source_sha("a.cu") != bench.source_sha("c.cu")
+
+
+def test_source_hash_covers_included_headers(tmp_path, monkeypatch):
+    """Device code in a header the kernel includes counts as the kernel's code."""
+    (tmp_path / "k.cu").write_text('#include "h.cuh"\nint g() { return f(1); }\n')
+    (tmp_path / "h.cuh").write_text("int f(int x) { return x + 1; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    before = bench.source_sha("k.cu")
+    (tmp_path / "h.cuh").write_text("// documented\nint f(int x) { return x + 1; }\n")
+    assert bench.source_sha("k.cu") == before
+    (tmp_path / "h.cuh").write_text("int f(int x) { return x + 2; }\n")
+    assert bench.source_sha("k.cu") != before
