@@ -216,15 +216,17 @@ def copies_for(bytes_per_call, cap_bytes=1 << 30):
 def time_calls(torch, fn, copies, stream, reps=21, min_chain_us=300.0, est_us=None):
     """Median device time of one call, in ms, over `reps` repetitions of a
     graph of back-to-back calls over the rotating copies (CUDA events on the
-    launching stream around each replay). Returns (ms_per_call, calls_per_rep)."""
+    launching stream around each replay: a graph captured on `stream` is
+    replayed on the current stream). Returns (ms_per_call, calls_per_rep)."""
+    launch = torch.cuda.current_stream()
     if est_us is None:
         g = GraphChain(torch, fn, copies, stream)
         g.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(launch)
         g.replay()
-        e1.record(stream)
+        e1.record(launch)
         torch.cuda.synchronize()
         est_us = max(1e-3, e0.elapsed_time(e1) * 1e3 / copies)
     chain = copies * max(1, math.ceil(min_chain_us / est_us / copies))
@@ -235,9 +237,9 @@ def time_calls(torch, fn, copies, stream, reps=21, min_chain_us=300.0, est_us=No
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(reps)]
     for a, b in ev:
-        a.record(stream)
+        a.record(launch)
         g.replay()
-        b.record(stream)
+        b.record(launch)
     torch.cuda.synchronize()
     return statistics.median(a.elapsed_time(b) for a, b in ev) / chain, chain
 
@@ -284,6 +286,45 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
     for shape in inputs.sweep_shapes():
         out[shape.name] = prefill_block(shape)
     out[inputs.LONG_SEQ.name] = prefill_block(inputs.LONG_SEQ)
+
+    # attention backward on the prefill layer: algorithmic FLOPs are the five
+    # products of the standard backward (S, dP, dV, dK, dQ: 2.5 x the
+    # forward's), halved for causal; the kernel's recomputed S and dP in the
+    # dQ units are not counted
+    shape = inputs.LLAMA3_8B_LAYER
+    q, k, v = inputs.prefill_inputs_for(shape)
+    dout = inputs.prefill_inputs(shape.B, shape.H_q, shape.H_kv, shape.N_q, shape.N_kv, shape.d,
+                                 torch.bfloat16, shape.seed + 1)[0]
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o, lse = ops.gqa_attn_fwd_lse(qd, kd, vd, causal=shape.causal, scale=shape.scale, stream=stream)
+    torch.cuda.synchronize()
+    nbytes = (q.numel() * 3 + k.numel() * 2) * 2 + lse.numel() * 4
+    copies = copies_for(nbytes)
+    bufs = [(qd.clone(), kd.clone(), vd.clone(), o.clone(), dout.to(dev), lse.clone())
+            for _ in range(copies)]
+    grads = (torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd))
+
+    def call_bwd(i, s):
+        a, b_, c, d_, e, f = bufs[i % copies]
+        ops.gqa_attn_bwd(a, b_, c, d_, e, f, *grads, causal=shape.causal, scale=shape.scale,
+                         stream=s)
+
+    for i in range(copies):
+        call_bwd(i, stream)
+    ms, chain = time_calls(torch, call_bwd, copies, stream)
+    assert ops.gqa_attn_get_device_error(stream=stream) == 0
+    ach = 2.5 * shape.flops / (ms * 1e-3) / 1e12
+    out["backward_" + shape.name] = {
+        "ms": round(ms, 6), "value": round(ach, 3), "unit": "TFLOP/s",
+        "shape": {"B": shape.B, "H_q": shape.H_q, "H_kv": shape.H_kv, "N": shape.N_q,
+                  "d": shape.d, "causal": shape.causal},
+        "flops": "2.5 x the forward's algorithmic FLOPs", "launches_per_call": 2,
+        "calls_per_rep": chain, "reps": 21, "l2": f"{copies} rotating copies",
+        "roofline": roofline_obj("tensor", ach, tc_peak, "TFLOP/s",
+                                 f"{peak_src} bf16_tflops (burst)",
+                                 f"bwd_prep_kernel<{shape.d}> + bwd_kernel<{shape.d}>")}
+    del bufs, grads, qd, kd, vd, o, lse
+    torch.cuda.empty_cache()
 
     for shape in inputs.decode_shapes():
         sl, q, kc, vc = inputs.decode_inputs_for(shape)

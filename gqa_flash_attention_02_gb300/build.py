@@ -22,7 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libgqa_attn.so")
 
-SOURCES = ["api.cu", "prefill_tc.cu", "decode_splitkv.cu", "attn_f32.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "prefill_tc.cu", "decode_splitkv.cu", "attn_f32.cu", "decode_noalloc.cu",
+           "attn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

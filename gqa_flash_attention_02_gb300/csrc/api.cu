@@ -443,6 +443,36 @@ int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 
+int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, void *dq, void *dk, void *dv, int B, int H_q, int H_kv, int N_q,
+                 int N_kv, int d, int causal, float scale, cudaStream_t stream) {
+  int rc = check_prefill_args(q, k, v, o, B, H_q, H_kv, N_q, N_kv, d, causal, scale);
+  if (rc != GQA_OK) return rc;
+  if (!dout || !lse || !dq || !dk || !dv) return GQA_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return GQA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  const long long units = static_cast<long long>(B) * H_kv * ((N_kv + kTileN - 1) / kTileN) +
+                          static_cast<long long>(B) * H_q * ((N_q + kTileM - 1) / kTileM);
+  if (units > INT32_MAX) return GQA_ERR_UNSUPPORTED;
+  Workspace *ws = nullptr;
+  rc = get_workspace(stream, bwd_workspace_bytes(B, H_q, N_q), &ws);
+  if (rc != GQA_OK) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_bf16_3d(&tq, q, d, N_q, static_cast<long>(B) * H_q, kTileM) ||
+      !encode_bf16_3d(&tdo, dout, d, N_q, static_cast<long>(B) * H_q, kTileM) ||
+      !encode_bf16_3d(&tk, k, d, N_kv, static_cast<long>(B) * H_kv, kTileN) ||
+      !encode_bf16_3d(&tv, v, d, N_kv, static_cast<long>(B) * H_kv, kTileN))
+    return cuda_fail(cudaErrorInvalidValue);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t e = launch_attn_bwd(tq, tk, tv, tdo, o, dout, lse, ws->partials, dq, dk, dv, B, H_q,
+                                  H_kv, N_q, N_kv, d, causal, scale, device_sms(dev),
+                                  ws->ctl + kCtlErr, stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
 const char *gqa_attn_status_string(int status) {
   switch (status) {
     case GQA_OK: return "GQA_OK";

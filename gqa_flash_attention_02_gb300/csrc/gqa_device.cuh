@@ -150,6 +150,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Contiguous (untiled) copy of `bytes` from global into shared memory,
+// completion signalled on `bar` as transaction bytes. Both addresses must be
+// 16-byte aligned and `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 3-D tiled prefetch of one box into L2 (no shared memory, no completion).
 // A prefetch changes no value a later read sees, so it may run before the
 // grid dependency wait. c0 as for tma_load_3d.

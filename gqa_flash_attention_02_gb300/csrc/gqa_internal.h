@@ -242,6 +242,18 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
 
 cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStream_t stream);
 
+// Attention backward: workspace floats for the per-row lse (log2 units) and
+// D = rowsum(dO * O), both padded to whole 128-row query tiles; tm_q / tm_do
+// view q / dO as [B*H_q][N_q][d], tm_k / tm_v view k / v as
+// [B*H_kv][N_kv][d], all with 128-row boxes.
+size_t bwd_workspace_bytes(int B, int H_q, int N_q);
+cudaError_t launch_attn_bwd(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                            const CUtensorMap &tm_v, const CUtensorMap &tm_do, const void *o,
+                            const void *dout, const float *lse, float *work, void *dq, void *dk,
+                            void *dv, int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+                            int causal, float scale, int num_sms, int *err_word,
+                            cudaStream_t stream);
+
 // bf16 tensor viewed as [planes][rows][d] for TMA: boxes of 64 columns x
 // box_rows rows, 128-byte swizzle, zero fill outside. False on failure.
 bool encode_tensor_map_bf16_3d(CUtensorMap *map, const void *base, int d, long rows, long planes,

@@ -141,8 +141,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   // two per special-function instruction on bf16 pairs (the exponent rounded
   // to bf16: the error against the float64 oracle grows from about 1.2e-4 to
   // 1.7e-4 mean and 7.7e-3 to 9.3e-3 max, well inside the bf16 bounds); at
-  // D = 64 that measured slower, so fp32 ex2 stays.
-  constexpr bool kEx2Bf16 = D == 128;
+  // D = 64 that measured slower, so fp32 ex2 stays. The log-sum-exp
+  // instantiation keeps fp32 exponentials at both sizes: O's normalisation
+  // absorbs the rounded exponent input (O is the exact softmax of scores
+  // perturbed by at most 2^-9 |x|), but the row sum itself, hence the lse,
+  // would carry that perturbation (measured up to 1e-2 at 16x query scale).
+  constexpr bool kEx2Bf16 = D == 128 && !kLse;
   // The running (reference) maximum is only raised, and O rescaled, when a
   // row's maximum grows past it by more than this many log2 units; until
   // then exponents up to this bound are allowed. The bf16 exponent input

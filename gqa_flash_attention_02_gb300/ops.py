@@ -31,7 +31,7 @@ EXPORTED = [
     "gqa_attn_decode_f32", "gqa_attn_status_string", "gqa_attn_get_device_error",
     "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
     "gqa_attn_decode_noalloc", "gqa_attn_fwd_lse", "gqa_attn_decode_lse",
-    "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse", "gqa_attn_fwd_bshd",
+    "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse", "gqa_attn_fwd_bshd", "gqa_attn_bwd",
 ]
 
 
@@ -86,6 +86,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.gqa_attn_fwd_varlen_lse.restype = _i
             lib.gqa_attn_fwd_bshd.argtypes = fwd
             lib.gqa_attn_fwd_bshd.restype = _i
+            lib.gqa_attn_bwd.argtypes = [_vp] * 9 + [_i] * 7 + [_f, _vp]
+            lib.gqa_attn_bwd.restype = _i
             lib.gqa_attn_status_string.argtypes = [_i]
             lib.gqa_attn_status_string.restype = ctypes.c_char_p
             lib.gqa_attn_get_device_error.argtypes = [_vp]
@@ -167,6 +169,34 @@ def _fwd(name, dtype, q, k, v, o, causal, scale, stream, lse=None):
                                float(scale), _stream(stream))
     _check(rc, name)
     return o
+
+
+# ---------------------------------------------------------------- backward
+
+def gqa_attn_bwd(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, causal=False, scale=None,
+                 stream=None):
+    """Gradients of bf16 prefill attention. q, o, dout [B,H_q,N_q,d], k, v [B,H_kv,N_kv,d]
+    (bf16), lse fp32 [B,H_q,N_q] from gqa_attn_fwd_lse -> (dq, dk, dv), bf16."""
+    B, H_q, N_q, d = q.shape
+    _, H_kv, N_kv, _ = k.shape
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if tuple(v.shape) != tuple(k.shape) or k.shape[0] != B or k.shape[3] != d or \
+            tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape) or \
+            tuple(dq.shape) != tuple(q.shape) or tuple(dk.shape) != tuple(k.shape) or \
+            tuple(dv.shape) != tuple(k.shape) or tuple(lse.shape) != tuple(q.shape[:3]):
+        raise ValueError("shape mismatch between q, k, v, o, dout, lse and the gradients")
+    bf = torch.bfloat16
+    rc = load().gqa_attn_bwd(_dev(q, bf, "q", 4), _dev(k, bf, "k", 4), _dev(v, bf, "v", 4),
+                             _dev(o, bf, "o", 4), _dev(dout, bf, "dout", 4),
+                             _dev(lse, torch.float32, "lse", 3), _dev(dq, bf, "dq", 4),
+                             _dev(dk, bf, "dk", 4), _dev(dv, bf, "dv", 4), B, H_q, H_kv, N_q,
+                             N_kv, d, int(bool(causal)), float(scale), _stream(stream))
+    _check(rc, "gqa_attn_bwd")
+    return dq, dk, dv
 
 
 # ---------------------------------------------------------------- ragged batches

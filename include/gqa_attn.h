@@ -243,6 +243,32 @@ int gqa_attn_decode_noalloc(const void *q, const void *k_cache,
                             int B, int H_q, int H_kv, int max_len, int d,
                             float scale, cudaStream_t stream);
 
+/*
+ * Attention backward (bf16 in / bf16 out, fp32 accumulation on the tensor
+ * cores): the gradients of O = softmax(scale Q K^T [+ causal mask]) V with
+ * respect to q, k and v, given dO = dL/dO.
+ *   q, o, dout, dq : [B][H_q][N_q][d] bf16     k, v, dk, dv : [B][H_kv][N_kv][d] bf16
+ *   lse : fp32 [B][H_q][N_q], the per-row log-sum-exp that gqa_attn_fwd_lse
+ *         returned with o for the same q, k, v, causal and scale (device
+ *         pointer, 4-byte aligned).
+ *   dq, dk, dv are written in full (every element), and must not overlap
+ *   the inputs. dK and dV of a K/V head are the sums over the H_q / H_kv
+ *   query heads that read it (the GQA reduction), accumulated in a fixed
+ *   order: the result is deterministic for a given input.
+ *   Causal alignment, d in {64, 128}, size limits and errors as gqa_attn_fwd.
+ * Three kernels are launched: a small one for D_i = sum_c dO_ic O_ic and
+ * the lse in log2 units (kept in the stream's workspace), then one grid of
+ * dK/dV units (per K/V head and 128-key block, looping over the group's
+ * query heads) and dQ units (per query head and 128-row tile).
+ * Pages: microLLM-rocm optimisation log, Experiments 051-057 (causal GQA
+ * attention backward: row recompute, softmax backward, dK/dV reduction over
+ * the query heads of a group).
+ */
+int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                 int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+                 int causal, float scale, cudaStream_t stream);
+
 /* Human-readable text for a gqa_status (never NULL; static storage). For
  * GQA_ERR_CUDA it includes the last CUDA error name seen by this thread. */
 const char *gqa_attn_status_string(int status);

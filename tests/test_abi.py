@@ -188,3 +188,27 @@ def test_prefill_plan_rejects_bad_sizes():
     lib = ops.load()
     assert lib.gqa_attn_prefill_plan(1, 6, 4, 128, 128, 0, -1, None) == -1
     assert lib.gqa_attn_prefill_plan(1, 4, 4, 256, 128, 1, -1, None) == -1
+
+
+def test_backward_validation():
+    f = ops.load().gqa_attn_bwd
+    ok = dict(B=1, H_q=4, H_kv=2, N_q=128, N_kv=128, d=64, causal=0, scale=0.125)
+    LSE = ctypes.c_void_p(0x30004)     # 4-byte aligned
+    LSE_MIS = ctypes.c_void_p(0x30002)
+
+    def call(q=A, k=A, v=A, o=A, do=A, lse=LSE, dq=A, dk=A, dv=A, **kw):
+        a = dict(ok, **kw)
+        return f(q, k, v, o, do, lse, dq, dk, dv, a["B"], a["H_q"], a["H_kv"], a["N_q"],
+                 a["N_kv"], a["d"], a["causal"], a["scale"], None)
+
+    assert call(do=None) == 1
+    assert call(lse=None) == 1
+    assert call(dk=None) == 1
+    assert call(dv=MIS) == 1
+    assert call(lse=LSE_MIS) == 1
+    assert call(B=0) == 1
+    assert call(H_q=6, H_kv=4) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(causal=1, N_q=256, N_kv=128) == 2
+    assert call(d=32) == 2
+    assert call(d=96) == 2

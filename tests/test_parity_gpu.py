@@ -293,9 +293,22 @@ def test_bf16_decode_deterministic():
 
 # ------------------------------------------------------------------ log-sum-exp output
 
-# The lse is ln of a sum whose terms carry up to bf16 (2^-8) relative error
-# (P is formed from bf16 exponentials at d = 128), so |d lse| <= ~4e-3.
+# The lse kernels sum fp32 exponentials of fp32 scores (the plain d = 128
+# prefill rounds the exponent input to bf16, the lse instantiation does
+# not), so the lse error is fp32 rounding of the scores and the sum; the
+# bound 5e-3 (natural-log units) also covers a sum of bf16-rounded weights
+# (up to 2^-8 relative error each).
 LSE_MAX = 5e-3
+
+
+def _plain_o_matches(o, o_plain, d, ref, what):
+    """The plain entry point's O: the same bits at d = 64 (the same
+    arithmetic), within the bf16 bounds of the oracle at d = 128 (the plain
+    kernel rounds the exponent input to bf16, the lse kernel does not)."""
+    if d == 64:
+        assert torch.equal(o, o_plain), what
+    else:
+        _check_bf16(o_plain.float().cpu().numpy(), ref, what)
 
 
 @pytest.mark.parametrize("d,causal,N", [(128, True, 640), (64, False, 384), (64, True, 1000)])
@@ -309,8 +322,8 @@ def test_bf16_prefill_lse_matches_oracle(d, causal, N):
     _check_bf16(o.float().cpu().numpy(), ref_o, "o with lse")
     err = np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max()
     assert err <= LSE_MAX, f"lse max err {err:.3e}"
-    # the plain entry point gives the same O
-    assert torch.equal(o, ops.gqa_attn_fwd(qd, kd, vd, causal=causal, scale=d ** -0.5))
+    _plain_o_matches(o, ops.gqa_attn_fwd(qd, kd, vd, causal=causal, scale=d ** -0.5), d, ref_o,
+                     "the plain entry point")
 
 
 @pytest.mark.parametrize("case", ["mixed", "one_long"])
