@@ -596,9 +596,10 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
               pk[c] = ex2_bf16x2(pack_bf16x2(x.x, x.y));
               p = make_float2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u));
             } else {
-              p.x = ex2(x.x);
-              p.y = ex2(x.y);
-              pk[c] = pack_bf16x2(p.x, p.y);
+              pk[c] = pack_bf16x2(ex2(x.x), ex2(x.y));
+              // the row sum takes the same bf16-rounded weights P.V uses,
+              // so O is an exact weighted average of V whatever the rounding
+              p = make_float2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u));
             }
             lsum[c & 3] = fadd2(lsum[c & 3], p);
           }
