@@ -353,6 +353,38 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
                                      "decode_kernel<128,5>")}
         del bufs, o
         torch.cuda.empty_cache()
+
+    # decode against the fp8 cache: bytes actually read (one byte per cached
+    # value, K and V once per K/V head, plus q, o and seqlens)
+    shape = inputs.decode_shapes()[-1]
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(shape.B, shape.H_q, shape.H_kv,
+                                                     shape.max_len, shape.d, seed=shape.seed)
+    in_bytes = q.numel() * 2 + k8.numel() + v8.numel()
+    copies = copies_for(in_bytes)
+    bufs = [(sl.to(dev), q.to(dev), k8.to(dev), v8.to(dev)) for _ in range(copies)]
+    ksd, vsd = ks.to(dev), vs.to(dev)
+    o = torch.empty_like(bufs[0][1])
+
+    def call8(i, s):
+        a, b_, c, d_ = bufs[i % copies]
+        ops.gqa_attn_decode_fp8(b_, c, d_, ksd, vsd, a, o, scale=shape.scale, stream=s)
+
+    for i in range(copies):
+        call8(i, stream)
+    ms, chain = time_calls(torch, call8, copies, stream)
+    assert ops.gqa_attn_get_device_error(stream=stream) == 0
+    nbytes = int(sl.sum()) * shape.H_kv * shape.d * 2 + 2 * shape.B * shape.H_q * shape.d * 2 + 4 * shape.B
+    ach = nbytes / (ms * 1e-3) / 1e9
+    out["decode_fp8_b64"] = {
+        "ms": round(ms, 6), "value": round(ach, 2), "unit": "GB/s",
+        "shape": {"B": shape.B, "H_q": shape.H_q, "H_kv": shape.H_kv, "max_len": shape.max_len,
+                  "d": shape.d, "sum_seqlens": int(sl.sum()), "cache": "e4m3, per-head scales"},
+        "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
+        "l2": f"{copies} rotating copies",
+        "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
+                                 "decode_kernel<128,4,1> (fp8 cache)")}
+    del bufs, o
+    torch.cuda.empty_cache()
     return out
 
 

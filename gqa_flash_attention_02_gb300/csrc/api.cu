@@ -188,6 +188,23 @@ bool encode_bf16_thd(CUtensorMap *map, const void *base, int d, long heads, long
   return r == CUDA_SUCCESS;
 }
 
+// 8-bit tensor (an fp8 K/V cache) viewed as [planes][rows][d] bytes; box =
+// d bytes x box_rows rows, unswizzled, zero fill outside the tensor.
+bool encode_u8_3d(CUtensorMap *map, const void *base, int d, long rows, long planes, int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace gqa {
@@ -470,6 +487,36 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
   cudaError_t e = launch_attn_bwd(tq, tk, tv, tdo, o, dout, lse, ws->partials, dq, dk, dv, B, H_q,
                                   H_kv, N_q, N_kv, d, causal, scale, device_sms(dev),
                                   ws->ctl + kCtlErr, stream);
+  return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+
+int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                        const float *k_scale, const float *v_scale, const int *seqlens, void *o,
+                        float *lse, int B, int H_q, int H_kv, int max_len, int d, float scale,
+                        cudaStream_t stream) {
+  int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
+  if (rc != GQA_OK) return rc;
+  if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(v_scale) & 3u) != 0)
+    return GQA_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int grid = decode_grid(B, H_q, H_kv, max_len, d, device_sms(dev), 0);
+  Workspace *ws = nullptr;
+  rc = get_workspace(stream, decode_partials_bytes(B, H_q, H_kv, d, grid), &ws,
+                     decode_planes(B, H_q, H_kv));
+  if (rc != GQA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
+      !encode_u8_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeFp8Unit) ||
+      !encode_u8_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeFp8Unit))
+    return cuda_fail(cudaErrorInvalidValue);
+  e = launch_decode_fp8(tq, tk, tv, q, seqlens, o, lse, ws->partials, ws->counters, B, H_q, H_kv,
+                        max_len, d, scale, k_scale, v_scale, grid, ws->ctl + kCtlErr, stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 

@@ -32,6 +32,7 @@
 //     nobody waits) merges the partials:
 //         M = max m_i,  L = sum 2^(m_i - M) l_i,  O = sum 2^(m_i - M) O_i / L.
 //     The CTA's last run is merged by the MMA warps themselves.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -46,7 +47,12 @@ constexpr int kMmaWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kEpilogueWarp = 5;
 constexpr int kThreads = 32 * (kMmaWarps + 2);
-constexpr int kSub = 64;     // cache rows per unit (16 per MMA warp)
+// Cache rows per unit: 64 for a bf16 cache (16 per MMA warp), 128 for an
+// fp8 cache (32 per MMA warp), so a unit is 16 KB of K and of V at d = 128
+// either way and each MMA warp's rows of a stage hold its accumulator
+// fragments when it hands a run to the epilogue warp.
+template <bool kFp8>
+constexpr int kSubOf = kFp8 ? 128 : 64;
 constexpr int kHeads = kDecodeHeads;  // query heads per plane (mma M)
 // Fewest units a CTA takes: fewer, longer runs (each run ends in a merge
 // step and a plane spans at most nsub / kMinUnits + 2 CTAs); no CTA range
@@ -86,14 +92,45 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same with f16 operands (P.V over an fp8 cache: e4m3 widens to f16
+// exactly, and P <= 1 keeps 11 significant bits in f16).
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 values (low byte first) widened to an f16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+// An f16 pair holding e4m3 values as a bf16 pair, exactly (3 significant
+// bits and exponents within both formats' ranges).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+  return pack_bf16x2(f.x, f.y);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
 // Barrier among the four MMA warps only (producer and epilogue keep going).
 __device__ __forceinline__ void mma_warps_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaWarps) : "memory");
 }
 
-template <int D, int NSTG>
+template <int D, int NSTG, bool kFp8>
 struct DecodeSmem {
-  static constexpr int kTile = kSub * D * 2;     // one K or V unit
+  static constexpr int kSub = kSubOf<kFp8>;
+  static constexpr int kTile = kSub * D * (kFp8 ? 1 : 2);  // one K or V unit
   static constexpr int kQTile = kHeads * D * 2;  // the plane's 16 query rows
   static constexpr int kStage = 2 * kTile + kQTile;
   static constexpr int kRingBytes = NSTG * kStage;
@@ -112,7 +149,8 @@ struct DecodeSmem {
   // warp: each MMA warp leaves its accumulator fragments in the K/V rows of
   // the stage that only it reads (16 K and 16 V rows: 2 D bytes per lane)
   // and its (m, l) in the stage's side buffer.
-  static_assert(32 * (D / 8) * 4 * 4 == 2 * (D / 64) * 16 * 128, "fragments fill the warp's rows");
+  static_assert(32 * (D / 8) * 4 * 4 == 2 * (kSub / kMmaWarps) * D * (kFp8 ? 1 : 2),
+                "fragments fill the warp's rows");
   static constexpr int kOffML = kRingBytes;                  // [NSTG][4 warps][32 lanes] float4
   static constexpr int kOffEp = kOffML + NSTG * kMmaWarps * 32 * 16;  // epilogue's merged state
   static constexpr int kOffQueue = kOffEp + kStateBytes;     // [NSTG] run entries of 16 ints
@@ -120,7 +158,11 @@ struct DecodeSmem {
   static constexpr int kOffLen = kOffMeta + NSTG * 16;
   static constexpr int kOffBar = kOffLen + kLenCache * 4;  // full, empty, ep_full [NSTG]
   static constexpr int kOffInfo = kOffBar + 3 * NSTG * 8;
-  static constexpr int kBytes = kOffInfo + 32;
+  // fp8 cache: per MMA warp, 16 rows of K widened to bf16 and of V to f16,
+  // in the 128-byte swizzled layout of a 16-row bf16 tile
+  static constexpr int kStagingTile = 16 * D * 2;
+  static constexpr int kOffStaging = (kOffInfo + 32 + 1023) / 1024 * 1024;
+  static constexpr int kBytes = kFp8 ? kOffStaging + kMmaWarps * 2 * kStagingTile : kOffInfo + 32;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kStage % 1024 == 0 && kStateBytes % 16 == 0 && kOffBar % 8 == 0, "alignment");
 };
@@ -133,6 +175,7 @@ struct DecodeParams {
   float *part;     // [(grid + planes)] slots of O [16][D] (unnormalised), m [16], l [16]
   int *counters;   // [planes], zero between launches (the last merger re-arms it)
   int *err_word;
+  const float *k_scale, *v_scale;  // fp8 cache: per K/V head dequantisation scales
   int B, H_q, H_kv, max_len, nhg;  // nhg = query-head groups of 16 per K/V head
   float scale_log2;
 };
@@ -143,6 +186,7 @@ __device__ __forceinline__ int seq_len(const DecodeParams &prm, const int *s_len
 
 // Units of a sequence of length len for each of its planes (0 for a length
 // outside [1, max_len]).
+template <int kSub>
 __device__ __forceinline__ int units_for(const DecodeParams &prm, int len) {
   return (len <= 0 || len > prm.max_len) ? 0 : (len + kSub - 1) / kSub;
 }
@@ -153,6 +197,7 @@ struct Pos {
   int b, pib, s, nsub;
 };
 
+template <int kSub>
 __device__ __forceinline__ void advance(const DecodeParams &prm, const int *s_len,
                                         int planes_per_b, Pos &p) {
   if (++p.s < p.nsub) return;
@@ -161,7 +206,7 @@ __device__ __forceinline__ void advance(const DecodeParams &prm, const int *s_le
   p.pib = 0;
   do {
     ++p.b;
-    p.nsub = (p.b < prm.B) ? units_for(prm, seq_len(prm, s_len, p.b)) : 1;  // past the end only at termination
+    p.nsub = (p.b < prm.B) ? units_for<kSub>(prm, seq_len(prm, s_len, p.b)) : 1;  // past the end only at termination
   } while (p.b < prm.B && p.nsub == 0);
 }
 
@@ -204,7 +249,7 @@ __device__ __forceinline__ void merge_row(float &m, float &l, float m2, float l2
 template <int D, int kItems, int kBatch, typename SelfFn>
 __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int jself, SelfFn self,
                                             int Gh, __nv_bfloat16 *o_plane, float *lse_plane,
-                                            int t, int nt) {
+                                            int t, int nt, float v_mul) {
   constexpr int kQuads = D / 4;
   constexpr int kSlot = kHeads * (D + 2);
   const int items = Gh * kQuads;
@@ -257,7 +302,7 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
       const int it = base + nt * k;
       if (it < items) {
         const int h = it / kQuads, q4 = it % kQuads;
-        const float il = 1.f / Lr[k];
+        const float il = v_mul / Lr[k];
         *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
             make_uint2(pack_bf16x2(Ar[k].x * il, Ar[k].y * il), pack_bf16x2(Ar[k].z * il, Ar[k].w * il));
         // the head's log-sum-exp (M, L are in log2 units of scale * q.k)
@@ -267,11 +312,31 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
   }
 }
 
-template <int D, int NSTG>
+// float4 index, inside a stage, of MMA warp w's accumulator n-tile t (plus
+// the lane) when the warp hands a run to the epilogue warp: the K and V rows
+// of the stage that only warp w reads hold exactly its 32 lanes x D/8
+// float4, lane-contiguous per n-tile (no bank conflicts). bf16 cache: rows
+// [16w, 16w+16) of each 64-column panel of K then V; fp8 cache: rows
+// [32w, 32w+32) of K (n-tiles 0 .. D/16-1), then of V.
+template <int D, bool kFp8>
+__device__ __forceinline__ int frag_slot(int w, int t) {
+  constexpr int NT = D / 8;
+  constexpr int kSub = kSubOf<kFp8>;
+  if constexpr (kFp8) {
+    constexpr int kRowsF4 = (kSub / kMmaWarps) * D / 16;  // float4 of a warp's rows of one tile
+    return (t < NT / 2 ? 0 : kSub * D / 16) + w * kRowsF4 + (t % (NT / 2)) * 32;
+  } else {
+    return (t >> 2) * kSub * 8 + w * 16 * 8 + (t & 3) * 32;
+  }
+}
+
+template <int D, int NSTG, bool kFp8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeParams prm) {
-  using L = DecodeSmem<D, NSTG>;
+  using L = DecodeSmem<D, NSTG, kFp8>;
+  constexpr int kSub = L::kSub;
+  constexpr int kRows = kSub / kMmaWarps;  // rows of a unit per MMA warp
   constexpr int NT = D / 8;                  // n-tiles of O per warp
   constexpr int kSlot = kHeads * (D + 2);    // floats per partial slot
   constexpr int kQuads = D / 4;              // float4 column groups per head
@@ -326,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (b < prm.B && b < kLenCache) s_len[b] = len[k];
         if (b < prm.B && (len[k] < 0 || len[k] > prm.max_len) && c == 0)
           record_error(prm.err_word, kErrBadSeqlen);
-        const int n = units_for(prm, len[k]);
+        const int n = units_for<kSub>(prm, len[k]);
         const int x = n * planes_per_b;
         int incl = x;
 #pragma unroll
@@ -370,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       int cum = 0;
       for (int b0 = 0; b0 < prm.B && sb == prm.B; b0 += 32) {
         const int b = b0 + lane;
-        const int n = (b < prm.B) ? units_for(prm, seq_len(prm, s_len, b)) : 0;
+        const int n = (b < prm.B) ? units_for<kSub>(prm, seq_len(prm, s_len, b)) : 0;
         const int x = n * planes_per_b;
         int incl = x;
 #pragma unroll
@@ -408,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // a sequence with no rows (or a rejected length) gets a zero output,
     // written by CTA b % G
     for (int b = c; b < prm.B; b += G) {
-      if (units_for(prm, seq_len(prm, s_len, b)) != 0) continue;
+      if (units_for<kSub>(prm, seq_len(prm, s_len, b)) != 0) continue;
       uint4 *ob = reinterpret_cast<uint4 *>(prm.o + static_cast<size_t>(b) * prm.H_q * D);
       for (int idx = tid; idx < prm.H_q * D / 8; idx += 32 * kMmaWarps) ob[idx] = make_uint4(0, 0, 0, 0);
       if (prm.lse != nullptr)
@@ -442,11 +507,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int plane_kv = p.b * prm.H_kv + h_kv;
         const uint32_t dst = s_base + st * L::kStage;
         mbar_arrive_expect_tx(full + 8 * st, L::kStage);
+        if constexpr (kFp8) {
+          // one box of kSub rows x D bytes each (unswizzled)
+          tma_load_3d(dst, &tm_k, full + 8 * st, 0, p.s * kSub, plane_kv);
+          tma_load_3d(dst + L::kTile, &tm_v, full + 8 * st, 0, p.s * kSub, plane_kv);
+        } else {
 #pragma unroll
-        for (int q = 0; q < D / 64; ++q) {
-          tma_load_3d(dst + q * kSub * 128, &tm_k, full + 8 * st, q * 64, p.s * kSub, plane_kv);
-          tma_load_3d(dst + L::kTile + q * kSub * 128, &tm_v, full + 8 * st, q * 64, p.s * kSub,
-                      plane_kv);
+          for (int q = 0; q < D / 64; ++q) {
+            tma_load_3d(dst + q * kSub * 128, &tm_k, full + 8 * st, q * 64, p.s * kSub, plane_kv);
+            tma_load_3d(dst + L::kTile + q * kSub * 128, &tm_v, full + 8 * st, q * 64, p.s * kSub,
+                        plane_kv);
+          }
         }
         // the plane's 16 query rows come with every unit (an L2 hit after the
         // first), so the MMA warps keep no Q fragments across units
@@ -454,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int q = 0; q < D / 64; ++q)
           tma_load_3d(dst + 2 * L::kTile + q * kHeads * 128, &tm_q, full + 8 * st, q * 64, row, 0);
-        advance(prm, s_len, planes_per_b, p);
+        advance<kSub>(prm, s_len, planes_per_b, p);
       }
     }
     return;
@@ -500,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         merge_row(m_hi, l_hi, ml.y, ml.w, w1h, w2h);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const float4 v = frag[(t >> 2) * kSub * 8 + w * 16 * 8 + (t & 3) * 32];
+          const float4 v = frag[frag_slot<D, kFp8>(w, t)];
           A[t][0] = fmaf(w1l, A[t][0], w2l * v.x);
           A[t][1] = fmaf(w1l, A[t][1], w2l * v.y);
           A[t][2] = fmaf(w1h, A[t][2], w2h * v.z);
@@ -520,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
       if (!split) {
         // the run is the whole plane: write O / l
-        const float il = 1.f / l_lo, ih = 1.f / l_hi;
+        const float vm = kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
+        const float il = vm / l_lo, ih = vm / l_hi;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (r_lo < Gh)
@@ -577,7 +649,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           l = sl[h];
         };
         merge_parts<D, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
-                             c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32);
+                             c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32,
+                             kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f);
         if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
       }
       __syncwarp();  // every lane is done with the state buffer
@@ -585,13 +658,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 
   // -------------------------------------------------------------- MMA warps
-  const float sl2 = prm.scale_log2;
-  const int wrow = warp * 16;  // this warp's first row in a unit
+  const int wrow = warp * kRows;  // this warp's first row in a unit
   int seg_first_i = 0, seg_first_s = 0;
   int ep_k = 0;  // runs queued for the epilogue warp so far
   int counter_seen = 0, counter_seen2 = 0;  // the last run's looks at its plane counter
   struct FinalRun {
     int plane = -1, c_first, c_last, run_units, nsub, Gh;
+    float vmul;
     __nv_bfloat16 *o_plane;
     float *lse_plane;
     float *state;
@@ -631,12 +704,55 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (warp == 0 && lane == 0 && i == n_units - 3 && i > seg_first_i && i + (nsub - s) >= n_units)
       counter_seen2 = ld_relaxed_gpu(prm.counters + b * planes_per_b + pib);  // a later look
     const int rows_here = min(kSub, len - s * kSub);  // valid rows in this unit
+    // fp8 cache: the K/V head's scales (K's folds into the exponent scale)
+    const float sl2 = kFp8 ? prm.scale_log2 * __ldg(prm.k_scale + h_kv) : prm.scale_log2;
     bool zeroed = false;
-    if (rows_here < kSub) {
+#pragma unroll 1
+    for (int grp = 0; grp < kRows / 16; ++grp) {
+    const int r0 = wrow + 16 * grp;  // first row of this 16-row group in the unit
+    // where the group's K (bf16) and V (bf16 or f16) rows are read from, and
+    // the row of its first key there, with the tile's row count
+    uint32_t kbase = kt, vbase = vt;
+    int rbase = r0, rtile = kSub;
+    if constexpr (kFp8) {
+      // Widen the group's 16 rows: K to bf16 (exact; Q stays bf16 for
+      // Q K^T), V to f16 (exact; P.V runs on f16), both into this warp's
+      // staging tiles in the swizzled 16-row layout; V rows past the
+      // sequence become zero.
+      constexpr int kUnitsPerRow = D / 16;  // 16-byte fp8 chunks per row
+      const uint32_t stk = s_base + L::kOffStaging + warp * 2 * L::kStagingTile;
+      const uint32_t stv = stk + L::kStagingTile;
+      __syncwarp();  // the previous group's reads of the staging are done
+#pragma unroll
+      for (int it = 0; it < 16 * kUnitsPerRow / 32; ++it) {
+        const int id = lane + 32 * it, rr = id / kUnitsPerRow, u = id % kUnitsPerRow;
+        const uint4 kraw = *reinterpret_cast<const uint4 *>(smem + (kt - s_base) + (r0 + rr) * D + 16 * u);
+        const uint4 vraw = *reinterpret_cast<const uint4 *>(smem + (vt - s_base) + (r0 + rr) * D + 16 * u);
+        const bool live = r0 + rr < rows_here;
+        const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w}, vw[4] = {vraw.x, vraw.y, vraw.z, vraw.w};
+        uint32_t ko[8], vo[8];
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          ko[2 * w4] = f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(kw[w4] & 0xffffu)));
+          ko[2 * w4 + 1] = f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(kw[w4] >> 16)));
+          vo[2 * w4] = live ? e4m3x2_to_f16x2(static_cast<uint16_t>(vw[w4] & 0xffffu)) : 0u;
+          vo[2 * w4 + 1] = live ? e4m3x2_to_f16x2(static_cast<uint16_t>(vw[w4] >> 16)) : 0u;
+        }
+        *reinterpret_cast<uint4 *>(smem + (stk - s_base) + swz(rr, 2 * u, 16)) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+        *reinterpret_cast<uint4 *>(smem + (stk - s_base) + swz(rr, 2 * u + 1, 16)) = make_uint4(ko[4], ko[5], ko[6], ko[7]);
+        *reinterpret_cast<uint4 *>(smem + (stv - s_base) + swz(rr, 2 * u, 16)) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+        *reinterpret_cast<uint4 *>(smem + (stv - s_base) + swz(rr, 2 * u + 1, 16)) = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+      }
+      __syncwarp();
+      kbase = stk;
+      vbase = stv;
+      rbase = 0;
+      rtile = 16;
+    } else if (rows_here < kSub) {
       // rows past the sequence (other sequences' data or NaN padding) must
       // not reach P.V: zero this warp's invalid V rows
       for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
-        const int r = wrow + idx / (D / 8), u = idx % (D / 8);
+        const int r = r0 + idx / (D / 8), u = idx % (D / 8);
         if (r >= rows_here) {
           *reinterpret_cast<uint4 *>(smem + (vt - s_base) + swz(r, u, kSub)) = make_uint4(0, 0, 0, 0);
           zeroed = true;
@@ -644,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       __syncwarp();
     }
-    // ---- S = Q K^T for this warp's 16 rows (two n-tiles of 8 keys)
+    // ---- S = Q K^T for the group's 16 rows (two n-tiles of 8 keys)
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
     {
       // A (16 heads x 16 of D) from the stage's Q tile: ldmatrix lanes 0-15
@@ -654,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // 24-31 keys 8-15 unit 2ks+1.
       const uint32_t qt = kt + 2 * L::kTile;
       const bool lo_ok = (lane >> 2) < Gh, hi_ok = (lane >> 2) + 8 < Gh;
-      const int key = wrow + (lane & 7) + ((lane >> 4) << 3);
+      const int key = rbase + (lane & 7) + ((lane >> 4) << 3);
       const int uo = (lane >> 3) & 1;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -662,13 +778,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ldsm_x4(qt + swz(lane & 15, 2 * ks + (lane >> 4), kHeads), qa[0], qa[1], qa[2], qa[3]);
         if (!lo_ok) qa[0] = qa[2] = 0u;
         if (!hi_ok) qa[1] = qa[3] = 0u;
-        ldsm_x4(kt + swz(key, 2 * ks + uo, kSub), b0, b1, b2, b3);
+        ldsm_x4(kbase + swz(key, 2 * ks + uo, rtile), b0, b1, b2, b3);
         mma_bf16(s0, qa, b0, b1);
         mma_bf16(s1, qa, b2, b3);
       }
     }
     // ---- online softmax on the fragments: rows (heads) lane/4 and lane/4+8
-    const int kc = wrow + 2 * (lane & 3);  // key of s?[0]; s?[1] is kc+1; s1 adds 8
+    const int kc = r0 + 2 * (lane & 3);  // key of s?[0]; s?[1] is kc+1; s1 adds 8
     float x[8] = {s0[0] * sl2, s0[1] * sl2, s1[0] * sl2, s1[1] * sl2,
                   s0[2] * sl2, s0[3] * sl2, s1[2] * sl2, s1[3] * sl2};
     const int keys[4] = {kc, kc + 1, kc + 8, kc + 9};
@@ -707,22 +823,38 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       acc[t][3] *= a_hi;
     }
     // P as the A operand (16 heads x 16 keys): keys 0-7 from n-tile 0, 8-15 from n-tile 1
-    const uint32_t pa[4] = {pack_bf16x2(pr[0], pr[1]), pack_bf16x2(pr[4], pr[5]),
-                            pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[6], pr[7])};
+    uint32_t pa[4];
+    if constexpr (kFp8) {
+      pa[0] = pack_f16x2(pr[0], pr[1]);
+      pa[1] = pack_f16x2(pr[4], pr[5]);
+      pa[2] = pack_f16x2(pr[2], pr[3]);
+      pa[3] = pack_f16x2(pr[6], pr[7]);
+    } else {
+      pa[0] = pack_bf16x2(pr[0], pr[1]);
+      pa[1] = pack_bf16x2(pr[4], pr[5]);
+      pa[2] = pack_bf16x2(pr[2], pr[3]);
+      pa[3] = pack_bf16x2(pr[6], pr[7]);
+    }
     // ---- O += P V (V rows = k, d = n): transposed ldmatrix of 8x8 blocks
     {
       // lanes 0-7: keys 0-7 unit u; 8-15: keys 8-15 unit u; 16-23: keys 0-7 unit u+1;
       // 24-31: keys 8-15 unit u+1  -> {b0,b1} for d-tile u and {b0,b1} for u+1
-      const int key = wrow + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int key = rbase + (lane & 7) + (((lane >> 3) & 1) << 3);
       const int uo = lane >> 4;
 #pragma unroll
       for (int u = 0; u < NT; u += 2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vt + swz(key, u + uo, kSub), b0, b1, b2, b3);
-        mma_bf16(acc[u], pa, b0, b1);
-        mma_bf16(acc[u + 1], pa, b2, b3);
+        ldsm_x4_t(vbase + swz(key, u + uo, rtile), b0, b1, b2, b3);
+        if constexpr (kFp8) {
+          mma_f16(acc[u], pa, b0, b1);
+          mma_f16(acc[u + 1], pa, b2, b3);
+        } else {
+          mma_bf16(acc[u], pa, b0, b1);
+          mma_bf16(acc[u + 1], pa, b2, b3);
+        }
       }
     }
+    }  // 16-row groups
 
     const bool final_run = (i == n_units - 1);
     if (!final_run && s != nsub - 1) {
@@ -747,10 +879,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // stage. The queue cannot overrun: every queued run holds a stage.
       const int qk = ep_k % NSTG;
       __syncwarp();  // the warp's reads of its rows are done
-      float4 *rows = reinterpret_cast<float4 *>(smem + st * L::kStage) + wrow * 8 + lane;
+      float4 *rows = reinterpret_cast<float4 *>(smem + st * L::kStage) + lane;
 #pragma unroll
       for (int t = 0; t < NT; ++t)
-        rows[(t >> 2) * kSub * 8 + (t & 3) * 32] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+        rows[frag_slot<D, kFp8>(warp, t)] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
       side_ml[(st * kMmaWarps + warp) * 32 + lane] = make_float4(m_lo, m_hi, l_lo, l_hi);
       if (warp == 0 && lane == 0) {
         int *qe = queue + 16 * qk;
@@ -821,7 +953,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int r_lo = lane >> 2, r_hi = r_lo + 8, cc = 2 * (lane & 3);
       if (!split) {
         // this run is the whole plane: write O / l
-        const float il = 1.f / l_lo, ih = 1.f / l_hi;
+        const float vm = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
+        const float il = vm / l_lo, ih = vm / l_hi;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           if (r_lo < Gh)
@@ -869,6 +1002,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       fin.run_units = run_units;
       fin.nsub = nsub;
       fin.Gh = Gh;
+      fin.vmul = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
       fin.o_plane = o_plane;
       fin.lse_plane = lse_plane;
       fin.state = state;
@@ -922,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       };
       merge_parts<D, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                               c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
-                              32 * kMmaWarps);
+                              32 * kMmaWarps, fin.vmul);
       if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
     }
   }
@@ -934,20 +1068,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (lane == 0) mbar_arrive(ep_full + 8 * qk);
 }
 
-template <int D, int NSTG>
+template <int D, int NSTG, bool kFp8>
 cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                             float *lse, float *partials, int *counters, int B, int H_q, int H_kv,
                             int max_len, float scale, int grid, int *err_word,
-                            cudaStream_t stream) {
-  using L = DecodeSmem<D, NSTG>;
+                            const float *k_scale, const float *v_scale, cudaStream_t stream) {
+  using L = DecodeSmem<D, NSTG, kFp8>;
+  static_assert(L::kAlloc <= 227 * 1024, "shared memory");
   static unsigned configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !(configured & (1u << dev))) {
-    e = cudaFuncSetAttribute(decode_kernel<D, NSTG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kAlloc);
+    e = cudaFuncSetAttribute(decode_kernel<D, NSTG, kFp8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured |= 1u << dev;
   }
@@ -959,14 +1094,16 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   prm.part = partials;
   prm.counters = counters;
   prm.err_word = err_word;
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
   prm.B = B;
   prm.H_q = H_q;
   prm.H_kv = H_kv;
   prm.max_len = max_len;
   prm.nhg = decode_head_groups(H_q, H_kv);
   prm.scale_log2 = scale * 1.4426950408889634f;
-  return launch_programmatic(decode_kernel<D, NSTG>, grid, kThreads, L::kAlloc, stream, tm_q, tm_k,
-                             tm_v, prm);
+  return launch_programmatic(decode_kernel<D, NSTG, kFp8>, grid, kThreads, L::kAlloc, stream, tm_q,
+                             tm_k, tm_v, prm);
 }
 
 }  // namespace
@@ -984,7 +1121,7 @@ size_t decode_planes(int B, int H_q, int H_kv) {
 
 bool decode_units_fit(int B, int H_q, int H_kv, int max_len) {
   const long long units = static_cast<long long>(decode_planes(B, H_q, H_kv)) *
-                          ((static_cast<long long>(max_len) + kSub - 1) / kSub);
+                          ((static_cast<long long>(max_len) + kSubOf<false> - 1) / kSubOf<false>);
   return units <= (1ll << 30);
 }
 
@@ -1010,11 +1147,30 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                int *err_word, cudaStream_t stream) {
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
   if (d == 64)
-    return launch_decode_d<64, 8>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters, B, H_q,
-                                  H_kv, max_len, scale, grid, err_word, stream);
+    return launch_decode_d<64, 8, false>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
+                                         B, H_q, H_kv, max_len, scale, grid, err_word, nullptr,
+                                         nullptr, stream);
   if (d == 128)
-    return launch_decode_d<128, 5>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters, B, H_q,
-                                   H_kv, max_len, scale, grid, err_word, stream);
+    return launch_decode_d<128, 5, false>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
+                                          B, H_q, H_kv, max_len, scale, grid, err_word, nullptr,
+                                          nullptr, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                              const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
+                              float *lse, float *partials, int *counters, int B, int H_q,
+                              int H_kv, int max_len, int d, float scale, const float *k_scale,
+                              const float *v_scale, int grid, int *err_word, cudaStream_t stream) {
+  if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
+  if (d == 64)
+    return launch_decode_d<64, 8, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
+                                        B, H_q, H_kv, max_len, scale, grid, err_word, k_scale,
+                                        v_scale, stream);
+  if (d == 128)
+    return launch_decode_d<128, 4, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
+                                         B, H_q, H_kv, max_len, scale, grid, err_word, k_scale,
+                                         v_scale, stream);
   return cudaErrorInvalidValue;
 }
 

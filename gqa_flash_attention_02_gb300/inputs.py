@@ -231,3 +231,23 @@ def token_positions(cu_seqlens, total):
     for b in range(len(cu) - 1):
         pos[cu[b]:cu[b + 1]] = torch.arange(cu[b + 1] - cu[b])
     return pos
+
+
+def decode_inputs_fp8(B, H_q, H_kv, max_len, d, seed=0, seqlens=None):
+    """decode_inputs with an fp8 cache: the same draws (q rounded to bf16),
+    with each K/V head of the caches quantised to OCP FP8 E4M3: its scale is
+    the largest |value| over the valid rows / 448 (fp32), its bytes
+    torch.float8_e4m3fn(value / scale) (round to nearest even); rows at or
+    beyond seqlens[b] hold the NaN code. Returns (seqlens, q, k8, v8,
+    k_scale, v_scale): k8, v8 float8_e4m3fn [B,H_kv,max_len,d], the scales
+    fp32 [H_kv]."""
+    seqlens, q, kc, vc = decode_inputs(B, H_q, H_kv, max_len, d, torch.float32, seed, seqlens)
+    pos = torch.arange(max_len).view(1, 1, max_len, 1)
+    dead = pos >= seqlens.long().view(B, 1, 1, 1)
+    out = []
+    for x in (kc, vc):
+        amax = torch.where(dead, torch.zeros_like(x), x).abs().amax(dim=(0, 2, 3))
+        sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+        out.append(((x / sc.view(1, H_kv, 1, 1)).to(torch.float8_e4m3fn), sc))
+    (k8, ks), (v8, vs) = out
+    return seqlens, q.to(torch.bfloat16), k8, v8, ks, vs

@@ -202,6 +202,35 @@ int gqa_attn_decode_chunked(const void *q, const void *k_cache,
                             float scale, int chunk_tokens, cudaStream_t stream);
 
 /*
+ * Decode against an fp8 K/V cache: the cache holds OCP FP8 E4M3 values
+ * (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest 448, codes
+ * 0x7F / 0xFF are NaN, no infinities), one byte each, and the value a byte
+ * stands for is its e4m3 value times the scale of its K/V head:
+ *   K[b][h][j][c] = e4m3(k_cache[b][h][j][c]) * k_scale[h]   (likewise V)
+ *   q       : [B][H_q][d] bf16         o : [B][H_q][d] bf16 (written)
+ *   k_cache, v_cache : [B][H_kv][max_len][d] bytes (16-byte aligned)
+ *   k_scale, v_scale : device fp32 [H_kv], 4-byte aligned, finite
+ *   seqlens : as gqa_attn_decode (rows [0, seqlens[b]) are valid; later rows
+ *             are never used, whatever their bytes)
+ *   lse     : optional fp32 [B][H_q] log-sum-exp as gqa_attn_decode_lse, or
+ *             NULL
+ * Same kernel design as gqa_attn_decode (persistent split-KV with the merge
+ * in the same launch), streaming half the cache bytes: units of 128 rows;
+ * each MMA warp widens its rows of K to bf16 (Q K^T on bf16 pairs, exact
+ * widening) and of V to f16 (P V on f16 pairs, exact widening), fp32
+ * accumulation; k_scale multiplies the exponent scale, v_scale the output.
+ * d in {64, 128}; limits and errors as gqa_attn_decode.
+ * Pages: microLLM-rocm optimisation log, Experiment 065 (the K/V cache
+ * stored narrower than fp32 with fp32 accumulation) and Experiments 354 and
+ * 359 (an 8-bit cache read fused into decode attention).
+ */
+int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                        const float *k_scale, const float *v_scale, const int *seqlens,
+                        void *o, float *lse,
+                        int B, int H_q, int H_kv, int max_len, int d,
+                        float scale, cudaStream_t stream);
+
+/*
  * Decode in fp32 (q, caches and o are float arrays, layouts as
  * gqa_attn_decode); d in {32, 64, 96, 128}.
  */

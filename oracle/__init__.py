@@ -25,7 +25,10 @@ What each function follows (page title and section):
   * a ragged batch as the list of its sequences, each attended on its own
     -- microLLM-rocm optimisation log, Experiment 101;
   * attention backward with the GQA head reduction of dK and dV (numpy,
-    float64) -- microLLM-rocm optimisation log, Experiments 051-057.
+    float64) -- microLLM-rocm optimisation log, Experiments 051-057;
+  * decode against an fp8 (e4m3) cache with per-K/V-head scales, the codes
+    decoded from the format's definition -- microLLM-rocm optimisation log,
+    Experiment 065.
 """
 from __future__ import annotations
 
@@ -275,6 +278,37 @@ def decode(q, k_cache, v_cache, seqlens, scale: float):
     if rc == -2:
         raise ValueError("oracle_decode: seqlens outside [0, max_len]")
     return o, lse
+
+
+def e4m3_value(codes):
+    """Values of OCP FP8 E4M3 codes (bytes) as float64, from the format's
+    definition: bit 7 sign, bits 6-3 exponent with bias 7, bits 2-0 mantissa;
+    exponent field 0 is subnormal, (m / 8) 2^-6; otherwise (1 + m / 8)
+    2^(e - 7); the codes S.1111.111 (0x7F, 0xFF) are NaN and there are no
+    infinities (largest finite value 448)."""
+    if hasattr(codes, "detach"):
+        import torch
+        t = codes.detach().cpu()
+        if t.dtype != torch.uint8:
+            t = t.view(torch.uint8)
+        codes = t.numpy()
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return np.where((c & 0x7F) == 0x7F, np.nan, sign * mag)
+
+
+def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seqlens, scale: float):
+    """Decode against an fp8 cache: the cache value of a byte is its e4m3
+    value times the scale of its K/V head (microLLM-rocm optimisation log,
+    Experiment 065: a narrower cache, attention in full precision); the
+    widened caches then go through ``decode``. Returns (o, lse)."""
+    ks, vs = _f64(k_scale), _f64(v_scale)
+    k = e4m3_value(k_codes) * ks[None, :, None, None]
+    v = e4m3_value(v_codes) * vs[None, :, None, None]
+    return decode(q, k, v, seqlens, scale)
 
 
 def lse_merge(o_parts, lse_parts):

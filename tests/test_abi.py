@@ -212,3 +212,25 @@ def test_backward_validation():
     assert call(causal=1, N_q=256, N_kv=128) == 2
     assert call(d=32) == 2
     assert call(d=96) == 2
+
+
+def test_decode_fp8_validation():
+    f = ops.load().gqa_attn_decode_fp8
+    SC = ctypes.c_void_p(0x40000)
+    SC_MIS = ctypes.c_void_p(0x40002)
+    ok = dict(B=2, H_q=8, H_kv=2, max_len=256, d=128, scale=0.1)
+
+    def call(q=A, k=A, v=A, ks=SC, vs=SC, sl=SEQ, o=A, lse=None, **kw):
+        a = dict(ok, **kw)
+        return f(q, k, v, ks, vs, sl, o, lse, a["B"], a["H_q"], a["H_kv"], a["max_len"], a["d"],
+                 a["scale"], None)
+
+    assert call(k=None) == 1
+    assert call(ks=None) == 1
+    assert call(vs=SC_MIS) == 1
+    assert call(v=MIS) == 1
+    assert call(lse=SC_MIS) == 1
+    assert call(H_q=6, H_kv=4) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(d=96) == 2
+    assert call(max_len=(1 << 20) + 1) == 2

@@ -1,0 +1,102 @@
+"""GPU parity of the decode against an fp8 (e4m3) K/V cache.
+
+The caches hold e4m3 bytes with a per-K/V-head scale (microLLM-rocm
+optimisation log, Experiment 065: the cache kept narrower than the
+arithmetic). The oracle widens every byte from the e4m3 definition, times
+its head's scale, in float64, and attends exactly; the kernel widens them
+exactly too (K to bf16, V to f16), so the comparison carries the same bf16
+bounds as the bf16 cache: max abs <= 2e-2, mean abs <= 2e-3 (lse max abs
+<= 5e-3). Rows past each sequence hold the NaN code, so a kernel that used
+one would fail.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_flash_attention_02_gb300 import inputs, ops
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX = 2e-2
+BF16_MEAN = 2e-3
+LSE_MAX = 5e-3
+
+
+def _run(sl, q, k8, v8, ks, vs, scale, with_lse=True):
+    sd, qd, kd, vd, ksd, vsd = (t.cuda() for t in (sl, q, k8, v8, ks, vs))
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    ops.gqa_attn_decode_fp8(qd, kd, vd, ksd, vsd, sd, o, lse, scale=scale)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    return o.float().cpu().numpy(), None if lse is None else lse.cpu().numpy()
+
+
+def _check(got, ref, lse, ref_lse, what):
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    d = np.abs(got.astype(np.float64) - ref)
+    assert d.max() <= BF16_MAX and d.mean() <= BF16_MEAN, f"{what}: max {d.max():.3e} mean {d.mean():.3e}"
+    if lse is not None:
+        lse = lse.astype(np.float64)
+        assert np.array_equal(np.isneginf(lse), np.isneginf(ref_lse)), what
+        m = np.isfinite(ref_lse)
+        assert np.abs(lse[m] - ref_lse[m]).max() <= LSE_MAX, what
+
+
+@pytest.mark.parametrize("shape", inputs.decode_shapes(), ids=lambda s: s.name)
+def test_fp8_decode_matches_oracle(shape):
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(shape.B, shape.H_q, shape.H_kv, shape.max_len,
+                                                     shape.d, seed=shape.seed)
+    got, lse = _run(sl, q, k8, v8, ks, vs, shape.scale)
+    ref, ref_lse = oracle.decode_fp8(q, k8, v8, ks, vs, sl, shape.scale)
+    _check(got, ref, lse, ref_lse, shape.name)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_decode_edge_lengths(d):
+    """Empty sequences, one row, unit boundaries (128 rows) and a full cache."""
+    lens = [0, 1, 127, 128, 129, 255, 256, 700]
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(8, 16, 2, 700, d, seed=500 + d, seqlens=lens)
+    got, lse = _run(sl, q, k8, v8, ks, vs, d ** -0.5)
+    assert np.all(got[0] == 0) and np.all(np.isneginf(lse[0]))
+    ref, ref_lse = oracle.decode_fp8(q, k8, v8, ks, vs, sl, d ** -0.5)
+    _check(got, ref, lse, ref_lse, f"edge lengths d {d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_decode_one_long_sequence_split_over_many_ctas(d):
+    """One 20000-row sequence: its plane is cut over many CTAs and merged."""
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(1, 8, 1, 20000, d, seed=510 + d, seqlens=[20000])
+    got, lse = _run(sl, q, k8, v8, ks, vs, d ** -0.5)
+    ref, ref_lse = oracle.decode_fp8(q, k8, v8, ks, vs, sl, d ** -0.5)
+    _check(got, ref, lse, ref_lse, f"one long sequence d {d}")
+
+
+def test_fp8_decode_scales_and_groups():
+    """Different scales per K/V head, a group of 24 query heads (two head
+    groups of 16 per K/V head), no lse output, deterministic."""
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(5, 48, 2, 1500, 128, seed=520,
+                                                     seqlens=[1500, 3, 900, 64, 1201])
+    ks = ks * torch.tensor([0.5, 2.0])
+    vs = vs * torch.tensor([4.0, 0.25])
+    a, _ = _run(sl, q, k8, v8, ks, vs, 0.09, with_lse=False)
+    b, _ = _run(sl, q, k8, v8, ks, vs, 0.09, with_lse=False)
+    assert np.array_equal(a, b)
+    ref, _ = oracle.decode_fp8(q, k8, v8, ks, vs, sl, 0.09)
+    _check(a, ref, None, None, "scales and groups")
+
+
+def test_fp8_decode_close_to_bf16_decode_of_the_same_values():
+    """The fp8 path and the bf16 path on the widened values (exact in bf16)
+    give the same operation."""
+    shape = inputs.decode_shapes()[1]
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(shape.B, shape.H_q, shape.H_kv, shape.max_len,
+                                                     shape.d, seed=530)
+    ones = torch.ones(shape.H_kv)
+    got, _ = _run(sl, q, k8, v8, ones, ones, shape.scale, with_lse=False)
+    kb, vb = k8.to(torch.bfloat16).cuda(), v8.to(torch.bfloat16).cuda()
+    o = ops.gqa_attn_decode(q.cuda(), kb, vb, sl.cuda(), scale=shape.scale)
+    torch.cuda.synchronize()
+    d = np.abs(got - o.float().cpu().numpy())
+    assert d.max() <= BF16_MAX and d.mean() <= BF16_MEAN

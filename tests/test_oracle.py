@@ -19,6 +19,7 @@ import pytest
 import torch
 
 import oracle
+from gqa_flash_attention_02_gb300 import inputs
 from gqa_flash_attention_02_gb300.inputs import decode_inputs, prefill_inputs, varlen_inputs
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
@@ -494,3 +495,58 @@ def test_pins_reject_planted_mistake(mutation):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake '{mutation}'"
+
+
+# ------------------------------------------------------------------ fp8 (e4m3) cache
+
+def test_e4m3_codes_closed_forms():
+    """Codes whose values follow from the format's definition by hand."""
+    cases = {0x00: 0.0, 0x80: -0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x38: 1.0, 0x39: 1.125, 0xB8: -1.0, 0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0,
+             0x77: 240.0, 0x30: 0.5}
+    got = oracle.e4m3_value(np.array(list(cases), dtype=np.uint8))
+    assert np.array_equal(got, np.array(list(cases.values())))
+    assert np.isnan(oracle.e4m3_value(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_e4m3_codes_match_torch_float8():
+    """Every code against torch's float8_e4m3fn widening (a library special case)."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_value(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+def test_decode_fp8_is_decode_of_the_widened_scaled_cache():
+    """decode_fp8 equals decode on e4m3(code) * scale, written out here with
+    torch's widening; a K scale folds into the softmax scale, a V scale
+    multiplies O and leaves the lse alone."""
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(3, 8, 2, 200, 64, seed=11,
+                                                     seqlens=[200, 1, 77])
+    o, lse = oracle.decode_fp8(q, k8, v8, ks, vs, sl, 0.125)
+    kw = k8.to(torch.float64) * ks.double().view(1, 2, 1, 1)
+    vw = v8.to(torch.float64) * vs.double().view(1, 2, 1, 1)
+    o2, lse2 = oracle.decode(q, kw, vw, sl, 0.125)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    one = torch.ones(2)
+    o_k, lse_k = oracle.decode_fp8(q, k8, v8, torch.full((2,), 0.5), one, sl, 0.125)
+    o_ref, lse_ref = oracle.decode_fp8(q, k8, v8, one, one, sl, 0.0625)
+    assert np.allclose(o_k, o_ref, atol=1e-13) and np.allclose(lse_k, lse_ref, atol=1e-13)
+    o_v, lse_v = oracle.decode_fp8(q, k8, v8, one, torch.full((2,), 3.0), sl, 0.125)
+    o_1, lse_1 = oracle.decode_fp8(q, k8, v8, one, one, sl, 0.125)
+    assert np.allclose(o_v, 3 * o_1, atol=1e-12) and np.array_equal(lse_v, lse_1)
+
+
+def test_decode_fp8_planted_mistakes_fail():
+    """A decoder that drops the subnormals, or uses bias 8, changes the result."""
+    codes = np.arange(256, dtype=np.uint8)
+    good = oracle.e4m3_value(codes)
+    c = codes.astype(np.int64)
+    e, m = (c >> 3) & 0xF, (c & 7) / 8.0
+    no_sub = np.where(e == 0, 0.0, np.abs(good))
+    bias8 = np.where(e == 0, m * 2.0 ** -7, (1 + m) * np.exp2(e - 8.0))
+    ok = ~np.isnan(good)
+    assert not np.array_equal(np.abs(good)[ok], no_sub[ok])
+    assert not np.array_equal(np.abs(good)[ok], bias8[ok])
