@@ -188,8 +188,29 @@ bool encode_bf16_thd(CUtensorMap *map, const void *base, int d, long heads, long
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor indexed [batch][head][row][d] with the given strides (elements;
+// d contiguous) for TMA as (column, row, head, batch): boxes of 64 columns x
+// box_rows rows, 128-byte swizzle, zero fill outside (so columns past d and
+// rows past `rows` read as zero).
+bool encode_bf16_4d(CUtensorMap *map, const void *base, int d, long rows, long heads, long batch,
+                    long long s_row, long long s_head, long long s_batch, int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s_row) * 2, static_cast<cuuint64_t>(s_head) * 2,
+                           static_cast<cuuint64_t>(s_batch) * 2};
+  cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_rows), 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 8-bit tensor (an fp8 K/V cache) viewed as [planes][rows][d] bytes; box =
-// d bytes x box_rows rows, unswizzled, zero fill outside the tensor.
+// d bytes x box_rows rows with the d-byte swizzle (128 B for d = 128, 64 B
+// for d = 64), zero fill outside the tensor.
 bool encode_u8_3d(CUtensorMap *map, const void *base, int d, long rows, long planes, int box_rows) {
   auto enc = encoder();
   if (!enc) return false;
@@ -200,7 +221,8 @@ bool encode_u8_3d(CUtensorMap *map, const void *base, int d, long rows, long pla
   cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -289,29 +311,65 @@ int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const i
 }
 }  // namespace
 
-extern "C" {
+namespace {
+// Dense prefill with the caller's strides (elements; d contiguous): the
+// tensor maps are 4-D (column, row, head, batch), so any batch and head
+// strides work, e.g. slices of a fused QKV buffer.
+bool d_supported_tc(int d) { return d == 32 || d == 64 || d == 96 || d == 128; }
 
-int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                     int H_q, int H_kv, int N_q, int N_kv, int d, int causal, float scale,
-                     cudaStream_t stream) {
+bool strides_ok(long long sb, long long sh, long long sn, int d) {
+  // TMA wants 16-byte multiples; rows must not overlap within a head
+  return sb > 0 && sh > 0 && sn >= d && sb % 8 == 0 && sh % 8 == 0 && sn % 8 == 0;
+}
+
+int fwd_dense(const void *q, long long q_sb, long long q_sh, long long q_sn, const void *k,
+              long long k_sb, long long k_sh, long long k_sn, const void *v, long long v_sb,
+              long long v_sh, long long v_sn, void *o, long long o_sb, long long o_sh,
+              long long o_sn, float *lse, int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+              int causal, float scale, cudaStream_t stream) {
   int rc = check_prefill_args(q, k, v, o, B, H_q, H_kv, N_q, N_kv, d, causal, scale);
   if (rc != GQA_OK) return rc;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (!d_supported_tc(d)) return GQA_ERR_UNSUPPORTED;
+  if (!strides_ok(q_sb, q_sh, q_sn, d) || !strides_ok(k_sb, k_sh, k_sn, d) ||
+      !strides_ok(v_sb, v_sh, v_sn, d) || !strides_ok(o_sb, o_sh, o_sn, d))
+    return GQA_ERR_INVALID_ARG;
   const PrefillPlan plan = make_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal);
   Workspace *ws = nullptr;
   rc = get_workspace(stream, 0, &ws);
   if (rc != GQA_OK) return rc;
   CUtensorMap tq, tk, tv;
-  if (!encode_bf16_3d(&tq, q, d, N_q, static_cast<long>(B) * H_q, kTileM) ||
-      !encode_bf16_3d(&tk, k, d, N_kv, static_cast<long>(B) * H_kv, kTileN) ||
-      !encode_bf16_3d(&tv, v, d, N_kv, static_cast<long>(B) * H_kv, kTileN))
+  if (!encode_bf16_4d(&tq, q, d, N_q, H_q, B, q_sn, q_sh, q_sb, kTileM) ||
+      !encode_bf16_4d(&tk, k, d, N_kv, H_kv, B, k_sn, k_sh, k_sb, kTileN) ||
+      !encode_bf16_4d(&tv, v, d, N_kv, H_kv, B, v_sn, v_sh, v_sb, kTileN))
     return cuda_fail(cudaErrorInvalidValue);
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t e =
-      launch_prefill_tc(tq, tk, tv, o, lse, plan, d, scale, ws->ctl, device_sms(dev), stream);
+  const OutView ov{o_sb, o_sh, o_sn, d};
+  cudaError_t e = launch_prefill_tc(tq, tk, tv, o, ov, lse, plan, scale, ws->ctl, device_sms(dev),
+                                    stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+}  // namespace
+
+extern "C" {
+
+int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H_q, int H_kv, int N_q, int N_kv, int d, int causal, float scale,
+                     cudaStream_t stream) {
+  const long long nq = N_q, nk = N_kv, dd = d;
+  return fwd_dense(q, nq * dd * H_q, nq * dd, dd, k, nk * dd * H_kv, nk * dd, dd, v,
+                   nk * dd * H_kv, nk * dd, dd, o, nq * dd * H_q, nq * dd, dd, lse, B, H_q, H_kv,
+                   N_q, N_kv, d, causal, scale, stream);
+}
+
+int gqa_attn_fwd_strided(const void *q, long long q_sb, long long q_sh, long long q_sn,
+                         const void *k, long long k_sb, long long k_sh, long long k_sn,
+                         const void *v, long long v_sb, long long v_sh, long long v_sn, void *o,
+                         long long o_sb, long long o_sh, long long o_sn, int B, int H_q, int H_kv,
+                         int N_q, int N_kv, int d, int causal, float scale, cudaStream_t stream) {
+  return fwd_dense(q, q_sb, q_sh, q_sn, k, k_sb, k_sh, k_sn, v, v_sb, v_sh, v_sn, o, o_sb, o_sh,
+                   o_sn, nullptr, B, H_q, H_kv, N_q, N_kv, d, causal, scale, stream);
 }
 
 }  // extern "C"
@@ -329,7 +387,7 @@ int fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
     return GQA_ERR_INVALID_ARG;
   if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128) return GQA_ERR_UNSUPPORTED;
   if (B > kVarlenMaxB) return GQA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_q) * H_q * d > kMaxElems ||
       static_cast<long long>(total_k) * H_kv * d > kMaxElems)
@@ -363,7 +421,8 @@ int fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
   if (e != cudaSuccess) return cuda_fail(e);
   int dev = 0;
   cudaGetDevice(&dev);
-  e = launch_prefill_tc_varlen(tq, tk, tv, o, lse, va, d, scale, ws->ctl, device_sms(dev), stream);
+  const OutView ov{0, d, static_cast<long long>(H_q) * d, d};  // [total_q][H_q][d]
+  e = launch_prefill_tc_varlen(tq, tk, tv, o, ov, lse, va, scale, ws->ctl, device_sms(dev), stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 }  // namespace

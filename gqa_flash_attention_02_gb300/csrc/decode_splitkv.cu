@@ -68,6 +68,16 @@ __device__ __forceinline__ uint32_t swz(int row, int u, int rows) {
   return static_cast<uint32_t>((u >> 3) * rows * 128 + row * 128 + (((u & 7) ^ (row & 7)) << 4));
 }
 
+// Byte offset of 16-byte chunk c of row `row` in an fp8 tile of D-byte rows
+// as TMA writes it: the 128-byte swizzle (D = 128) XORs the chunk index with
+// row % 8, the 64-byte swizzle (D = 64) with (row / 2) % 4, so the 8 rows
+// of an ldmatrix read fall in different banks.
+template <int D>
+__device__ __forceinline__ uint32_t swz8(int row, int c) {
+  const int x = D == 128 ? (row & 7) : ((row >> 1) & 3);
+  return static_cast<uint32_t>(row * D + ((c ^ x) << 4));
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -158,11 +168,7 @@ struct DecodeSmem {
   static constexpr int kOffLen = kOffMeta + NSTG * 16;
   static constexpr int kOffBar = kOffLen + kLenCache * 4;  // full, empty, ep_full [NSTG]
   static constexpr int kOffInfo = kOffBar + 3 * NSTG * 8;
-  // fp8 cache: per MMA warp, 16 rows of K widened to bf16 and of V to f16,
-  // in the 128-byte swizzled layout of a 16-row bf16 tile
-  static constexpr int kStagingTile = 16 * D * 2;
-  static constexpr int kOffStaging = (kOffInfo + 32 + 1023) / 1024 * 1024;
-  static constexpr int kBytes = kFp8 ? kOffStaging + kMmaWarps * 2 * kStagingTile : kOffInfo + 32;
+  static constexpr int kBytes = kOffInfo + 32;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kStage % 1024 == 0 && kStateBytes % 16 == 0 && kOffBar % 8 == 0, "alignment");
 };
@@ -246,7 +252,7 @@ __device__ __forceinline__ void merge_row(float &m, float &l, float m2, float l2
 // log-sum-exp. Every item's arithmetic is the same whichever CTA or
 // warp runs it, so the result does not depend on who merges. kBatch parts'
 // loads are in flight together.
-template <int D, int kItems, int kBatch, typename SelfFn>
+template <int D, bool kFp8, int kItems, int kBatch, typename SelfFn>
 __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int jself, SelfFn self,
                                             int Gh, __nv_bfloat16 *o_plane, float *lse_plane,
                                             int t, int nt, float v_mul) {
@@ -303,12 +309,44 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
       if (it < items) {
         const int h = it / kQuads, q4 = it % kQuads;
         const float il = v_mul / Lr[k];
-        *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
-            make_uint2(pack_bf16x2(Ar[k].x * il, Ar[k].y * il), pack_bf16x2(Ar[k].z * il, Ar[k].w * il));
+        if constexpr (kFp8) {
+          // fragment columns 4q4 .. 4q4+3 are columns 4(q4 % 2) .. +3 of
+          // n-tile q4 / 2, i.e. dims 16 (t / 2) + (t % 2) + 2 n (see write_o_row)
+          const int t = q4 >> 1, base = 16 * (t >> 1) + (t & 1) + 8 * (q4 & 1);
+          __nv_bfloat16 *row = o_plane + h * D + base;
+          row[0] = __float2bfloat16_rn(Ar[k].x * il);
+          row[2] = __float2bfloat16_rn(Ar[k].y * il);
+          row[4] = __float2bfloat16_rn(Ar[k].z * il);
+          row[6] = __float2bfloat16_rn(Ar[k].w * il);
+        } else {
+          *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
+              make_uint2(pack_bf16x2(Ar[k].x * il, Ar[k].y * il), pack_bf16x2(Ar[k].z * il, Ar[k].w * il));
+        }
         // the head's log-sum-exp (M, L are in log2 units of scale * q.k)
         if (lse_plane != nullptr && q4 == 0) lse_plane[h] = (Mr[k] + log2f(Lr[k])) * 0.6931471805599453f;
       }
     }
+  }
+}
+
+// Writes one head's row of O (times il, as bf16) from accumulator
+// fragments: entries e0, e0 + 1 of each n-tile are the lane's columns cc,
+// cc + 1 of the tile. With an fp8 cache n-tile 2ch holds the even dims of the
+// 16-dim chunk ch and n-tile 2ch + 1 its odd dims (the order P.V produces
+// them in), so the lane's four values are dims 16ch + 2cc .. 16ch + 2cc + 3.
+template <int D, bool kFp8>
+__device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)[D / 8][4], int e0,
+                                            int cc, float il) {
+  if constexpr (kFp8) {
+#pragma unroll
+    for (int ch = 0; ch < D / 16; ++ch)
+      *reinterpret_cast<uint2 *>(dst + 16 * ch + 2 * cc) =
+          make_uint2(pack_bf16x2(A[2 * ch][e0] * il, A[2 * ch + 1][e0] * il),
+                     pack_bf16x2(A[2 * ch][e0 + 1] * il, A[2 * ch + 1][e0 + 1] * il));
+  } else {
+#pragma unroll
+    for (int t = 0; t < D / 8; ++t)
+      *reinterpret_cast<uint32_t *>(dst + t * 8 + cc) = pack_bf16x2(A[t][e0] * il, A[t][e0 + 1] * il);
   }
 }
 
@@ -593,15 +631,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // the run is the whole plane: write O / l
         const float vm = kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (r_lo < Gh)
-            *reinterpret_cast<uint32_t *>(o_plane + r_lo * D + t * 8 + cc) =
-                pack_bf16x2(A[t][0] * il, A[t][1] * il);
-          if (r_hi < Gh)
-            *reinterpret_cast<uint32_t *>(o_plane + r_hi * D + t * 8 + cc) =
-                pack_bf16x2(A[t][2] * ih, A[t][3] * ih);
-        }
+        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * D, A, 0, cc, il);
+        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * D, A, 2, cc, ih);
         if (lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -648,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           m = sm[h];
           l = sl[h];
         };
-        merge_parts<D, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+        merge_parts<D, kFp8, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32,
                              kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f);
         if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
@@ -710,67 +741,66 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll 1
     for (int grp = 0; grp < kRows / 16; ++grp) {
     const int r0 = wrow + 16 * grp;  // first row of this 16-row group in the unit
-    // where the group's K (bf16) and V (bf16 or f16) rows are read from, and
-    // the row of its first key there, with the tile's row count
-    uint32_t kbase = kt, vbase = vt;
-    int rbase = r0, rtile = kSub;
-    if constexpr (kFp8) {
-      // Widen the group's 16 rows: K to bf16 (exact; Q stays bf16 for
-      // Q K^T), V to f16 (exact; P.V runs on f16), both into this warp's
-      // staging tiles in the swizzled 16-row layout; V rows past the
-      // sequence become zero.
-      constexpr int kUnitsPerRow = D / 16;  // 16-byte fp8 chunks per row
-      const uint32_t stk = s_base + L::kOffStaging + warp * 2 * L::kStagingTile;
-      const uint32_t stv = stk + L::kStagingTile;
-      __syncwarp();  // the previous group's reads of the staging are done
-#pragma unroll
-      for (int it = 0; it < 16 * kUnitsPerRow / 32; ++it) {
-        const int id = lane + 32 * it, rr = id / kUnitsPerRow, u = id % kUnitsPerRow;
-        const uint4 kraw = *reinterpret_cast<const uint4 *>(smem + (kt - s_base) + (r0 + rr) * D + 16 * u);
-        const uint4 vraw = *reinterpret_cast<const uint4 *>(smem + (vt - s_base) + (r0 + rr) * D + 16 * u);
-        const bool live = r0 + rr < rows_here;
-        const uint32_t kw[4] = {kraw.x, kraw.y, kraw.z, kraw.w}, vw[4] = {vraw.x, vraw.y, vraw.z, vraw.w};
-        uint32_t ko[8], vo[8];
-#pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) {
-          ko[2 * w4] = f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(kw[w4] & 0xffffu)));
-          ko[2 * w4 + 1] = f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(kw[w4] >> 16)));
-          vo[2 * w4] = live ? e4m3x2_to_f16x2(static_cast<uint16_t>(vw[w4] & 0xffffu)) : 0u;
-          vo[2 * w4 + 1] = live ? e4m3x2_to_f16x2(static_cast<uint16_t>(vw[w4] >> 16)) : 0u;
+    if constexpr (!kFp8) {
+      if (rows_here < kSub) {
+        // rows past the sequence (other sequences' data or NaN padding) must
+        // not reach P.V: zero this warp's invalid V rows
+        for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+          const int r = r0 + idx / (D / 8), u = idx % (D / 8);
+          if (r >= rows_here) {
+            *reinterpret_cast<uint4 *>(smem + (vt - s_base) + swz(r, u, kSub)) = make_uint4(0, 0, 0, 0);
+            zeroed = true;
+          }
         }
-        *reinterpret_cast<uint4 *>(smem + (stk - s_base) + swz(rr, 2 * u, 16)) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
-        *reinterpret_cast<uint4 *>(smem + (stk - s_base) + swz(rr, 2 * u + 1, 16)) = make_uint4(ko[4], ko[5], ko[6], ko[7]);
-        *reinterpret_cast<uint4 *>(smem + (stv - s_base) + swz(rr, 2 * u, 16)) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
-        *reinterpret_cast<uint4 *>(smem + (stv - s_base) + swz(rr, 2 * u + 1, 16)) = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+        __syncwarp();
       }
-      __syncwarp();
-      kbase = stk;
-      vbase = stv;
-      rbase = 0;
-      rtile = 16;
-    } else if (rows_here < kSub) {
-      // rows past the sequence (other sequences' data or NaN padding) must
-      // not reach P.V: zero this warp's invalid V rows
-      for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
-        const int r = r0 + idx / (D / 8), u = idx % (D / 8);
-        if (r >= rows_here) {
-          *reinterpret_cast<uint4 *>(smem + (vt - s_base) + swz(r, u, kSub)) = make_uint4(0, 0, 0, 0);
-          zeroed = true;
-        }
-      }
-      __syncwarp();
     }
     // ---- S = Q K^T for the group's 16 rows (two n-tiles of 8 keys)
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-    {
+    const uint32_t qt = kt + 2 * L::kTile;
+    const bool lo_ok = (lane >> 2) < Gh, hi_ok = (lane >> 2) + 8 < Gh;
+    if constexpr (kFp8) {
+      // The fp8 K rows are read as 8x8 matrices of 16-bit pairs: lane l gets
+      // key row l/4 of a matrix and bytes 4(l%4)..+3, the dims 4t..4t+3 (t =
+      // l%4) of a 16-dim chunk. Widened to two bf16 pairs they are the B
+      // fragment of one k16 step under a permutation of the contraction
+      // index (k 2t,2t+1 <-> dims 4t,4t+1; k 2t+8,2t+9 <-> dims 4t+2,4t+3),
+      // and Q's A fragment is read under the same permutation (8 bytes of
+      // dims 4t..4t+3 per row), so S is unchanged. Matrices: keys 0-7 and
+      // 8-15 of the group x chunks 2cp and 2cp+1.
+      const int mat = lane >> 3;
+      const int key = r0 + (lane & 7) + ((mat >> 1) << 3);
+      const int t = lane & 3, g = lane >> 2;
+#pragma unroll
+      for (int cp = 0; cp < D / 32; ++cp) {
+        uint32_t r[4];
+        ldsm_x4(kt + swz8<D>(key, 2 * cp + (mat & 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // chunk 2cp + h
+          const int ch = 2 * cp + h;
+          uint32_t qa[4];
+          const uint2 lo = *reinterpret_cast<const uint2 *>(smem + (qt - s_base) +
+                                                            swz(g, 2 * ch + (t >> 1), kHeads) + 8 * (t & 1));
+          const uint2 hi = *reinterpret_cast<const uint2 *>(smem + (qt - s_base) +
+                                                            swz(g + 8, 2 * ch + (t >> 1), kHeads) + 8 * (t & 1));
+          qa[0] = lo_ok ? lo.x : 0u;
+          qa[2] = lo_ok ? lo.y : 0u;
+          qa[1] = hi_ok ? hi.x : 0u;
+          qa[3] = hi_ok ? hi.y : 0u;
+          const uint32_t k0 = r[h], k1 = r[2 + h];  // keys 0-7, keys 8-15
+          mma_bf16(s0, qa, f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k0 & 0xffffu))),
+                   f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k0 >> 16))));
+          mma_bf16(s1, qa, f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k1 & 0xffffu))),
+                   f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k1 >> 16))));
+        }
+      }
+    } else {
       // A (16 heads x 16 of D) from the stage's Q tile: ldmatrix lanes 0-15
       // address rows 0-15 at a k-step's first 8 columns, lanes 16-31 the
       // next 8; rows past the group are zero. B (K^T): lanes 0-7 keys 0-7
       // unit 2ks; 8-15 keys 0-7 unit 2ks+1; 16-23 keys 8-15 unit 2ks;
       // 24-31 keys 8-15 unit 2ks+1.
-      const uint32_t qt = kt + 2 * L::kTile;
-      const bool lo_ok = (lane >> 2) < Gh, hi_ok = (lane >> 2) + 8 < Gh;
-      const int key = rbase + (lane & 7) + ((lane >> 4) << 3);
+      const int key = r0 + (lane & 7) + ((lane >> 4) << 3);
       const int uo = (lane >> 3) & 1;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
@@ -778,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ldsm_x4(qt + swz(lane & 15, 2 * ks + (lane >> 4), kHeads), qa[0], qa[1], qa[2], qa[3]);
         if (!lo_ok) qa[0] = qa[2] = 0u;
         if (!hi_ok) qa[1] = qa[3] = 0u;
-        ldsm_x4(kbase + swz(key, 2 * ks + uo, rtile), b0, b1, b2, b3);
+        ldsm_x4(kt + swz(key, 2 * ks + uo, kSub), b0, b1, b2, b3);
         mma_bf16(s0, qa, b0, b1);
         mma_bf16(s1, qa, b2, b3);
       }
@@ -822,36 +852,55 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       acc[t][2] *= a_hi;
       acc[t][3] *= a_hi;
     }
-    // P as the A operand (16 heads x 16 keys): keys 0-7 from n-tile 0, 8-15 from n-tile 1
-    uint32_t pa[4];
-    if constexpr (kFp8) {
-      pa[0] = pack_f16x2(pr[0], pr[1]);
-      pa[1] = pack_f16x2(pr[4], pr[5]);
-      pa[2] = pack_f16x2(pr[2], pr[3]);
-      pa[3] = pack_f16x2(pr[6], pr[7]);
-    } else {
-      pa[0] = pack_bf16x2(pr[0], pr[1]);
-      pa[1] = pack_bf16x2(pr[4], pr[5]);
-      pa[2] = pack_bf16x2(pr[2], pr[3]);
-      pa[3] = pack_bf16x2(pr[6], pr[7]);
-    }
     // ---- O += P V (V rows = k, d = n): transposed ldmatrix of 8x8 blocks
-    {
+    if constexpr (kFp8) {
+      // P as f16 (16 heads x 16 keys). The fp8 V rows are read transposed
+      // as 16-bit pairs: lane l gets keys 2t, 2t+1 of a matrix at bytes
+      // 2c, 2c+1 (c = l/4), i.e. two dims of a 16-dim chunk for two keys;
+      // one byte permute splits them into the key pairs of dim 2c and of dim
+      // 2c+1, widened to f16 pairs: B fragments of two n-tiles, one holding
+      // the chunk's even dims, the other its odd dims (the accumulator's
+      // column order that the final O stores undo). Keys 8-15 of the group
+      // are rows past the sequence when r0 + 8 >= rows_here: P is 0 there,
+      // and any NaN bytes are replaced by zero before they reach the MMA.
+      const uint32_t pa[4] = {pack_f16x2(pr[0], pr[1]), pack_f16x2(pr[4], pr[5]),
+                              pack_f16x2(pr[2], pr[3]), pack_f16x2(pr[6], pr[7])};
+      const int key = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int t = lane & 3;
+      const bool dead0 = r0 + 2 * t >= rows_here, dead1 = r0 + 2 * t + 1 >= rows_here;
+      const bool dead8 = r0 + 8 + 2 * t >= rows_here, dead9 = r0 + 9 + 2 * t >= rows_here;
+#pragma unroll
+      for (int cp = 0; cp < D / 32; ++cp) {
+        uint32_t r[4];
+        ldsm_x4_t(vt + swz8<D>(key, 2 * cp + (lane >> 4)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int ch = 2 * cp + h;
+          // keys 0-7 (r[2h]) and 8-15 (r[2h+1]); zero the bytes of keys past the sequence
+          uint32_t lo = r[2 * h], hi = r[2 * h + 1];
+          lo = (dead0 ? 0u : (lo & 0x0000ffffu)) | (dead1 ? 0u : (lo & 0xffff0000u));
+          hi = (dead8 ? 0u : (hi & 0x0000ffffu)) | (dead9 ? 0u : (hi & 0xffff0000u));
+          const uint32_t plo = __byte_perm(lo, 0, 0x3120), phi = __byte_perm(hi, 0, 0x3120);
+          mma_f16(acc[2 * ch], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(plo & 0xffffu)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(phi & 0xffffu)));
+          mma_f16(acc[2 * ch + 1], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(plo >> 16)),
+                  e4m3x2_to_f16x2(static_cast<uint16_t>(phi >> 16)));
+        }
+      }
+    } else {
+      // P as the A operand (16 heads x 16 keys): keys 0-7 from n-tile 0, 8-15 from n-tile 1
+      const uint32_t pa[4] = {pack_bf16x2(pr[0], pr[1]), pack_bf16x2(pr[4], pr[5]),
+                              pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[6], pr[7])};
       // lanes 0-7: keys 0-7 unit u; 8-15: keys 8-15 unit u; 16-23: keys 0-7 unit u+1;
       // 24-31: keys 8-15 unit u+1  -> {b0,b1} for d-tile u and {b0,b1} for u+1
-      const int key = rbase + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int key = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
       const int uo = lane >> 4;
 #pragma unroll
       for (int u = 0; u < NT; u += 2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vbase + swz(key, u + uo, rtile), b0, b1, b2, b3);
-        if constexpr (kFp8) {
-          mma_f16(acc[u], pa, b0, b1);
-          mma_f16(acc[u + 1], pa, b2, b3);
-        } else {
-          mma_bf16(acc[u], pa, b0, b1);
-          mma_bf16(acc[u + 1], pa, b2, b3);
-        }
+        ldsm_x4_t(vt + swz(key, u + uo, kSub), b0, b1, b2, b3);
+        mma_bf16(acc[u], pa, b0, b1);
+        mma_bf16(acc[u + 1], pa, b2, b3);
       }
     }
     }  // 16-row groups
@@ -955,15 +1004,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // this run is the whole plane: write O / l
         const float vm = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (r_lo < Gh)
-            *reinterpret_cast<uint32_t *>(o_plane + r_lo * D + t * 8 + cc) =
-                pack_bf16x2(acc[t][0] * il, acc[t][1] * il);
-          if (r_hi < Gh)
-            *reinterpret_cast<uint32_t *>(o_plane + r_hi * D + t * 8 + cc) =
-                pack_bf16x2(acc[t][2] * ih, acc[t][3] * ih);
-        }
+        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * D, acc, 0, cc, il);
+        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * D, acc, 2, cc, ih);
         if (lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -1054,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         m = st_m[h];
         l = st_l[h];
       };
-      merge_parts<D, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+      merge_parts<D, kFp8, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                               c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
                               32 * kMmaWarps, fin.vmul);
       if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
@@ -1168,7 +1210,7 @@ cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                         B, H_q, H_kv, max_len, scale, grid, err_word, k_scale,
                                         v_scale, stream);
   if (d == 128)
-    return launch_decode_d<128, 4, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
+    return launch_decode_d<128, 5, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
                                          B, H_q, H_kv, max_len, scale, grid, err_word, k_scale,
                                          v_scale, stream);
   return cudaErrorInvalidValue;

@@ -196,11 +196,22 @@ GQA_HD int varlen_kv_blocks(int len_q, int len_k, int causal, int qt) {
   return nb < n_kt ? nb : n_kt;
 }
 
+// Where the prefill kernels write O: strides in elements (batch, head, row;
+// for ragged batches `sn` is the token stride and `sb` unused) and the head
+// dim d, the columns stored (the kernel's D may pad it with zero columns).
+struct OutView {
+  long long sb, sh, sn;
+  int d;
+};
+
 // Launchers (return a cudaError_t; arguments already validated).
-// lse: optional per-row log-sum-exp output (null: not written).
+// lse: optional per-row log-sum-exp output (null: not written). For the
+// dense prefill tm_q, tm_k, tm_v are 4-D maps (column, row, head, batch)
+// with 64-column x 128-row boxes.
 cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                              const CUtensorMap &tm_v, void *o, float *lse, const PrefillPlan &plan,
-                              int d, float scale, int *ctl, int num_sms, cudaStream_t stream);
+                              const CUtensorMap &tm_v, void *o, const OutView &ov, float *lse,
+                              const PrefillPlan &plan, float scale, int *ctl, int num_sms,
+                              cudaStream_t stream);
 
 // The varlen plan kernel (one block) writes the unit list to `units` and its
 // length to ctl[kCtlVarlenUnits]; bad offsets set kErrBadSeqlen in
@@ -208,8 +219,8 @@ cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
 // q, k, v through THD tensor maps: [total][H][d] with 128-token boxes.
 cudaError_t launch_varlen_plan(const VarlenArgs &va, int4 *units, int *ctl, cudaStream_t stream);
 cudaError_t launch_prefill_tc_varlen(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                     const CUtensorMap &tm_v, void *o, float *lse,
-                                     const VarlenArgs &va, int d, float scale, int *ctl,
+                                     const CUtensorMap &tm_v, void *o, const OutView &ov,
+                                     float *lse, const VarlenArgs &va, float scale, int *ctl,
                                      int num_sms, cudaStream_t stream);
 
 cudaError_t launch_attn_f32(const float *q, const float *k, const float *v, float *o, int B,

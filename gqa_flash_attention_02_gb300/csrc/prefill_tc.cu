@@ -118,7 +118,8 @@ struct TcParams {
   __nv_bfloat16 *o;
   float *lse;     // per row natural-log sum of exp(scale q.k), or null: [B][H_q][N_q]
                   // (dense) or [H_q][total_q] (ragged batch)
-  int o_align32;  // o is 32-byte aligned (rows are then too: D * 2 bytes each)
+  int o_align32;  // every row of O starts on a 32-byte boundary (base and strides)
+  OutView ov;     // O's strides (elements) and the columns stored (the head dim)
   PrefillPlan plan;
   VarlenArgs va;  // ragged batches only
   float scale_log2;
@@ -214,12 +215,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
       for (int t = 0; t < 2; ++t)
         if (w.t[t].kv_blocks > 0)
           for (int p = 0; p < D / 64; ++p)
-            tma_prefetch_l2_3d(&tm_q, p * 64, w.t[t].q_tile * kTileM, w.b * plan.H_q + w.t[t].h_q);
+            tma_prefetch_l2_4d(&tm_q, p * 64, w.t[t].q_tile * kTileM, w.t[t].h_q, w.b);
       const int nb = min(2, max(w.t[0].kv_blocks, w.t[1].kv_blocks));
       for (int j = 0; j < nb; ++j)
         for (int p = 0; p < D / 64; ++p) {
-          tma_prefetch_l2_3d(&tm_k, p * 64, j * kTileN, w.b * plan.H_kv + w.h_kv);
-          tma_prefetch_l2_3d(&tm_v, p * 64, j * kTileN, w.b * plan.H_kv + w.h_kv);
+          tma_prefetch_l2_4d(&tm_k, p * 64, j * kTileN, w.h_kv, w.b);
+          tma_prefetch_l2_4d(&tm_v, p * 64, j * kTileN, w.h_kv, w.b);
         }
     }
   }
@@ -321,14 +322,13 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
             if constexpr (kVarlen)  // [total_q][H_q][d]: (column, head, token)
               tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64, tt.h_q,
                           q0 + tt.q_tile * kTileM);
-            else
-              tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64,
-                          tt.q_tile * kTileM, w.b * plan.H_q + tt.h_q);
+            else  // [B][H_q][N_q][d] with the caller's strides: (column, row, head, batch)
+              tma_load_4d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64,
+                          tt.q_tile * kTileM, tt.h_q, w.b);
           }
         }
         __syncwarp();
       }
-      const int kv_plane = w.b * plan.H_kv + w.h_kv;
       for (int j = 0; j < nb && ok; ++j) {
 #pragma unroll
         for (int kind = 0; kind < 2; ++kind) {  // K_j then V_j
@@ -346,8 +346,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
                 tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
                             p * 64, w.h_kv, k0 + j * kTileN);
               else
-                tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
-                            p * 64, j * kTileN, kv_plane);
+                tma_load_4d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
+                            p * 64, j * kTileN, w.h_kv, w.b);
             }
           }
           __syncwarp();
@@ -673,15 +673,18 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
       const float inv_l = 1.f / l_sum;
       // O row: [B][H_q][N_q][D] dense, [total_q][H_q][D] ragged (rows past
       // the sequence belong to the next one and are not stored)
-      size_t o_row, lse_at;
+      // (o_sn is the token stride for ragged batches, the row stride otherwise)
+      long long o_at;
+      size_t lse_at;
       if constexpr (kVarlen) {
-        o_row = static_cast<size_t>(q0 + q_row) * plan.H_q + h_q;
+        o_at = static_cast<long long>(q0 + q_row) * prm.ov.sn + static_cast<long long>(h_q) * prm.ov.sh;
         lse_at = static_cast<size_t>(h_q) * prm.va.total_q + q0 + q_row;
       } else {
-        o_row = (static_cast<size_t>(b) * plan.H_q + h_q) * plan.N_q + q_row;
-        lse_at = o_row;
+        o_at = static_cast<long long>(b) * prm.ov.sb + static_cast<long long>(h_q) * prm.ov.sh +
+               static_cast<long long>(q_row) * prm.ov.sn;
+        lse_at = (static_cast<size_t>(b) * plan.H_q + h_q) * plan.N_q + q_row;
       }
-      __nv_bfloat16 *dst = prm.o + o_row * D;
+      __nv_bfloat16 *dst = prm.o + o_at;
       const bool store = q_row < len_q;
       // log-sum-exp of the row in natural-log units: l is relative to
       // 2^m_ref with m_ref in log2 units of scale * q.k
@@ -703,7 +706,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
         for (int c = 0; c < 16; ++c)
           pk[c] = pack_bf16x2(__uint_as_float(ov[c0 + 2 * c]) * inv_l,
                               __uint_as_float(ov[c0 + 2 * c + 1]) * inv_l);
-        if (store) {
+        if (store && c0 < prm.ov.d) {  // columns past the head dim are padding
           // a lane writes its own row: whole 32-byte sectors when O allows
           if (prm.o_align32) {
             st_global_v8(dst + c0, pk);
@@ -763,8 +766,8 @@ constexpr auto prefill_entry() {
 
 template <int D, bool kLse, bool kVarlen>
 cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                     void *o, float *lse, const PrefillPlan &plan, const VarlenArgs &va, int grid,
-                     float scale, int *ctl, cudaStream_t stream) {
+                     void *o, const OutView &ov, float *lse, const PrefillPlan &plan,
+                     const VarlenArgs &va, int grid, float scale, int *ctl, cudaStream_t stream) {
   using L = TcLayout<D>;
   static unsigned configured = 0;  // one bit per device ordinal
   int dev = 0;
@@ -786,7 +789,11 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
   TcParams prm;
   prm.o = static_cast<__nv_bfloat16 *>(o);
   prm.lse = lse;
-  prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
+  prm.o_align32 = ((reinterpret_cast<uintptr_t>(o) | static_cast<uintptr_t>(ov.sb * 2) |
+                     static_cast<uintptr_t>(ov.sh * 2) | static_cast<uintptr_t>(ov.sn * 2)) & 31u) == 0
+                       ? 1
+                       : 0;
+  prm.ov = ov;
   prm.plan = plan;
   prm.va = va;
   // A zero scale (uniform weights over the visible keys) is taken as a
@@ -801,19 +808,25 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
                              stream, tm_q, tm_k, tm_v, prm);
 }
 
+// Head dims 32 and 64 run the D = 64 kernel, 96 and 128 the D = 128 one: the
+// TMA boxes are 64 columns wide and read zeros past the head dim, so the
+// extra columns of Q and K add nothing to S and those of V leave zero
+// columns in O, which the epilogue does not store.
 template <bool kVarlen>
 cudaError_t launch_any(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       void *o, float *lse, const PrefillPlan &plan, const VarlenArgs &va, int d,
-                       int grid, float scale, int *ctl, cudaStream_t stream) {
+                       void *o, const OutView &ov, float *lse, const PrefillPlan &plan,
+                       const VarlenArgs &va, int grid, float scale, int *ctl, cudaStream_t stream) {
   const bool with_lse = lse != nullptr;
-  if (d == 64)
-    return with_lse
-               ? launch_d<64, true, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream)
-               : launch_d<64, false, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream);
-  if (d == 128)
-    return with_lse
-               ? launch_d<128, true, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream)
-               : launch_d<128, false, kVarlen>(tm_q, tm_k, tm_v, o, lse, plan, va, grid, scale, ctl, stream);
+  if (ov.d == 32 || ov.d == 64)
+    return with_lse ? launch_d<64, true, kVarlen>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid,
+                                                  scale, ctl, stream)
+                    : launch_d<64, false, kVarlen>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid,
+                                                   scale, ctl, stream);
+  if (ov.d == 96 || ov.d == 128)
+    return with_lse ? launch_d<128, true, kVarlen>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid,
+                                                   scale, ctl, stream)
+                    : launch_d<128, false, kVarlen>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid,
+                                                    scale, ctl, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -963,11 +976,12 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenA
 }  // namespace
 
 cudaError_t launch_prefill_tc(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                              const CUtensorMap &tm_v, void *o, float *lse, const PrefillPlan &plan,
-                              int d, float scale, int *ctl, int num_sms, cudaStream_t stream) {
+                              const CUtensorMap &tm_v, void *o, const OutView &ov, float *lse,
+                              const PrefillPlan &plan, float scale, int *ctl, int num_sms,
+                              cudaStream_t stream) {
   const VarlenArgs none = {};
-  return launch_any<false>(tm_q, tm_k, tm_v, o, lse, plan, none, d, min(num_sms, plan.total_units),
-                           scale, ctl, stream);
+  return launch_any<false>(tm_q, tm_k, tm_v, o, ov, lse, plan, none,
+                           min(num_sms, plan.total_units), scale, ctl, stream);
 }
 
 cudaError_t launch_varlen_plan(const VarlenArgs &va, int4 *units, int *ctl, cudaStream_t stream) {
@@ -986,14 +1000,14 @@ cudaError_t launch_varlen_plan(const VarlenArgs &va, int4 *units, int *ctl, cuda
 }
 
 cudaError_t launch_prefill_tc_varlen(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                     const CUtensorMap &tm_v, void *o, float *lse,
-                                     const VarlenArgs &va, int d, float scale, int *ctl,
+                                     const CUtensorMap &tm_v, void *o, const OutView &ov,
+                                     float *lse, const VarlenArgs &va, float scale, int *ctl,
                                      int num_sms, cudaStream_t stream) {
   // the schedule fields the kernel reads; the unit count comes from the plan kernel
   PrefillPlan plan = make_prefill_plan(1, va.H_q, va.H_kv, 1, 1, va.causal);
   const long long most = varlen_max_units(va.B, va.H_q, va.H_kv, va.total_q);
   const int grid = static_cast<int>(most < num_sms ? (most < 1 ? 1 : most) : num_sms);
-  return launch_any<true>(tm_q, tm_k, tm_v, o, lse, plan, va, d, grid, scale, ctl, stream);
+  return launch_any<true>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid, scale, ctl, stream);
 }
 
 }  // namespace gqa

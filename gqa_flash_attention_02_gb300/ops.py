@@ -32,7 +32,7 @@ EXPORTED = [
     "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
     "gqa_attn_decode_noalloc", "gqa_attn_fwd_lse", "gqa_attn_decode_lse",
     "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse", "gqa_attn_fwd_bshd", "gqa_attn_bwd",
-    "gqa_attn_decode_fp8",
+    "gqa_attn_decode_fp8", "gqa_attn_fwd_strided",
 ]
 
 
@@ -91,6 +91,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.gqa_attn_bwd.restype = _i
             lib.gqa_attn_decode_fp8.argtypes = [_vp] * 8 + [_i] * 5 + [_f, _vp]
             lib.gqa_attn_decode_fp8.restype = _i
+            _ll = ctypes.c_longlong
+            lib.gqa_attn_fwd_strided.argtypes = ([_vp, _ll, _ll, _ll] * 4 + [_i] * 7 + [_f, _vp])
+            lib.gqa_attn_fwd_strided.restype = _i
             lib.gqa_attn_status_string.argtypes = [_i]
             lib.gqa_attn_status_string.restype = ctypes.c_char_p
             lib.gqa_attn_get_device_error.argtypes = [_vp]
@@ -171,6 +174,30 @@ def _fwd(name, dtype, q, k, v, o, causal, scale, stream, lse=None):
     rc = getattr(load(), name)(*args, B, H_q, H_kv, N_q, N_kv, d, int(bool(causal)),
                                float(scale), _stream(stream))
     _check(rc, name)
+    return o
+
+
+def gqa_attn_fwd_strided(q, k, v, o=None, causal=False, scale=None, stream=None):
+    """bf16 prefill on strided views: q, o [B,H_q,N_q,d] and k, v [B,H_kv,N_kv,d]
+    as torch views with any batch / head / row strides (the last dim contiguous),
+    e.g. slices of a fused QKV buffer. ``o`` defaults to a packed tensor."""
+    B, H_q, N_q, d = q.shape
+    _, H_kv, N_kv, _ = k.shape
+    if o is None:
+        o = torch.empty((B, H_q, N_q, d), dtype=q.dtype, device=q.device)
+    if scale is None:
+        scale = d ** -0.5
+    args = []
+    for name, t, shape in (("q", q, (B, H_q, N_q, d)), ("k", k, (B, H_kv, N_kv, d)),
+                           ("v", v, (B, H_kv, N_kv, d)), ("o", o, (B, H_q, N_q, d))):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+        if tuple(t.shape) != shape or t.stride(3) != 1:
+            raise ValueError(f"{name} must be {shape} with a contiguous last dim")
+        args += [ctypes.c_void_p(t.data_ptr()), t.stride(0), t.stride(1), t.stride(2)]
+    rc = load().gqa_attn_fwd_strided(*args, B, H_q, H_kv, N_q, N_kv, d, int(bool(causal)),
+                                     float(scale), _stream(stream))
+    _check(rc, "gqa_attn_fwd_strided")
     return o
 
 

@@ -55,7 +55,7 @@ typedef enum gqa_status {
     GQA_OK = 0,
     GQA_ERR_INVALID_ARG = 1,    /* dims <= 0, H_q % H_kv != 0, non-finite scale,
                                    null or misaligned pointer */
-    GQA_ERR_UNSUPPORTED = 2,    /* d not in {64, 128}; causal with N_q > N_kv;
+    GQA_ERR_UNSUPPORTED = 2,    /* head dim not supported by the call; causal with N_q > N_kv;
                                    a size beyond the documented limits */
     GQA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
     GQA_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out */
@@ -68,7 +68,9 @@ typedef enum gqa_status {
  * cores, TMEM accumulators, TMA-staged tiles, persistent tile scheduler).
  *   q : [B][H_q][N_q][d]  bf16      k, v : [B][H_kv][N_kv][d]  bf16
  *   o : [B][H_q][N_q][d]  bf16 (written)
- *   d in {64, 128}; 1 <= B*H_q*N_q*d < 2^31 elements per tensor.
+ *   d in {32, 64, 96, 128} (32 and 96 run the 64- and 128-column kernels on
+ *   tiles the TMA pads with zero columns); 1 <= B*H_q*N_q*d < 2^31 elements
+ *   per tensor.
  * Pages: BootstrapAI evolution log, collab-014 "Kernel 9 GQA" (semantics),
  * and the persistent-kernel entry (atomic work counter over tiles).
  */
@@ -91,6 +93,26 @@ int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float
                      int causal, float scale, cudaStream_t stream);
 
 /*
+ * gqa_attn_fwd on tensors with arbitrary batch, head and row strides, so a
+ * view needs no copy (for example q, k and v sliced out of a fused QKV
+ * projection's [B][N][H_q + 2 H_kv][d] output, or a [B][N][H][d] layout).
+ * Element (b, h, i, c) of q is at q + b*q_sb + h*q_sh + i*q_sn + c; the same
+ * for k, v (head index h_kv, row j) and o. Strides are in elements, the head
+ * dim is contiguous; every stride must be a positive multiple of 8 (16
+ * bytes, a rule of the TMA tensor maps) and each row stride at least d. o
+ * must not overlap q, k or v. d in {32, 64, 96, 128}; everything else as
+ * gqa_attn_fwd (which is this call with the packed strides).
+ * Pages: microLLM-rocm optimisation log, Experiments 202-206 (attention on
+ * the token-major BTHD layout without strided copies).
+ */
+int gqa_attn_fwd_strided(const void *q, long long q_sb, long long q_sh, long long q_sn,
+                         const void *k, long long k_sb, long long k_sh, long long k_sn,
+                         const void *v, long long v_sb, long long v_sh, long long v_sn,
+                         void *o, long long o_sb, long long o_sh, long long o_sn,
+                         int B, int H_q, int H_kv, int N_q, int N_kv, int d,
+                         int causal, float scale, cudaStream_t stream);
+
+/*
  * Ragged-batch ("varlen") prefill: B sequences of different lengths packed
  * token-major, one call. bf16 in / bf16 out, fp32 accumulation, same kernel
  * design as gqa_attn_fwd.
@@ -101,7 +123,7 @@ int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float
  *       and key tokens [cu_seqlens_k[b], cu_seqlens_k[b+1]).
  *   Causal alignment is bottom-right inside each sequence: its query row i
  *   sees its key j iff j <= i + (len_k - len_q).
- *   d in {64, 128}; 1 <= B <= 4096; each of total_q*H_q*d, total_k*H_kv*d
+ *   d in {32, 64, 96, 128}; 1 <= B <= 4096; each of total_q*H_q*d, total_k*H_kv*d
  *   below 2^31; at most 4096 blocks of 128 keys per sequence.
  * The offsets live on the device, so the library checks them there: a
  * sequence whose offsets are decreasing, outside [0, total], with keys

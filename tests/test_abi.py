@@ -100,7 +100,7 @@ def test_varlen_validation(fn):
     assert call(tq=-1) == 1
     assert call(H_q=8, H_kv=3) == 1
     assert call(scale=float("nan")) == 1
-    assert call(d=96) == 2
+    assert call(d=80) == 2   # head dims 32, 64, 96, 128 only
     assert call(B=4097) == 2                        # above the sequences-per-call limit
     assert call(tq=1 << 22, H_q=1 << 10, H_kv=1 << 8) == 2
     assert call(tq=0) == 0                          # no query rows: nothing launched
@@ -121,7 +121,7 @@ def test_bshd_validation():
     assert call(N_q=0) == 1
     assert call(H_q=6, H_kv=4) == 1
     assert call(causal=1, N_q=400, N_kv=300) == 2   # bottom-right mask undefined
-    assert call(d=32) == 2
+    assert call(d=48) == 2
     assert call(B=5000, N_q=10, N_kv=10) == 2       # above the sequences-per-call limit
 
 
@@ -234,3 +234,26 @@ def test_decode_fp8_validation():
     assert call(scale=float("nan")) == 1
     assert call(d=96) == 2
     assert call(max_len=(1 << 20) + 1) == 2
+
+
+def test_strided_validation():
+    f = ops.load().gqa_attn_fwd_strided
+    dims = dict(B=2, H_q=8, H_kv=2, N_q=300, N_kv=300, d=128, causal=1, scale=0.088)
+    # packed [B][H][N][d] strides
+    qs = (8 * 300 * 128, 300 * 128, 128)
+    ks = (2 * 300 * 128, 300 * 128, 128)
+
+    def call(q=A, k=A, v=A, o=A, q_st=qs, k_st=ks, v_st=ks, o_st=qs, **kw):
+        a = dict(dims, **kw)
+        return f(q, *q_st, k, *k_st, v, *v_st, o, *o_st, a["B"], a["H_q"], a["H_kv"], a["N_q"],
+                 a["N_kv"], a["d"], a["causal"], a["scale"], None)
+
+    assert call(q=None) == 1
+    assert call(o=MIS) == 1
+    assert call(q_st=(qs[0], qs[1], 100)) == 1       # row stride below d
+    assert call(k_st=(ks[0], 12, 128)) == 1           # head stride not a multiple of 8
+    assert call(v_st=(0, ks[1], 128)) == 1            # zero batch stride
+    assert call(o_st=(qs[0], qs[1], -128)) == 1       # negative row stride
+    assert call(d=80) == 2
+    assert call(causal=1, N_q=400, N_kv=300) == 2
+    assert call(H_q=6, H_kv=4) == 1
