@@ -188,6 +188,24 @@ bool encode_bf16_thd(CUtensorMap *map, const void *base, int d, long heads, long
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor viewed as [planes][rows][d] with a row and a plane stride
+// (elements; d contiguous); boxes of 64 columns x box_rows rows, 128-byte
+// swizzle, zero fill outside.
+bool encode_bf16_3d_strided(CUtensorMap *map, const void *base, int d, long rows, long planes,
+                            long long s_row, long long s_plane, int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(s_row) * 2, static_cast<cuuint64_t>(s_plane) * 2};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // bf16 tensor indexed [batch][head][row][d] with the given strides (elements;
 // d contiguous) for TMA as (column, row, head, batch): boxes of 64 columns x
 // box_rows rows, 128-byte swizzle, zero fill outside (so columns past d and
@@ -338,14 +356,26 @@ int fwd_dense(const void *q, long long q_sb, long long q_sh, long long q_sn, con
   Workspace *ws = nullptr;
   rc = get_workspace(stream, 0, &ws);
   if (rc != GQA_OK) return rc;
+  // When each batch's heads follow one another at the head stride (packed
+  // and row-padded layouts), the heads of all batches form one run of
+  // planes and 3-D maps serve (column, row, batch * H + head); other views
+  // take 4-D maps (column, row, head, batch).
+  const bool plane_uniform =
+      q_sb == q_sh * H_q && k_sb == k_sh * H_kv && v_sb == v_sh * H_kv;
   CUtensorMap tq, tk, tv;
-  if (!encode_bf16_4d(&tq, q, d, N_q, H_q, B, q_sn, q_sh, q_sb, kTileM) ||
-      !encode_bf16_4d(&tk, k, d, N_kv, H_kv, B, k_sn, k_sh, k_sb, kTileN) ||
-      !encode_bf16_4d(&tv, v, d, N_kv, H_kv, B, v_sn, v_sh, v_sb, kTileN))
-    return cuda_fail(cudaErrorInvalidValue);
+  bool enc_ok;
+  if (plane_uniform)
+    enc_ok = encode_bf16_3d_strided(&tq, q, d, N_q, static_cast<long>(B) * H_q, q_sn, q_sh, kTileM) &&
+             encode_bf16_3d_strided(&tk, k, d, N_kv, static_cast<long>(B) * H_kv, k_sn, k_sh, kTileN) &&
+             encode_bf16_3d_strided(&tv, v, d, N_kv, static_cast<long>(B) * H_kv, v_sn, v_sh, kTileN);
+  else
+    enc_ok = encode_bf16_4d(&tq, q, d, N_q, H_q, B, q_sn, q_sh, q_sb, kTileM) &&
+             encode_bf16_4d(&tk, k, d, N_kv, H_kv, B, k_sn, k_sh, k_sb, kTileN) &&
+             encode_bf16_4d(&tv, v, d, N_kv, H_kv, B, v_sn, v_sh, v_sb, kTileN);
+  if (!enc_ok) return cuda_fail(cudaErrorInvalidValue);
   int dev = 0;
   cudaGetDevice(&dev);
-  const OutView ov{o_sb, o_sh, o_sn, d};
+  const OutView ov{o_sb, o_sh, o_sn, d, plane_uniform ? 0 : 1};
   cudaError_t e = launch_prefill_tc(tq, tk, tv, o, ov, lse, plan, scale, ws->ctl, device_sms(dev),
                                     stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
@@ -421,7 +451,7 @@ int fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
   if (e != cudaSuccess) return cuda_fail(e);
   int dev = 0;
   cudaGetDevice(&dev);
-  const OutView ov{0, d, static_cast<long long>(H_q) * d, d};  // [total_q][H_q][d]
+  const OutView ov{0, d, static_cast<long long>(H_q) * d, d, 0};  // [total_q][H_q][d]
   e = launch_prefill_tc_varlen(tq, tk, tv, o, ov, lse, va, scale, ws->ctl, device_sms(dev), stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }

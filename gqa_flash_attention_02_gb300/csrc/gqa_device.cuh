@@ -403,6 +403,15 @@ __device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
   return y;
 }
 
+// lo_acc += low bf16 of `pair`, hi_acc += its high bf16, each by one
+// mixed-precision add (bf16 operand widened exactly, fp32 sum).
+__device__ __forceinline__ void add_bf16x2_to(float &lo_acc, float &hi_acc, uint32_t pair) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(lo_acc), "+f"(hi_acc)
+      : "r"(pair));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);

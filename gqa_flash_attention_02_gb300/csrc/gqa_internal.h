@@ -47,6 +47,9 @@ constexpr int kErrBadSeqlen = 1 << 1;
 
 constexpr int kTileM = 128;  // query rows per tile
 constexpr int kTileN = 128;  // key rows per K/V block
+// Dense prefill units hold one query tile instead of two when pairs would
+// number fewer than this (the SM count of a GB300).
+constexpr int kSingleTileUnitsBelow = 148;
 
 // ------------------------------------------------------------------------
 // Persistent prefill schedule.
@@ -67,7 +70,8 @@ struct PrefillPlan {
   int group;           // g
   int n_qt, n_kt;      // query tiles per head, key blocks per head
   int tiles_per_group; // g * n_qt
-  int pairs_per_group; // ceil(tiles_per_group / 2)
+  int tpu;             // query tiles per unit: 2, or 1 for problems too small to fill the GPU
+  int pairs_per_group; // units per group: ceil(tiles_per_group / tpu)
   int total_units;     // B * H_kv * pairs_per_group
   int kv_offset;       // N_kv - N_q (bottom-right causal alignment)
 };
@@ -88,7 +92,12 @@ GQA_HD PrefillPlan make_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv
   p.n_qt = (N_q + kTileM - 1) / kTileM;
   p.n_kt = (N_kv + kTileN - 1) / kTileN;
   p.tiles_per_group = p.group * p.n_qt;
-  p.pairs_per_group = (p.tiles_per_group + 1) / 2;
+  // Two tiles per unit share every K/V block load; but when pairing leaves
+  // fewer units than the GPU has SMs, single tiles run twice as many CTAs
+  // (each SM then works on one tile at full speed instead of idling).
+  const int pairs = (p.tiles_per_group + 1) / 2;
+  p.tpu = static_cast<long long>(B) * H_kv * pairs < kSingleTileUnitsBelow ? 1 : 2;
+  p.pairs_per_group = (p.tiles_per_group + p.tpu - 1) / p.tpu;
   p.total_units = B * H_kv * p.pairs_per_group;
   p.kv_offset = N_kv - N_q;
   return p;
@@ -113,8 +122,8 @@ GQA_HD Unit decode_unit(const PrefillPlan &p, int u) {
   w.h_kv = bh - w.b * p.H_kv;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
-    const int f = 2 * rank + s;
-    if (f < p.tiles_per_group) {
+    const int f = p.tpu * rank + s;
+    if (s < p.tpu && f < p.tiles_per_group) {
       const int qt = p.n_qt - 1 - f / p.group;
       w.t[s].h_q = w.h_kv * p.group + (f % p.group);
       w.t[s].q_tile = qt;
@@ -202,6 +211,7 @@ GQA_HD int varlen_kv_blocks(int len_q, int len_k, int causal, int qt) {
 struct OutView {
   long long sb, sh, sn;
   int d;
+  int tma4;  // dense prefill: q/k/v tensor maps are 4-D (column, row, head, batch)
 };
 
 // Launchers (return a cudaError_t; arguments already validated).

@@ -120,6 +120,8 @@ struct TcParams {
                   // (dense) or [H_q][total_q] (ragged batch)
   int o_align32;  // every row of O starts on a 32-byte boundary (base and strides)
   OutView ov;     // O's strides (elements) and the columns stored (the head dim)
+  int tma4;       // dense q/k/v maps are 4-D (column, row, head, batch); else 3-D
+                  // (column, row, batch * heads + head) for plane-uniform strides
   PrefillPlan plan;
   VarlenArgs va;  // ragged batches only
   float scale_log2;
@@ -215,12 +217,20 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
       for (int t = 0; t < 2; ++t)
         if (w.t[t].kv_blocks > 0)
           for (int p = 0; p < D / 64; ++p)
-            tma_prefetch_l2_4d(&tm_q, p * 64, w.t[t].q_tile * kTileM, w.t[t].h_q, w.b);
+            if (prm.tma4)
+              tma_prefetch_l2_4d(&tm_q, p * 64, w.t[t].q_tile * kTileM, w.t[t].h_q, w.b);
+            else
+              tma_prefetch_l2_3d(&tm_q, p * 64, w.t[t].q_tile * kTileM, w.b * plan.H_q + w.t[t].h_q);
       const int nb = min(2, max(w.t[0].kv_blocks, w.t[1].kv_blocks));
       for (int j = 0; j < nb; ++j)
         for (int p = 0; p < D / 64; ++p) {
-          tma_prefetch_l2_4d(&tm_k, p * 64, j * kTileN, w.h_kv, w.b);
-          tma_prefetch_l2_4d(&tm_v, p * 64, j * kTileN, w.h_kv, w.b);
+          if (prm.tma4) {
+            tma_prefetch_l2_4d(&tm_k, p * 64, j * kTileN, w.h_kv, w.b);
+            tma_prefetch_l2_4d(&tm_v, p * 64, j * kTileN, w.h_kv, w.b);
+          } else {
+            tma_prefetch_l2_3d(&tm_k, p * 64, j * kTileN, w.b * plan.H_kv + w.h_kv);
+            tma_prefetch_l2_3d(&tm_v, p * 64, j * kTileN, w.b * plan.H_kv + w.h_kv);
+          }
         }
     }
   }
@@ -322,9 +332,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
             if constexpr (kVarlen)  // [total_q][H_q][d]: (column, head, token)
               tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64, tt.h_q,
                           q0 + tt.q_tile * kTileM);
-            else  // [B][H_q][N_q][d] with the caller's strides: (column, row, head, batch)
+            else if (prm.tma4)  // [B][H_q][N_q][d] with the caller's strides: (column, row, head, batch)
               tma_load_4d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64,
                           tt.q_tile * kTileM, tt.h_q, w.b);
+            else  // (column, row, batch * H_q + head)
+              tma_load_3d(dst + p * L::kPanelBytes, &tm_q, bar(L::kQFull + t), p * 64,
+                          tt.q_tile * kTileM, w.b * plan.H_q + tt.h_q);
           }
         }
         __syncwarp();
@@ -345,9 +358,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
               if constexpr (kVarlen)  // [total_k][H_kv][d]: (column, head, token)
                 tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
                             p * 64, w.h_kv, k0 + j * kTileN);
-              else
+              else if (prm.tma4)
                 tma_load_4d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
                             p * 64, j * kTileN, w.h_kv, w.b);
+              else
+                tma_load_3d(dst + p * L::kPanelBytes, kind ? &tm_v : &tm_k, bar(L::kKVFull + st),
+                            p * 64, j * kTileN, w.b * plan.H_kv + w.h_kv);
             }
           }
           __syncwarp();
@@ -582,30 +598,36 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
         auto make_half = [&](int h, float m) -> float {
           const float2 sl2v = make_float2(sl2, sl2);
           const float2 negm = make_float2(-m, -m);
-          float2 lsum[4];  // four partial sums: no long dependency chain
+          // The row sum adds the very bf16 weights P.V uses (so O is an
+          // exact weighted average of V whatever their rounding): unpacked
+          // into fp32 pairs on the bf16-exponent path, widened inside
+          // mixed-precision adds on the fp32 one (each measured the faster
+          // there); eight partial sums keep the dependency chains short.
+          float lsum[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) lsum[i] = make_float2(0.f, 0.f);
+          for (int i = 0; i < 8; ++i) lsum[i] = 0.f;
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const float2 x = ffma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2v, negm);
-            float2 p;
             if constexpr (kEx2Bf16) {
               // two exponentials per special-function instruction, already
               // in P's bf16 pair format; the exponent is rounded to bf16
               pk[c] = ex2_bf16x2(pack_bf16x2(x.x, x.y));
-              p = make_float2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u));
             } else {
               pk[c] = pack_bf16x2(ex2(x.x), ex2(x.y));
-              // the row sum takes the same bf16-rounded weights P.V uses,
-              // so O is an exact weighted average of V whatever the rounding
-              p = make_float2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u));
             }
-            lsum[c & 3] = fadd2(lsum[c & 3], p);
+            if constexpr (kEx2Bf16) {
+              const float2 p = make_float2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u));
+              const float2 a = fadd2(make_float2(lsum[2 * (c & 3)], lsum[2 * (c & 3) + 1]), p);
+              lsum[2 * (c & 3)] = a.x;
+              lsum[2 * (c & 3) + 1] = a.y;
+            } else {
+              add_bf16x2_to(lsum[2 * (c & 3)], lsum[2 * (c & 3) + 1], pk[c]);
+            }
           }
           tmem_st32(tm_p + h * 32u, pk);
-          const float2 a = fadd2(lsum[0], lsum[1]), b = fadd2(lsum[2], lsum[3]);
-          return (a.x + b.x) + (a.y + b.y);
+          return ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) + ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
         };
         // row maximum of s * scale * log2e: the maximum of s for a
         // non-negative scale, its minimum for a negative one
@@ -794,6 +816,7 @@ cudaError_t launch_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUt
                        ? 1
                        : 0;
   prm.ov = ov;
+  prm.tma4 = ov.tma4;
   prm.plan = plan;
   prm.va = va;
   // A zero scale (uniform weights over the visible keys) is taken as a

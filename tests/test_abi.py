@@ -181,7 +181,23 @@ def test_prefill_plan_covers_each_tile_once_heavy_first(case):
     assert extents == sorted(extents, reverse=True), "units are not heavy-first"
     if g % 2 == 0:
         for (_, _, t0, t1) in units:
-            assert t0[1] == t1[1], "even groups pair tiles of the same q_tile"
+            if t1[2] > 0:
+                assert t0[1] == t1[1], "even groups pair tiles of the same q_tile"
+
+
+@pytest.mark.parametrize("case,tiles_per_unit", [
+    ((2, 8, 8, 1024, 1024, 0), 1),     # 64 pairs would leave most of 148 SMs idle
+    ((2, 8, 1, 1024, 1024, 1), 1),
+    ((1, 32, 8, 2048, 2048, 1), 2),    # the LLaMA-3-8B layer: 256 pairs
+    ((4, 16, 4, 4096, 4096, 1), 2),
+])
+def test_prefill_plan_splits_small_problems_into_single_tiles(case, tiles_per_unit):
+    units = ops.gqa_attn_prefill_plan(*case)
+    B, H_q, H_kv, N_q = case[:4]
+    n_tiles = B * H_q * -(-N_q // 128)
+    assert len(units) == -(-n_tiles // tiles_per_unit) if tiles_per_unit == 1 else len(units) >= n_tiles // 2
+    if tiles_per_unit == 1:
+        assert all(t1[2] == 0 for (_, _, _, t1) in units)
 
 
 def test_prefill_plan_rejects_bad_sizes():
