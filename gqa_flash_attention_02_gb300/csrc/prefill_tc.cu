@@ -257,10 +257,27 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
     // (written before this grid's dependency wait returned)
     int total_units = plan.total_units;
     if constexpr (kVarlen) total_units = __ldcg(prm.ctl + kCtlVarlenUnits);
+    // A CTA's first unit is unit blockIdx.x, taken without an atomic (the
+    // heaviest units go to the first CTAs); the counter hands out units
+    // grid, grid + 1, ... after that. Every CTA's last fetch fails, so the
+    // fetches number max(total, grid) + (successful ones) and the one that
+    // draws max(total, grid) - 1 is the grid's last: it re-arms the counter
+    // for the next launch (which reads it only after this grid completes).
+    const int grid = static_cast<int>(gridDim.x);
+    bool first = true;
     while (ok) {
       int u = 0;
-      if (lane == 0) u = atomicAdd(prm.ctl + kCtlWork, 1);
-      u = __shfl_sync(0xffffffffu, u, 0);
+      if (first && static_cast<int>(blockIdx.x) < total_units) {
+        u = static_cast<int>(blockIdx.x);
+      } else {
+        int c = 0;
+        if (lane == 0) {
+          c = atomicAdd(prm.ctl + kCtlWork, 1);
+          if (c == max(total_units, grid) - 1) atomicExch(prm.ctl + kCtlWork, 0);
+        }
+        u = grid + __shfl_sync(0xffffffffu, c, 0);
+      }
+      first = false;
       const int slot = it & 1;
       Unit w;
       int q0 = 0, len_q = 0, k0 = 0, len_k = 0;
@@ -750,15 +767,6 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
-  }
-  if (tid == 0) {
-    // The last CTA to finish re-arms the work counter for the next launch.
-    __threadfence();
-    const int done = atomicAdd(prm.ctl + kCtlDone, 1);
-    if (done == static_cast<int>(gridDim.x) - 1) {
-      atomicExch(prm.ctl + kCtlWork, 0);
-      atomicExch(prm.ctl + kCtlDone, 0);
-    }
   }
 }
 
