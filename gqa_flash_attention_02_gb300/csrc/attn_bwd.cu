@@ -22,13 +22,22 @@
 //       and every query tile that sees the block, so the GQA reduction
 //       happens in the tensor-memory accumulators, in a fixed order (no
 //       atomics: the result is deterministic). Per (head, tile) t, with the
-//       key rows as tensor-memory lanes:
-//         S^T = K Q_t^T, dP^T = V dO_t^T  (tcgen05, A and B from shared memory)
-//         P^T, dS^T  (8 warps, fp32, written back as bf16 over S^T and dP^T)
-//         dV += P^T dO_t, dK += dS^T Q_t  (tcgen05, A from tensor memory)
-//       Q_t, dO_t and the tile's lse / D arrive through a two-stage TMA ring.
+//       key rows as tensor-memory lanes, and per query half h of the tile:
+//         S^T_h = K Q_th^T, dP^T_h = V dO_th^T  (tcgen05, N = 64, A and B
+//                                               from shared memory)
+//         P^T_h, dS^T_h  (4 warps, fp32, written back as bf16 over S^T_h
+//                         and dP^T_h)
+//         dV += P^T_h dO_th, dK += dS^T_h Q_th  (tcgen05, K = 64, A from
+//                                                tensor memory)
+//       The two halves have their own barriers and warps, so the products
+//       of one half run while the softmax warps of the other half work;
+//       the K-steps reach dV and dK in the same order as one K = 128
+//       product would. Q_t, dO_t and the tile's lse / D arrive through a
+//       two-stage TMA ring.
 //     - dQ units (b, h_q, 128-row query tile), heaviest tiles first: Q and
-//       dO stay in shared memory, K/V blocks stream through a TMA ring:
+//       dO stay in shared memory, K/V blocks stream through two TMA rings
+//       (K blocks stay until their dQ product completes, V blocks only
+//       until their dP product does):
 //         S = Q K_j^T, dP = dO V_j^T; dS (8 warps); dQ += dS K_j.
 //       S and dP have their own tensor-memory columns apart from dS, so the
 //       next block's two products run while the softmax warps work on dS.
@@ -36,7 +45,8 @@
 //   dV [256, 256+D), dK [256+D, 256+2D); dQ units S [0,128), dP [128,256),
 //   dS [256,320), dQ [320, 320+D).
 //   Warps 0-7 compute P and dS (warps w and w+4 share the lanes of warp
-//   w % 4 and take one half of the 128 columns each) and store the results;
+//   w % 4 and take one half of the 128 columns each: in dK/dV units, one
+//   query half each) and store the results;
 //   warp 8 issues the TMA loads, warp 9 the tcgen05 products. Every wait is
 //   bounded: a stuck pipeline records kErrTimeout and unwinds.
 #include <cuda_runtime.h>
@@ -66,14 +76,19 @@ enum {
   kDrain,
   kRingFull0 = 8,
   kRingEmpty0 = 16,
-  kNumBars = 24
+  kSFull1 = 24,   // dK/dV units: S^T and dP^T of query half 1 complete
+  kDsFull1,       // dK/dV units: P^T and dS^T of query half 1 written
+  kNumBars
 };
 
 template <int D>
 struct BwdLayout {
   static constexpr int kTile = kTileM * D * 2;    // 128 rows x D bf16
   static constexpr int kPanel = 128 * 128;        // 128 rows x 64 columns
-  static constexpr int kRing = D == 128 ? 4 : 8;  // dQ units: K/V ring stages
+  // dQ units: K and V blocks in rings of their own; a K block is read until
+  // its dQ product completes, a V block only until its dP product does
+  static constexpr int kRingK = D == 128 ? 3 : 5, kRingV = D == 128 ? 2 : 3;
+  static constexpr int kRing = kRingK + kRingV;
   // dQ units: Q | dO | K/V ring
   static constexpr int kOffQ = 0, kOffDO = kTile, kOffRing = 2 * kTile;
   static constexpr int kEndQ = kOffRing + kRing * kTile;
@@ -164,8 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                const BwdParams prm) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // offset (not integer) arithmetic on smem_raw keeps the pointer in the
+  // shared window, so accesses through it compile to shared-memory loads
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t s_base = smem_addr(smem);
   auto bar = [&](int i) -> uint32_t { return s_base + L::kOffBar + 8u * static_cast<uint32_t>(i); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffTmem);
@@ -210,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kInFull), 1);
     mbar_init(bar(kSFull), 1);
     mbar_init(bar(kSFree), kSoftmaxWarps);
-    mbar_init(bar(kDsFull), kSoftmaxWarps);
+    mbar_init(bar(kDsFull), kv_unit ? kSoftmaxWarps / 2 : kSoftmaxWarps);
+    mbar_init(bar(kSFull1), 1);
+    mbar_init(bar(kDsFull1), kSoftmaxWarps / 2);
     mbar_init(bar(kDsFree), 1);
     mbar_init(bar(kAccFull), 1);
     mbar_init(bar(kDrain), 1);
@@ -259,20 +277,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(s_base + L::kOffDO + p * L::kPanel, &tm_do, bar(kInFull), p * 64,
                       qt * kTileM, plane_q);
         }
-        // K_j then V_j through the ring
-        for (int it = 0; it < 2 * n_iter && ok; ++it) {
-          const int st = it % L::kRing;
-          const uint32_t ph = (it / L::kRing) & 1;
-          if (!mbar_wait(bar(kRingEmpty0 + st), ph ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t dst = s_base + L::kOffRing + st * L::kTile;
-          mbar_arrive_expect_tx(bar(kRingFull0 + st), L::kTile);
+        // K_j and V_j, each through its own ring
+        for (int j = 0; j < n_iter && ok; ++j) {
 #pragma unroll
-          for (int p = 0; p < D / 64; ++p)
-            tma_load_3d(dst + p * L::kPanel, (it & 1) ? &tm_v : &tm_k, bar(kRingFull0 + st), p * 64,
-                        (it >> 1) * kTileN, plane_kv);
+          for (int kind = 0; kind < 2; ++kind) {
+            const int n = kind ? L::kRingV : L::kRingK;
+            const int slot = (kind ? L::kRingK : 0) + j % n;
+            if (!mbar_wait(bar(kRingEmpty0 + slot), ((j / n) & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = s_base + L::kOffRing + slot * L::kTile;
+            mbar_arrive_expect_tx(bar(kRingFull0 + slot), L::kTile);
+#pragma unroll
+            for (int p = 0; p < D / 64; ++p)
+              tma_load_3d(dst + p * L::kPanel, kind ? &tm_v : &tm_k, bar(kRingFull0 + slot), p * 64,
+                          j * kTileN, plane_kv);
+          }
         }
       } else {
         mbar_arrive_expect_tx(bar(kInFull), 2 * L::kTile);
@@ -352,20 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring_mn = sdesc_lo(s_base + L::kOffRing, L::kPanel);
       const uint32_t tS = tmem, tDP = tmem + 128, tDS = tmem + 256, tDQ = tmem + 320;
       ok = mbar_wait_warp(bar(kInFull), 0, abort_flag);
-      int it = 0, st_k_prev = 0;
+      int st_k_prev = 0;
       for (int j = 0; j < n_iter && ok; ++j) {
-        const int st_k = it % L::kRing;
-        if (!mbar_wait_warp(bar(kRingFull0 + st_k), (it / L::kRing) & 1, abort_flag)) {
+        const int st_k = j % L::kRingK, st_v = L::kRingK + j % L::kRingV;
+        if (!mbar_wait_warp(bar(kRingFull0 + st_k), (j / L::kRingK) & 1, abort_flag) ||
+            !mbar_wait_warp(bar(kRingFull0 + st_v), (j / L::kRingV) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        ++it;
-        const int st_v = it % L::kRing;
-        if (!mbar_wait_warp(bar(kRingFull0 + st_v), (it / L::kRing) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        ++it;
         // S and dP of the previous block have been read by the softmax warps
         if (j > 0 && !mbar_wait_warp(bar(kSFree), (j - 1) & 1, abort_flag)) {
           ok = false;
@@ -405,27 +420,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k_lo = sdesc_lo(s_base + L::kOffK, 16);
       const uint32_t v_lo = sdesc_lo(s_base + L::kOffV, 16);
       const uint32_t tST = tmem, tDPT = tmem + 128, tDV = tmem + 256, tDK = tmem + 256 + D;
+      constexpr uint32_t idesc_half = idesc_bf16_f32(128, 64, false, false);
+      // S^T and dP^T of query half h of stage st: N = 64, B rows [64h, 64h+64)
+      auto issue_s = [&](int st, int h) {
+        const uint32_t stq = s_base + L::kOffStage + st * 2 * L::kTile + h * 64 * 128;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off =
+                static_cast<uint32_t>(((kk >> 2) * L::kPanel + (kk & 3) * 32) >> 4);
+            mma_ss_w(tST + 64u * h, k_lo + off, kHi, sdesc_lo(stq, 16) + off, kHi, idesc_half,
+                     kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off =
+                static_cast<uint32_t>(((kk >> 2) * L::kPanel + (kk & 3) * 32) >> 4);
+            mma_ss_w(tDPT + 64u * h, v_lo + off, kHi, sdesc_lo(stq + L::kTile, 16) + off, kHi,
+                     idesc_half, kk > 0 ? 1u : 0u);
+          }
+        }
+        __syncwarp();
+        commit(h ? kSFull1 : kSFull);
+      };
+      // dV += P^T dO and dK += dS^T Q over query half h (K = 64): P^T and
+      // dS^T sit in the first 32 columns of that half's S^T and dP^T
+      auto issue_acc = [&](int st, int h, bool acc) {
+        const uint32_t stq = s_base + L::kOffStage + st * 2 * L::kTile;
+        const uint32_t do_mn = sdesc_lo(stq + L::kTile, L::kPanel);
+        const uint32_t q_mn = sdesc_lo(stq, L::kPanel);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_w(tDV, tST + 64u * h + 8u * kk, do_mn + 128u * (4 * h + kk), kHi, idesc_acc,
+                     (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts_w(tDK, tDPT + 64u * h + 8u * kk, q_mn + 128u * (4 * h + kk), kHi, idesc_acc,
+                     (acc || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+      };
       ok = mbar_wait_warp(bar(kInFull), 0, abort_flag);
+      if (ok && n_iter > 0) {
+        ok = mbar_wait_warp(bar(kRingFull0), 0, abort_flag);
+        if (ok) {
+          tc_fence_after_sync();
+          issue_s(0, 0);
+          issue_s(0, 1);
+        }
+      }
+      // the halves alternate so that one half's products run while the
+      // softmax warps of the other half work
       for (int t = 0; t < n_iter && ok; ++t) {
         const int st = t & 1;
-        if (!mbar_wait_warp(bar(kRingFull0 + st), (t >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!mbar_wait_warp(bar(h ? kDsFull1 : kDsFull), t & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_acc(st, h, t > 0 || h > 0);
+          if (h == 1) commit(kRingEmpty0 + st);  // Q_t, dO_t and the vectors are free
+          if (t + 1 < n_iter) {
+            if (h == 0) {
+              if (!mbar_wait_warp(bar(kRingFull0 + (st ^ 1)), ((t + 1) >> 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+            }
+            issue_s(st ^ 1, h);
+          }
         }
-        tc_fence_after_sync();
-        const uint32_t stq = s_base + L::kOffStage + st * 2 * L::kTile;  // Q_t, then dO_t
-        mma_ss(tST, k_lo, sdesc_lo(stq, 16));
-        mma_ss(tDPT, v_lo, sdesc_lo(stq + L::kTile, 16));
-        commit(kSFull);
-        if (!mbar_wait_warp(bar(kDsFull), t & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // P^T sits in S^T's columns [0,32) and [64,96), dS^T in dP^T's
-        mma_ts(tDV, tST, tST + 64, sdesc_lo(stq + L::kTile, L::kPanel), t > 0);
-        mma_ts(tDK, tDPT, tDPT + 64, sdesc_lo(stq, L::kPanel), t > 0);
-        commit(kRingEmpty0 + st);  // Q_t, dO_t and the vectors are free
       }
       if (ok) commit(kAccFull);
     }
@@ -524,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 *vec = reinterpret_cast<const float4 *>(smem + L::kOffVec);
       for (int t = 0; t < n_iter; ++t) {
         const int st = t & 1, qtt = qt_first + t % ntq;
-        if (!mbar_wait_warp(bar(kSFull), t & 1, abort_flag)) {
+        if (!mbar_wait_warp(bar(half ? kSFull1 : kSFull), t & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -560,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tmem + lane_off + 128u + half * 64u, dpk);
         tmem_st_wait();
         tc_fence_before_sync();
-        arrive(kDsFull);
+        arrive(half ? kDsFull1 : kDsFull);
       }
       if (ok) {
         if (!mbar_wait_warp(bar(kAccFull), 0, abort_flag)) {

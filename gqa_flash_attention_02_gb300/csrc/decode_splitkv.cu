@@ -381,8 +381,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   constexpr int kPer = kHeads * kQuads / (32 * kMmaWarps);  // merge items per MMA thread
   constexpr int kEpPer = kHeads * kQuads / 32;              // merge items per epilogue lane
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // offset (not integer) arithmetic on smem_raw keeps the pointer in the
+  // shared window, so accesses through it compile to shared-memory loads
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t s_base = smem_addr(smem);
   const uint32_t full = s_base + L::kOffBar;
   const uint32_t empty = full + 8 * NSTG;

@@ -159,8 +159,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   // about 0.1 % of (warp, key block) steps after the first block.
   constexpr float kRescaleThreshold = kEx2Bf16 ? 4.0f : 8.0f;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // offset (not integer) arithmetic on smem_raw keeps the pointer in the
+  // shared window, so accesses through it compile to shared-memory loads
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t s_base = smem_addr(smem);
   const uint32_t bars = s_base + L::kOffBar;
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
