@@ -14,8 +14,10 @@
 //   dV_j  =       sum_{h_q of the group} sum_i P_ij dO_i
 //
 // Two launches:
-//   * bwd_prep_kernel: D_i and lse_i in log2 units into a workspace padded
-//     to whole 128-row tiles (pad rows: D = 0, lse = +inf, so P = 0 there).
+//   * bwd_prep_kernel: -D_i and -lse_i in log2 units into a workspace
+//     padded to whole 128-row tiles (pad rows: 0 and -inf, so P = 0 there);
+//     negated so that x = s scale log2(e) - lse and dP - D are single
+//     packed fp32 operations.
 //   * bwd_kernel: one grid with two kinds of CTA, one work unit each.
 //     - dK/dV units (b, h_kv, 128-key block), first: K and V of the block
 //       stay in shared memory; the CTA sweeps every query head of the group
@@ -51,6 +53,8 @@
 //   bounded: a stuck pipeline records kErrTimeout and unwinds.
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "gqa_device.cuh"
 #include "gqa_internal.h"
@@ -107,8 +111,8 @@ struct BwdLayout {
 
 struct BwdParams {
   __nv_bfloat16 *dq, *dk, *dv;
-  const float *lse2;   // [B*H_q][nq_pad]: lse in log2 units, +inf on pad rows
-  const float *delta;  // [B*H_q][nq_pad]: D_i, 0 on pad rows
+  const float *lse2;   // [B*H_q][nq_pad]: -lse in log2 units, -inf on pad rows
+  const float *delta;  // [B*H_q][nq_pad]: -D_i, 0 on pad rows
   int B, H_q, H_kv, N_q, N_kv, group, n_qt, n_kt, nq_pad, causal, kv_offset;
   int n_kv_units;      // blocks [0, n_kv_units) are dK/dV units, the rest dQ units
   float scale, scale_log2;
@@ -129,7 +133,7 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
   return s;
 }
 
-// D_i = sum_c dO_ic O_ic and lse_i * log2(e), for every row of the padded
+// -D_i = -sum_c dO_ic O_ic and -lse_i * log2(e), for every row of the padded
 // [B*H_q][nq_pad] layout; 8 lanes per row, each over D/8 contiguous columns.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *o,
@@ -161,12 +165,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *o,
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 4);
     if (sub == 0 && r < total) {
-      float l2 = INFINITY;  // pad rows (and a row with no visible key): P = 0
+      float l2 = -INFINITY;  // pad rows (and a row with no visible key): P = 0
       if (valid) {
         const float l = __ldg(lse + static_cast<size_t>(bh) * N_q + i);
-        if (l != -INFINITY) l2 = l * 1.4426950408889634f;
+        if (l != -INFINITY) l2 = l * -1.4426950408889634f;
       }
-      delta[r] = valid ? acc : 0.f;
+      delta[r] = valid ? -acc : 0.f;
       lse2[r] = l2;
     }
   }
@@ -535,7 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // thread = query row i; columns = keys
       const int i = qt * kTileM + row;
       const size_t vrow = static_cast<size_t>(b * prm.H_q + h_q) * prm.nq_pad + i;
-      const float lse2_i = __ldg(prm.lse2 + vrow), delta_i = __ldg(prm.delta + vrow);
+      // -lse_i log2(e) and -D_i, as pairs for the packed fp32 operations
+      const float nl2 = __ldg(prm.lse2 + vrow), nd = __ldg(prm.delta + vrow);
+      const float2 nl2v = make_float2(nl2, nl2), ndv = make_float2(nd, nd);
+      const float2 sl2v = make_float2(sl2, sl2);
       int lim = prm.N_kv - 1;  // last visible key (bottom-right causal)
       if (prm.causal) lim = min(lim, i + prm.kv_offset);
       for (int j = 0; j < n_iter; ++j) {
@@ -550,19 +557,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before_sync();
         arrive(kSFree);
         const int kbase = j * kTileN + half * 64;
-        const bool edge = __any_sync(0xffffffffu, kbase + 63 > lim);
+        // columns c > cut of this half are past the last visible key
+        const int cut = lim - kbase;
         uint32_t pk[32];
+        // dS for the 64 columns; kMasked only on blocks that reach past a
+        // row's last visible key (a warp-uniform choice, so the common
+        // blocks carry no per-element compare)
+        auto make_ds = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), sl2, -lse2_i));
-          float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -lse2_i));
-          if (edge) {
-            p0 = kbase + 2 * c > lim ? 0.f : p0;
-            p1 = kbase + 2 * c + 1 > lim ? 0.f : p1;
+          for (int c = 0; c < 32; ++c) {
+            float2 p = ffma2(make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])),
+                             sl2v, nl2v);
+            p.x = ex2(p.x);
+            p.y = ex2(p.y);
+            if constexpr (kMasked) {
+              p.x = 2 * c > cut ? 0.f : p.x;
+              p.y = 2 * c + 1 > cut ? 0.f : p.y;
+            }
+            const float2 ds = fmul2(
+                p, fadd2(make_float2(__uint_as_float(pv[2 * c]), __uint_as_float(pv[2 * c + 1])), ndv));
+            pk[c] = pack_bf16x2(ds.x, ds.y);
           }
-          pk[c] = pack_bf16x2(p0 * (__uint_as_float(pv[2 * c]) - delta_i),
-                              p1 * (__uint_as_float(pv[2 * c + 1]) - delta_i));
-        }
+        };
+        if (__any_sync(0xffffffffu, cut < 63))
+          make_ds(std::true_type{});
+        else
+          make_ds(std::false_type{});
         // dS's columns are free once the previous block's dQ product completed
         if (j > 0 && !mbar_wait_warp(bar(kDsFree), (j - 1) & 1, abort_flag)) {
           ok = false;
@@ -601,27 +622,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld64_wait(tmem + lane_off + 128u + half * 64u, pv);
         const float4 *lse2v = vec + st * 64 + half * 16;  // this half's 64 rows
         const float4 *dltv = lse2v + 32;
-        const int ibase = qtt * kTileM + half * 64;
-        // key j is visible to query row i iff j <= i + kv_offset
-        const bool edge = prm.causal && __any_sync(0xffffffffu, j > ibase + prm.kv_offset);
+        // key j is visible to query row i iff j <= i + kv_offset: here the
+        // columns c < cut are not
+        const int cut = j - (qtt * kTileM + half * 64) - prm.kv_offset;
         uint32_t ppk[32], dpk[32];
+        // P^T and dS^T for the 64 columns; kMasked only on tiles that cross
+        // the causal diagonal (a warp-uniform choice, so the common tiles
+        // carry no per-element compare)
+        auto make_p_ds = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const float4 l4 = lse2v[c4], d4 = dltv[c4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], ds[4];
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l4 = lse2v[c4], d4 = dltv[c4];  // -lse log2(e) and -D
+            float2 p[2], ds[2];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            p[e] = ex2(fmaf(__uint_as_float(sv[c]), sl2, -lv[e]));
-            if (edge && j > ibase + c + prm.kv_offset) p[e] = 0.f;
-            ds[e] = p[e] * (__uint_as_float(pv[c]) - dv[e]);
+            for (int e = 0; e < 2; ++e) {
+              const int c = 4 * c4 + 2 * e;
+              p[e] = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                           make_float2(sl2, sl2), e ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+              p[e].x = ex2(p[e].x);
+              p[e].y = ex2(p[e].y);
+              if constexpr (kMasked) {
+                p[e].x = c < cut ? 0.f : p[e].x;
+                p[e].y = c + 1 < cut ? 0.f : p[e].y;
+              }
+              ds[e] = fmul2(p[e], fadd2(make_float2(__uint_as_float(pv[c]), __uint_as_float(pv[c + 1])),
+                                        e ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y)));
+            }
+            ppk[2 * c4] = pack_bf16x2(p[0].x, p[0].y);
+            ppk[2 * c4 + 1] = pack_bf16x2(p[1].x, p[1].y);
+            dpk[2 * c4] = pack_bf16x2(ds[0].x, ds[0].y);
+            dpk[2 * c4 + 1] = pack_bf16x2(ds[1].x, ds[1].y);
           }
-          ppk[2 * c4] = pack_bf16x2(p[0], p[1]);
-          ppk[2 * c4 + 1] = pack_bf16x2(p[2], p[3]);
-          dpk[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-          dpk[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
+        };
+        if (prm.causal && __any_sync(0xffffffffu, cut > 0))
+          make_p_ds(std::true_type{});
+        else
+          make_p_ds(std::false_type{});
         // P^T over S^T and dS^T over dP^T, in this half's own columns
         tmem_st32(tmem + lane_off + half * 64u, ppk);
         tmem_st32(tmem + lane_off + 128u + half * 64u, dpk);
