@@ -333,7 +333,7 @@ namespace {
 // Dense prefill with the caller's strides (elements; d contiguous): the
 // tensor maps are 4-D (column, row, head, batch), so any batch and head
 // strides work, e.g. slices of a fused QKV buffer.
-bool d_supported_tc(int d) { return d == 32 || d == 64 || d == 96 || d == 128; }
+bool d_supported_tc(int d) { return d == 32 || d == 64 || d == 96 || d == 128 || d == 256; }
 
 bool strides_ok(long long sb, long long sh, long long sn, int d) {
   // TMA wants 16-byte multiples; rows must not overlap within a head
@@ -352,7 +352,7 @@ int fwd_dense(const void *q, long long q_sb, long long q_sh, long long q_sn, con
   if (!strides_ok(q_sb, q_sh, q_sn, d) || !strides_ok(k_sb, k_sh, k_sn, d) ||
       !strides_ok(v_sb, v_sh, v_sn, d) || !strides_ok(o_sb, o_sh, o_sn, d))
     return GQA_ERR_INVALID_ARG;
-  const PrefillPlan plan = make_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal);
+  const PrefillPlan plan = make_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal, d == 256);
   Workspace *ws = nullptr;
   rc = get_workspace(stream, 0, &ws);
   if (rc != GQA_OK) return rc;

@@ -85,7 +85,10 @@ struct Unit {
   UnitTile t[2];
 };
 
-GQA_HD PrefillPlan make_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv, int causal) {
+// single_tiles: one tile per unit whatever the size (head dim 256, where one
+// tile's S and O fill the tensor memory).
+GQA_HD PrefillPlan make_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv, int causal,
+                                     int single_tiles = 0) {
   PrefillPlan p;
   p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_kv = N_kv; p.causal = causal ? 1 : 0;
   p.group = H_q / H_kv;
@@ -96,7 +99,7 @@ GQA_HD PrefillPlan make_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv
   // fewer units than the GPU has SMs, single tiles run twice as many CTAs
   // (each SM then works on one tile at full speed instead of idling).
   const int pairs = (p.tiles_per_group + 1) / 2;
-  p.tpu = static_cast<long long>(B) * H_kv * pairs < kSingleTileUnitsBelow ? 1 : 2;
+  p.tpu = (single_tiles || static_cast<long long>(B) * H_kv * pairs < kSingleTileUnitsBelow) ? 1 : 2;
   p.pairs_per_group = (p.tiles_per_group + p.tpu - 1) / p.tpu;
   p.total_units = B * H_kv * p.pairs_per_group;
   p.kv_offset = N_kv - N_q;

@@ -76,9 +76,13 @@ template <int D>
 struct TcLayout {
   static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
   static constexpr int kPanelBytes = 128 * 128;   // 128 rows x 64 columns
-  static constexpr int kStages = (D == 128) ? 5 : 8;  // K or V tiles in the ring
+  // At D = 256 a tile's S and O fill the 512 tensor-memory columns, so a
+  // unit is one query tile, and one Q tile and two K/V tiles fill the
+  // shared memory.
+  static constexpr int kQTiles = D == 256 ? 1 : 2;
+  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 5 : 8);  // K or V tiles in the ring
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffKV = kQTiles * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   // barrier indices
   // P arrives in two halves: kPFull for keys 0-63 of a block, kPFullB for 64-127
@@ -94,6 +98,7 @@ struct TcLayout {
   static constexpr int kOffDesc = (kOffAbort + 4 + 15) / 16 * 16;
   static constexpr int kBytes = kOffDesc + 2 * kDescInts * 4;
   static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
 // Extreme of a 128-column score row in eight independent chains of
@@ -729,33 +734,39 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
       // log-sum-exp of the row in natural-log units: l is relative to
       // 2^m_ref with m_ref in log2 units of scale * q.k
       if (kLse && store) prm.lse[lse_at] = (m_ref + log2f(l_sum)) * 0.6931471805599453f;
-      // the whole row of O in one tensor-memory load; O_t is then free for
-      // the next unit's PV while the row is converted and stored
-      uint32_t ov[D];
-      __syncwarp();
-      if constexpr (D == 128)
-        tmem_ld128_wait(tm_o, ov);
-      else
-        tmem_ld64_wait(tm_o, ov);
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kOEmpty + t));
+      // The row of O in tensor-memory loads of up to 128 columns; O_t is
+      // free for the next unit's PV once the last has completed
+      constexpr int kChunk = D > 128 ? 128 : D;
+#pragma unroll 1
+      for (int cb = 0; cb < D; cb += kChunk) {
+        uint32_t ov[kChunk];
+        __syncwarp();
+        if constexpr (kChunk == 128)
+          tmem_ld128_wait(tm_o + cb, ov);
+        else
+          tmem_ld64_wait(tm_o + cb, ov);
+        if (cb + kChunk == D) {
+          tc_fence_before_sync();
+          mbar_arrive(bar(L::kOEmpty + t));
+        }
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t pk[16];
+        for (int c0 = 0; c0 < kChunk; c0 += 32) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[c] = pack_bf16x2(__uint_as_float(ov[c0 + 2 * c]) * inv_l,
-                              __uint_as_float(ov[c0 + 2 * c + 1]) * inv_l);
-        if (store && c0 < prm.ov.d) {  // columns past the head dim are padding
-          // a lane writes its own row: whole 32-byte sectors when O allows
-          if (prm.o_align32) {
-            st_global_v8(dst + c0, pk);
-            st_global_v8(dst + c0 + 16, pk + 8);
-          } else {
-            uint4 *g = reinterpret_cast<uint4 *>(dst + c0);
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(ov[c0 + 2 * c]) * inv_l,
+                                __uint_as_float(ov[c0 + 2 * c + 1]) * inv_l);
+          if (store && cb + c0 < prm.ov.d) {  // columns past the head dim are padding
+            // a lane writes its own row: whole 32-byte sectors when O allows
+            if (prm.o_align32) {
+              st_global_v8(dst + cb + c0, pk);
+              st_global_v8(dst + cb + c0 + 16, pk + 8);
+            } else {
+              uint4 *g = reinterpret_cast<uint4 *>(dst + cb + c0);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              g[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+              for (int v4 = 0; v4 < 4; ++v4)
+                g[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
           }
         }
       }
@@ -859,6 +870,13 @@ cudaError_t launch_any(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
                                                    scale, ctl, stream)
                     : launch_d<128, false, kVarlen>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid,
                                                     scale, ctl, stream);
+  if constexpr (!kVarlen) {
+    if (ov.d == 256)  // one query tile per unit (the plan says so)
+      return with_lse ? launch_d<256, true, false>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid,
+                                                   scale, ctl, stream)
+                      : launch_d<256, false, false>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid,
+                                                    scale, ctl, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -68,9 +68,10 @@ typedef enum gqa_status {
  * cores, TMEM accumulators, TMA-staged tiles, persistent tile scheduler).
  *   q : [B][H_q][N_q][d]  bf16      k, v : [B][H_kv][N_kv][d]  bf16
  *   o : [B][H_q][N_q][d]  bf16 (written)
- *   d in {32, 64, 96, 128} (32 and 96 run the 64- and 128-column kernels on
- *   tiles the TMA pads with zero columns); 1 <= B*H_q*N_q*d < 2^31 elements
- *   per tensor.
+ *   d in {32, 64, 96, 128, 256} (32 and 96 run the 64- and 128-column
+ *   kernels on tiles the TMA pads with zero columns; at 256 one query
+ *   tile's S and O fill the tensor memory, so each CTA works on one tile
+ *   at a time); 1 <= B*H_q*N_q*d < 2^31 elements per tensor.
  * Pages: BootstrapAI evolution log, collab-014 "Kernel 9 GQA" (semantics),
  * and the persistent-kernel entry (atomic work counter over tiles).
  */
@@ -100,8 +101,8 @@ int gqa_attn_fwd_lse(const void *q, const void *k, const void *v, void *o, float
  * for k, v (head index h_kv, row j) and o. Strides are in elements, the head
  * dim is contiguous; every stride must be a positive multiple of 8 (16
  * bytes, a rule of the TMA tensor maps) and each row stride at least d. o
- * must not overlap q, k or v. d in {32, 64, 96, 128}; everything else as
- * gqa_attn_fwd (which is this call with the packed strides).
+ * must not overlap q, k or v. d in {32, 64, 96, 128, 256}; everything else
+ * as gqa_attn_fwd (which is this call with the packed strides).
  * Pages: microLLM-rocm optimisation log, Experiments 202-206 (attention on
  * the token-major BTHD layout without strided copies).
  */
@@ -338,6 +339,7 @@ int gqa_attn_get_device_error(cudaStream_t stream);
  * one CTA processes against one K/V stream. Units are handed out by an
  * atomic counter in index order; units with more visible key blocks come
  * first (heavy-first causal order).
+ * This is the plan for head dims up to 128 (at 256 every unit is one tile).
  * Returns the number of units, or -1 for invalid sizes. When `unit` is in
  * range, writes out[0..7] = {b, h_kv, h_q0, q_tile0, kv_blocks0,
  * h_q1, q_tile1, kv_blocks1}; the second tile has kv_blocks1 == 0 (and

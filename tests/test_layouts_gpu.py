@@ -8,6 +8,9 @@ token-major layout without strided copies).
   gqa_attn_fwd on packed copies (the same units, the same arithmetic).
 * Head dims 32 and 96 (zero-padded tiles of the 64- and 128-column kernels)
   through the dense, lse, ragged-batch and token-major entry points.
+* Head dim 256 (one query tile per CTA: its S and O fill the tensor memory)
+  through the dense, lse and strided entry points, with ragged tile tails,
+  more keys than queries, and MHA / GQA / MQA groupings.
 Bounds: the bf16 ones of the other tests (max abs 2e-2, mean abs 2e-3; lse
 max abs 5e-3).
 """
@@ -121,3 +124,41 @@ def test_head_dims_32_96_ragged_and_token_major(d):
     torch.cuda.synchronize()
     ref, _ = oracle.prefill(q, k, v, False, d ** -0.5, n_threads=THREADS)
     _check(ob.transpose(1, 2).float().cpu().numpy(), ref, f"token-major d {d}")
+
+
+@pytest.mark.parametrize("shape", [(2, 8, 2, 300, 300, True), (1, 4, 4, 200, 520, True),
+                                   (2, 6, 1, 129, 129, False), (1, 16, 4, 640, 640, True)],
+                         ids=lambda s: "-".join(map(str, s)))
+def test_head_dim_256_dense_and_lse(shape):
+    B, H_q, H_kv, N_q, N_kv, causal = shape
+    d = 256
+    q, k, v = inputs.prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, torch.bfloat16, seed=650 + N_q)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_fwd(qd, kd, vd, o, causal=causal, scale=d ** -0.5)
+    o2, lse = ops.gqa_attn_fwd_lse(qd, kd, vd, causal=causal, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, ref_lse = oracle.prefill(q, k, v, causal, d ** -0.5, n_threads=THREADS)
+    _check(o.float().cpu().numpy(), ref, f"d 256 {shape}")
+    _check(o2.float().cpu().numpy(), ref, f"d 256 {shape} lse kernel")
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max() <= LSE_MAX
+
+
+def test_head_dim_256_strided_fused_qkv():
+    B, H_q, H_kv, N, d = 2, 4, 2, 200, 256
+    Ht = H_q + 2 * H_kv
+    g = torch.Generator("cpu").manual_seed(660)
+    buf = torch.randn(B, N, Ht, d, generator=g).to(torch.bfloat16).cuda()
+    q = buf[:, :, :H_q].transpose(1, 2)
+    k = buf[:, :, H_q:H_q + H_kv].transpose(1, 2)
+    v = buf[:, :, H_q + H_kv:].transpose(1, 2)
+    o_tok = torch.full((B, N, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ops.gqa_attn_fwd_strided(q, k, v, o_tok.transpose(1, 2), causal=True, scale=d ** -0.5)
+    packed = ops.gqa_attn_fwd(q.contiguous(), k.contiguous(), v.contiguous(), causal=True,
+                              scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    assert torch.equal(o_tok.transpose(1, 2), packed), "strided and packed calls differ"
+    ref, _ = oracle.prefill(q.cpu(), k.cpu(), v.cpu(), True, d ** -0.5, n_threads=THREADS)
+    _check(packed.float().cpu().numpy(), ref, "d 256 fused QKV")

@@ -79,7 +79,7 @@ def _varlen_lse(q, k, v, cu_q, cu_k, causal, scale):
 # ------------------------------------------------------------------ rising logits
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_rising_logits_prefill(d, causal):
     """Every row's maximum jumps at every key block (5 blocks)."""
     N = 640
@@ -111,7 +111,7 @@ def test_rising_logits_varlen(d):
 # ------------------------------------------------------------------ a dominant late key
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_dominant_late_key_prefill(d, causal):
     """Key 990 of 1000 (the last of 8 blocks) dominates every row that sees it."""
     N, key = 1000, 990
