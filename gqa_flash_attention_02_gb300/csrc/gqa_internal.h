@@ -39,6 +39,28 @@ cudaError_t launch_programmatic(void (*kernel)(KArgs...), int grid, int block, s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// The same in thread-block clusters of `cluster` consecutive CTAs (grid a
+// multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic_cluster(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                                        int cluster, cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 #endif
 
 // Bits of the device error word kept in each workspace.
@@ -104,6 +126,13 @@ GQA_HD PrefillPlan make_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv
   p.total_units = B * H_kv * p.pairs_per_group;
   p.kv_offset = N_kv - N_q;
   return p;
+}
+
+// CTAs per cluster of the dense prefill: g / 2 when units pair the tiles of
+// a group of 4 or 8 query heads (head dims up to 128; ranks c*m .. c*m+c-1
+// are then the g tiles of one q_tile), else 1.
+GQA_HD int cluster_size_for(const PrefillPlan &p, int d) {
+  return (p.tpu == 2 && d <= 128 && (p.group == 4 || p.group == 8)) ? p.group / 2 : 1;
 }
 
 // Number of key blocks query tile `qt` must visit.
