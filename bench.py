@@ -250,14 +250,31 @@ def roofline_obj(bound, achieved, peak, unit, peak_src, kernel, traffic=None):
             "traffic": traffic}
 
 
-def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
+def prefill_cluster_size(torch, ops, shape):
+    """CTAs per cluster the dense prefill uses for `shape` (for naming the
+    kernel instantiation): g / 2 for two-tile units of a 4- or 8-head group
+    from four units per SM up, else 1."""
+    units = ops.gqa_attn_prefill_plan(shape.B, shape.H_q, shape.H_kv, shape.N_q, shape.N_kv,
+                                      shape.causal)
+    g = shape.H_q // shape.H_kv
+    pairs = any(u[3][2] > 0 for u in units)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if pairs and g in (4, 8) and shape.d <= 128 and len(units) >= 4 * sms:
+        return g // 2
+    return 1
+
+
+def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src, only=None):
     """Per-workload throughput beside the headline step: the MHA/GQA/MQA sweep
     (six variants), the long-sequence case and decode at B = 1, 8, 64. Each
     is the median over 21 repetitions of a graph of back-to-back calls over
-    rotating input copies."""
+    rotating input copies. ``only``: the groups to run (sweep, long, backward,
+    decode, decode_fp8), all when None."""
     out = {}
+    want = lambda group: only is None or group in only
 
     def prefill_block(shape):
+        cluster = prefill_cluster_size(torch, ops, shape)
         q, k, v = inputs.prefill_inputs_for(shape)
         nbytes = (q.numel() + k.numel() + v.numel()) * 2
         copies = copies_for(nbytes)
@@ -281,12 +298,22 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
                 "calls_per_rep": chain, "reps": 21, "l2": f"{copies} rotating copies",
                 "roofline": roofline_obj("tensor", ach, tc_peak, "TFLOP/s",
                                          f"{peak_src} bf16_tflops (burst)",
-                                         f"prefill_tc_kernel<{shape.d}, 0>")}
+                                         f"prefill_tc_kernel<{shape.d}, 0, {cluster}>")}
 
-    for shape in inputs.sweep_shapes():
+    for shape in inputs.sweep_shapes() if want("sweep") else []:
         out[shape.name] = prefill_block(shape)
-    out[inputs.LONG_SEQ.name] = prefill_block(inputs.LONG_SEQ)
+    if want("long"):
+        out[inputs.LONG_SEQ.name] = prefill_block(inputs.LONG_SEQ)
+    if want("backward"):
+        backward_block(torch, ops, inputs, dev, stream, tc_peak, peak_src, out)
+    if want("decode"):
+        decode_blocks(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out)
+    if want("decode_fp8"):
+        decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out)
+    return out
 
+
+def backward_block(torch, ops, inputs, dev, stream, tc_peak, peak_src, out):
     # attention backward on the prefill layer: algorithmic FLOPs are the five
     # products of the standard backward (S, dP, dV, dK, dQ: 2.5 x the
     # forward's), halved for causal; the kernel's recomputed S and dP in the
@@ -326,6 +353,8 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
     del bufs, grads, qd, kd, vd, o, lse
     torch.cuda.empty_cache()
 
+
+def decode_blocks(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
     for shape in inputs.decode_shapes():
         sl, q, kc, vc = inputs.decode_inputs_for(shape)
         in_bytes = (q.numel() + kc.numel() + vc.numel()) * 2
@@ -350,10 +379,12 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
             "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
             "l2": f"{copies} rotating copies",
             "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                     "decode_kernel<128,5>")}
+                                     "decode_kernel<128,5,0>")}
         del bufs, o
         torch.cuda.empty_cache()
 
+
+def decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
     # decode against the fp8 cache: bytes actually read (one byte per cached
     # value, K and V once per K/V head, plus q, o and seqlens)
     shape = inputs.decode_shapes()[-1]
@@ -382,10 +413,9 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src):
         "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
         "l2": f"{copies} rotating copies",
         "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                 "decode_kernel<128,4,1> (fp8 cache)")}
+                                 "decode_kernel<128,5,1> (fp8 cache)")}
     del bufs, o
     torch.cuda.empty_cache()
-    return out
 
 
 def run_ours(args):
@@ -513,8 +543,9 @@ def run_ours(args):
             dist.barrier()
         wall = time.perf_counter() - t0
         var_ms, var_chain = time_calls(torch, call_var, var_copies, cap, min_chain_us=2000.0)
+        only = set(args.configs.split(",")) if args.configs else None
         blocks = None if args.no_configs else config_blocks(
-            torch, ops, inputs, dev, cap, tc_peak, hbm_peak, peak_src)
+            torch, ops, inputs, dev, cap, tc_peak, hbm_peak, peak_src, only)
     tot_pre = statistics.median(e[0].elapsed_time(e[1]) for e in ev)   # ms for K calls
     tot_dec = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     gpu_err = ops.gqa_attn_get_device_error(stream=cap)  # the graphs' error word
@@ -601,18 +632,18 @@ def run_ours(args):
         "repetitions": reps,
         "roofline": roofline_obj(
             "tensor", pre_ach, tc_peak, "TFLOP/s", f"{peak_src} bf16_tflops (burst)",
-            "prefill_tc_kernel<128, 0> (no lse output)",
+            "prefill_tc_kernel<128, 0, 1> (no lse output, no clusters)",
             recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
-                             "prefill_tc_kernel<128, 0>")),
+                             "prefill_tc_kernel<128, 0, 1>")),
         "decode": {
             "value": round(dec_gbs, 2),
             "unit": "GB/s",
             "ms": round(dec_ms, 6),
             "roofline": roofline_obj(
                 "hbm", dec_ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                "decode_kernel<128,5> (persistent split-KV + in-kernel merge)",
+                "decode_kernel<128,5,0> (persistent split-KV + in-kernel merge)",
                 recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
-                                 "decode_kernel<128,5>")),
+                                 "decode_kernel<128,5,0>")),
             "e2e": {"value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},
         },
@@ -756,6 +787,9 @@ def main(argv=None):
                     help="repetitions of the K-step region (default: at least 21, about 1 s)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload blocks after the step (profiling runs)")
+    ap.add_argument("--configs", default="",
+                    help="comma-separated groups of per-workload blocks to run (sweep, long, "
+                         "backward, decode, decode_fp8; profiling runs); default all")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
