@@ -298,7 +298,9 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src, 
                 "calls_per_rep": chain, "reps": 21, "l2": f"{copies} rotating copies",
                 "roofline": roofline_obj("tensor", ach, tc_peak, "TFLOP/s",
                                          f"{peak_src} bf16_tflops (burst)",
-                                         f"prefill_tc_kernel<{shape.d}, 0, {cluster}>")}
+                                         f"prefill_tc_kernel<{shape.d}, 0, {cluster}>",
+                                         recorded_traffic("gqa_flash_attention_02_gb300/csrc/prefill_tc.cu",
+                                                          f"prefill_tc_kernel<{shape.d}, 0, {cluster}> {shape.name}"))}
 
     for shape in inputs.sweep_shapes() if want("sweep") else []:
         out[shape.name] = prefill_block(shape)
@@ -413,7 +415,9 @@ def decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
         "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
         "l2": f"{copies} rotating copies",
         "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                 "decode_kernel<128,5,1> (fp8 cache)")}
+                                 "decode_kernel<128,5,1> (fp8 cache)",
+                                 recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
+                                                  "decode_kernel<128,5,1>"))}
     del bufs, o
     torch.cuda.empty_cache()
 
