@@ -168,6 +168,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   // the fp32 path takes 2^8. On iid N(0,1) inputs either bound is crossed in
   // about 0.1 % of (warp, key block) steps after the first block.
   constexpr float kRescaleThreshold = kEx2Bf16 ? 4.0f : 8.0f;
+  constexpr float kRescaleBound = kEx2Bf16 ? 16.0f : 256.0f;  // 2^threshold
   extern __shared__ uint8_t smem_raw[];
   // offset (not integer) arithmetic on smem_raw keeps the pointer in the
   // shared window, so accesses through it compile to shared-memory loads
@@ -754,7 +755,15 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
           // do not wait for the block maximum.
 #pragma unroll
           for (int h = 0; h < kEarly; ++h) sum += make_half(h, m_ref);
-          const float m_blk = row_max();
+          // When the whole block's weights are in `sum` (P handed over in one
+          // piece), each weight is at most their sum: if no row's sum
+          // exceeds 2^threshold, no row's block maximum exceeds the
+          // reference by more than the threshold, and the maximum need not
+          // be computed (measured 160.5 -> 152.5 us on the d = 64 long
+          // sequence, 13.0 -> 12.5 us on the sweep). Otherwise, and when P
+          // goes in halves, the maximum decides.
+          const bool maybe = kSplitP || __any_sync(0xffffffffu, sum > kRescaleBound);
+          const float m_blk = maybe ? row_max() : m_ref;
           const bool raise = m_blk > m_ref + kRescaleThreshold;
           if (__any_sync(0xffffffffu, raise)) {
             // rare: some row's maximum jumped; redo this warp's early halves
