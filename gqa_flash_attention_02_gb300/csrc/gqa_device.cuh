@@ -483,14 +483,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 2^x for a bf16 pair (ex2.approx on bf16x2: one special-function
-// instruction for both; flush-to-zero).
-__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
-  uint32_t y;
-  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-
 // lo_acc += low bf16 of `pair`, hi_acc += its high bf16, each by one
 // mixed-precision add (bf16 operand widened exactly, fp32 sum).
 __device__ __forceinline__ void add_bf16x2_to(float &lo_acc, float &hi_acc, uint32_t pair) {

@@ -150,25 +150,17 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   // the first 64 keys overlaps the exponentials of the other 64; at D = 64
   // the PV is short and the extra hand-over costs more than it hides.
   constexpr bool kSplitP = D == 128;
-  // At D = 128 the softmax bounds the block rate and P's exponentials run
-  // two per special-function instruction on bf16 pairs (the exponent rounded
-  // to bf16: the error against the float64 oracle grows from about 1.2e-4 to
-  // 1.7e-4 mean and 7.7e-3 to 9.3e-3 max, well inside the bf16 bounds); at
-  // D = 64 that measured slower, so fp32 ex2 stays. The log-sum-exp
-  // instantiation keeps fp32 exponentials at both sizes: O's normalisation
-  // absorbs the rounded exponent input (O is the exact softmax of scores
-  // perturbed by at most 2^-9 |x|), but the row sum itself, hence the lse,
-  // would carry that perturbation (measured up to 1e-2 at 16x query scale).
-  constexpr bool kEx2Bf16 = D == 128 && !kLse;
+  // P's exponentials are fp32 (ex2) at every head dim. (Two per
+  // special-function instruction on bf16 pairs, with the exponent input
+  // rounded to bf16, measured no faster at D = 128 -- the special-function
+  // pipe takes twice as long per pair instruction -- and less accurate.)
   // The running (reference) maximum is only raised, and O rescaled, when a
   // row's maximum grows past it by more than this many log2 units; until
-  // then exponents up to this bound are allowed. The bf16 exponent input
-  // has an absolute rounding error of up to 2^-9 |x|, so there the bound is
-  // 2^4 (the error of the largest terms stays that of an exponent near 0);
-  // the fp32 path takes 2^8. On iid N(0,1) inputs either bound is crossed in
-  // about 0.1 % of (warp, key block) steps after the first block.
-  constexpr float kRescaleThreshold = kEx2Bf16 ? 4.0f : 8.0f;
-  constexpr float kRescaleBound = kEx2Bf16 ? 16.0f : 256.0f;  // 2^threshold
+  // then exponents up to this bound are allowed (weights up to 2^8, exact
+  // enough in fp32 and in P's bf16). On iid N(0,1) inputs the bound is
+  // crossed in about 0.1 % of (warp, key block) steps after the first block.
+  constexpr float kRescaleThreshold = 8.0f;
+  constexpr float kRescaleBound = 256.0f;  // 2^threshold
   extern __shared__ uint8_t smem_raw[];
   // offset (not integer) arithmetic on smem_raw keeps the pointer in the
   // shared window, so accesses through it compile to shared-memory loads
@@ -705,10 +697,9 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
           const float2 sl2v = make_float2(sl2, sl2);
           const float2 negm = make_float2(-m, -m);
           // The row sum adds the very bf16 weights P.V uses (so O is an
-          // exact weighted average of V whatever their rounding): unpacked
-          // into fp32 pairs on the bf16-exponent path, widened inside
-          // mixed-precision adds on the fp32 one (each measured the faster
-          // there); eight partial sums keep the dependency chains short.
+          // exact weighted average of V whatever their rounding), widened
+          // inside mixed-precision adds; eight partial sums keep the
+          // dependency chains short.
           float lsum[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) lsum[i] = 0.f;
@@ -716,21 +707,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const float2 x = ffma2(make_float2(s[h * 64 + 2 * c], s[h * 64 + 2 * c + 1]), sl2v, negm);
-            if constexpr (kEx2Bf16) {
-              // two exponentials per special-function instruction, already
-              // in P's bf16 pair format; the exponent is rounded to bf16
-              pk[c] = ex2_bf16x2(pack_bf16x2(x.x, x.y));
-            } else {
-              pk[c] = pack_bf16x2(ex2(x.x), ex2(x.y));
-            }
-            if constexpr (kEx2Bf16) {
-              const float2 p = make_float2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u));
-              const float2 a = fadd2(make_float2(lsum[2 * (c & 3)], lsum[2 * (c & 3) + 1]), p);
-              lsum[2 * (c & 3)] = a.x;
-              lsum[2 * (c & 3) + 1] = a.y;
-            } else {
-              add_bf16x2_to(lsum[2 * (c & 3)], lsum[2 * (c & 3) + 1], pk[c]);
-            }
+            pk[c] = pack_bf16x2(ex2(x.x), ex2(x.y));
+            add_bf16x2_to(lsum[2 * (c & 3)], lsum[2 * (c & 3) + 1], pk[c]);
           }
           tmem_st32(tm_p + h * 32u, pk);
           return ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) + ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));

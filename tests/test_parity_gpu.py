@@ -293,22 +293,19 @@ def test_bf16_decode_deterministic():
 
 # ------------------------------------------------------------------ log-sum-exp output
 
-# The lse kernels sum fp32 exponentials of fp32 scores (the plain d = 128
-# prefill rounds the exponent input to bf16, the lse instantiation does
-# not), so the lse error is fp32 rounding of the scores and the sum; the
-# bound 5e-3 (natural-log units) also covers a sum of bf16-rounded weights
-# (up to 2^-8 relative error each).
+# The lse kernels sum fp32 exponentials of fp32 scores, so the lse error is
+# fp32 rounding of the scores and the sum; the bound 5e-3 (natural-log
+# units) also covers a sum of bf16-rounded weights (up to 2^-8 relative
+# error each).
 LSE_MAX = 5e-3
 
 
 def _plain_o_matches(o, o_plain, d, ref, what):
-    """The plain entry point's O: the same bits at d = 64 (the same
-    arithmetic), within the bf16 bounds of the oracle at d = 128 (the plain
-    kernel rounds the exponent input to bf16, the lse kernel does not)."""
-    if d == 64:
-        assert torch.equal(o, o_plain), what
-    else:
-        _check_bf16(o_plain.float().cpu().numpy(), ref, what)
+    """The plain entry point's O: the same bits as the lse kernel's (the same
+    arithmetic; the lse instantiation only adds the lse store), and within
+    the bf16 bounds of the oracle."""
+    assert torch.equal(o, o_plain), what
+    _check_bf16(o_plain.float().cpu().numpy(), ref, what)
 
 
 @pytest.mark.parametrize("d,causal,N", [(128, True, 640), (64, False, 384), (64, True, 1000)])

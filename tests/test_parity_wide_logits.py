@@ -3,10 +3,9 @@ online softmax (BootstrapAI evolution log, collab-005 "Kernel 2 tiling").
 
 The tensor-core prefill keeps a reference maximum per row and raises it
 (rescaling O in tensor memory) only when a later key block's maximum exceeds
-it by more than a threshold: 2^4 where the exponent is rounded to bf16
-(d = 128), 2^8 where it stays fp32 (d = 64). On iid N(0,1) inputs at scale
-1/sqrt(d) that almost never happens after the first block, so these cases
-build inputs where it must:
+it by more than a threshold of 2^8 (log2 units). On iid N(0,1) inputs at
+scale 1/sqrt(d) that almost never happens after the first block, so these
+cases build inputs where it must:
 
   * rising logits: q[..., 0] = 8 and k[..., j, 0] = 0.1 j, so every row's
     score grows by 0.8 per key; times scale * log2(e) that is more than 10
@@ -16,8 +15,8 @@ build inputs where it must:
     or 64 against q[..., 0] >= 2, so its score leads the others' by tens of
     natural-log units): the rows that see it raise their maximum at that
     block;
-  * q scaled by 4, 8 and 16: scores whose spread stresses the bf16-rounded
-    exponent (its absolute error grows with the exponent's size);
+  * q scaled by 4, 8 and 16: wide score spreads, where the bf16 rounding of
+    the weights and the lag of the reference maximum weigh most;
   * a zero scale (uniform weights) and a negative one.
 
 Everything is compared element by element with the float64 oracle at the
