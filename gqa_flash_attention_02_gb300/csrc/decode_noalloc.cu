@@ -70,7 +70,7 @@ extern "C" int gqa_attn_decode_noalloc(const void *q, const void *k_cache, const
   if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_len <= 0 || d <= 0 || H_q % H_kv != 0)
     return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128) return GQA_ERR_UNSUPPORTED;
   if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
   if (max_len > (1 << 20) ||
       static_cast<long long>(B) * H_kv * max_len * d > (1ll << 31) - 1)

@@ -183,6 +183,8 @@ struct DecodeParams {
   int *err_word;
   const float *k_scale, *v_scale;  // fp8 cache: per K/V head dequantisation scales
   int B, H_q, H_kv, max_len, nhg;  // nhg = query-head groups of 16 per K/V head
+  int od;          // the head dim: O's row stride and the columns stored (<= D; the TMA
+                   // boxes read zeros past it, as for the prefill's padded head dims)
   float scale_log2;
 };
 
@@ -255,7 +257,7 @@ __device__ __forceinline__ void merge_row(float &m, float &l, float m2, float l2
 template <int D, bool kFp8, int kItems, int kBatch, typename SelfFn>
 __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int jself, SelfFn self,
                                             int Gh, __nv_bfloat16 *o_plane, float *lse_plane,
-                                            int t, int nt, float v_mul) {
+                                            int t, int nt, float v_mul, int od) {
   constexpr int kQuads = D / 4;
   constexpr int kSlot = kHeads * (D + 2);
   const int items = Gh * kQuads;
@@ -313,14 +315,15 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
           // fragment columns 4q4 .. 4q4+3 are columns 4(q4 % 2) .. +3 of
           // n-tile q4 / 2, i.e. dims 16 (t / 2) + (t % 2) + 2 n (see write_o_row)
           const int t = q4 >> 1, base = 16 * (t >> 1) + (t & 1) + 8 * (q4 & 1);
-          __nv_bfloat16 *row = o_plane + h * D + base;
+          __nv_bfloat16 *row = o_plane + h * od + base;
           row[0] = __float2bfloat16_rn(Ar[k].x * il);
           row[2] = __float2bfloat16_rn(Ar[k].y * il);
           row[4] = __float2bfloat16_rn(Ar[k].z * il);
           row[6] = __float2bfloat16_rn(Ar[k].w * il);
         } else {
-          *reinterpret_cast<uint2 *>(o_plane + h * D + 4 * q4) =
-              make_uint2(pack_bf16x2(Ar[k].x * il, Ar[k].y * il), pack_bf16x2(Ar[k].z * il, Ar[k].w * il));
+          if (4 * q4 < od)  // columns past the head dim are padding
+            *reinterpret_cast<uint2 *>(o_plane + h * od + 4 * q4) =
+                make_uint2(pack_bf16x2(Ar[k].x * il, Ar[k].y * il), pack_bf16x2(Ar[k].z * il, Ar[k].w * il));
         }
         // the head's log-sum-exp (M, L are in log2 units of scale * q.k)
         if (lse_plane != nullptr && q4 == 0) lse_plane[h] = (Mr[k] + log2f(Lr[k])) * 0.6931471805599453f;
@@ -336,7 +339,7 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
 // them in), so the lane's four values are dims 16ch + 2cc .. 16ch + 2cc + 3.
 template <int D, bool kFp8>
 __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)[D / 8][4], int e0,
-                                            int cc, float il) {
+                                            int cc, float il, int od) {
   if constexpr (kFp8) {
 #pragma unroll
     for (int ch = 0; ch < D / 16; ++ch)
@@ -346,7 +349,8 @@ __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)
   } else {
 #pragma unroll
     for (int t = 0; t < D / 8; ++t)
-      *reinterpret_cast<uint32_t *>(dst + t * 8 + cc) = pack_bf16x2(A[t][e0] * il, A[t][e0 + 1] * il);
+      if (t * 8 < od)  // columns past the head dim are padding
+        *reinterpret_cast<uint32_t *>(dst + t * 8 + cc) = pack_bf16x2(A[t][e0] * il, A[t][e0 + 1] * il);
   }
 }
 
@@ -513,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // written by CTA b % G
     for (int b = c; b < prm.B; b += G) {
       if (units_for<kSub>(prm, seq_len(prm, s_len, b)) != 0) continue;
-      uint4 *ob = reinterpret_cast<uint4 *>(prm.o + static_cast<size_t>(b) * prm.H_q * D);
-      for (int idx = tid; idx < prm.H_q * D / 8; idx += 32 * kMmaWarps) ob[idx] = make_uint4(0, 0, 0, 0);
+      uint4 *ob = reinterpret_cast<uint4 *>(prm.o + static_cast<size_t>(b) * prm.H_q * prm.od);
+      for (int idx = tid; idx < prm.H_q * prm.od / 8; idx += 32 * kMmaWarps) ob[idx] = make_uint4(0, 0, 0, 0);
       if (prm.lse != nullptr)
         for (int h = tid; h < prm.H_q; h += 32 * kMmaWarps) prm.lse[static_cast<size_t>(b) * prm.H_q + h] = -INFINITY;
     }
@@ -626,14 +630,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
       l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
       l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-      __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D;
+      __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * prm.od;
       float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
       if (!split) {
         // the run is the whole plane: write O / l
         const float vm = kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * D, A, 0, cc, il);
-        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * D, A, 2, cc, ih);
+        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * prm.od, A, 0, cc, il, prm.od);
+        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * prm.od, A, 2, cc, ih, prm.od);
         if (lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -682,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         };
         merge_parts<D, kFp8, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32,
-                             kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f);
+                             kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f, prm.od);
         if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
       }
       __syncwarp();  // every lane is done with the state buffer
@@ -988,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mma_warps_sync();
     if (warp == 1) put(0);
     mma_warps_sync();
-    __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * D;
+    __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * prm.od;
     float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
     // a split run's merged state stays behind the tree slots in the stage
     float *state = tree + L::kTreeBytes / 4;
@@ -1005,8 +1009,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // this run is the whole plane: write O / l
         const float vm = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * D, acc, 0, cc, il);
-        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * D, acc, 2, cc, ih);
+        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * prm.od, acc, 0, cc, il, prm.od);
+        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * prm.od, acc, 2, cc, ih, prm.od);
         if (lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -1099,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       };
       merge_parts<D, kFp8, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                               c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
-                              32 * kMmaWarps, fin.vmul);
+                              32 * kMmaWarps, fin.vmul, prm.od);
       if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
     }
   }
@@ -1115,7 +1119,7 @@ template <int D, int NSTG, bool kFp8>
 cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                             float *lse, float *partials, int *counters, int B, int H_q, int H_kv,
-                            int max_len, float scale, int grid, int *err_word,
+                            int max_len, int od, float scale, int grid, int *err_word,
                             const float *k_scale, const float *v_scale, cudaStream_t stream) {
   using L = DecodeSmem<D, NSTG, kFp8>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory");
@@ -1144,6 +1148,7 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   prm.H_kv = H_kv;
   prm.max_len = max_len;
   prm.nhg = decode_head_groups(H_q, H_kv);
+  prm.od = od;
   prm.scale_log2 = scale * 1.4426950408889634f;
   return launch_programmatic(decode_kernel<D, NSTG, kFp8>, grid, kThreads, L::kAlloc, stream, tm_q,
                              tm_k, tm_v, prm);
@@ -1155,7 +1160,8 @@ int decode_head_groups(int H_q, int H_kv) { return (H_q / H_kv + kHeads - 1) / k
 
 size_t decode_partials_bytes(int B, int H_q, int H_kv, int d, int grid) {
   const size_t planes = static_cast<size_t>(B) * H_kv * decode_head_groups(H_q, H_kv);
-  return (static_cast<size_t>(grid) + planes) * kHeads * (static_cast<size_t>(d) + 2) * sizeof(float);
+  const size_t D = d <= 64 ? 64 : 128;  // the kernel's head dim (32 and 96 are padded)
+  return (static_cast<size_t>(grid) + planes) * kHeads * (D + 2) * sizeof(float);
 }
 
 size_t decode_planes(int B, int H_q, int H_kv) {
@@ -1189,13 +1195,14 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                int H_kv, int max_len, int d, float scale, int grid,
                                int *err_word, cudaStream_t stream) {
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
-  if (d == 64)
+  // head dims 32 and 96 run the 64- and 128-column kernels on zero-padded boxes
+  if (d == 32 || d == 64)
     return launch_decode_d<64, 8, false>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                         B, H_q, H_kv, max_len, scale, grid, err_word, nullptr,
+                                         B, H_q, H_kv, max_len, d, scale, grid, err_word, nullptr,
                                          nullptr, stream);
-  if (d == 128)
+  if (d == 96 || d == 128)
     return launch_decode_d<128, 5, false>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                          B, H_q, H_kv, max_len, scale, grid, err_word, nullptr,
+                                          B, H_q, H_kv, max_len, d, scale, grid, err_word, nullptr,
                                           nullptr, stream);
   return cudaErrorInvalidValue;
 }
@@ -1208,11 +1215,11 @@ cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
   if (d == 64)
     return launch_decode_d<64, 8, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                        B, H_q, H_kv, max_len, scale, grid, err_word, k_scale,
+                                        B, H_q, H_kv, max_len, 64, scale, grid, err_word, k_scale,
                                         v_scale, stream);
   if (d == 128)
     return launch_decode_d<128, 5, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                         B, H_q, H_kv, max_len, scale, grid, err_word, k_scale,
+                                         B, H_q, H_kv, max_len, 128, scale, grid, err_word, k_scale,
                                          v_scale, stream);
   return cudaErrorInvalidValue;
 }

@@ -186,8 +186,9 @@ int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o,
  *             length 0 yields O = 0. Out-of-range values make the call
  *             record GQA_ERR_BAD_SEQLEN (read with gqa_attn_get_device_error)
  *             and leave that sequence's output at 0.
- *   d in {64, 128}; max_len <= 1 << 20; at most 2^30 row units
- *   (B * H_kv * ceil(H_q / H_kv / 16) * ceil(max_len / 64)), else
+ *   d in {32, 64, 96, 128} (32 and 96 run the 64- and 128-column kernels on
+ *   tiles the TMA pads with zero columns); max_len <= 1 << 20; at most 2^30
+ *   row units (B * H_kv * ceil(H_q / H_kv / 16) * ceil(max_len / 64)), else
  *   GQA_ERR_UNSUPPORTED.
  * Pages: microLLM-rocm optimisation log, Experiments 064-065 (batched cached
  * GQA decode, bf16 cache with fp32 accumulation) and 282-284 (split-sequence
@@ -274,8 +275,9 @@ int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
  * library's own device memory, present on every GPU that loads the library
  * until the process exits.
  *   - Arguments, layouts and results as gqa_attn_decode (same kernel), with
- *     the grid trimmed so the partials fit: (grid + P) * 16 * (d + 2) * 4
- *     bytes <= 4 MiB, where P = B * H_kv * ceil(H_q / H_kv / 16) <= 16384.
+ *     the grid trimmed so the partials fit: (grid + P) * 16 * (D + 2) * 4
+ *     bytes <= 4 MiB, where P = B * H_kv * ceil(H_q / H_kv / 16) <= 16384
+ *     and D is the kernel's head dim (64 for d <= 64, else 128).
  *     Larger problems return GQA_ERR_UNSUPPORTED (use gqa_attn_decode).
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call

@@ -11,6 +11,9 @@ token-major layout without strided copies).
 * Head dim 256 (one query tile per CTA: its S and O fill the tensor memory)
   through the dense, lse and strided entry points, with ragged tile tails,
   more keys than queries, and MHA / GQA / MQA groupings.
+* Decode at head dims 32 and 96 (the 64- and 128-column decode kernels on
+  zero-padded boxes), through the plain, lse, chunked and allocation-free
+  entry points, with NaN past every sequence and planes split over CTAs.
 Bounds: the bf16 ones of the other tests (max abs 2e-2, mean abs 2e-3; lse
 max abs 5e-3).
 """
@@ -162,3 +165,25 @@ def test_head_dim_256_strided_fused_qkv():
     assert torch.equal(o_tok.transpose(1, 2), packed), "strided and packed calls differ"
     ref, _ = oracle.prefill(q.cpu(), k.cpu(), v.cpu(), True, d ** -0.5, n_threads=THREADS)
     _check(packed.float().cpu().numpy(), ref, "d 256 fused QKV")
+
+
+@pytest.mark.parametrize("shape", [(8, 12, 2, 700), (3, 16, 16, 300), (64, 8, 1, 520)],
+                         ids=lambda s: "-".join(map(str, s)))
+@pytest.mark.parametrize("d", [32, 96])
+def test_decode_head_dims_32_96(d, shape):
+    B, H_q, H_kv, L = shape
+    sl, q, kc, vc = inputs.decode_inputs(B, H_q, H_kv, L, d, torch.bfloat16, seed=670 + d + B)
+    sld, qd, kcd, vcd = sl.cuda(), q.cuda(), kc.cuda(), vc.cuda()
+    scale = d ** -0.5
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_decode(qd, kcd, vcd, sld, o, scale=scale)
+    o2, lse = ops.gqa_attn_decode_lse(qd, kcd, vcd, sld, scale=scale)
+    o3 = ops.gqa_attn_decode(qd, kcd, vcd, sld, scale=scale, chunk_tokens=128)
+    o4 = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_decode_noalloc(qd, kcd, vcd, sld, o4, scale=scale)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, ref_lse = oracle.decode(q, kc, vc, sl, scale)
+    for got, what in ((o, "plain"), (o2, "lse"), (o3, "chunked"), (o4, "no-alloc")):
+        _check(got.float().cpu().numpy(), ref, f"decode d {d} {shape} {what}")
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max() <= LSE_MAX
