@@ -381,7 +381,7 @@ def decode_blocks(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
             "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
             "l2": f"{copies} rotating copies",
             "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                     "decode_kernel<128,5,0>")}
+                                     "decode_kernel<128,5,0,128>")}
         del bufs, o
         torch.cuda.empty_cache()
 
@@ -415,9 +415,9 @@ def decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
         "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
         "l2": f"{copies} rotating copies",
         "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                 "decode_kernel<128,5,1> (fp8 cache)",
+                                 "decode_kernel<128,5,1,128> (fp8 cache)",
                                  recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
-                                                  "decode_kernel<128,5,1>"))}
+                                                  "decode_kernel<128,5,1,128>"))}
     del bufs, o
     torch.cuda.empty_cache()
 
@@ -645,9 +645,9 @@ def run_ours(args):
             "ms": round(dec_ms, 6),
             "roofline": roofline_obj(
                 "hbm", dec_ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                "decode_kernel<128,5,0> (persistent split-KV + in-kernel merge)",
+                "decode_kernel<128,5,0,128> (persistent split-KV + in-kernel merge)",
                 recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
-                                 "decode_kernel<128,5,0>")),
+                                 "decode_kernel<128,5,0,128>")),
             "e2e": {"value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},
         },

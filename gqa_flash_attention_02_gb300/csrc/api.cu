@@ -417,14 +417,15 @@ int fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
     return GQA_ERR_INVALID_ARG;
   if (H_q % H_kv != 0) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
-  if (d != 32 && d != 64 && d != 96 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
   if (B > kVarlenMaxB) return GQA_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_q) * H_q * d > kMaxElems ||
       static_cast<long long>(total_k) * H_kv * d > kMaxElems)
     return GQA_ERR_UNSUPPORTED;
   if (total_q == 0) return GQA_OK;  // no query rows: nothing to compute
   if (total_k == 0) return GQA_ERR_INVALID_ARG;  // rows with no keys
-  const long long most = varlen_max_units(B, H_q, H_kv, total_q);
+  const int tpu = d == 256 ? 1 : 2;  // one query tile per unit at head dim 256
+  const long long most = varlen_max_units(B, H_q, H_kv, total_q, tpu);
   if (most > (1ll << 30)) return GQA_ERR_UNSUPPORTED;
   Workspace *ws = nullptr;
   int rc = get_workspace(stream, 0, &ws, 0, static_cast<size_t>(most));
@@ -447,6 +448,7 @@ int fwd_packed(const void *q, const void *k, const void *v, void *o, float *lse,
   va.causal = causal ? 1 : 0;
   va.total_q = total_q;
   va.total_k = total_k;
+  va.tpu = tpu;
   cudaError_t e = launch_varlen_plan(va, ws->units, ws->ctl, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   int dev = 0;

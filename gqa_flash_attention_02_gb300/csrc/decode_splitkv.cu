@@ -183,8 +183,6 @@ struct DecodeParams {
   int *err_word;
   const float *k_scale, *v_scale;  // fp8 cache: per K/V head dequantisation scales
   int B, H_q, H_kv, max_len, nhg;  // nhg = query-head groups of 16 per K/V head
-  int od;          // the head dim: O's row stride and the columns stored (<= D; the TMA
-                   // boxes read zeros past it, as for the prefill's padded head dims)
   float scale_log2;
 };
 
@@ -372,7 +370,9 @@ __device__ __forceinline__ int frag_slot(int w, int t) {
   }
 }
 
-template <int D, int NSTG, bool kFp8>
+// OD: the head dim, O's row stride and the columns stored (<= D; the TMA
+// boxes read zeros past it, as for the prefill's padded head dims).
+template <int D, int NSTG, bool kFp8, int OD>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeParams prm) {
@@ -517,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // written by CTA b % G
     for (int b = c; b < prm.B; b += G) {
       if (units_for<kSub>(prm, seq_len(prm, s_len, b)) != 0) continue;
-      uint4 *ob = reinterpret_cast<uint4 *>(prm.o + static_cast<size_t>(b) * prm.H_q * prm.od);
-      for (int idx = tid; idx < prm.H_q * prm.od / 8; idx += 32 * kMmaWarps) ob[idx] = make_uint4(0, 0, 0, 0);
+      uint4 *ob = reinterpret_cast<uint4 *>(prm.o + static_cast<size_t>(b) * prm.H_q * OD);
+      for (int idx = tid; idx < prm.H_q * OD / 8; idx += 32 * kMmaWarps) ob[idx] = make_uint4(0, 0, 0, 0);
       if (prm.lse != nullptr)
         for (int h = tid; h < prm.H_q; h += 32 * kMmaWarps) prm.lse[static_cast<size_t>(b) * prm.H_q + h] = -INFINITY;
     }
@@ -630,14 +630,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
       l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
       l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-      __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * prm.od;
+      __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * OD;
       float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
       if (!split) {
         // the run is the whole plane: write O / l
         const float vm = kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * prm.od, A, 0, cc, il, prm.od);
-        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * prm.od, A, 2, cc, ih, prm.od);
+        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * OD, A, 0, cc, il, OD);
+        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * OD, A, 2, cc, ih, OD);
         if (lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         };
         merge_parts<D, kFp8, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32,
-                             kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f, prm.od);
+                             kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f, OD);
         if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
       }
       __syncwarp();  // every lane is done with the state buffer
@@ -992,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mma_warps_sync();
     if (warp == 1) put(0);
     mma_warps_sync();
-    __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * prm.od;
+    __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * OD;
     float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
     // a split run's merged state stays behind the tree slots in the stage
     float *state = tree + L::kTreeBytes / 4;
@@ -1009,8 +1009,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // this run is the whole plane: write O / l
         const float vm = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * prm.od, acc, 0, cc, il, prm.od);
-        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * prm.od, acc, 2, cc, ih, prm.od);
+        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * OD, acc, 0, cc, il, OD);
+        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * OD, acc, 2, cc, ih, OD);
         if (lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -1103,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       };
       merge_parts<D, kFp8, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                               c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
-                              32 * kMmaWarps, fin.vmul, prm.od);
+                              32 * kMmaWarps, fin.vmul, OD);
       if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
     }
   }
@@ -1115,11 +1115,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (lane == 0) mbar_arrive(ep_full + 8 * qk);
 }
 
-template <int D, int NSTG, bool kFp8>
+template <int D, int NSTG, bool kFp8, int OD>
 cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                             float *lse, float *partials, int *counters, int B, int H_q, int H_kv,
-                            int max_len, int od, float scale, int grid, int *err_word,
+                            int max_len, float scale, int grid, int *err_word,
                             const float *k_scale, const float *v_scale, cudaStream_t stream) {
   using L = DecodeSmem<D, NSTG, kFp8>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory");
@@ -1128,7 +1128,7 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !(configured & (1u << dev))) {
-    e = cudaFuncSetAttribute(decode_kernel<D, NSTG, kFp8>,
+    e = cudaFuncSetAttribute(decode_kernel<D, NSTG, kFp8, OD>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured |= 1u << dev;
@@ -1148,9 +1148,8 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   prm.H_kv = H_kv;
   prm.max_len = max_len;
   prm.nhg = decode_head_groups(H_q, H_kv);
-  prm.od = od;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  return launch_programmatic(decode_kernel<D, NSTG, kFp8>, grid, kThreads, L::kAlloc, stream, tm_q,
+  return launch_programmatic(decode_kernel<D, NSTG, kFp8, OD>, grid, kThreads, L::kAlloc, stream, tm_q,
                              tm_k, tm_v, prm);
 }
 
@@ -1196,15 +1195,18 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                int *err_word, cudaStream_t stream) {
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
   // head dims 32 and 96 run the 64- and 128-column kernels on zero-padded boxes
-  if (d == 32 || d == 64)
-    return launch_decode_d<64, 8, false>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                         B, H_q, H_kv, max_len, d, scale, grid, err_word, nullptr,
-                                         nullptr, stream);
-  if (d == 96 || d == 128)
-    return launch_decode_d<128, 5, false>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                          B, H_q, H_kv, max_len, d, scale, grid, err_word, nullptr,
-                                          nullptr, stream);
-  return cudaErrorInvalidValue;
+#define GQA_DECODE_BF16(D_, NSTG_, OD_)                                                      \
+  launch_decode_d<D_, NSTG_, false, OD_>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,       \
+                                         counters, B, H_q, H_kv, max_len, scale, grid, err_word, \
+                                         nullptr, nullptr, stream)
+  switch (d) {
+    case 32: return GQA_DECODE_BF16(64, 8, 32);
+    case 64: return GQA_DECODE_BF16(64, 8, 64);
+    case 96: return GQA_DECODE_BF16(128, 5, 96);
+    case 128: return GQA_DECODE_BF16(128, 5, 128);
+    default: return cudaErrorInvalidValue;
+  }
+#undef GQA_DECODE_BF16
 }
 
 cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
@@ -1214,13 +1216,13 @@ cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                               const float *v_scale, int grid, int *err_word, cudaStream_t stream) {
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
   if (d == 64)
-    return launch_decode_d<64, 8, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                        B, H_q, H_kv, max_len, 64, scale, grid, err_word, k_scale,
-                                        v_scale, stream);
+    return launch_decode_d<64, 8, true, 64>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,
+                                            counters, B, H_q, H_kv, max_len, scale, grid, err_word,
+                                            k_scale, v_scale, stream);
   if (d == 128)
-    return launch_decode_d<128, 5, true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters,
-                                         B, H_q, H_kv, max_len, 128, scale, grid, err_word, k_scale,
-                                         v_scale, stream);
+    return launch_decode_d<128, 5, true, 128>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,
+                                              counters, B, H_q, H_kv, max_len, scale, grid,
+                                              err_word, k_scale, v_scale, stream);
   return cudaErrorInvalidValue;
 }
 

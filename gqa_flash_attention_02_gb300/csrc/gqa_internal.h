@@ -208,6 +208,7 @@ struct VarlenArgs {
   const int4 *units;       // the plan kernel's list: {b, h_kv, pair, key blocks}
   int B, H_q, H_kv, group, causal, total_q, total_k;
   int uni_q, uni_k;        // the lengths when cu_q / cu_k are null ([B][N][H][d] batches)
+  int tpu;                 // query tiles per listed unit: 2, or 1 at head dim 256
 };
 
 // First row of sequence b: from the offsets, or b * n for equal lengths.
@@ -220,10 +221,11 @@ GQA_HD int varlen_start(const int *cu, int n, int b) {
 }
 
 // Units a call can list at most (workspace sizing): every sequence's query
-// tiles, paired, for each K/V head.
-GQA_HD long long varlen_max_units(int B, int H_q, int H_kv, long long total_q) {
+// tiles, paired (tpu = 2) or one by one (tpu = 1), for each K/V head.
+GQA_HD long long varlen_max_units(int B, int H_q, int H_kv, long long total_q, int tpu = 2) {
   const long long group = H_q / H_kv;
   const long long tiles = total_q / kTileM + B;  // sum over b of ceil(len_q / 128)
+  if (tpu == 1) return static_cast<long long>(H_kv) * group * tiles;
   return static_cast<long long>(H_kv) * ((group * tiles + B) / 2 + B);
 }
 

@@ -342,7 +342,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
       int q0 = 0, len_q = 0, k0 = 0, len_k = 0;
       if (u < total_units) {
         if constexpr (kVarlen) {
-          // the listed unit: sequence b, K/V head, pair of query tiles
+          // the listed unit: sequence b, K/V head, pair of query tiles (one
+          // tile at head dim 256)
           const int4 un = __ldcg(prm.va.units + u);
           const int g = prm.va.group;
           w.b = un.x;
@@ -354,8 +355,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
           const int n_qt = (len_q + kTileM - 1) / kTileM;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            const int f = 2 * un.z + t;
-            if (f < g * n_qt) {
+            const int f = L::kQTiles * un.z + t;
+            if (t < L::kQTiles && f < g * n_qt) {
               w.t[t].q_tile = n_qt - 1 - f / g;
               w.t[t].h_q = w.h_kv * g + f % g;
               w.t[t].kv_blocks = varlen_kv_blocks(len_q, len_k, prm.va.causal, w.t[t].q_tile);
@@ -947,12 +948,12 @@ cudaError_t launch_dc(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CU
                                                        grid, scale, ctl, stream)
                     : launch_d<128, false, kVarlen, kC>(tm_q, tm_k, tm_v, o, ov, lse, plan, va,
                                                         grid, scale, ctl, stream);
-  if constexpr (!kVarlen && kC == 1) {
+  if constexpr (kC == 1) {
     if (ov.d == 256)  // one query tile per unit (the plan says so)
-      return with_lse ? launch_d<256, true, false, 1>(tm_q, tm_k, tm_v, o, ov, lse, plan, va,
-                                                      grid, scale, ctl, stream)
-                      : launch_d<256, false, false, 1>(tm_q, tm_k, tm_v, o, ov, lse, plan, va,
-                                                       grid, scale, ctl, stream);
+      return with_lse ? launch_d<256, true, kVarlen, 1>(tm_q, tm_k, tm_v, o, ov, lse, plan, va,
+                                                        grid, scale, ctl, stream)
+                      : launch_d<256, false, kVarlen, 1>(tm_q, tm_k, tm_v, o, ov, lse, plan, va,
+                                                         grid, scale, ctl, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -1049,7 +1050,7 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenA
     s_lq[b] = lq;
     s_lk[b] = len_k;
     if (lq > 0) {
-      local += va.H_kv * ((va.group * ((lq + kTileM - 1) / kTileM) + 1) / 2);
+      local += va.H_kv * ((va.group * ((lq + kTileM - 1) / kTileM) + va.tpu - 1) / va.tpu);
       atomicMax(&s_max_nb, n_kt);
     }
   }
@@ -1060,13 +1061,13 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenA
     if (b >= va.B) break;
     s_pre[b] = run;
     if (s_lq[b] > 0)
-      run += va.H_kv * ((va.group * ((s_lq[b] + kTileM - 1) / kTileM) + 1) / 2);
+      run += va.H_kv * ((va.group * ((s_lq[b] + kTileM - 1) / kTileM) + va.tpu - 1) / va.tpu);
   }
   if (tid == 0) s_pre[va.B] = total;
   const int max_nb = s_max_nb;
   for (int i = tid; i <= max_nb; i += kPlanThreads) s_bin[i] = 0;
   __syncthreads();
-  // unit x -> (b, h_kv, pair, key blocks)
+  // unit x -> (b, h_kv, pair (or tile, when tpu = 1), key blocks)
   auto unit_at = [&](int x) -> int4 {
     int lo = 0, hi = va.B - 1;  // last b with s_pre[b] <= x
     while (lo < hi) {
@@ -1080,8 +1081,8 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(const VarlenA
     int nb = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const int f = 2 * pair + t;
-      if (f < va.group * n_qt)
+      const int f = va.tpu * pair + t;
+      if (t < va.tpu && f < va.group * n_qt)
         nb = max(nb, varlen_kv_blocks(len_q, len_k, va.causal, n_qt - 1 - f / va.group));
     }
     return make_int4(b, r % va.H_kv, pair, nb);
@@ -1157,7 +1158,9 @@ cudaError_t launch_prefill_tc_varlen(const CUtensorMap &tm_q, const CUtensorMap 
                                      int num_sms, cudaStream_t stream) {
   // the schedule fields the kernel reads; the unit count comes from the plan kernel
   PrefillPlan plan = make_prefill_plan(1, va.H_q, va.H_kv, 1, 1, va.causal);
-  const long long most = varlen_max_units(va.B, va.H_q, va.H_kv, va.total_q);
+  // the kernel takes L::kQTiles query tiles per listed unit
+  if (va.tpu != (ov.d == 256 ? 1 : 2)) return cudaErrorInvalidValue;
+  const long long most = varlen_max_units(va.B, va.H_q, va.H_kv, va.total_q, va.tpu);
   const int grid = static_cast<int>(most < num_sms ? (most < 1 ? 1 : most) : num_sms);
   return launch_any<true>(tm_q, tm_k, tm_v, o, ov, lse, plan, va, grid, 1, scale, ctl, stream);
 }

@@ -124,8 +124,9 @@ int gqa_attn_fwd_strided(const void *q, long long q_sb, long long q_sh, long lon
  *       and key tokens [cu_seqlens_k[b], cu_seqlens_k[b+1]).
  *   Causal alignment is bottom-right inside each sequence: its query row i
  *   sees its key j iff j <= i + (len_k - len_q).
- *   d in {32, 64, 96, 128}; 1 <= B <= 4096; each of total_q*H_q*d, total_k*H_kv*d
- *   below 2^31; at most 4096 blocks of 128 keys per sequence.
+ *   d in {32, 64, 96, 128, 256} (at 256 each work unit holds one query
+ *   tile instead of two); 1 <= B <= 4096; each of total_q*H_q*d,
+ *   total_k*H_kv*d below 2^31; at most 4096 blocks of 128 keys per sequence.
  * The offsets live on the device, so the library checks them there: a
  * sequence whose offsets are decreasing, outside [0, total], with keys
  * missing (len_q > 0 with len_k == 0, or len_k < len_q when causal) or longer

@@ -100,8 +100,8 @@ def test_varlen_validation(fn):
     assert call(tq=-1) == 1
     assert call(H_q=8, H_kv=3) == 1
     assert call(scale=float("nan")) == 1
-    assert call(d=80) == 2   # head dims 32, 64, 96, 128 only
-    assert call(d=256) == 2  # (256 runs on the dense entry points only)
+    assert call(d=80) == 2   # head dims 32, 64, 96, 128, 256 only
+    assert call(d=512) == 2
     assert call(B=4097) == 2                        # above the sequences-per-call limit
     assert call(tq=1 << 22, H_q=1 << 10, H_kv=1 << 8) == 2
     assert call(tq=0) == 0                          # no query rows: nothing launched

@@ -9,8 +9,9 @@ token-major layout without strided copies).
 * Head dims 32 and 96 (zero-padded tiles of the 64- and 128-column kernels)
   through the dense, lse, ragged-batch and token-major entry points.
 * Head dim 256 (one query tile per CTA: its S and O fill the tensor memory)
-  through the dense, lse and strided entry points, with ragged tile tails,
-  more keys than queries, and MHA / GQA / MQA groupings.
+  through the dense, lse, strided, ragged-batch and token-major entry
+  points, with ragged tile tails, more keys than queries, empty sequences,
+  and MHA / GQA / MQA groupings.
 * Decode at head dims 32 and 96 (the 64- and 128-column decode kernels on
   zero-padded boxes), through the plain, lse, chunked and allocation-free
   entry points, with NaN past every sequence and planes split over CTAs.
@@ -165,6 +166,45 @@ def test_head_dim_256_strided_fused_qkv():
     assert torch.equal(o_tok.transpose(1, 2), packed), "strided and packed calls differ"
     ref, _ = oracle.prefill(q.cpu(), k.cpu(), v.cpu(), True, d ** -0.5, n_threads=THREADS)
     _check(packed.float().cpu().numpy(), ref, "d 256 fused QKV")
+
+
+@pytest.mark.parametrize("case", [([300, 1, 129, 77], [400, 1, 129, 200], 8, 2, True),
+                                  ([500, 37], [20, 700], 4, 1, False),
+                                  ([0, 130, 0, 5], [0, 130, 10, 5], 4, 4, True)],
+                         ids=lambda c: "-".join(map(str, c[0])))
+def test_head_dim_256_ragged(case):
+    """Ragged batches at d = 256: one query tile per listed unit; the lse
+    and plain kernels give the same O bits, repeated calls too."""
+    lens_q, lens_k, H_q, H_kv, causal = case
+    d = 256
+    q, k, v, cu_q, cu_k = inputs.varlen_inputs(lens_q, lens_k, H_q, H_kv, d, torch.bfloat16,
+                                               seed=670 + sum(lens_q))
+    qd, kd, vd, cqd, ckd = (t.cuda() for t in (q, k, v, cu_q, cu_k))
+    o = torch.full_like(qd, float("nan"))
+    ops.gqa_attn_fwd_varlen(qd, kd, vd, cqd, ckd, o, causal=causal, scale=d ** -0.5)
+    o2, lse = ops.gqa_attn_fwd_varlen_lse(qd, kd, vd, cqd, ckd, causal=causal, scale=d ** -0.5)
+    o3 = ops.gqa_attn_fwd_varlen(qd, kd, vd, cqd, ckd, causal=causal, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, ref_lse = oracle.prefill_varlen(q, k, v, cu_q, cu_k, causal, d ** -0.5, n_threads=THREADS)
+    _check(o.float().cpu().numpy(), ref, f"ragged d 256 {case}")
+    assert torch.equal(o, o2) and torch.equal(o, o3)
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max() <= LSE_MAX
+
+
+def test_head_dim_256_token_major():
+    B, H_q, H_kv, N_q, N_kv, d = 2, 8, 2, 200, 330, 256
+    q, k, v = inputs.prefill_inputs(B, H_q, H_kv, N_q, N_kv, d, torch.bfloat16, seed=680)
+    tok = lambda t: t.transpose(1, 2).contiguous()
+    ob = ops.gqa_attn_fwd_bshd(tok(q).cuda(), tok(k).cuda(), tok(v).cuda(), causal=True,
+                               scale=d ** -0.5)
+    od = ops.gqa_attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    ref, _ = oracle.prefill(q, k, v, True, d ** -0.5, n_threads=THREADS)
+    _check(ob.transpose(1, 2).float().cpu().numpy(), ref, "token-major d 256")
+    # the same tiles in the same order of key blocks: the same bits as the dense path
+    assert torch.equal(ob.transpose(1, 2), od)
 
 
 @pytest.mark.parametrize("shape", [(8, 12, 2, 700), (3, 16, 16, 300), (64, 8, 1, 520)],
