@@ -164,8 +164,9 @@ struct DecodeSmem {
   static constexpr int kOffML = kRingBytes;                  // [NSTG][4 warps][32 lanes] float4
   static constexpr int kOffEp = kOffML + NSTG * kMmaWarps * 32 * 16;  // epilogue's merged state
   static constexpr int kOffQueue = kOffEp + kStateBytes;     // [NSTG] run entries of 16 ints
-  static constexpr int kOffMeta = kOffQueue + NSTG * 64;     // per stage: b, pib, s, len
-  static constexpr int kOffLen = kOffMeta + NSTG * 16;
+  static constexpr int kOffMeta = kOffQueue + NSTG * 64;     // per stage: b, pib, s, len,
+                                                             // c_first, c_last, -, -
+  static constexpr int kOffLen = kOffMeta + NSTG * 32;
   static constexpr int kOffBar = kOffLen + kLenCache * 4;  // full, empty, ep_full [NSTG]
   static constexpr int kOffInfo = kOffBar + 3 * NSTG * 8;
   static constexpr int kBytes = kOffInfo + 32;
@@ -530,22 +531,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    // Walks the CTA's units; per unit it leaves (b, pib, s, len) in the
-    // stage's metadata and loads K, V and the plane's 16 query rows with one
-    // completion barrier.
+    // Walks the CTA's units; per unit it leaves (b, pib, s, len) and the
+    // first and last CTA of the unit's plane in the stage's metadata (the
+    // owners take two divisions: off the MMA warps' path) and loads K, V and
+    // the plane's 16 query rows with one completion barrier.
     if (lane == 0) {
       Pos p{info[1], info[2], info[3], info[6]};
+      int c_first = 0, c_last = 0;
       for (int i = 0; i < n_units; ++i) {
+        if (i == 0 || p.s == 0) {
+          const int plane_first = u0 + i - p.s;  // global unit of (plane, s = 0)
+          c_first = owner_of(plane_first, sp);
+          c_last = owner_of(plane_first + p.nsub - 1, sp);
+        }
         const int st = i % NSTG;
         if (i >= NSTG && !mbar_wait(empty + 8 * st, ((i / NSTG) & 1) ^ 1, nullptr)) {
           record_error(prm.err_word, kErrTimeout);
           break;
         }
-        int *meta = stage_meta + 4 * st;
+        int *meta = stage_meta + 8 * st;
         meta[0] = p.b;
         meta[1] = p.pib;
         meta[2] = p.s;
         meta[3] = seq_len(prm, s_len, p.b);
+        meta[4] = c_first;
+        meta[5] = c_last;
         const int h_kv = p.pib / prm.nhg, hg = p.pib - h_kv * prm.nhg;
         const int plane_kv = p.b * prm.H_kv + h_kv;
         const uint32_t dst = s_base + st * L::kStage;
@@ -658,6 +668,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       __syncwarp();
       bool last = __shfl_sync(0xffffffffu, done, 0) + run_units == nsub;
+      // the first look is relaxed: a fence then orders the reads it allows
+      if (last) fence_acq_rel_gpu();
       if (!last) {
         float4 *dst = reinterpret_cast<float4 *>(prm.part + static_cast<size_t>(c + plane) * kSlot);
 #pragma unroll
@@ -669,14 +681,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           reinterpret_cast<float *>(dst)[kHeads * D + lane] = sm[lane];
           reinterpret_cast<float *>(dst)[kHeads * D + kHeads + lane] = sl[lane];
         }
-        fence_acq_rel_gpu();
+        // the count publishes the part (release, for the warp's stores
+        // before the barrier) and, for the run that completes it, acquires
+        // the other parts
         __syncwarp();
         int prev = 0;
-        if (lane == 0) prev = atomicAdd(prm.counters + plane, run_units);
+        if (lane == 0) prev = atom_add_acq_rel_gpu(prm.counters + plane, run_units);
         last = __shfl_sync(0xffffffffu, prev, 0) + run_units == nsub;
       }
       if (last) {
-        fence_acq_rel_gpu();
         __syncwarp();
         auto self = [&](int, int it, float4 &v, float &m, float &l) {
           const int h = it / kQuads;
@@ -695,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   // -------------------------------------------------------------- MMA warps
   const int wrow = warp * kRows;  // this warp's first row in a unit
-  int seg_first_i = 0, seg_first_s = 0;
+  int seg_first_i = 0;
   int ep_k = 0;  // runs queued for the epilogue warp so far
   int counter_seen = 0, counter_seen2 = 0;  // the last run's looks at its plane counter
   struct FinalRun {
@@ -714,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (lane == 0) record_error(prm.err_word, kErrTimeout);
       break;  // every MMA warp times out on the same phase
     }
-    const int *meta = stage_meta + 4 * st;
+    const int *meta = stage_meta + 8 * st;
     const int b = meta[0], pib = meta[1], s = meta[2], len = meta[3];
     const int nsub = (len + kSub - 1) / kSub;
     const int h_kv = pib / prm.nhg, hg = pib - h_kv * prm.nhg;
@@ -725,7 +738,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (i == 0 || s == 0) {
       // a new run
       seg_first_i = i;
-      seg_first_s = s;
       // The CTA's last run reads its plane's unit counter now; the value is
       // used at the run's end (a fence then orders the reads it allows), so
       // the load's latency hides behind the run's units.
@@ -742,24 +754,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int rows_here = min(kSub, len - s * kSub);  // valid rows in this unit
     // fp8 cache: the K/V head's scales (K's folds into the exponent scale)
     const float sl2 = kFp8 ? prm.scale_log2 * __ldg(prm.k_scale + h_kv) : prm.scale_log2;
-    bool zeroed = false;
 #pragma unroll 1
     for (int grp = 0; grp < kRows / 16; ++grp) {
     const int r0 = wrow + 16 * grp;  // first row of this 16-row group in the unit
-    if constexpr (!kFp8) {
-      if (rows_here < kSub) {
-        // rows past the sequence (other sequences' data or NaN padding) must
-        // not reach P.V: zero this warp's invalid V rows
-        for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
-          const int r = r0 + idx / (D / 8), u = idx % (D / 8);
-          if (r >= rows_here) {
-            *reinterpret_cast<uint4 *>(smem + (vt - s_base) + swz(r, u, kSub)) = make_uint4(0, 0, 0, 0);
-            zeroed = true;
-          }
-        }
-        __syncwarp();
-      }
-    }
     // ---- S = Q K^T for the group's 16 rows (two n-tiles of 8 keys)
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t qt = kt + 2 * L::kTile;
@@ -900,10 +897,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // 24-31: keys 8-15 unit u+1  -> {b0,b1} for d-tile u and {b0,b1} for u+1
       const int key = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
       const int uo = lane >> 4;
+      // Rows past the sequence (other sequences' data or NaN padding) must
+      // not reach P.V: their P is 0, and their V values are cleared in the
+      // fragments (b0, b2: keys 2t, 2t+1 of the group; b1, b3: keys 2t+8,
+      // 2t+9; t = lane % 4; the lower half of a pair is the lower key).
+      const bool partial = r0 + 16 > rows_here;  // warp-uniform
+      const int k2 = r0 + 2 * (lane & 3);
+      const uint32_t keep_lo = (k2 < rows_here ? 0x0000ffffu : 0u) | (k2 + 1 < rows_here ? 0xffff0000u : 0u);
+      const uint32_t keep_hi = (k2 + 8 < rows_here ? 0x0000ffffu : 0u) | (k2 + 9 < rows_here ? 0xffff0000u : 0u);
 #pragma unroll
       for (int u = 0; u < NT; u += 2) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vt + swz(key, u + uo, kSub), b0, b1, b2, b3);
+        if (partial) {
+          b0 &= keep_lo;
+          b2 &= keep_lo;
+          b1 &= keep_hi;
+          b3 &= keep_hi;
+        }
         mma_bf16(acc[u], pa, b0, b1);
         mma_bf16(acc[u + 1], pa, b2, b3);
       }
@@ -912,16 +923,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     const bool final_run = (i == n_units - 1);
     if (!final_run && s != nsub - 1) {
-      // release the stage to the producer (generic-proxy writes made visible
-      // to the TMA that will overwrite it)
-      if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
+      // release the stage to the producer
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + 8 * st);
       continue;
     }
     // ---- the run ends here; stage st stays held
-    const int plane_first = u0 + seg_first_i - seg_first_s;  // global unit of (plane, s = 0)
-    const int c_first = owner_of(plane_first, sp), c_last = owner_of(plane_first + nsub - 1, sp);
+    // (the stage's metadata stays until the stage is released)
+    const int c_first = meta[4], c_last = meta[5];
     const bool split = c_first != c_last;
     const int plane = b * planes_per_b + pib;
     const int run_units = i - seg_first_i + 1;
@@ -1081,20 +1090,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         dst[kHeads * D + tid] = st_m[tid];
         dst[kHeads * D + kHeads + tid] = st_l[tid];
       }
-      fence_acq_rel_gpu();
+      // the count publishes the part (release, for the stores of all MMA
+      // threads before the barrier) and, for the run that completes it,
+      // acquires the other parts
       mma_warps_sync();
-      if (tid == 0) {
-        const bool l0 = atomicAdd(prm.counters + plane, run_units) + run_units == nsub;
-        if (l0) fence_acq_rel_gpu();
-        info[4] = l0 ? 1 : 0;
-      }
+      if (tid == 0)
+        info[4] = atom_add_acq_rel_gpu(prm.counters + plane, run_units) + run_units == nsub ? 1 : 0;
       mma_warps_sync();
       last = info[4] != 0;
     }
     if (last) {
       // ---- the plane's last run: merge the parts of CTAs c_first..c_last
-      // (CTA cs in slot cs + plane; this CTA's own part in shared memory)
-      fence_acq_rel_gpu();
+      // (CTA cs in slot cs + plane; this CTA's own part in shared memory;
+      // the acquiring thread passed a barrier with the others since)
       auto self = [&](int, int it, float4 &v, float &m, float &l) {
         const int h = it / kQuads;
         v = *reinterpret_cast<const float4 *>(state + h * L::kRow + 4 * (it % kQuads));

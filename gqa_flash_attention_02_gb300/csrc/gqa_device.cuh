@@ -504,6 +504,17 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
+// Atomic add at GPU scope with acquire-release semantics; returns the old
+// value. Release covers this thread's earlier writes and those of threads
+// that reached a barrier with it before the add; acquire makes what the
+// earlier adders released visible to this thread's later reads (and, after
+// a barrier, to the other threads').
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Relaxed load at GPU scope (not cached in L1): a value another CTA wrote
 // with an atomic; pair it with a fence before reading data it guards.
 __device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
