@@ -700,7 +700,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         merge_parts<D, kFp8, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32,
                              kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f, OD);
-        if (lane == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
+        // re-arm for the next launch (every other count of the plane was
+        // observed before this store)
+        if (lane == 0) st_relaxed_gpu(prm.counters + plane, 0);
       }
       __syncwarp();  // every lane is done with the state buffer
     }
@@ -1112,7 +1114,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       merge_parts<D, kFp8, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                               c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
                               32 * kMmaWarps, fin.vmul, OD);
-      if (tid == 0) atomicExch(prm.counters + plane, 0);  // re-arm for the next launch
+      // re-arm for the next launch (every other count of the plane was
+      // observed before this store)
+      if (tid == 0) st_relaxed_gpu(prm.counters + plane, 0);
     }
   }
   // tell the epilogue warp that no more runs follow (every queued run holds

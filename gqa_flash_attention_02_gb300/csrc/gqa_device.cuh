@@ -515,6 +515,12 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
   return old;
 }
 
+// Relaxed store at GPU scope. Unlike an atomic exchange it returns nothing,
+// so the thread does not wait for the round trip (nor does its exit).
+__device__ __forceinline__ void st_relaxed_gpu(int *p, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Relaxed load at GPU scope (not cached in L1): a value another CTA wrote
 // with an atomic; pair it with a fence before reading data it guards.
 __device__ __forceinline__ int ld_relaxed_gpu(const int *p) {

@@ -300,7 +300,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
         int c = 0;
         if (lane == 0) {
           c = atomicAdd(prm.ctl + kCtlWork, 1);
-          if (c == max(total_cu, grid) - 1) atomicExch(prm.ctl + kCtlWork, 0);
+          if (c == max(total_cu, grid) - 1) st_relaxed_gpu(prm.ctl + kCtlWork, 0);
         }
         u = grid + __shfl_sync(0xffffffffu, c, 0);
         if (csize > 1) {
