@@ -305,7 +305,7 @@ int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const i
   int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
   if (rc != GQA_OK) return rc;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
-  if (d != 32 && d != 64 && d != 96 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
   if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
   if (chunk_tokens != 0 &&
       (chunk_tokens < 0 || chunk_tokens % kDecodeChunkUnit != 0 || chunk_tokens > kDecodeChunkMax))
@@ -320,8 +320,8 @@ int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const i
   if (rc != GQA_OK) return rc;
   CUtensorMap tq, tk, tv;
   if (!encode_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
-      !encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit) ||
-      !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeChunkUnit))
+      !encode_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, decode_box_rows(d)) ||
+      !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, decode_box_rows(d)))
     return cuda_fail(cudaErrorInvalidValue);
   e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, lse, ws->partials, ws->counters, B, H_q, H_kv,
                          max_len, d, scale, grid, ws->ctl + kCtlErr, stream);

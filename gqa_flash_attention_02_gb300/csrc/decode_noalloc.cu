@@ -70,7 +70,7 @@ extern "C" int gqa_attn_decode_noalloc(const void *q, const void *k_cache, const
   if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_len <= 0 || d <= 0 || H_q % H_kv != 0)
     return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
-  if (d != 32 && d != 64 && d != 96 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128 && d != 256) return GQA_ERR_UNSUPPORTED;
   if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
   if (max_len > (1 << 20) ||
       static_cast<long long>(B) * H_kv * max_len * d > (1ll << 31) - 1)
@@ -104,9 +104,9 @@ extern "C" int gqa_attn_decode_noalloc(const void *q, const void *k_cache, const
   CUtensorMap tq, tk, tv;
   if (!encode_tensor_map_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
       !encode_tensor_map_bf16_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv,
-                                 kDecodeChunkUnit) ||
+                                 decode_box_rows(d)) ||
       !encode_tensor_map_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv,
-                                 kDecodeChunkUnit))
+                                 decode_box_rows(d)))
     return GQA_ERR_CUDA;
   e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, nullptr, partials, counters, B, H_q, H_kv, max_len, d,
                          scale, grid, err_word, stream);

@@ -47,12 +47,19 @@ constexpr int kMmaWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kEpilogueWarp = 5;
 constexpr int kThreads = 32 * (kMmaWarps + 2);
-// Cache rows per unit: 64 for a bf16 cache (16 per MMA warp), 128 for an
-// fp8 cache (32 per MMA warp), so a unit is 16 KB of K and of V at d = 128
-// either way and each MMA warp's rows of a stage hold its accumulator
-// fragments when it hands a run to the epilogue warp.
-template <bool kFp8>
-constexpr int kSubOf = kFp8 ? 128 : 64;
+// At head dim 256 a warp's 16-head x d fp32 accumulator would not fit in
+// its registers, so two MMA warps share each 16-row group of a unit: both
+// compute the group's S over all 256 dims and each keeps O for its 128
+// columns. Elsewhere each MMA warp has its own rows and all d columns.
+template <int D>
+constexpr int kDimSplitOf = D == 256 ? 2 : 1;
+// Cache rows per unit: 16 per row group of a bf16 cache (64 rows, or 32 at
+// d = 256), 32 per MMA warp of an fp8 cache (128 rows), so a unit is 16 KB
+// of K and of V at d = 128 and 256 alike, and each MMA warp's share of a
+// stage's rows holds its accumulator fragments when it hands a run to the
+// epilogue warp.
+template <int D, bool kFp8>
+constexpr int kSubFor = kFp8 ? 128 : 64 / kDimSplitOf<D>;
 constexpr int kHeads = kDecodeHeads;  // query heads per plane (mma M)
 // Fewest units a CTA takes: fewer, longer runs (each run ends in a merge
 // step and a plane spans at most nsub / kMinUnits + 2 CTAs); no CTA range
@@ -139,7 +146,8 @@ __device__ __forceinline__ void mma_warps_sync() {
 
 template <int D, int NSTG, bool kFp8>
 struct DecodeSmem {
-  static constexpr int kSub = kSubOf<kFp8>;
+  static constexpr int kSub = kSubFor<D, kFp8>;
+  static constexpr int kDimSplit = kDimSplitOf<D>;
   static constexpr int kTile = kSub * D * (kFp8 ? 1 : 2);  // one K or V unit
   static constexpr int kQTile = kHeads * D * 2;  // the plane's 16 query rows
   static constexpr int kStage = 2 * kTile + kQTile;
@@ -152,14 +160,15 @@ struct DecodeSmem {
   // (m, l, O) fragments through two slots of 32 lanes x (D/8 * 4
   // accumulators + m_lo, m_hi, l_lo, l_hi) in the stage of the run's last
   // unit and keep the merged state there, behind the slots.
-  static constexpr int kLaneFloats = D / 8 * 4 + 4;
+  static constexpr int kLaneFloats = D / 8 / kDimSplit * 4 + 4;
   static constexpr int kTreeBytes = 2 * 32 * kLaneFloats * 4;
   static_assert(kTreeBytes + kStateBytes <= kStage, "run-end scratch");
   // A run that ends before the CTA's last unit is finished by the epilogue
   // warp: each MMA warp leaves its accumulator fragments in the K/V rows of
-  // the stage that only it reads (16 K and 16 V rows: 2 D bytes per lane)
-  // and its (m, l) in the stage's side buffer.
-  static_assert(32 * (D / 8) * 4 * 4 == 2 * (kSub / kMmaWarps) * D * (kFp8 ? 1 : 2),
+  // its row group in its columns of the stage (16 K and 16 V rows: 2 D /
+  // kDimSplit bytes per lane) and its (m, l) in the stage's side buffer.
+  static_assert(32 * (D / 8 / kDimSplit) * 4 * 4 ==
+                    2 * (kSub * kDimSplit / kMmaWarps) * (D / kDimSplit) * (kFp8 ? 1 : 2),
                 "fragments fill the warp's rows");
   static constexpr int kOffML = kRingBytes;                  // [NSTG][4 warps][32 lanes] float4
   static constexpr int kOffEp = kOffML + NSTG * kMmaWarps * 32 * 16;  // epilogue's merged state
@@ -336,9 +345,10 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
 // cc + 1 of the tile. With an fp8 cache n-tile 2ch holds the even dims of the
 // 16-dim chunk ch and n-tile 2ch + 1 its odd dims (the order P.V produces
 // them in), so the lane's four values are dims 16ch + 2cc .. 16ch + 2cc + 3.
-template <int D, bool kFp8>
-__device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)[D / 8][4], int e0,
-                                            int cc, float il, int od) {
+// (bf16 cache at d = 256: the NTW n-tiles of one warp's columns from col0.)
+template <int D, bool kFp8, int NTW = D / 8>
+__device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)[NTW][4], int e0,
+                                            int cc, float il, int od, int col0 = 0) {
   if constexpr (kFp8) {
 #pragma unroll
     for (int ch = 0; ch < D / 16; ++ch)
@@ -347,9 +357,10 @@ __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)
                      pack_bf16x2(A[2 * ch][e0 + 1] * il, A[2 * ch + 1][e0 + 1] * il));
   } else {
 #pragma unroll
-    for (int t = 0; t < D / 8; ++t)
-      if (t * 8 < od)  // columns past the head dim are padding
-        *reinterpret_cast<uint32_t *>(dst + t * 8 + cc) = pack_bf16x2(A[t][e0] * il, A[t][e0 + 1] * il);
+    for (int t = 0; t < NTW; ++t)
+      if (col0 + t * 8 < od)  // columns past the head dim are padding
+        *reinterpret_cast<uint32_t *>(dst + col0 + t * 8 + cc) =
+            pack_bf16x2(A[t][e0] * il, A[t][e0 + 1] * il);
   }
 }
 
@@ -358,12 +369,20 @@ __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)
 // of the stage that only warp w reads hold exactly its 32 lanes x D/8
 // float4, lane-contiguous per n-tile (no bank conflicts). bf16 cache: rows
 // [16w, 16w+16) of each 64-column panel of K then V; fp8 cache: rows
-// [32w, 32w+32) of K (n-tiles 0 .. D/16-1), then of V.
+// [32w, 32w+32) of K (n-tiles 0 .. D/16-1), then of V. At d = 256 warp w
+// has row group r = w % 2 and column half h = w / 2: rows [16r, 16r+16) of
+// K panels 2h, 2h+1, then of the same V panels (its 16 n-tiles; the K rows
+// are free once both warps of the group have computed their S).
 template <int D, bool kFp8>
 __device__ __forceinline__ int frag_slot(int w, int t) {
   constexpr int NT = D / 8;
-  constexpr int kSub = kSubOf<kFp8>;
-  if constexpr (kFp8) {
+  constexpr int kSub = kSubFor<D, kFp8>;
+  if constexpr (D == 256) {
+    constexpr int kRowGroups = kMmaWarps / kDimSplitOf<D>;
+    const int c = t >> 2;  // 2 KB chunk: K (c < 2) or V panel 2h + (c & 1)
+    const int panel = (c >> 1) * (D / 64) + (w / kRowGroups) * 2 + (c & 1);
+    return panel * kSub * 8 + (w % kRowGroups) * 16 * 8 + (t & 3) * 32;
+  } else if constexpr (kFp8) {
     constexpr int kRowsF4 = (kSub / kMmaWarps) * D / 16;  // float4 of a warp's rows of one tile
     return (t < NT / 2 ? 0 : kSub * D / 16) + w * kRowsF4 + (t % (NT / 2)) * 32;
   } else {
@@ -379,11 +398,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                   const __grid_constant__ CUtensorMap tm_v, const DecodeParams prm) {
   using L = DecodeSmem<D, NSTG, kFp8>;
   constexpr int kSub = L::kSub;
-  constexpr int kRows = kSub / kMmaWarps;  // rows of a unit per MMA warp
-  constexpr int NT = D / 8;                  // n-tiles of O per warp
+  constexpr int kDimSplit = L::kDimSplit;    // MMA warps per row group
+  constexpr int kRowGroups = kMmaWarps / kDimSplit;
+  constexpr int kRows = kSub / kRowGroups;   // rows of a unit per row group
+  constexpr int NT = D / 8;                  // n-tiles of O
+  constexpr int NTW = NT / kDimSplit;        // n-tiles of O per MMA warp
+  constexpr int DW = D / kDimSplit;          // columns of O per MMA warp
   constexpr int kSlot = kHeads * (D + 2);    // floats per partial slot
   constexpr int kQuads = D / 4;              // float4 column groups per head
-  constexpr int kPer = kHeads * kQuads / (32 * kMmaWarps);  // merge items per MMA thread
+  constexpr int kPer = kHeads * kQuads / (32 * kMmaWarps);  // state items per MMA thread
+  constexpr int kMergeItems = kPer < 4 ? kPer : 4;  // merge items in flight per MMA thread
   constexpr int kEpPer = kHeads * kQuads / 32;              // merge items per epilogue lane
   extern __shared__ uint8_t smem_raw[];
   // offset (not integer) arithmetic on smem_raw keeps the pointer in the
@@ -587,8 +611,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (warp == kEpilogueWarp) {
     // ------------------------------------------------------------ epilogue
     // Finishes the runs that end before the CTA's last unit, so the MMA
-    // warps go on streaming meanwhile. Per queued run it folds the four MMA
-    // warps' (m, l, O) states, in warp order, from the run's last stage (then
+    // warps go on streaming meanwhile. Per queued run it folds the MMA
+    // warps' (m, l, O) states, in warp order (per column half at d = 256,
+    // over the half's two row groups), from the run's last stage (then
     // releases the stage), and either writes O (the run is the whole plane)
     // or publishes a partial: the state goes to slot c + plane, then (fence)
     // the plane's unit counter; the run that completes the count merges the
@@ -611,55 +636,65 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // the fold below (relaxed: a fence orders what it allows to be read).
       int done = 0;
       if (split && lane == 0) done = ld_relaxed_gpu(prm.counters + plane);
-      float A[NT][4];
-      float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) A[t][0] = A[t][1] = A[t][2] = A[t][3] = 0.f;
-      const float4 *frag = reinterpret_cast<const float4 *>(smem + st * L::kStage) + lane;
-#pragma unroll
-      for (int w = 0; w < kMmaWarps; ++w) {
-        const float4 ml = side_ml[(st * kMmaWarps + w) * 32 + lane];
-        float w1l, w2l, w1h, w2h;
-        merge_row(m_lo, l_lo, ml.x, ml.z, w1l, w2l);
-        merge_row(m_hi, l_hi, ml.y, ml.w, w1h, w2h);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const float4 v = frag[frag_slot<D, kFp8>(w, t)];
-          A[t][0] = fmaf(w1l, A[t][0], w2l * v.x);
-          A[t][1] = fmaf(w1l, A[t][1], w2l * v.y);
-          A[t][2] = fmaf(w1h, A[t][2], w2h * v.z);
-          A[t][3] = fmaf(w1h, A[t][3], w2h * v.w);
-        }
-      }
-      // the stage is free for the producer again
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cnt(empty + 8 * st, kMmaWarps);
-      // full row sums: the four lanes of a quad hold different keys
-      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-      l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
       __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * OD;
       float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
-      if (!split) {
-        // the run is the whole plane: write O / l
-        const float vm = kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
-        const float il = vm / l_lo, ih = vm / l_hi;
-        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * OD, A, 0, cc, il, OD);
-        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * OD, A, 2, cc, ih, OD);
-        if (lse_plane != nullptr && (lane & 3) == 0) {
-          // log-sum-exp per head (m, l in log2 units of scale * q.k)
-          if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
-          if (r_hi < Gh) lse_plane[r_hi] = (m_hi + log2f(l_hi)) * 0.6931471805599453f;
-        }
-        continue;
-      }
+      const float4 *frag = reinterpret_cast<const float4 *>(smem + st * L::kStage) + lane;
+      float A[NTW][4];
+      float m_lo, m_hi, l_lo, l_hi;
+      // one pass per column share (d = 256: two), each over its row groups
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        *reinterpret_cast<float2 *>(so + r_lo * L::kRow + t * 8 + cc) = make_float2(A[t][0], A[t][1]);
-        *reinterpret_cast<float2 *>(so + r_hi * L::kRow + t * 8 + cc) = make_float2(A[t][2], A[t][3]);
+      for (int h = 0; h < kDimSplit; ++h) {
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
+#pragma unroll
+        for (int t = 0; t < NTW; ++t) A[t][0] = A[t][1] = A[t][2] = A[t][3] = 0.f;
+#pragma unroll
+        for (int r = 0; r < kRowGroups; ++r) {
+          const int w = r + kRowGroups * h;
+          const float4 ml = side_ml[(st * kMmaWarps + w) * 32 + lane];
+          float w1l, w2l, w1h, w2h;
+          merge_row(m_lo, l_lo, ml.x, ml.z, w1l, w2l);
+          merge_row(m_hi, l_hi, ml.y, ml.w, w1h, w2h);
+#pragma unroll
+          for (int t = 0; t < NTW; ++t) {
+            const float4 v = frag[frag_slot<D, kFp8>(w, t)];
+            A[t][0] = fmaf(w1l, A[t][0], w2l * v.x);
+            A[t][1] = fmaf(w1l, A[t][1], w2l * v.y);
+            A[t][2] = fmaf(w1h, A[t][2], w2h * v.z);
+            A[t][3] = fmaf(w1h, A[t][3], w2h * v.w);
+          }
+        }
+        if (h == kDimSplit - 1) {
+          // the stage is free for the producer again
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cnt(empty + 8 * st, kMmaWarps);
+        }
+        // full row sums: the four lanes of a quad hold different keys
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+        if (!split) {
+          // the run is the whole plane: write O / l
+          const float vm = kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
+          const float il = vm / l_lo, ih = vm / l_hi;
+          if (r_lo < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_lo * OD, A, 0, cc, il, OD, h * DW);
+          if (r_hi < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_hi * OD, A, 2, cc, ih, OD, h * DW);
+          if (h == 0 && lse_plane != nullptr && (lane & 3) == 0) {
+            // log-sum-exp per head (m, l in log2 units of scale * q.k)
+            if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
+            if (r_hi < Gh) lse_plane[r_hi] = (m_hi + log2f(l_hi)) * 0.6931471805599453f;
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < NTW; ++t) {
+            *reinterpret_cast<float2 *>(so + r_lo * L::kRow + h * DW + t * 8 + cc) = make_float2(A[t][0], A[t][1]);
+            *reinterpret_cast<float2 *>(so + r_hi * L::kRow + h * DW + t * 8 + cc) = make_float2(A[t][2], A[t][3]);
+          }
+        }
       }
+      if (!split) continue;
       if ((lane & 3) == 0) {
         sm[r_lo] = m_lo;
         sl[r_lo] = l_lo;
@@ -709,7 +744,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 
   // -------------------------------------------------------------- MMA warps
-  const int wrow = warp * kRows;  // this warp's first row in a unit
+  const int wgrp = warp % kRowGroups;   // this warp's row group
+  const int whalf = warp / kRowGroups;  // and its share of the columns (d = 256)
+  const int wrow = wgrp * kRows;        // this warp's first row in a unit
   int seg_first_i = 0;
   int ep_k = 0;  // runs queued for the epilogue warp so far
   int counter_seen = 0, counter_seen2 = 0;  // the last run's looks at its plane counter
@@ -720,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     float *lse_plane;
     float *state;
   } fin;
-  float acc[NT][4];
+  float acc[NTW][4];
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
 
   for (int i = 0; i < n_units; ++i) {
@@ -747,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         counter_seen = ld_relaxed_gpu(prm.counters + b * planes_per_b + pib);
       counter_seen2 = 0;
 #pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      for (int t = 0; t < NTW; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
       m_lo = m_hi = -INFINITY;
       l_lo = l_hi = 0.f;
     }
@@ -850,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     m_lo = mn_lo;
     m_hi = mn_hi;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
+    for (int t = 0; t < NTW; ++t) {
       acc[t][0] *= a_lo;
       acc[t][1] *= a_lo;
       acc[t][2] *= a_hi;
@@ -908,9 +945,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint32_t keep_lo = (k2 < rows_here ? 0x0000ffffu : 0u) | (k2 + 1 < rows_here ? 0xffff0000u : 0u);
       const uint32_t keep_hi = (k2 + 8 < rows_here ? 0x0000ffffu : 0u) | (k2 + 9 < rows_here ? 0xffff0000u : 0u);
 #pragma unroll
-      for (int u = 0; u < NT; u += 2) {
+      for (int u = 0; u < NTW; u += 2) {  // the warp's n-tiles (8 columns each)
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vt + swz(key, u + uo, kSub), b0, b1, b2, b3);
+        ldsm_x4_t(vt + swz(key, whalf * NTW + u + uo, kSub), b0, b1, b2, b3);
         if (partial) {
           b0 &= keep_lo;
           b2 &= keep_lo;
@@ -943,10 +980,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // (m, l) to the stage's side buffer; the epilogue warp releases the
       // stage. The queue cannot overrun: every queued run holds a stage.
       const int qk = ep_k % NSTG;
-      __syncwarp();  // the warp's reads of its rows are done
+      if constexpr (kDimSplit > 1) {
+        // the group's K rows hold both its warps' fragments: both must be
+        // done with their S (named barriers 2, 3: one per row group)
+        if (wgrp == 0)
+          asm volatile("bar.sync 2, %0;" ::"n"(32 * kDimSplit) : "memory");
+        else
+          asm volatile("bar.sync 3, %0;" ::"n"(32 * kDimSplit) : "memory");
+      } else {
+        __syncwarp();  // the warp's reads of its rows are done
+      }
       float4 *rows = reinterpret_cast<float4 *>(smem + st * L::kStage) + lane;
 #pragma unroll
-      for (int t = 0; t < NT; ++t)
+      for (int t = 0; t < NTW; ++t)
         rows[frag_slot<D, kFp8>(warp, t)] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
       side_ml[(st * kMmaWarps + warp) * 32 + lane] = make_float4(m_lo, m_hi, l_lo, l_hi);
       if (warp == 0 && lane == 0) {
@@ -971,24 +1017,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     // The CTA's last run: the four warps merge their (m, l, O) fragments
     // in the held stage (a lane with the same lane of another warp holds the
-    // same heads and columns): warps 2,3 -> 0,1, then warp 1 -> warp 0.
+    // same heads and columns): warps 2,3 -> 0,1, then warp 1 -> warp 0. At
+    // d = 256 the second row group's warps hand their states to the first's
+    // (warp 1 -> 0, 3 -> 2), and warps 0 and 2 finish a column half each.
     float *tree = reinterpret_cast<float *>(smem + st * L::kStage);
     float *mine = tree + lane * L::kLaneFloats;
     auto put = [&](int slot) {
       float *dst = mine + slot * 32 * L::kLaneFloats;
 #pragma unroll
-      for (int t = 0; t < NT; ++t)
+      for (int t = 0; t < NTW; ++t)
         *reinterpret_cast<float4 *>(dst + 4 * t) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
-      *reinterpret_cast<float4 *>(dst + 4 * NT) = make_float4(m_lo, m_hi, l_lo, l_hi);
+      *reinterpret_cast<float4 *>(dst + 4 * NTW) = make_float4(m_lo, m_hi, l_lo, l_hi);
     };
     auto take = [&](int slot) {
       const float *src = mine + slot * 32 * L::kLaneFloats;
-      const float4 ml = *reinterpret_cast<const float4 *>(src + 4 * NT);
+      const float4 ml = *reinterpret_cast<const float4 *>(src + 4 * NTW);
       float w1l, w2l, w1h, w2h;
       merge_row(m_lo, l_lo, ml.x, ml.z, w1l, w2l);
       merge_row(m_hi, l_hi, ml.y, ml.w, w1h, w2h);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
+      for (int t = 0; t < NTW; ++t) {
         const float4 a = *reinterpret_cast<const float4 *>(src + 4 * t);
         acc[t][0] = fmaf(w1l, acc[t][0], w2l * a.x);
         acc[t][1] = fmaf(w1l, acc[t][1], w2l * a.y);
@@ -997,19 +1045,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     };
     mma_warps_sync();  // every warp is done reading stage st
-    if (warp >= 2) put(warp - 2);
-    mma_warps_sync();
-    if (warp < 2) take(warp);
-    mma_warps_sync();
-    if (warp == 1) put(0);
-    mma_warps_sync();
+    if constexpr (kRowGroups == 4) {
+      if (warp >= 2) put(warp - 2);
+      mma_warps_sync();
+      if (warp < 2) take(warp);
+      mma_warps_sync();
+      if (warp == 1) put(0);
+      mma_warps_sync();
+    } else {
+      if (wgrp == 1) put(whalf);
+      mma_warps_sync();
+    }
     __nv_bfloat16 *o_plane = prm.o + (static_cast<size_t>(b) * prm.H_q + hq0) * OD;
     float *lse_plane = prm.lse == nullptr ? nullptr : prm.lse + static_cast<size_t>(b) * prm.H_q + hq0;
     // a split run's merged state stays behind the tree slots in the stage
     float *state = tree + L::kTreeBytes / 4;
     float *st_m = state + kHeads * L::kRow, *st_l = st_m + kHeads;
-    if (warp == 0) {
-      take(0);
+    if (wgrp == 0) {
+      take(kRowGroups == 4 ? 0 : whalf);
       // full row sums: the four lanes of a quad hold different keys
       l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
       l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
@@ -1020,26 +1073,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // this run is the whole plane: write O / l
         const float vm = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-        if (r_lo < Gh) write_o_row<D, kFp8>(o_plane + r_lo * OD, acc, 0, cc, il, OD);
-        if (r_hi < Gh) write_o_row<D, kFp8>(o_plane + r_hi * OD, acc, 2, cc, ih, OD);
-        if (lse_plane != nullptr && (lane & 3) == 0) {
+        if (r_lo < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_lo * OD, acc, 0, cc, il, OD, whalf * DW);
+        if (r_hi < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_hi * OD, acc, 2, cc, ih, OD, whalf * DW);
+        if (whalf == 0 && lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
           if (r_hi < Gh) lse_plane[r_hi] = (m_hi + log2f(l_hi)) * 0.6931471805599453f;
         }
       } else {
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          *reinterpret_cast<float2 *>(state + r_lo * L::kRow + t * 8 + cc) = make_float2(acc[t][0], acc[t][1]);
-          *reinterpret_cast<float2 *>(state + r_hi * L::kRow + t * 8 + cc) = make_float2(acc[t][2], acc[t][3]);
+        for (int t = 0; t < NTW; ++t) {
+          *reinterpret_cast<float2 *>(state + r_lo * L::kRow + whalf * DW + t * 8 + cc) =
+              make_float2(acc[t][0], acc[t][1]);
+          *reinterpret_cast<float2 *>(state + r_hi * L::kRow + whalf * DW + t * 8 + cc) =
+              make_float2(acc[t][2], acc[t][3]);
         }
-        if ((lane & 3) == 0) {
+        if (whalf == 0 && (lane & 3) == 0) {
           st_m[r_lo] = m_lo;
           st_l[r_lo] = l_lo;
           st_m[r_hi] = m_hi;
           st_l[r_hi] = l_hi;
         }
-        if (lane == 0) {
+        if (warp == 0 && lane == 0) {
           // If every other run of the plane had counted in (their partials
           // published before their count) when one of the early looks at the
           // counter was made, this run is the last one and merges without
@@ -1111,7 +1166,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         m = st_m[h];
         l = st_l[h];
       };
-      merge_parts<D, kFp8, kPer, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+      merge_parts<D, kFp8, kMergeItems, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                               c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
                               32 * kMmaWarps, fin.vmul, OD);
       // re-arm for the next launch (every other count of the plane was
@@ -1171,7 +1226,7 @@ int decode_head_groups(int H_q, int H_kv) { return (H_q / H_kv + kHeads - 1) / k
 
 size_t decode_partials_bytes(int B, int H_q, int H_kv, int d, int grid) {
   const size_t planes = static_cast<size_t>(B) * H_kv * decode_head_groups(H_q, H_kv);
-  const size_t D = d <= 64 ? 64 : 128;  // the kernel's head dim (32 and 96 are padded)
+  const size_t D = d <= 64 ? 64 : (d <= 128 ? 128 : 256);  // the kernel's head dim (32, 96 padded)
   return (static_cast<size_t>(grid) + planes) * kHeads * (D + 2) * sizeof(float);
 }
 
@@ -1181,7 +1236,7 @@ size_t decode_planes(int B, int H_q, int H_kv) {
 
 bool decode_units_fit(int B, int H_q, int H_kv, int max_len) {
   const long long units = static_cast<long long>(decode_planes(B, H_q, H_kv)) *
-                          ((static_cast<long long>(max_len) + kSubOf<false> - 1) / kSubOf<false>);
+                          ((static_cast<long long>(max_len) + kDecodeMinUnit - 1) / kDecodeMinUnit);
   return units <= (1ll << 30);
 }
 
@@ -1216,6 +1271,7 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
     case 64: return GQA_DECODE_BF16(64, 8, 64);
     case 96: return GQA_DECODE_BF16(128, 5, 96);
     case 128: return GQA_DECODE_BF16(128, 5, 128);
+    case 256: return GQA_DECODE_BF16(256, 4, 256);
     default: return cudaErrorInvalidValue;
   }
 #undef GQA_DECODE_BF16

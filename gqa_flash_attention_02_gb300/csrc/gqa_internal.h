@@ -272,10 +272,14 @@ cudaError_t launch_attn_f32(const float *q, const float *k, const float *v, floa
                             const int *seqlens, int kv_row_capacity, int *err_word,
                             cudaStream_t stream);
 
-// Decode: the valid cache rows are cut into 64-row units (one TMA box) and
-// balanced over a persistent grid; a CTA's run over part of a (b, h_kv,
-// head group) plane leaves a partial result merged in the same launch.
+// Decode: the valid cache rows are cut into 64-row units (one TMA box; 32
+// rows at head dim 256) and balanced over a persistent grid; a CTA's run
+// over part of a (b, h_kv, head group) plane leaves a partial result merged
+// in the same launch.
 constexpr int kDecodeChunkUnit = 64;    // rows per unit (the TMA box height)
+constexpr int kDecodeMinUnit = 32;      // the smallest unit (head dim 256)
+// Rows of the K/V TMA box (= rows per unit) of a bf16 cache at head dim d.
+GQA_HD int decode_box_rows(int d) { return d == 256 ? kDecodeMinUnit : kDecodeChunkUnit; }
 constexpr int kDecodeHeads = 16;        // query heads per plane (the Q box height)
 constexpr int kDecodeChunkMax = 2048;   // largest rows-per-CTA sizing hint
 int decode_head_groups(int H_q, int H_kv);                     // query heads per K/V head / 16, rounded up

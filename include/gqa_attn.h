@@ -187,10 +187,11 @@ int gqa_attn_fwd_f32(const void *q, const void *k, const void *v, void *o,
  *             length 0 yields O = 0. Out-of-range values make the call
  *             record GQA_ERR_BAD_SEQLEN (read with gqa_attn_get_device_error)
  *             and leave that sequence's output at 0.
- *   d in {32, 64, 96, 128} (32 and 96 run the 64- and 128-column kernels on
- *   tiles the TMA pads with zero columns); max_len <= 1 << 20; at most 2^30
- *   row units (B * H_kv * ceil(H_q / H_kv / 16) * ceil(max_len / 64)), else
- *   GQA_ERR_UNSUPPORTED.
+ *   d in {32, 64, 96, 128, 256} (32 and 96 run the 64- and 128-column
+ *   kernels on tiles the TMA pads with zero columns; at 256 two warps share
+ *   each 16-row group of a 32-row unit, 128 columns each); max_len <= 1 << 20;
+ *   at most 2^30 row units (B * H_kv * ceil(H_q / H_kv / 16) *
+ *   ceil(max_len / 32)), else GQA_ERR_UNSUPPORTED.
  * Pages: microLLM-rocm optimisation log, Experiments 064-065 (batched cached
  * GQA decode, bf16 cache with fp32 accumulation) and 282-284 (split-sequence
  * cached attention).
@@ -278,7 +279,8 @@ int gqa_attn_decode_f32(const void *q, const void *k_cache, const void *v_cache,
  *   - Arguments, layouts and results as gqa_attn_decode (same kernel), with
  *     the grid trimmed so the partials fit: (grid + P) * 16 * (D + 2) * 4
  *     bytes <= 4 MiB, where P = B * H_kv * ceil(H_q / H_kv / 16) <= 16384
- *     and D is the kernel's head dim (64 for d <= 64, else 128).
+ *     and D is the kernel's head dim (64 for d <= 64, 128 for d <= 128,
+ *     else 256).
  *     Larger problems return GQA_ERR_UNSUPPORTED (use gqa_attn_decode).
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call

@@ -13,8 +13,9 @@ token-major layout without strided copies).
   points, with ragged tile tails, more keys than queries, empty sequences,
   and MHA / GQA / MQA groupings.
 * Decode at head dims 32 and 96 (the 64- and 128-column decode kernels on
-  zero-padded boxes), through the plain, lse, chunked and allocation-free
-  entry points, with NaN past every sequence and planes split over CTAs.
+  zero-padded boxes) and 256 (two MMA warps per row group, a column half
+  each), through the plain, lse, chunked and allocation-free entry points,
+  with NaN past every sequence and planes split over CTAs.
 Bounds: the bf16 ones of the other tests (max abs 2e-2, mean abs 2e-3; lse
 max abs 5e-3).
 """
@@ -207,10 +208,14 @@ def test_head_dim_256_token_major():
     assert torch.equal(ob.transpose(1, 2), od)
 
 
-@pytest.mark.parametrize("shape", [(8, 12, 2, 700), (3, 16, 16, 300), (64, 8, 1, 520)],
+@pytest.mark.parametrize("shape", [(8, 12, 2, 700), (3, 16, 16, 300), (64, 8, 1, 520),
+                                   (1, 32, 8, 2048), (2, 16, 2, 4000)],
                          ids=lambda s: "-".join(map(str, s)))
-@pytest.mark.parametrize("d", [32, 96])
-def test_decode_head_dims_32_96(d, shape):
+@pytest.mark.parametrize("d", [32, 96, 256])
+def test_decode_head_dims(d, shape):
+    """Decode at head dims 32 and 96 (the 64- and 128-column kernels on
+    zero-padded boxes) and 256 (two MMA warps per 16-row group, 128 columns
+    each); the last two shapes spread a plane over many CTAs."""
     B, H_q, H_kv, L = shape
     sl, q, kc, vc = inputs.decode_inputs(B, H_q, H_kv, L, d, torch.bfloat16, seed=670 + d + B)
     sld, qd, kcd, vcd = sl.cuda(), q.cuda(), kc.cuda(), vc.cuda()
@@ -223,6 +228,7 @@ def test_decode_head_dims_32_96(d, shape):
     ops.gqa_attn_decode_noalloc(qd, kcd, vcd, sld, o4, scale=scale)
     torch.cuda.synchronize()
     assert ops.gqa_attn_get_device_error() == 0
+    assert torch.equal(o, o2), "the lse kernel's O differs from the plain kernel's"
     ref, ref_lse = oracle.decode(q, kc, vc, sl, scale)
     for got, what in ((o, "plain"), (o2, "lse"), (o3, "chunked"), (o4, "no-alloc")):
         _check(got.float().cpu().numpy(), ref, f"decode d {d} {shape} {what}")
