@@ -61,6 +61,11 @@ def _code_text(path):
     return [ln for ln in lines if ln]
 
 
+E2E_MODE = ("pipelined over steps: step i's H2D copies (one stream per input tensor), "
+            "step i-1's kernel and step i-2's D2H copy overlap, two device buffers; "
+            "serial_value: copies and kernel back to back on one stream")
+
+
 def source_sha(rel):
     """Hash of a kernel source and of the local headers it includes
     (recursively, ``#include "..."`` next to the file), with comments and
@@ -588,9 +593,69 @@ def run_ours(args):
     e2e_pre = statistics.median(e[0].elapsed_time(e[1]) for e in eev)
     e2e_dec = statistics.median(e[1].elapsed_time(e[2]) for e in eev)
 
+    # The same calls pipelined as a serving loop would run them: step i's
+    # inputs go up (one stream per input tensor, so several copy engines
+    # work at once) while step i-1 computes and step i-2's result comes down
+    # on another stream (two device buffers); every step still copies its
+    # inputs from pinned host memory and reads its result back.
+    s_ins = [torch.cuda.Stream() for _ in range(4)]
+    s_out = torch.cuda.Stream()
+
+    def pipelined(host_in, host_out_like, run, n):
+        nbuf = 2
+        dins = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(nbuf)]
+        douts = [torch.empty(host_out_like.shape, dtype=host_out_like.dtype, device=dev)
+                 for _ in range(nbuf)]
+        houts = [torch.empty(host_out_like.shape, dtype=host_out_like.dtype).pin_memory()
+                 for _ in range(nbuf)]
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        in_done = [[ev() for _ in host_in] for _ in range(n)]
+        comp_done = [ev() for _ in range(n)]
+        out_done = [ev() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for si in s_ins:
+            si.wait_event(t0)
+        s_out.wait_event(t0)
+        for i in range(n):
+            b = i % nbuf
+            for j, (d, h) in enumerate(zip(dins[b], host_in)):
+                si = s_ins[j % len(s_ins)]
+                with torch.cuda.stream(si):
+                    if i >= nbuf:
+                        si.wait_event(comp_done[i - nbuf])   # buffer b's last reader
+                    d.copy_(h, non_blocking=True)
+                    in_done[i][j].record(si)
+            for e in in_done[i]:
+                stream.wait_event(e)
+            if i >= nbuf:
+                stream.wait_event(out_done[i - nbuf])      # buffer b's result is down
+            run(dins[b], douts[b])
+            comp_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                houts[b].copy_(douts[b], non_blocking=True)
+                out_done[i].record(s_out)
+        stream.wait_event(out_done[n - 1])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n
+
+    def run_pre(din, dout):
+        ops.gqa_attn_fwd(din[0], din[1], din[2], dout, causal=True, scale=ps.scale, stream=stream)
+
+    def run_dec(din, dout):
+        ops.gqa_attn_decode(din[1], din[2], din[3], din[0], dout, scale=ds.scale, stream=stream)
+
+    pipe_steps = max(8, min(args.steps, 64))
+    pipelined((hq, hk, hv), o_pre, run_pre, 4)  # warm-up
+    pipe_pre = min(pipelined((hq, hk, hv), o_pre, run_pre, pipe_steps) for _ in range(3))
+    pipelined((hsl, hdq, hkc, hvc), o_dec, run_dec, 4)
+    pipe_dec = min(pipelined((hsl, hdq, hkc, hvc), o_dec, run_dec, pipe_steps) for _ in range(3))
+
     # ---- max over ranks
-    tot_pre, tot_dec, wall, e2e_pre, e2e_dec, var_ms = max_over_ranks(
-        [tot_pre, tot_dec, wall, e2e_pre, e2e_dec, var_ms], dev, world)
+    tot_pre, tot_dec, wall, e2e_pre, e2e_dec, pipe_pre, pipe_dec, var_ms = max_over_ranks(
+        [tot_pre, tot_dec, wall, e2e_pre, e2e_dec, pipe_pre, pipe_dec, var_ms], dev, world)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -648,8 +713,10 @@ def run_ours(args):
                 "decode_kernel<128,5,0,128> (persistent split-KV + in-kernel merge)",
                 recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
                                  "decode_kernel<128,5,0,128>")),
-            "e2e": {"value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
-                    "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec},
+            "e2e": {"value": round(dec_bytes / (pipe_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec,
+                    "mode": E2E_MODE,
+                    "serial_value": round(dec_bytes / (e2e_dec * 1e-3) / 1e9, 2)},
         },
         "varlen": {
             "value": round(job_throughput(world, 1, vs.flops, var_ms, 1e12), 3),
@@ -671,8 +738,10 @@ def run_ours(args):
                                  "prefill_varlen_kernel<128, 0>")),
         },
         "configs": blocks,
-        "e2e": {"value": round(pre_flops / (e2e_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre},
+        "e2e": {"value": round(pre_flops / (pipe_pre * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre,
+                "mode": E2E_MODE,
+                "serial_value": round(pre_flops / (e2e_pre * 1e-3) / 1e12, 3)},
         "gpu_launches": 2 * K * reps,  # one prefill + one decode launch per step, per repetition
         "wall_ms_per_step": round(wall * 1e3 / (K * reps), 6),
         "clocks": clocks,
