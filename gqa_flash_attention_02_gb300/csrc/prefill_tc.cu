@@ -94,7 +94,11 @@ struct TcLayout {
   // (kXFull, in those CTAs) and learns when they have read it (kXEmpty, in
   // the leader)
   static constexpr int kXFull = 19 + 2 * kStages, kXEmpty = kXFull + 2;
-  static constexpr int kNumBars = kXEmpty + 2;
+  // d = 64 (P in columns of its own): S_t consumed by the softmax (the next
+  // S may overwrite it) and P_t consumed by the P V of the block (the next
+  // P may overwrite it)
+  static constexpr int kSEmpty = kXEmpty + 2, kPEmpty = kSEmpty + 2;
+  static constexpr int kNumBars = kPEmpty + 2;
   static constexpr int kOffSched = kOffBar + kNumBars * 8;
   static constexpr int kOffX = kOffSched + 8;  // two slots of the leader's hand-out
   static constexpr int kOffTmem = kOffX + 8;
@@ -150,6 +154,12 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
   // the first 64 keys overlaps the exponentials of the other 64; at D = 64
   // the PV is short and the extra hand-over costs more than it hides.
   constexpr bool kSplitP = D == 128;
+  // At d = 64 the tensor memory holds, per tile, S (128 columns), O (64) and
+  // P (64, bf16 pairs) side by side: the next block's S is computed while
+  // the softmax still works on this block's, instead of after its P V (at
+  // d = 128 P overwrites half of S: 2 x (128 + 128) columns fill the 512).
+  constexpr bool kSepP = D == 64;
+  constexpr uint32_t kPCol = 384;  // P_t at columns [384 + 64 t, 448 + 64 t) when kSepP
   // P's exponentials are fp32 (ex2) at every head dim. (Two per
   // special-function instruction on bf16 pairs, with the exponent input
   // rounded to bf16, measured no faster at D = 128 -- the special-function
@@ -188,6 +198,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
       mbar_init(bar(L::kOEmpty + t), 128);
       mbar_init(bar(L::kSchedFull + t), 1);
       mbar_init(bar(L::kSchedEmpty + t), 9);  // MMA lane + 8 softmax warps
+      mbar_init(bar(L::kSEmpty + t), 128);
+      mbar_init(bar(L::kPEmpty + t), 1);
     }
     mbar_init(bar(L::kDrain), 1);
     for (int s = 0; s < L::kStages; ++s) {
@@ -473,6 +485,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
     const uint32_t v_lo0 = sdesc_lo(s_base + L::kOffKV, L::kPanelBytes);
     int it = 0, kv_it = 0, vc0 = 0, vc1 = 0;
     uint32_t pc0 = 0, pc1 = 0;
+    uint32_t sc0 = 0, sc1 = 0;  // S issued per tile (d = 64: their reads by the softmax gate the next)
     bool ok = true;
 
     auto issue_qk = [&](int t, int st) {
@@ -493,7 +506,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
     auto issue_pv = [&](int t, int st, bool accumulate, int half) {
       const uint32_t b_lo = v_lo0 + static_cast<uint32_t>(st * L::kTileBytes >> 4);
       const uint32_t d = tmem + 256u + D * t;
-      const uint32_t a = tmem + 128u * t + 64u;
+      const uint32_t a = kSepP ? tmem + kPCol + 64u * t : tmem + 128u * t + 64u;
       if (elect_one()) {
 #pragma unroll
         for (int k4 = 0; k4 < kTileN / 32; ++k4) {  // 16 key rows (2048 B) per K-step
@@ -566,55 +579,117 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
       if (nbt0 > 0 && !mbar_wait_warp(bar(L::kQFull + 0), vc0 & 1, abort_flag)) ok = false;
       if (ok && nbt1 > 0 && !mbar_wait_warp(bar(L::kQFull + 1), vc1 & 1, abort_flag)) ok = false;
       if (!ok) break;
-      // block 0: S_t = Q_t K_0^T
       int st_k, st_v;
-      if (!wait_kv(st_k)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after_sync();
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int nbt = t ? nbt1 : nbt0;
-        if (nbt == 0) continue;
-        issue_qk(t, st_k);
-        commit(L::kSFull + t);
-        if (nbt == 1) commit(L::kQEmpty + t);
-      }
-      // blocks 1..nb-1: O_t += P_t V_{j-1}, then S_t = Q_t K_j^T
-      for (int j = 1; j < nb && ok; ++j) {
-        release_kv(st_k);  // K_{j-1} no longer read after this point
-        if (!wait_kv(st_v) || !wait_kv(st_k)) { ok = false; break; }
+      if constexpr (kSepP) {
+        // S_t[j] as soon as the softmax has read S_t[j-1] (and K_j is in),
+        // P V of block j-1 once P_t[j-1] is complete; per block the two
+        // tiles' S go first, as the softmax reads S long before its P.
+        auto s_free = [&](int t) -> bool {  // the softmax has read this tile's previous S
+          uint32_t &sc = t ? sc1 : sc0;
+          const bool r = sc == 0 || mbar_wait_warp(bar(L::kSEmpty + t), (sc - 1) & 1, abort_flag);
+          ++sc;
+          return r;
+        };
+        if (!wait_kv(st_k)) { ok = false; break; }
         __syncwarp();
         tc_fence_after_sync();
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int nbt = t ? nbt1 : nbt0;
-          if (!ok) continue;
-          if (j - 1 < nbt) {
-            if (!do_pv(t, j - 1, st_v)) { ok = false; continue; }
-            if (j - 1 == nbt - 1) commit(L::kOFull + t);
-          }
-          if (j < nbt) {
+          if (!ok || nbt == 0) continue;
+          if (!s_free(t)) { ok = false; continue; }
+          tc_fence_after_sync();
+          issue_qk(t, st_k);
+          commit(L::kSFull + t);
+          if (nbt == 1) commit(L::kQEmpty + t);
+        }
+        for (int j = 1; j < nb && ok; ++j) {
+          release_kv(st_k);  // K_{j-1} no longer read after this point
+          if (!wait_kv(st_v) || !wait_kv(st_k)) { ok = false; break; }
+          __syncwarp();
+          tc_fence_after_sync();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int nbt = t ? nbt1 : nbt0;
+            if (!ok || j >= nbt) continue;
+            if (!s_free(t)) { ok = false; continue; }
+            tc_fence_after_sync();
             issue_qk(t, st_k);
             commit(L::kSFull + t);
             if (j == nbt - 1) commit(L::kQEmpty + t);
           }
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int nbt = t ? nbt1 : nbt0;
+            if (!ok || j - 1 >= nbt) continue;
+            if (!do_pv(t, j - 1, st_v)) { ok = false; continue; }
+            commit(j - 1 == nbt - 1 ? L::kOFull + t : L::kPEmpty + t);
+          }
+          release_kv(st_v);
+        }
+        if (!ok) break;
+        release_kv(st_k);
+        if (!wait_kv(st_v)) { ok = false; break; }
+        __syncwarp();
+        tc_fence_after_sync();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nbt = t ? nbt1 : nbt0;
+          if (!ok || nbt != nb) continue;
+          if (!do_pv(t, nb - 1, st_v)) { ok = false; continue; }
+          commit(L::kOFull + t);
+        }
+        release_kv(st_v);
+      } else {
+        // block 0: S_t = Q_t K_0^T
+        if (!wait_kv(st_k)) { ok = false; break; }
+        __syncwarp();
+        tc_fence_after_sync();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nbt = t ? nbt1 : nbt0;
+          if (nbt == 0) continue;
+          issue_qk(t, st_k);
+          commit(L::kSFull + t);
+          if (nbt == 1) commit(L::kQEmpty + t);
+        }
+        // blocks 1..nb-1: O_t += P_t V_{j-1}, then S_t = Q_t K_j^T
+        for (int j = 1; j < nb && ok; ++j) {
+          release_kv(st_k);  // K_{j-1} no longer read after this point
+          if (!wait_kv(st_v) || !wait_kv(st_k)) { ok = false; break; }
+          __syncwarp();
+          tc_fence_after_sync();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int nbt = t ? nbt1 : nbt0;
+            if (!ok) continue;
+            if (j - 1 < nbt) {
+              if (!do_pv(t, j - 1, st_v)) { ok = false; continue; }
+              if (j - 1 == nbt - 1) commit(L::kOFull + t);
+            }
+            if (j < nbt) {
+              issue_qk(t, st_k);
+              commit(L::kSFull + t);
+              if (j == nbt - 1) commit(L::kQEmpty + t);
+            }
+          }
+          release_kv(st_v);
+        }
+        if (!ok) break;
+        // last block: O_t += P_t V_{nb-1}
+        release_kv(st_k);
+        if (!wait_kv(st_v)) { ok = false; break; }
+        __syncwarp();
+        tc_fence_after_sync();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nbt = t ? nbt1 : nbt0;
+          if (!ok || nbt != nb) continue;
+          if (!do_pv(t, nb - 1, st_v)) { ok = false; continue; }
+          commit(L::kOFull + t);
         }
         release_kv(st_v);
       }
-      if (!ok) break;
-      // last block: O_t += P_t V_{nb-1}
-      release_kv(st_k);
-      if (!wait_kv(st_v)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after_sync();
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int nbt = t ? nbt1 : nbt0;
-        if (!ok || nbt != nb) continue;
-        if (!do_pv(t, nb - 1, st_v)) { ok = false; continue; }
-        commit(L::kOFull + t);
-      }
-      release_kv(st_v);
       if (nbt0 > 0) ++vc0;
       if (nbt1 > 0) ++vc1;
     }
@@ -630,7 +705,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
     const int row = (warp & 3) * 32 + lane;        // row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tm_s = tmem + lane_off + t * 128u;
-    const uint32_t tm_p = tm_s + 64u;
+    const uint32_t tm_p = kSepP ? tmem + lane_off + kPCol + 64u * t : tm_s + 64u;
     const uint32_t tm_o = tmem + lane_off + 256u + t * D;
     const float sl2 = prm.scale_log2;
     // a masked score: whatever the sign of the scale, it scales to -inf
@@ -638,6 +713,7 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
     const float s_masked = sl2 >= 0.f ? -INFINITY : INFINITY;
     int it = 0, vc = 0;
     uint32_t scnt = 0;
+    uint32_t pwc = 0;  // d = 64: P V completions waited for (one per block after a unit's first)
     bool ok = true;
     while (ok) {
       const int slot = it & 1;
@@ -682,6 +758,11 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
         tc_fence_after_sync();
         uint32_t sr[128];
         tmem_ld128_wait(tm_s, sr);
+        if constexpr (kSepP) {
+          // S_t is in registers: the next block's S may overwrite it
+          tc_fence_before_sync();
+          mbar_arrive(bar(L::kSEmpty + t));
+        }
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
@@ -722,6 +803,16 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
         // halves computed before the row maximum is known: the first one
         // when P is handed over in halves, else both
         constexpr int kEarly = kSplitP ? 1 : 2;
+        if constexpr (kSepP) {
+          // P_t[j-1] has been read by its P V before this block's P
+          // overwrites it (and O, last written by that P V, may be rescaled
+          // below)
+          if (j > 0) {
+            if (!mbar_wait_warp(bar(L::kPEmpty + t), pwc & 1, abort_flag)) { ok = false; break; }
+            ++pwc;
+            tc_fence_after_sync();
+          }
+        }
         float alpha = 1.f, sum = 0.f;
         if (j == 0) {
           m_ref = row_max();  // first block: its O is overwritten, nothing to rescale
@@ -749,7 +840,8 @@ __device__ __forceinline__ void prefill_body(const CUtensorMap &tm_q, const CUte
             // with the raised maxima (rows that did not jump keep theirs,
             // alpha = 1) and rescale O before any of this block's PV. O_t
             // was last written by the PV of block j-1, which completed
-            // before S_t[j] was committed.
+            // before S_t[j] was committed (d = 64: before kPEmpty, waited
+            // for above).
             if (raise) {
               alpha = ex2(m_ref - m_blk);
               m_ref = m_blk;
