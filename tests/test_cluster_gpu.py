@@ -1,8 +1,8 @@
 """GPU parity for the clustered dense prefill: units that pair the tiles of
 a group of 4 or 8 query heads run in clusters of g / 2 CTAs, and each K/V
 block is loaded once for the whole group and multicast to the cluster
-(the benchmark spec's one K/V tile load per query-head group; BootstrapAI
-evolution log, collab-014 "Kernel 9 GQA").
+(one K/V tile load per query-head group, the GQA saving of the
+BootstrapAI evolution log, collab-014 "Kernel 9 GQA").
 
 Shapes have at least four two-tile units per SM (the clustered schedule
 is used from there up), with g = 4 (clusters of 2) and g = 8 (clusters of
