@@ -356,7 +356,7 @@ def backward_block(torch, ops, inputs, dev, stream, tc_peak, peak_src, out):
         "calls_per_rep": chain, "reps": 21, "l2": f"{copies} rotating copies",
         "roofline": roofline_obj("tensor", ach, tc_peak, "TFLOP/s",
                                  f"{peak_src} bf16_tflops (burst)",
-                                 f"bwd_prep_kernel<{shape.d}> + bwd_kernel<{shape.d}>")}
+                                 f"bwd_prep_kernel<{shape.d}, {shape.d}> + bwd_kernel<{shape.d}, {shape.d}>")}
     del bufs, grads, qd, kd, vd, o, lse
     torch.cuda.empty_cache()
 

@@ -560,7 +560,7 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return GQA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128) return GQA_ERR_UNSUPPORTED;
   const long long units = static_cast<long long>(B) * H_kv * ((N_kv + kTileN - 1) / kTileN) +
                           static_cast<long long>(B) * H_q * ((N_q + kTileM - 1) / kTileM);
   if (units > INT32_MAX) return GQA_ERR_UNSUPPORTED;

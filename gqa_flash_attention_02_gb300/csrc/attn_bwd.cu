@@ -135,7 +135,10 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b) {
 
 // -D_i = -sum_c dO_ic O_ic and -lse_i * log2(e), for every row of the padded
 // [B*H_q][nq_pad] layout; 8 lanes per row, each over D/8 contiguous columns.
-template <int D>
+// OD: the head dim, the row stride of o, dO, dQ, dK, dV and the columns
+// stored (<= D; the TMA boxes read zeros past it, so at d = 32 and 96 the
+// 64- and 128-column kernels compute on zero-padded tiles).
+template <int D, int OD>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *o,
                                                        const __nv_bfloat16 *dout,
                                                        const float *lse, float *lse2,
@@ -155,11 +158,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *o,
     const bool valid = r < total && i < N_q;
     float acc = 0.f;
     if (valid) {
-      const size_t base = (static_cast<size_t>(bh) * N_q + i) * D + sub * (D / 8);
+      const size_t base = (static_cast<size_t>(bh) * N_q + i) * OD + sub * (D / 8);
 #pragma unroll
       for (int c = 0; c < D / 8; c += 8)
-        acc += dot8_bf16(__ldg(reinterpret_cast<const uint4 *>(o + base + c)),
-                         __ldg(reinterpret_cast<const uint4 *>(dout + base + c)));
+        if (sub * (D / 8) + c < OD)  // columns past the head dim do not exist
+          acc += dot8_bf16(__ldg(reinterpret_cast<const uint4 *>(o + base + c)),
+                           __ldg(reinterpret_cast<const uint4 *>(dout + base + c)));
     }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *o,
   }
 }
 
-template <int D>
+template <int D, int OD>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -516,7 +520,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(i));
     };
     // an accumulator row: D/2 columns from tensor memory, times mul, to bf16 at dst
-    auto store_half_row = [&](uint32_t taddr, __nv_bfloat16 *dst, float mul, bool store, bool zero) {
+    // half h of a row: columns [h D/2, (h+1) D/2), of which those below OD
+    // exist in memory
+    auto store_half_row = [&](uint32_t taddr, __nv_bfloat16 *dst, int half, float mul, bool store,
+                              bool zero) {
       uint32_t v[D / 2];
       if constexpr (D == 128)
         tmem_ld64_wait(taddr, v);
@@ -526,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 *g = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
       for (int c = 0; c < D / 2; c += 8) {
+        if (OD < D && half * (D / 2) + c >= OD) continue;  // columns past the head dim
         uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -601,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           tc_fence_after_sync();
           __nv_bfloat16 *dst = prm.dq +
-                               (static_cast<size_t>(b * prm.H_q + h_q) * prm.N_q + i) * D + half * (D / 2);
-          store_half_row(tmem + lane_off + 320u + half * (D / 2), dst, prm.scale, i < prm.N_q,
+                               (static_cast<size_t>(b * prm.H_q + h_q) * prm.N_q + i) * OD + half * (D / 2);
+          store_half_row(tmem + lane_off + 320u + half * (D / 2), dst, half, prm.scale, i < prm.N_q,
                          n_iter == 0);
         }
       }
@@ -671,10 +679,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         } else {
           tc_fence_after_sync();
-          const size_t at = (static_cast<size_t>(b * prm.H_kv + h_kv) * prm.N_kv + j) * D + half * (D / 2);
+          const size_t at = (static_cast<size_t>(b * prm.H_kv + h_kv) * prm.N_kv + j) * OD + half * (D / 2);
           const bool store = j < prm.N_kv, zero = n_iter == 0;
-          store_half_row(tmem + lane_off + 256u + half * (D / 2), prm.dv + at, 1.f, store, zero);
-          store_half_row(tmem + lane_off + 256u + D + half * (D / 2), prm.dk + at, prm.scale, store, zero);
+          store_half_row(tmem + lane_off + 256u + half * (D / 2), prm.dv + at, half, 1.f, store, zero);
+          store_half_row(tmem + lane_off + 256u + D + half * (D / 2), prm.dk + at, half, prm.scale, store,
+                         zero);
         }
       }
     }
@@ -689,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int OD>
 cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                          const CUtensorMap &tm_do, const void *o, const void *dout,
                          const float *lse, float *work, void *dq, void *dk, void *dv, int B,
@@ -701,7 +710,7 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !(configured & (1u << dev))) {
-    e = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    e = cudaFuncSetAttribute(bwd_kernel<D, OD>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured |= 1u << dev;
   }
@@ -714,7 +723,7 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
   const long long prep_rows = static_cast<long long>(rows) * nq_pad;
   long long prep_grid = (prep_rows + 31) / 32;
   if (prep_grid > 8LL * num_sms) prep_grid = 8LL * num_sms;
-  e = launch_programmatic(bwd_prep_kernel<D>, static_cast<int>(prep_grid), 256, 0, stream,
+  e = launch_programmatic(bwd_prep_kernel<D, OD>, static_cast<int>(prep_grid), 256, 0, stream,
                           static_cast<const __nv_bfloat16 *>(o),
                           static_cast<const __nv_bfloat16 *>(dout), lse, lse2, delta, rows, N_q,
                           nq_pad);
@@ -741,7 +750,7 @@ cudaError_t launch_bwd_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const
   prm.scale_log2 = scale * 1.4426950408889634f;
   prm.err_word = err_word;
   const long long grid = static_cast<long long>(prm.n_kv_units) + static_cast<long long>(B) * H_q * n_qt;
-  return launch_programmatic(bwd_kernel<D>, static_cast<int>(grid), kThreads, L::kAlloc, stream,
+  return launch_programmatic(bwd_kernel<D, OD>, static_cast<int>(grid), kThreads, L::kAlloc, stream,
                              tm_q, tm_k, tm_v, tm_do, prm);
 }
 
@@ -758,13 +767,18 @@ cudaError_t launch_attn_bwd(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             void *dv, int B, int H_q, int H_kv, int N_q, int N_kv, int d,
                             int causal, float scale, int num_sms, int *err_word,
                             cudaStream_t stream) {
-  if (d == 64)
-    return launch_bwd_d<64>(tm_q, tm_k, tm_v, tm_do, o, dout, lse, work, dq, dk, dv, B, H_q, H_kv,
-                            N_q, N_kv, causal, scale, num_sms, err_word, stream);
-  if (d == 128)
-    return launch_bwd_d<128>(tm_q, tm_k, tm_v, tm_do, o, dout, lse, work, dq, dk, dv, B, H_q, H_kv,
-                             N_q, N_kv, causal, scale, num_sms, err_word, stream);
-  return cudaErrorInvalidValue;
+  // head dims 32 and 96 run the 64- and 128-column kernels on zero-padded tiles
+#define GQA_BWD(D_, OD_)                                                                     \
+  launch_bwd_d<D_, OD_>(tm_q, tm_k, tm_v, tm_do, o, dout, lse, work, dq, dk, dv, B, H_q, H_kv, \
+                        N_q, N_kv, causal, scale, num_sms, err_word, stream)
+  switch (d) {
+    case 32: return GQA_BWD(64, 32);
+    case 64: return GQA_BWD(64, 64);
+    case 96: return GQA_BWD(128, 96);
+    case 128: return GQA_BWD(128, 128);
+    default: return cudaErrorInvalidValue;
+  }
+#undef GQA_BWD
 }
 
 }  // namespace gqa

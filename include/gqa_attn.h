@@ -312,7 +312,9 @@ int gqa_attn_decode_noalloc(const void *q, const void *k_cache,
  *   the inputs. dK and dV of a K/V head are the sums over the H_q / H_kv
  *   query heads that read it (the GQA reduction), accumulated in a fixed
  *   order: the result is deterministic for a given input.
- *   Causal alignment, d in {64, 128}, size limits and errors as gqa_attn_fwd.
+ *   Causal alignment, size limits and errors as gqa_attn_fwd; d in {32, 64,
+ *   96, 128} (32 and 96 run the 64- and 128-column kernels on tiles the TMA
+ *   pads with zero columns).
  * Three kernels are launched: a small one for D_i = sum_c dO_ic O_ic and
  * the lse in log2 units (kept in the stream's workspace), then one grid of
  * dK/dV units (per K/V head and 128-key block, looping over the group's

@@ -60,6 +60,9 @@ SHAPES = [
     (2, 2, 1, 1, 129, 128, False),     # a single query row
     (1, 16, 2, 257, 257, 128, True),   # group of 8
     (1, 4, 1, 640, 640, 128, False),   # 5 key blocks through the K/V ring
+    (1, 4, 2, 300, 300, 32, True),     # d = 32 and 96: zero-padded tiles of the
+    (2, 6, 2, 200, 520, 96, True),     #   64- and 128-column kernels
+    (1, 8, 1, 256, 700, 96, False),
 ]
 
 
