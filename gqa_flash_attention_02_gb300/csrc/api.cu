@@ -229,18 +229,21 @@ bool encode_bf16_4d(CUtensorMap *map, const void *base, int d, long rows, long h
 // 8-bit tensor (an fp8 K/V cache) viewed as [planes][rows][d] bytes; box =
 // d bytes x box_rows rows with the d-byte swizzle (128 B for d = 128, 64 B
 // for d = 64), zero fill outside the tensor.
-bool encode_u8_3d(CUtensorMap *map, const void *base, int d, long rows, long planes, int box_rows) {
+// fp8 cache [planes][rows][d] bytes; boxes of box_cols (the kernel's width,
+// 64 or 128 >= d: zeros past d) x box_rows, swizzled as the kernel reads them.
+bool encode_u8_3d(CUtensorMap *map, const void *base, int d, long rows, long planes, int box_cols,
+                  int box_rows) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(planes)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
                            static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d)};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   box_cols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -591,7 +594,7 @@ int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
       (reinterpret_cast<uintptr_t>(v_scale) & 3u) != 0)
     return GQA_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 96 && d != 128) return GQA_ERR_UNSUPPORTED;
   if (!decode_units_fit(B, H_q, H_kv, max_len)) return GQA_ERR_UNSUPPORTED;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -603,8 +606,10 @@ int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
   if (rc != GQA_OK) return rc;
   CUtensorMap tq, tk, tv;
   if (!encode_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
-      !encode_u8_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeFp8Unit) ||
-      !encode_u8_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, kDecodeFp8Unit))
+      !encode_u8_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, d <= 64 ? 64 : 128,
+                    kDecodeFp8Unit) ||
+      !encode_u8_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, d <= 64 ? 64 : 128,
+                    kDecodeFp8Unit))
     return cuda_fail(cudaErrorInvalidValue);
   e = launch_decode_fp8(tq, tk, tv, q, seqlens, o, lse, ws->partials, ws->counters, B, H_q, H_kv,
                         max_len, d, scale, k_scale, v_scale, grid, ws->ctl + kCtlErr, stream);

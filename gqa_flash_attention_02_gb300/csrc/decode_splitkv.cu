@@ -323,11 +323,13 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
           // fragment columns 4q4 .. 4q4+3 are columns 4(q4 % 2) .. +3 of
           // n-tile q4 / 2, i.e. dims 16 (t / 2) + (t % 2) + 2 n (see write_o_row)
           const int t = q4 >> 1, base = 16 * (t >> 1) + (t & 1) + 8 * (q4 & 1);
-          __nv_bfloat16 *row = o_plane + h * od + base;
-          row[0] = __float2bfloat16_rn(Ar[k].x * il);
-          row[2] = __float2bfloat16_rn(Ar[k].y * il);
-          row[4] = __float2bfloat16_rn(Ar[k].z * il);
-          row[6] = __float2bfloat16_rn(Ar[k].w * il);
+          if (16 * (t >> 1) < od) {  // 16-dim chunks past the head dim are padding
+            __nv_bfloat16 *row = o_plane + h * od + base;
+            row[0] = __float2bfloat16_rn(Ar[k].x * il);
+            row[2] = __float2bfloat16_rn(Ar[k].y * il);
+            row[4] = __float2bfloat16_rn(Ar[k].z * il);
+            row[6] = __float2bfloat16_rn(Ar[k].w * il);
+          }
         } else {
           if (4 * q4 < od)  // columns past the head dim are padding
             *reinterpret_cast<uint2 *>(o_plane + h * od + 4 * q4) =
@@ -352,7 +354,8 @@ __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)
   if constexpr (kFp8) {
 #pragma unroll
     for (int ch = 0; ch < D / 16; ++ch)
-      *reinterpret_cast<uint2 *>(dst + 16 * ch + 2 * cc) =
+      if (16 * ch < od)  // 16-dim chunks past the head dim are padding
+        *reinterpret_cast<uint2 *>(dst + 16 * ch + 2 * cc) =
           make_uint2(pack_bf16x2(A[2 * ch][e0] * il, A[2 * ch + 1][e0] * il),
                      pack_bf16x2(A[2 * ch][e0 + 1] * il, A[2 * ch + 1][e0 + 1] * il));
   } else {
@@ -1283,15 +1286,19 @@ cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                               int H_kv, int max_len, int d, float scale, const float *k_scale,
                               const float *v_scale, int grid, int *err_word, cudaStream_t stream) {
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
-  if (d == 64)
-    return launch_decode_d<64, 8, true, 64>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,
-                                            counters, B, H_q, H_kv, max_len, scale, grid, err_word,
-                                            k_scale, v_scale, stream);
-  if (d == 128)
-    return launch_decode_d<128, 5, true, 128>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,
-                                              counters, B, H_q, H_kv, max_len, scale, grid,
-                                              err_word, k_scale, v_scale, stream);
-  return cudaErrorInvalidValue;
+  // head dims 32 and 96 run the 64- and 128-column kernels on zero-padded boxes
+#define GQA_DECODE_FP8(D_, NSTG_, OD_)                                                     \
+  launch_decode_d<D_, NSTG_, true, OD_>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,      \
+                                        counters, B, H_q, H_kv, max_len, scale, grid, err_word, \
+                                        k_scale, v_scale, stream)
+  switch (d) {
+    case 32: return GQA_DECODE_FP8(64, 8, 32);
+    case 64: return GQA_DECODE_FP8(64, 8, 64);
+    case 96: return GQA_DECODE_FP8(128, 5, 96);
+    case 128: return GQA_DECODE_FP8(128, 5, 128);
+    default: return cudaErrorInvalidValue;
+  }
+#undef GQA_DECODE_FP8
 }
 
 // ---------------------------------------------------------------- self-test

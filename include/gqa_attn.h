@@ -245,7 +245,8 @@ int gqa_attn_decode_chunked(const void *q, const void *k_cache,
  * each MMA warp widens its rows of K to bf16 (Q K^T on bf16 pairs, exact
  * widening) and of V to f16 (P V on f16 pairs, exact widening), fp32
  * accumulation; k_scale multiplies the exponent scale, v_scale the output.
- * d in {64, 128}; limits and errors as gqa_attn_decode.
+ * d in {32, 64, 96, 128} (32 and 96 run the 64- and 128-column kernels on
+ * boxes that read zeros past d); limits and errors as gqa_attn_decode.
  * Pages: microLLM-rocm optimisation log, Experiment 065 (the K/V cache
  * stored narrower than fp32 with fp32 accumulation) and Experiments 354 and
  * 359 (an 8-bit cache read fused into decode attention).

@@ -249,7 +249,8 @@ def test_decode_fp8_validation():
     assert call(lse=SC_MIS) == 1
     assert call(H_q=6, H_kv=4) == 1
     assert call(scale=float("nan")) == 1
-    assert call(d=96) == 2
+    assert call(d=48) == 2   # head dims 32, 64, 96, 128 only
+    assert call(d=256) == 2
     assert call(max_len=(1 << 20) + 1) == 2
 
 

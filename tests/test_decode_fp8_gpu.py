@@ -53,7 +53,7 @@ def test_fp8_decode_matches_oracle(shape):
     _check(got, ref, lse, ref_lse, shape.name)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
 def test_fp8_decode_edge_lengths(d):
     """Empty sequences, one row, unit boundaries (128 rows) and a full cache."""
     lens = [0, 1, 127, 128, 129, 255, 256, 700]
@@ -64,13 +64,35 @@ def test_fp8_decode_edge_lengths(d):
     _check(got, ref, lse, ref_lse, f"edge lengths d {d}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
 def test_fp8_decode_one_long_sequence_split_over_many_ctas(d):
     """One 20000-row sequence: its plane is cut over many CTAs and merged."""
     sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(1, 8, 1, 20000, d, seed=510 + d, seqlens=[20000])
     got, lse = _run(sl, q, k8, v8, ks, vs, d ** -0.5)
     ref, ref_lse = oracle.decode_fp8(q, k8, v8, ks, vs, sl, d ** -0.5)
     _check(got, ref, lse, ref_lse, f"one long sequence d {d}")
+
+
+@pytest.mark.parametrize("shape", [(8, 12, 2, 700), (64, 8, 1, 520), (2, 16, 2, 4000)],
+                         ids=lambda s: "-".join(map(str, s)))
+@pytest.mark.parametrize("d", [32, 96])
+def test_fp8_decode_padded_head_dims(d, shape):
+    """Head dims 32 and 96 run the 64- and 128-column kernels on boxes that
+    read zeros past the head dim; O rows are d wide, so a store past the
+    head dim would land in the next head's row or in the guard after the
+    last one (checked to stay NaN)."""
+    B, H_q, H_kv, L = shape
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(B, H_q, H_kv, L, d, seed=540 + d + B)
+    sd, qd, kd, vd, ksd, vsd = (t.cuda() for t in (sl, q, k8, v8, ks, vs))
+    buf = torch.full((B * H_q * d + 256,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = buf[: B * H_q * d].view(B, H_q, d)
+    lse = torch.full((B, H_q), float("nan"), dtype=torch.float32, device="cuda")
+    ops.gqa_attn_decode_fp8(qd, kd, vd, ksd, vsd, sd, o, lse, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert ops.gqa_attn_get_device_error() == 0
+    assert torch.isnan(buf[B * H_q * d:]).all(), "store past the last row"
+    ref, ref_lse = oracle.decode_fp8(q, k8, v8, ks, vs, sl, d ** -0.5)
+    _check(o.float().cpu().numpy(), ref, lse.cpu().numpy(), ref_lse, f"fp8 d {d} {shape}")
 
 
 def test_fp8_decode_scales_and_groups():
