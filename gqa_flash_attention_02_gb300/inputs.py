@@ -251,3 +251,25 @@ def decode_inputs_fp8(B, H_q, H_kv, max_len, d, seed=0, seqlens=None):
         out.append(((x / sc.view(1, H_kv, 1, 1)).to(torch.float8_e4m3fn), sc))
     (k8, ks), (v8, vs) = out
     return seqlens, q.to(torch.bfloat16), k8, v8, ks, vs
+
+
+def decode_inputs_int8(B, H_q, H_kv, max_len, d, seed=0, seqlens=None):
+    """decode_inputs with an int8 cache: the same draws (q rounded to bf16),
+    with each K/V head of the caches quantised symmetrically to int8: its
+    scale is the largest |value| over the valid rows / 127 (fp32), its codes
+    round(value / scale) (to nearest even) in [-127, 127]; rows at or beyond
+    seqlens[b] hold -128, a code the quantiser never writes. Returns
+    (seqlens, q, k8, v8, k_scale, v_scale): k8, v8 int8 [B,H_kv,max_len,d],
+    the scales fp32 [H_kv]."""
+    seqlens, q, kc, vc = decode_inputs(B, H_q, H_kv, max_len, d, torch.float32, seed, seqlens)
+    pos = torch.arange(max_len).view(1, 1, max_len, 1)
+    dead = pos >= seqlens.long().view(B, 1, 1, 1)
+    out = []
+    for x in (kc, vc):
+        x = torch.where(dead, torch.zeros_like(x), x)
+        amax = x.abs().amax(dim=(0, 2, 3))
+        sc = torch.where(amax > 0, amax / 127.0, torch.ones_like(amax)).to(torch.float32)
+        codes = torch.round(x / sc.view(1, H_kv, 1, 1)).clamp(-127, 127).to(torch.int8)
+        out.append((torch.where(dead, torch.full_like(codes, -128), codes), sc))
+    (k8, ks), (v8, vs) = out
+    return seqlens, q.to(torch.bfloat16), k8, v8, ks, vs

@@ -28,7 +28,11 @@ What each function follows (page title and section):
     float64) -- microLLM-rocm optimisation log, Experiments 051-057;
   * decode against an fp8 (e4m3) cache with per-K/V-head scales, the codes
     decoded from the format's definition -- microLLM-rocm optimisation log,
-    Experiment 065.
+    Experiment 065;
+  * decode against an int8 cache (one-byte two's-complement codes with an
+    explicit per-K/V-head scale) -- microLLM-rocm optimisation log,
+    Experiments 352 and 354 (the one-byte tensor with an explicit scale, read
+    and widened inside the decode kernel).
 """
 from __future__ import annotations
 
@@ -308,6 +312,30 @@ def decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seqlens, scale: float):
     ks, vs = _f64(k_scale), _f64(v_scale)
     k = e4m3_value(k_codes) * ks[None, :, None, None]
     v = e4m3_value(v_codes) * vs[None, :, None, None]
+    return decode(q, k, v, seqlens, scale)
+
+
+def int8_value(codes):
+    """Values of int8 codes (bytes, two's complement) as float64: bit 7
+    weighs -128, bits 6-0 weigh 64, 32, ..., 1."""
+    if hasattr(codes, "detach"):
+        import torch
+        t = codes.detach().cpu()
+        if t.dtype != torch.uint8:
+            t = t.view(torch.uint8)
+        codes = t.numpy()
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return ((c & 0x7F) - (c & 0x80)).astype(np.float64)
+
+
+def decode_int8(q, k_codes, v_codes, k_scale, v_scale, seqlens, scale: float):
+    """Decode against an int8 cache: the cache value of a byte is its int8
+    value times the scale of its K/V head (microLLM-rocm optimisation log,
+    Experiments 352 and 354: a one-byte tensor with an explicit scale); the
+    widened caches then go through ``decode``. Returns (o, lse)."""
+    ks, vs = _f64(k_scale), _f64(v_scale)
+    k = int8_value(k_codes) * ks[None, :, None, None]
+    v = int8_value(v_codes) * vs[None, :, None, None]
     return decode(q, k, v, seqlens, scale)
 
 

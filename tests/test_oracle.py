@@ -550,3 +550,74 @@ def test_decode_fp8_planted_mistakes_fail():
     ok = ~np.isnan(good)
     assert not np.array_equal(np.abs(good)[ok], no_sub[ok])
     assert not np.array_equal(np.abs(good)[ok], bias8[ok])
+
+
+# ------------------------------------------------------------------ int8 cache
+
+def test_int8_codes_closed_forms():
+    """Two's-complement codes whose values follow by hand."""
+    cases = {0x00: 0.0, 0x01: 1.0, 0x7F: 127.0, 0x80: -128.0, 0x81: -127.0, 0xFF: -1.0,
+             0xC0: -64.0, 0x40: 64.0, 0x2A: 42.0, 0xD6: -42.0}
+    got = oracle.int8_value(np.array(list(cases), dtype=np.uint8))
+    assert np.array_equal(got, np.array(list(cases.values())))
+
+
+def test_int8_codes_match_torch_int8():
+    """Every code against torch's int8 widening (a library special case)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.int8).to(torch.float64).numpy()
+    assert np.array_equal(oracle.int8_value(codes), ref)
+    t = torch.from_numpy(codes).view(torch.int8)
+    assert np.array_equal(oracle.int8_value(t), ref)
+
+
+def test_int8_planted_mistakes_fail():
+    """Reading the bytes as unsigned, or as offset binary (code - 128),
+    gives other values."""
+    codes = np.arange(256, dtype=np.uint8)
+    good = oracle.int8_value(codes)
+    assert not np.array_equal(good, codes.astype(np.float64))
+    assert not np.array_equal(good, codes.astype(np.float64) - 128.0)
+
+
+def test_decode_int8_is_decode_of_the_widened_scaled_cache():
+    """decode_int8 equals decode on int8(code) * scale, written out here with
+    torch's widening; a K scale folds into the softmax scale, a V scale
+    multiplies O and leaves the lse alone; the rows past each sequence
+    (code -128) are never used."""
+    sl, q, k8, v8, ks, vs = inputs.decode_inputs_int8(3, 8, 2, 200, 64, seed=12,
+                                                      seqlens=[200, 1, 77])
+    assert int(k8[1, :, 1:].min()) == -128 and int(k8[0].min()) >= -127
+    o, lse = oracle.decode_int8(q, k8, v8, ks, vs, sl, 0.125)
+    kw = k8.to(torch.float64) * ks.double().view(1, 2, 1, 1)
+    vw = v8.to(torch.float64) * vs.double().view(1, 2, 1, 1)
+    o2, lse2 = oracle.decode(q, kw, vw, sl, 0.125)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    k_other, v_other = k8.clone(), v8.clone()
+    k_other[1, :, 1:] = 5
+    v_other[2, :, 77:] = 7
+    o3, lse3 = oracle.decode_int8(q, k_other, v_other, ks, vs, sl, 0.125)
+    assert np.array_equal(o, o3) and np.array_equal(lse, lse3)
+    one = torch.ones(2)
+    o_k, lse_k = oracle.decode_int8(q, k8, v8, torch.full((2,), 0.5), one, sl, 0.125)
+    o_ref, lse_ref = oracle.decode_int8(q, k8, v8, one, one, sl, 0.0625)
+    assert np.allclose(o_k, o_ref, atol=1e-13) and np.allclose(lse_k, lse_ref, atol=1e-13)
+    o_v, lse_v = oracle.decode_int8(q, k8, v8, one, torch.full((2,), 3.0), sl, 0.125)
+    o_1, lse_1 = oracle.decode_int8(q, k8, v8, one, one, sl, 0.125)
+    assert np.allclose(o_v, 3 * o_1, atol=1e-10) and np.array_equal(lse_v, lse_1)
+
+
+def test_decode_int8_one_dominant_code():
+    """Closed form: one key whose codes are q's signs times 127, all other
+    keys zero, with a large K scale: that key takes all the weight, so O is
+    its V row (codes times the V scale) to double precision."""
+    B, H_q, H_kv, L, d = 1, 2, 1, 5, 8
+    q = torch.tensor([[[1.0, -1, 1, 1, -1, 1, -1, -1], [2.0, -1, 3, 1, -1, 1, -2, -1]]],
+                     dtype=torch.bfloat16)
+    k8 = torch.zeros(B, H_kv, L, d, dtype=torch.int8)
+    k8[0, 0, 3] = torch.tensor([127, -127, 127, 127, -127, 127, -127, -127], dtype=torch.int8)
+    v8 = torch.arange(B * H_kv * L * d).view(B, H_kv, L, d).remainder(251).sub(125).to(torch.int8)
+    sl = torch.tensor([L], dtype=torch.int32)
+    o, _ = oracle.decode_int8(q, k8, v8, torch.tensor([1.0]), torch.tensor([0.25]), sl, 1.0)
+    want = v8[0, 0, 3].double().numpy() * 0.25
+    assert np.abs(o[0] - want[None, :]).max() < 1e-12
