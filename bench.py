@@ -274,7 +274,7 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src, 
     (six variants), the long-sequence case and decode at B = 1, 8, 64. Each
     is the median over 21 repetitions of a graph of back-to-back calls over
     rotating input copies. ``only``: the groups to run (sweep, long, backward,
-    decode, decode_fp8), all when None."""
+    decode, decode_fp8, decode_int8), all when None."""
     out = {}
     want = lambda group: only is None or group in only
 
@@ -316,7 +316,9 @@ def config_blocks(torch, ops, inputs, dev, stream, tc_peak, hbm_peak, peak_src, 
     if want("decode"):
         decode_blocks(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out)
     if want("decode_fp8"):
-        decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out)
+        decode_byte_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out, "fp8")
+    if want("decode_int8"):
+        decode_byte_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out, "int8")
     return out
 
 
@@ -386,17 +388,20 @@ def decode_blocks(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
             "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
             "l2": f"{copies} rotating copies",
             "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                     "decode_kernel<128,5,0,128>")}
+                                     "decode_kernel<128,5,0,128,0>")}
         del bufs, o
         torch.cuda.empty_cache()
 
 
-def decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
-    # decode against the fp8 cache: bytes actually read (one byte per cached
+def decode_byte_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out, kind):
+    # decode against a one-byte cache (kind "fp8": e4m3 codes, "int8": int8
+    # codes; per-K/V-head scales): bytes actually read (one byte per cached
     # value, K and V once per K/V head, plus q, o and seqlens)
     shape = inputs.decode_shapes()[-1]
-    sl, q, k8, v8, ks, vs = inputs.decode_inputs_fp8(shape.B, shape.H_q, shape.H_kv,
-                                                     shape.max_len, shape.d, seed=shape.seed)
+    make = inputs.decode_inputs_fp8 if kind == "fp8" else inputs.decode_inputs_int8
+    entry = ops.gqa_attn_decode_fp8 if kind == "fp8" else ops.gqa_attn_decode_int8
+    sl, q, k8, v8, ks, vs = make(shape.B, shape.H_q, shape.H_kv, shape.max_len, shape.d,
+                                 seed=shape.seed)
     in_bytes = q.numel() * 2 + k8.numel() + v8.numel()
     copies = copies_for(in_bytes)
     bufs = [(sl.to(dev), q.to(dev), k8.to(dev), v8.to(dev)) for _ in range(copies)]
@@ -405,7 +410,7 @@ def decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
 
     def call8(i, s):
         a, b_, c, d_ = bufs[i % copies]
-        ops.gqa_attn_decode_fp8(b_, c, d_, ksd, vsd, a, o, scale=shape.scale, stream=s)
+        entry(b_, c, d_, ksd, vsd, a, o, scale=shape.scale, stream=s)
 
     for i in range(copies):
         call8(i, stream)
@@ -413,16 +418,18 @@ def decode_fp8_block(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
     assert ops.gqa_attn_get_device_error(stream=stream) == 0
     nbytes = int(sl.sum()) * shape.H_kv * shape.d * 2 + 2 * shape.B * shape.H_q * shape.d * 2 + 4 * shape.B
     ach = nbytes / (ms * 1e-3) / 1e9
-    out["decode_fp8_b64"] = {
+    kernel = f"decode_kernel<128,5,1,128,{1 if kind == 'int8' else 0}>"
+    out[f"decode_{kind}_b64"] = {
         "ms": round(ms, 6), "value": round(ach, 2), "unit": "GB/s",
         "shape": {"B": shape.B, "H_q": shape.H_q, "H_kv": shape.H_kv, "max_len": shape.max_len,
-                  "d": shape.d, "sum_seqlens": int(sl.sum()), "cache": "e4m3, per-head scales"},
+                  "d": shape.d, "sum_seqlens": int(sl.sum()),
+                  "cache": ("e4m3" if kind == "fp8" else "int8") + ", per-head scales"},
         "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
         "l2": f"{copies} rotating copies",
         "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                 "decode_kernel<128,5,1,128> (fp8 cache)",
+                                 f"{kernel} ({kind} cache)",
                                  recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
-                                                  "decode_kernel<128,5,1,128>"))}
+                                                  kernel))}
     del bufs, o
     torch.cuda.empty_cache()
 
@@ -710,9 +717,9 @@ def run_ours(args):
             "ms": round(dec_ms, 6),
             "roofline": roofline_obj(
                 "hbm", dec_ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                "decode_kernel<128,5,0,128> (persistent split-KV + in-kernel merge)",
+                "decode_kernel<128,5,0,128,0> (persistent split-KV + in-kernel merge)",
                 recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
-                                 "decode_kernel<128,5,0,128>")),
+                                 "decode_kernel<128,5,0,128,0>")),
             "e2e": {"value": round(dec_bytes / (pipe_dec * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d_dec, "d2h_bytes_per_step": d2h_dec,
                     "mode": E2E_MODE,
@@ -862,7 +869,7 @@ def main(argv=None):
                     help="skip the per-workload blocks after the step (profiling runs)")
     ap.add_argument("--configs", default="",
                     help="comma-separated groups of per-workload blocks to run (sweep, long, "
-                         "backward, decode, decode_fp8; profiling runs); default all")
+                         "backward, decode, decode_fp8, decode_int8; profiling runs); default all")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

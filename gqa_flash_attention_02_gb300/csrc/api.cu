@@ -584,10 +584,13 @@ int gqa_attn_bwd(const void *q, const void *k, const void *v, const void *o, con
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 
-int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
-                        const float *k_scale, const float *v_scale, const int *seqlens, void *o,
-                        float *lse, int B, int H_q, int H_kv, int max_len, int d, float scale,
-                        cudaStream_t stream) {
+namespace {
+// Decode against a one-byte cache (e4m3 or int8 codes, per-K/V-head scales):
+// checks, workspace, maps, launch.
+int decode_byte_cache(bool int8, const void *q, const void *k_cache, const void *v_cache,
+                      const float *k_scale, const float *v_scale, const int *seqlens, void *o,
+                      float *lse, int B, int H_q, int H_kv, int max_len, int d, float scale,
+                      cudaStream_t stream) {
   int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
   if (rc != GQA_OK) return rc;
   if (!k_scale || !v_scale || (reinterpret_cast<uintptr_t>(k_scale) & 3u) != 0 ||
@@ -607,13 +610,32 @@ int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
   CUtensorMap tq, tk, tv;
   if (!encode_bf16_3d(&tq, q, d, static_cast<long>(B) * H_q, 1, kDecodeHeads) ||
       !encode_u8_3d(&tk, k_cache, d, max_len, static_cast<long>(B) * H_kv, d <= 64 ? 64 : 128,
-                    kDecodeFp8Unit) ||
+                    kDecodeByteUnit) ||
       !encode_u8_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, d <= 64 ? 64 : 128,
-                    kDecodeFp8Unit))
+                    kDecodeByteUnit))
     return cuda_fail(cudaErrorInvalidValue);
-  e = launch_decode_fp8(tq, tk, tv, q, seqlens, o, lse, ws->partials, ws->counters, B, H_q, H_kv,
-                        max_len, d, scale, k_scale, v_scale, grid, ws->ctl + kCtlErr, stream);
+  e = (int8 ? launch_decode_int8 : launch_decode_fp8)(tq, tk, tv, q, seqlens, o, lse, ws->partials,
+                                                      ws->counters, B, H_q, H_kv, max_len, d, scale,
+                                                      k_scale, v_scale, grid, ws->ctl + kCtlErr,
+                                                      stream);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
+}
+}  // namespace
+
+int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
+                        const float *k_scale, const float *v_scale, const int *seqlens, void *o,
+                        float *lse, int B, int H_q, int H_kv, int max_len, int d, float scale,
+                        cudaStream_t stream) {
+  return decode_byte_cache(false, q, k_cache, v_cache, k_scale, v_scale, seqlens, o, lse, B, H_q,
+                           H_kv, max_len, d, scale, stream);
+}
+
+int gqa_attn_decode_int8(const void *q, const void *k_cache, const void *v_cache,
+                         const float *k_scale, const float *v_scale, const int *seqlens, void *o,
+                         float *lse, int B, int H_q, int H_kv, int max_len, int d, float scale,
+                         cudaStream_t stream) {
+  return decode_byte_cache(true, q, k_cache, v_cache, k_scale, v_scale, seqlens, o, lse, B, H_q,
+                           H_kv, max_len, d, scale, stream);
 }
 
 const char *gqa_attn_status_string(int status) {

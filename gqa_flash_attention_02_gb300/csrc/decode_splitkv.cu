@@ -58,8 +58,8 @@ constexpr int kDimSplitOf = D == 256 ? 2 : 1;
 // of K and of V at d = 128 and 256 alike, and each MMA warp's share of a
 // stage's rows holds its accumulator fragments when it hands a run to the
 // epilogue warp.
-template <int D, bool kFp8>
-constexpr int kSubFor = kFp8 ? 128 : 64 / kDimSplitOf<D>;
+template <int D, bool kByte>
+constexpr int kSubFor = kByte ? 128 : 64 / kDimSplitOf<D>;
 constexpr int kHeads = kDecodeHeads;  // query heads per plane (mma M)
 // Fewest units a CTA takes: fewer, longer runs (each run ends in a merge
 // step and a plane spans at most nsub / kMinUnits + 2 CTAs); no CTA range
@@ -127,8 +127,26 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   return r;
 }
 
-// An f16 pair holding e4m3 values as a bf16 pair, exactly (3 significant
-// bits and exponents within both formats' ranges).
+// Two one-byte cache codes (the low 16 bits of v, low byte first) widened
+// to an f16 pair, exactly. e4m3: the conversion instruction. int8: the byte
+// with its sign bit flipped (x + 128, in 0..255) becomes the low mantissa
+// bits of an f16 of exponent 10 (unit spacing on [1024, 2048)), i.e. the
+// value 1152 + x, and subtracting 1152 leaves x.
+template <bool kI8>
+__device__ __forceinline__ uint32_t byte2_to_f16x2(uint32_t v) {
+  if constexpr (kI8) {
+    const uint32_t r = __byte_perm(v, 0u, 0x4140u) ^ 0x64806480u;
+    uint32_t out;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(out) : "r"(r), "r"(0x64806480u));
+    return out;
+  } else {
+    return e4m3x2_to_f16x2(static_cast<uint16_t>(v & 0xffffu));
+  }
+}
+
+// An f16 pair holding one-byte cache values (e4m3, or integers in
+// [-128, 127]) as a bf16 pair, exactly (at most 8 significant bits and
+// exponents within both formats' ranges).
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
   const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
   return pack_bf16x2(f.x, f.y);
@@ -144,11 +162,11 @@ __device__ __forceinline__ void mma_warps_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kMmaWarps) : "memory");
 }
 
-template <int D, int NSTG, bool kFp8>
+template <int D, int NSTG, bool kByte>
 struct DecodeSmem {
-  static constexpr int kSub = kSubFor<D, kFp8>;
+  static constexpr int kSub = kSubFor<D, kByte>;
   static constexpr int kDimSplit = kDimSplitOf<D>;
-  static constexpr int kTile = kSub * D * (kFp8 ? 1 : 2);  // one K or V unit
+  static constexpr int kTile = kSub * D * (kByte ? 1 : 2);  // one K or V unit
   static constexpr int kQTile = kHeads * D * 2;  // the plane's 16 query rows
   static constexpr int kStage = 2 * kTile + kQTile;
   static constexpr int kRingBytes = NSTG * kStage;
@@ -168,7 +186,7 @@ struct DecodeSmem {
   // its row group in its columns of the stage (16 K and 16 V rows: 2 D /
   // kDimSplit bytes per lane) and its (m, l) in the stage's side buffer.
   static_assert(32 * (D / 8 / kDimSplit) * 4 * 4 ==
-                    2 * (kSub * kDimSplit / kMmaWarps) * (D / kDimSplit) * (kFp8 ? 1 : 2),
+                    2 * (kSub * kDimSplit / kMmaWarps) * (D / kDimSplit) * (kByte ? 1 : 2),
                 "fragments fill the warp's rows");
   static constexpr int kOffML = kRingBytes;                  // [NSTG][4 warps][32 lanes] float4
   static constexpr int kOffEp = kOffML + NSTG * kMmaWarps * 32 * 16;  // epilogue's merged state
@@ -262,7 +280,7 @@ __device__ __forceinline__ void merge_row(float &m, float &l, float m2, float l2
 // log-sum-exp. Every item's arithmetic is the same whichever CTA or
 // warp runs it, so the result does not depend on who merges. kBatch parts'
 // loads are in flight together.
-template <int D, bool kFp8, int kItems, int kBatch, typename SelfFn>
+template <int D, bool kByte, int kItems, int kBatch, typename SelfFn>
 __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int jself, SelfFn self,
                                             int Gh, __nv_bfloat16 *o_plane, float *lse_plane,
                                             int t, int nt, float v_mul, int od) {
@@ -319,7 +337,7 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
       if (it < items) {
         const int h = it / kQuads, q4 = it % kQuads;
         const float il = v_mul / Lr[k];
-        if constexpr (kFp8) {
+        if constexpr (kByte) {
           // fragment columns 4q4 .. 4q4+3 are columns 4(q4 % 2) .. +3 of
           // n-tile q4 / 2, i.e. dims 16 (t / 2) + (t % 2) + 2 n (see write_o_row)
           const int t = q4 >> 1, base = 16 * (t >> 1) + (t & 1) + 8 * (q4 & 1);
@@ -348,10 +366,10 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
 // 16-dim chunk ch and n-tile 2ch + 1 its odd dims (the order P.V produces
 // them in), so the lane's four values are dims 16ch + 2cc .. 16ch + 2cc + 3.
 // (bf16 cache at d = 256: the NTW n-tiles of one warp's columns from col0.)
-template <int D, bool kFp8, int NTW = D / 8>
+template <int D, bool kByte, int NTW = D / 8>
 __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)[NTW][4], int e0,
                                             int cc, float il, int od, int col0 = 0) {
-  if constexpr (kFp8) {
+  if constexpr (kByte) {
 #pragma unroll
     for (int ch = 0; ch < D / 16; ++ch)
       if (16 * ch < od)  // 16-dim chunks past the head dim are padding
@@ -376,16 +394,16 @@ __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)
 // has row group r = w % 2 and column half h = w / 2: rows [16r, 16r+16) of
 // K panels 2h, 2h+1, then of the same V panels (its 16 n-tiles; the K rows
 // are free once both warps of the group have computed their S).
-template <int D, bool kFp8>
+template <int D, bool kByte>
 __device__ __forceinline__ int frag_slot(int w, int t) {
   constexpr int NT = D / 8;
-  constexpr int kSub = kSubFor<D, kFp8>;
+  constexpr int kSub = kSubFor<D, kByte>;
   if constexpr (D == 256) {
     constexpr int kRowGroups = kMmaWarps / kDimSplitOf<D>;
     const int c = t >> 2;  // 2 KB chunk: K (c < 2) or V panel 2h + (c & 1)
     const int panel = (c >> 1) * (D / 64) + (w / kRowGroups) * 2 + (c & 1);
     return panel * kSub * 8 + (w % kRowGroups) * 16 * 8 + (t & 3) * 32;
-  } else if constexpr (kFp8) {
+  } else if constexpr (kByte) {
     constexpr int kRowsF4 = (kSub / kMmaWarps) * D / 16;  // float4 of a warp's rows of one tile
     return (t < NT / 2 ? 0 : kSub * D / 16) + w * kRowsF4 + (t % (NT / 2)) * 32;
   } else {
@@ -395,11 +413,11 @@ __device__ __forceinline__ int frag_slot(int w, int t) {
 
 // OD: the head dim, O's row stride and the columns stored (<= D; the TMA
 // boxes read zeros past it, as for the prefill's padded head dims).
-template <int D, int NSTG, bool kFp8, int OD>
+template <int D, int NSTG, bool kByte, int OD, bool kI8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const DecodeParams prm) {
-  using L = DecodeSmem<D, NSTG, kFp8>;
+  using L = DecodeSmem<D, NSTG, kByte>;
   constexpr int kSub = L::kSub;
   constexpr int kDimSplit = L::kDimSplit;    // MMA warps per row group
   constexpr int kRowGroups = kMmaWarps / kDimSplit;
@@ -587,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int plane_kv = p.b * prm.H_kv + h_kv;
         const uint32_t dst = s_base + st * L::kStage;
         mbar_arrive_expect_tx(full + 8 * st, L::kStage);
-        if constexpr (kFp8) {
+        if constexpr (kByte) {
           // one box of kSub rows x D bytes each (unswizzled)
           tma_load_3d(dst, &tm_k, full + 8 * st, 0, p.s * kSub, plane_kv);
           tma_load_3d(dst + L::kTile, &tm_v, full + 8 * st, 0, p.s * kSub, plane_kv);
@@ -660,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           merge_row(m_hi, l_hi, ml.y, ml.w, w1h, w2h);
 #pragma unroll
           for (int t = 0; t < NTW; ++t) {
-            const float4 v = frag[frag_slot<D, kFp8>(w, t)];
+            const float4 v = frag[frag_slot<D, kByte>(w, t)];
             A[t][0] = fmaf(w1l, A[t][0], w2l * v.x);
             A[t][1] = fmaf(w1l, A[t][1], w2l * v.y);
             A[t][2] = fmaf(w1h, A[t][2], w2h * v.z);
@@ -680,10 +698,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
         if (!split) {
           // the run is the whole plane: write O / l
-          const float vm = kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
+          const float vm = kByte ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f;
           const float il = vm / l_lo, ih = vm / l_hi;
-          if (r_lo < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_lo * OD, A, 0, cc, il, OD, h * DW);
-          if (r_hi < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_hi * OD, A, 2, cc, ih, OD, h * DW);
+          if (r_lo < Gh) write_o_row<D, kByte, NTW>(o_plane + r_lo * OD, A, 0, cc, il, OD, h * DW);
+          if (r_hi < Gh) write_o_row<D, kByte, NTW>(o_plane + r_hi * OD, A, 2, cc, ih, OD, h * DW);
           if (h == 0 && lse_plane != nullptr && (lane & 3) == 0) {
             // log-sum-exp per head (m, l in log2 units of scale * q.k)
             if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -735,9 +753,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           m = sm[h];
           l = sl[h];
         };
-        merge_parts<D, kFp8, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+        merge_parts<D, kByte, 6, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                              c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, lane, 32,
-                             kFp8 ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f, OD);
+                             kByte ? __ldg(prm.v_scale + (plane % planes_per_b) / prm.nhg) : 1.f, OD);
         // re-arm for the next launch (every other count of the plane was
         // observed before this store)
         if (lane == 0) st_relaxed_gpu(prm.counters + plane, 0);
@@ -795,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       counter_seen2 = ld_relaxed_gpu(prm.counters + b * planes_per_b + pib);  // a later look
     const int rows_here = min(kSub, len - s * kSub);  // valid rows in this unit
     // fp8 cache: the K/V head's scales (K's folds into the exponent scale)
-    const float sl2 = kFp8 ? prm.scale_log2 * __ldg(prm.k_scale + h_kv) : prm.scale_log2;
+    const float sl2 = kByte ? prm.scale_log2 * __ldg(prm.k_scale + h_kv) : prm.scale_log2;
 #pragma unroll 1
     for (int grp = 0; grp < kRows / 16; ++grp) {
     const int r0 = wrow + 16 * grp;  // first row of this 16-row group in the unit
@@ -803,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t qt = kt + 2 * L::kTile;
     const bool lo_ok = (lane >> 2) < Gh, hi_ok = (lane >> 2) + 8 < Gh;
-    if constexpr (kFp8) {
+    if constexpr (kByte) {
       // The fp8 K rows are read as 8x8 matrices of 16-bit pairs: lane l gets
       // key row l/4 of a matrix and bytes 4(l%4)..+3, the dims 4t..4t+3 (t =
       // l%4) of a 16-dim chunk. Widened to two bf16 pairs they are the B
@@ -832,10 +850,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           qa[1] = hi_ok ? hi.x : 0u;
           qa[3] = hi_ok ? hi.y : 0u;
           const uint32_t k0 = r[h], k1 = r[2 + h];  // keys 0-7, keys 8-15
-          mma_bf16(s0, qa, f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k0 & 0xffffu))),
-                   f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k0 >> 16))));
-          mma_bf16(s1, qa, f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k1 & 0xffffu))),
-                   f16x2_to_bf16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(k1 >> 16))));
+          mma_bf16(s0, qa, f16x2_to_bf16x2(byte2_to_f16x2<kI8>(k0)),
+                   f16x2_to_bf16x2(byte2_to_f16x2<kI8>(k0 >> 16)));
+          mma_bf16(s1, qa, f16x2_to_bf16x2(byte2_to_f16x2<kI8>(k1)),
+                   f16x2_to_bf16x2(byte2_to_f16x2<kI8>(k1 >> 16)));
         }
       }
     } else {
@@ -897,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       acc[t][3] *= a_hi;
     }
     // ---- O += P V (V rows = k, d = n): transposed ldmatrix of 8x8 blocks
-    if constexpr (kFp8) {
+    if constexpr (kByte) {
       // P as f16 (16 heads x 16 keys). The fp8 V rows are read transposed
       // as 16-bit pairs: lane l gets keys 2t, 2t+1 of a matrix at bytes
       // 2c, 2c+1 (c = l/4), i.e. two dims of a 16-dim chunk for two keys;
@@ -925,10 +943,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           lo = (dead0 ? 0u : (lo & 0x0000ffffu)) | (dead1 ? 0u : (lo & 0xffff0000u));
           hi = (dead8 ? 0u : (hi & 0x0000ffffu)) | (dead9 ? 0u : (hi & 0xffff0000u));
           const uint32_t plo = __byte_perm(lo, 0, 0x3120), phi = __byte_perm(hi, 0, 0x3120);
-          mma_f16(acc[2 * ch], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(plo & 0xffffu)),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(phi & 0xffffu)));
-          mma_f16(acc[2 * ch + 1], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(plo >> 16)),
-                  e4m3x2_to_f16x2(static_cast<uint16_t>(phi >> 16)));
+          mma_f16(acc[2 * ch], pa, byte2_to_f16x2<kI8>(plo), byte2_to_f16x2<kI8>(phi));
+          mma_f16(acc[2 * ch + 1], pa, byte2_to_f16x2<kI8>(plo >> 16), byte2_to_f16x2<kI8>(phi >> 16));
         }
       }
     } else {
@@ -996,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       float4 *rows = reinterpret_cast<float4 *>(smem + st * L::kStage) + lane;
 #pragma unroll
       for (int t = 0; t < NTW; ++t)
-        rows[frag_slot<D, kFp8>(warp, t)] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+        rows[frag_slot<D, kByte>(warp, t)] = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
       side_ml[(st * kMmaWarps + warp) * 32 + lane] = make_float4(m_lo, m_hi, l_lo, l_hi);
       if (warp == 0 && lane == 0) {
         int *qe = queue + 16 * qk;
@@ -1074,10 +1090,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int r_lo = lane >> 2, r_hi = r_lo + 8, cc = 2 * (lane & 3);
       if (!split) {
         // this run is the whole plane: write O / l
-        const float vm = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
+        const float vm = kByte ? __ldg(prm.v_scale + h_kv) : 1.f;
         const float il = vm / l_lo, ih = vm / l_hi;
-        if (r_lo < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_lo * OD, acc, 0, cc, il, OD, whalf * DW);
-        if (r_hi < Gh) write_o_row<D, kFp8, NTW>(o_plane + r_hi * OD, acc, 2, cc, ih, OD, whalf * DW);
+        if (r_lo < Gh) write_o_row<D, kByte, NTW>(o_plane + r_lo * OD, acc, 0, cc, il, OD, whalf * DW);
+        if (r_hi < Gh) write_o_row<D, kByte, NTW>(o_plane + r_hi * OD, acc, 2, cc, ih, OD, whalf * DW);
         if (whalf == 0 && lse_plane != nullptr && (lane & 3) == 0) {
           // log-sum-exp per head (m, l in log2 units of scale * q.k)
           if (r_lo < Gh) lse_plane[r_lo] = (m_lo + log2f(l_lo)) * 0.6931471805599453f;
@@ -1118,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       fin.run_units = run_units;
       fin.nsub = nsub;
       fin.Gh = Gh;
-      fin.vmul = kFp8 ? __ldg(prm.v_scale + h_kv) : 1.f;
+      fin.vmul = kByte ? __ldg(prm.v_scale + h_kv) : 1.f;
       fin.o_plane = o_plane;
       fin.lse_plane = lse_plane;
       fin.state = state;
@@ -1169,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         m = st_m[h];
         l = st_l[h];
       };
-      merge_parts<D, kFp8, kMergeItems, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
+      merge_parts<D, kByte, kMergeItems, 4>(prm.part + static_cast<size_t>(c_first + plane) * kSlot,
                               c_last - c_first + 1, c - c_first, self, Gh, o_plane, lse_plane, tid,
                               32 * kMmaWarps, fin.vmul, OD);
       // re-arm for the next launch (every other count of the plane was
@@ -1185,20 +1201,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (lane == 0) mbar_arrive(ep_full + 8 * qk);
 }
 
-template <int D, int NSTG, bool kFp8, int OD>
+template <int D, int NSTG, bool kByte, int OD, bool kI8 = false>
 cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                             float *lse, float *partials, int *counters, int B, int H_q, int H_kv,
                             int max_len, float scale, int grid, int *err_word,
                             const float *k_scale, const float *v_scale, cudaStream_t stream) {
-  using L = DecodeSmem<D, NSTG, kFp8>;
+  using L = DecodeSmem<D, NSTG, kByte>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory");
   static unsigned configured = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !(configured & (1u << dev))) {
-    e = cudaFuncSetAttribute(decode_kernel<D, NSTG, kFp8, OD>,
+    e = cudaFuncSetAttribute(decode_kernel<D, NSTG, kByte, OD, kI8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured |= 1u << dev;
@@ -1219,7 +1235,7 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   prm.max_len = max_len;
   prm.nhg = decode_head_groups(H_q, H_kv);
   prm.scale_log2 = scale * 1.4426950408889634f;
-  return launch_programmatic(decode_kernel<D, NSTG, kFp8, OD>, grid, kThreads, L::kAlloc, stream, tm_q,
+  return launch_programmatic(decode_kernel<D, NSTG, kByte, OD, kI8>, grid, kThreads, L::kAlloc, stream, tm_q,
                              tm_k, tm_v, prm);
 }
 
@@ -1280,25 +1296,46 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
 #undef GQA_DECODE_BF16
 }
 
+namespace {
+template <bool kI8>
+cudaError_t launch_decode_byte(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                               const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
+                               float *lse, float *partials, int *counters, int B, int H_q,
+                               int H_kv, int max_len, int d, float scale, const float *k_scale,
+                               const float *v_scale, int grid, int *err_word, cudaStream_t stream) {
+  if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
+  // head dims 32 and 96 run the 64- and 128-column kernels on zero-padded boxes
+#define GQA_DECODE_BYTE(D_, NSTG_, OD_)                                                       \
+  launch_decode_d<D_, NSTG_, true, OD_, kI8>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,    \
+                                             counters, B, H_q, H_kv, max_len, scale, grid,      \
+                                             err_word, k_scale, v_scale, stream)
+  switch (d) {
+    case 32: return GQA_DECODE_BYTE(64, 8, 32);
+    case 64: return GQA_DECODE_BYTE(64, 8, 64);
+    case 96: return GQA_DECODE_BYTE(128, 5, 96);
+    case 128: return GQA_DECODE_BYTE(128, 5, 128);
+    default: return cudaErrorInvalidValue;
+  }
+#undef GQA_DECODE_BYTE
+}
+}  // namespace
+
 cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                               const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                               float *lse, float *partials, int *counters, int B, int H_q,
                               int H_kv, int max_len, int d, float scale, const float *k_scale,
                               const float *v_scale, int grid, int *err_word, cudaStream_t stream) {
-  if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
-  // head dims 32 and 96 run the 64- and 128-column kernels on zero-padded boxes
-#define GQA_DECODE_FP8(D_, NSTG_, OD_)                                                     \
-  launch_decode_d<D_, NSTG_, true, OD_>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,      \
-                                        counters, B, H_q, H_kv, max_len, scale, grid, err_word, \
-                                        k_scale, v_scale, stream)
-  switch (d) {
-    case 32: return GQA_DECODE_FP8(64, 8, 32);
-    case 64: return GQA_DECODE_FP8(64, 8, 64);
-    case 96: return GQA_DECODE_FP8(128, 5, 96);
-    case 128: return GQA_DECODE_FP8(128, 5, 128);
-    default: return cudaErrorInvalidValue;
-  }
-#undef GQA_DECODE_FP8
+  return launch_decode_byte<false>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters, B, H_q,
+                                   H_kv, max_len, d, scale, k_scale, v_scale, grid, err_word, stream);
+}
+
+cudaError_t launch_decode_int8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                               const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
+                               float *lse, float *partials, int *counters, int B, int H_q,
+                               int H_kv, int max_len, int d, float scale, const float *k_scale,
+                               const float *v_scale, int grid, int *err_word, cudaStream_t stream) {
+  return launch_decode_byte<true>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials, counters, B, H_q,
+                                  H_kv, max_len, d, scale, k_scale, v_scale, grid, err_word, stream);
 }
 
 // ---------------------------------------------------------------- self-test

@@ -299,16 +299,22 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                int H_kv, int max_len, int d, float scale, int grid,
                                int *err_word, cudaStream_t stream);
 
-// The same decode over an fp8 (e4m3) cache: tm_k / tm_v view the caches as
-// [B * H_kv][max_len][d] bytes with unswizzled boxes of d bytes x 128 rows
-// (kDecodeFp8Unit); k_scale / v_scale are the per-K/V-head dequantisation
-// scales (device fp32 [H_kv]).
-constexpr int kDecodeFp8Unit = 128;
+// The same decode over a one-byte cache, fp8 (e4m3) or int8 codes: tm_k /
+// tm_v view the caches as [B * H_kv][max_len][d] bytes with boxes of 64 (d
+// <= 64) or 128 bytes x 128 rows (kDecodeByteUnit), swizzled by the box
+// width; k_scale / v_scale are the per-K/V-head dequantisation scales
+// (device fp32 [H_kv]).
+constexpr int kDecodeByteUnit = 128;
 cudaError_t launch_decode_fp8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                               const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                               float *lse, float *partials, int *counters, int B, int H_q,
                               int H_kv, int max_len, int d, float scale, const float *k_scale,
                               const float *v_scale, int grid, int *err_word, cudaStream_t stream);
+cudaError_t launch_decode_int8(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                               const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
+                               float *lse, float *partials, int *counters, int B, int H_q,
+                               int H_kv, int max_len, int d, float scale, const float *k_scale,
+                               const float *v_scale, int grid, int *err_word, cudaStream_t stream);
 
 cudaError_t launch_wait_timeout_selftest(int timeout_us, int *err_word, cudaStream_t stream);
 

@@ -32,7 +32,7 @@ EXPORTED = [
     "gqa_attn_prefill_plan", "gqa_attn_selftest_wait_timeout", "gqa_attn_shutdown",
     "gqa_attn_decode_noalloc", "gqa_attn_fwd_lse", "gqa_attn_decode_lse",
     "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse", "gqa_attn_fwd_bshd", "gqa_attn_bwd",
-    "gqa_attn_decode_fp8", "gqa_attn_fwd_strided",
+    "gqa_attn_decode_fp8", "gqa_attn_fwd_strided", "gqa_attn_decode_int8",
 ]
 
 
@@ -91,6 +91,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.gqa_attn_bwd.restype = _i
             lib.gqa_attn_decode_fp8.argtypes = [_vp] * 8 + [_i] * 5 + [_f, _vp]
             lib.gqa_attn_decode_fp8.restype = _i
+            lib.gqa_attn_decode_int8.argtypes = [_vp] * 8 + [_i] * 5 + [_f, _vp]
+            lib.gqa_attn_decode_int8.restype = _i
             _ll = ctypes.c_longlong
             lib.gqa_attn_fwd_strided.argtypes = ([_vp, _ll, _ll, _ll] * 4 + [_i] * 7 + [_f, _vp])
             lib.gqa_attn_fwd_strided.restype = _i
@@ -323,11 +325,8 @@ def gqa_attn_decode_noalloc(q, k_cache, v_cache, seqlens, o, scale=None, stream=
                    scale, None, stream)
 
 
-def gqa_attn_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seqlens, o=None, lse=None,
-                        scale=None, stream=None):
-    """Decode against an fp8 (e4m3) cache. q [B,H_q,d] bf16; caches [B,H_kv,max_len,d] of
-    torch.float8_e4m3fn (or uint8 bytes); k_scale, v_scale fp32 [H_kv]; seqlens int32 [B].
-    Returns o [B,H_q,d] bf16 (and fills lse [B,H_q] fp32 when given)."""
+def _decode_byte_cache(entry, dtypes, q, k_cache, v_cache, k_scale, v_scale, seqlens, o, lse,
+                       scale, stream):
     B, H_q, d = q.shape
     _, H_kv, max_len, _ = k_cache.shape
     if o is None:
@@ -335,9 +334,9 @@ def gqa_attn_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seqlens, o=None, 
     if scale is None:
         scale = d ** -0.5
     for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
-        if not t.is_cuda or t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) \
-                or t.dim() != 4 or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous 4-d CUDA float8_e4m3fn / uint8 tensor")
+        if not t.is_cuda or t.dtype not in dtypes or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-d CUDA tensor of "
+                             f"{' / '.join(str(x) for x in dtypes)}")
     if tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[0] != B or \
             k_cache.shape[3] != d or tuple(o.shape) != tuple(q.shape) or \
             tuple(seqlens.shape) != (B,) or tuple(k_scale.shape) != (H_kv,) or \
@@ -348,14 +347,33 @@ def gqa_attn_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seqlens, o=None, 
         if tuple(lse.shape) != (B, H_q):
             raise ValueError("lse must be [B, H_q]")
         lse_p = _dev(lse, torch.float32, "lse", 2)
-    rc = load().gqa_attn_decode_fp8(
+    rc = getattr(load(), entry)(
         _dev(q, torch.bfloat16, "q", 3), ctypes.c_void_p(k_cache.data_ptr()),
         ctypes.c_void_p(v_cache.data_ptr()), _dev(k_scale, torch.float32, "k_scale", 1),
         _dev(v_scale, torch.float32, "v_scale", 1), _dev(seqlens, torch.int32, "seqlens", 1),
         _dev(o, torch.bfloat16, "o", 3), lse_p, B, H_q, H_kv, max_len, d, float(scale),
         _stream(stream))
-    _check(rc, "gqa_attn_decode_fp8")
+    _check(rc, entry)
     return o
+
+
+def gqa_attn_decode_fp8(q, k_cache, v_cache, k_scale, v_scale, seqlens, o=None, lse=None,
+                        scale=None, stream=None):
+    """Decode against an fp8 (e4m3) cache. q [B,H_q,d] bf16; caches [B,H_kv,max_len,d] of
+    torch.float8_e4m3fn (or uint8 bytes); k_scale, v_scale fp32 [H_kv]; seqlens int32 [B].
+    Returns o [B,H_q,d] bf16 (and fills lse [B,H_q] fp32 when given)."""
+    dtypes = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t is not None)
+    return _decode_byte_cache("gqa_attn_decode_fp8", dtypes, q, k_cache, v_cache, k_scale,
+                              v_scale, seqlens, o, lse, scale, stream)
+
+
+def gqa_attn_decode_int8(q, k_cache, v_cache, k_scale, v_scale, seqlens, o=None, lse=None,
+                         scale=None, stream=None):
+    """Decode against an int8 cache. q [B,H_q,d] bf16; caches [B,H_kv,max_len,d] torch.int8
+    (two's-complement codes); k_scale, v_scale fp32 [H_kv]; seqlens int32 [B].
+    Returns o [B,H_q,d] bf16 (and fills lse [B,H_q] fp32 when given)."""
+    return _decode_byte_cache("gqa_attn_decode_int8", (torch.int8,), q, k_cache, v_cache,
+                              k_scale, v_scale, seqlens, o, lse, scale, stream)
 
 
 def gqa_attn_decode_f32(q, k_cache, v_cache, seqlens, o=None, scale=None, stream=None):

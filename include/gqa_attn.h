@@ -258,6 +258,27 @@ int gqa_attn_decode_fp8(const void *q, const void *k_cache, const void *v_cache,
                         float scale, cudaStream_t stream);
 
 /*
+ * Decode against an int8 K/V cache: the cache holds one-byte two's-complement
+ * codes (-128 .. 127), and the value a byte stands for is its integer times
+ * the scale of its K/V head:
+ *   K[b][h][j][c] = int8(k_cache[b][h][j][c]) * k_scale[h]   (likewise V)
+ * Arguments, layouts, limits and errors as gqa_attn_decode_fp8 (k_cache,
+ * v_cache: [B][H_kv][max_len][d] bytes, 16-byte aligned; d in {32, 64, 96,
+ * 128}). Same kernel as the fp8 cache; each MMA warp widens its rows
+ * exactly: the byte, sign bit flipped, becomes the low mantissa bits of the
+ * f16 1024, minus 1152 (K then to bf16, V kept in f16).
+ * Pages: microLLM-rocm optimisation log, Experiments 352 and 354 (a
+ * one-byte tensor with an explicit scale, read and widened inside the
+ * decode kernel) and Experiment 065 (the K/V cache narrower than the
+ * arithmetic).
+ */
+int gqa_attn_decode_int8(const void *q, const void *k_cache, const void *v_cache,
+                         const float *k_scale, const float *v_scale, const int *seqlens,
+                         void *o, float *lse,
+                         int B, int H_q, int H_kv, int max_len, int d,
+                         float scale, cudaStream_t stream);
+
+/*
  * Decode in fp32 (q, caches and o are float arrays, layouts as
  * gqa_attn_decode); d in {32, 64, 96, 128}.
  */

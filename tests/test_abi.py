@@ -254,6 +254,31 @@ def test_decode_fp8_validation():
     assert call(max_len=(1 << 20) + 1) == 2
 
 
+def test_decode_int8_validation():
+    """The int8 entry checks what the fp8 one checks."""
+    f = ops.load().gqa_attn_decode_int8
+    SC = ctypes.c_void_p(0x40000)
+    SC_MIS = ctypes.c_void_p(0x40002)
+    ok = dict(B=2, H_q=8, H_kv=2, max_len=256, d=128, scale=0.1)
+
+    def call(q=A, k=A, v=A, ks=SC, vs=SC, sl=SEQ, o=A, lse=None, **kw):
+        a = dict(ok, **kw)
+        return f(q, k, v, ks, vs, sl, o, lse, a["B"], a["H_q"], a["H_kv"], a["max_len"], a["d"],
+                 a["scale"], None)
+
+    assert call(q=None) == 1
+    assert call(vs=None) == 1
+    assert call(ks=SC_MIS) == 1
+    assert call(k=MIS) == 1
+    assert call(lse=SC_MIS) == 1
+    assert call(H_q=6, H_kv=4) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(B=0) == 1
+    assert call(d=48) == 2
+    assert call(d=256) == 2
+    assert call(max_len=(1 << 20) + 1) == 2
+
+
 def test_strided_validation():
     f = ops.load().gqa_attn_fwd_strided
     dims = dict(B=2, H_q=8, H_kv=2, N_q=300, N_kv=300, d=128, causal=1, scale=0.088)
