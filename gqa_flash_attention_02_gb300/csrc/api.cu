@@ -304,7 +304,7 @@ bool d_supported_simt(int d) { return d == 32 || d == 64 || d == 96 || d == 128;
 namespace {
 int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const int *seqlens,
                 void *o, float *lse, int B, int H_q, int H_kv, int max_len, int d, float scale,
-                int chunk_tokens, cudaStream_t stream) {
+                int chunk_tokens, cudaStream_t stream, const int *seqlens_first = nullptr) {
   int rc = check_decode_args(q, k_cache, v_cache, seqlens, o, B, H_q, H_kv, max_len, d, scale);
   if (rc != GQA_OK) return rc;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return GQA_ERR_INVALID_ARG;
@@ -327,7 +327,7 @@ int decode_bf16(const void *q, const void *k_cache, const void *v_cache, const i
       !encode_bf16_3d(&tv, v_cache, d, max_len, static_cast<long>(B) * H_kv, decode_box_rows(d)))
     return cuda_fail(cudaErrorInvalidValue);
   e = launch_decode_bf16(tq, tk, tv, q, seqlens, o, lse, ws->partials, ws->counters, B, H_q, H_kv,
-                         max_len, d, scale, grid, ws->ctl + kCtlErr, stream);
+                         max_len, d, scale, grid, ws->ctl + kCtlErr, stream, seqlens_first);
   return e == cudaSuccess ? GQA_OK : cuda_fail(e);
 }
 }  // namespace
@@ -713,6 +713,17 @@ int gqa_attn_selftest_wait_timeout(int timeout_us, cudaStream_t stream) {
   cudaError_t e = launch_wait_timeout_selftest(timeout_us, ws->ctl + kCtlErr, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   return gqa_attn_get_device_error(stream);
+}
+
+int gqa_attn_selftest_decode_early_lengths(const void *q, const void *k_cache,
+                                           const void *v_cache, const int *seqlens,
+                                           const int *seqlens_early, void *o, float *lse, int B,
+                                           int H_q, int H_kv, int max_len, int d, float scale,
+                                           cudaStream_t stream) {
+  if (seqlens_early == nullptr || (reinterpret_cast<uintptr_t>(seqlens_early) & 3u) != 0)
+    return GQA_ERR_INVALID_ARG;
+  return decode_bf16(q, k_cache, v_cache, seqlens, o, lse, B, H_q, H_kv, max_len, d, scale, 0,
+                     stream, seqlens_early);
 }
 
 void gqa_attn_shutdown(void) {

@@ -204,6 +204,7 @@ struct DecodeSmem {
 struct DecodeParams {
   const __nv_bfloat16 *q;
   const int *seqlens;
+  const int *seqlens_first;  // read before the dependency wait: seqlens (a decoy only in the self-test)
   __nv_bfloat16 *o;
   float *lse;      // [B][H_q] natural-log sum of exp(scale q.k), or null
   float *part;     // [(grid + planes)] slots of O [16][D] (unnormalised), m [16], l [16]
@@ -257,6 +258,56 @@ __device__ __forceinline__ int split_first(const Split &sp, int c) {
 __device__ __forceinline__ int owner_of(int u, const Split &sp) {
   const int t = sp.r * (sp.q + 1);
   return u < t ? u / (sp.q + 1) : sp.r + (u - t) / sp.q;
+}
+
+// Where CTA c starts when B <= 128 (warp-wide; lane holds the lengths of
+// sequences 32k + lane): total units U, effective grid G (every CTA takes at
+// least kMinUnits units), and the CTA's first unit as (sequence sb, plane
+// spib, unit ss of the plane's snsub); sb = B when the CTA has none.
+struct Start {
+  int U, G, sb, spib, ss, snsub;
+};
+
+template <int kSub>
+__device__ __forceinline__ Start locate_start(const DecodeParams &prm, const int (&len)[4],
+                                              int lane, int c, int planes_per_b) {
+  Start st{0, 1, prm.B, 0, 0, 1};
+  int n_first[4], before_first[4];  // units of sequence 32k + lane and units before it
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int b = 32 * k + lane;
+    const int n = b < prm.B ? units_for<kSub>(prm, len[k]) : 0;
+    const int x = n * planes_per_b;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    n_first[k] = n;
+    before_first[k] = st.U + incl - x;
+    st.U += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  st.G = max(1, min(static_cast<int>(gridDim.x), st.U / kMinUnits));
+  const Split sp{st.U / st.G, st.U % st.G};
+  const int u0 = (c < st.G) ? split_first(sp, c) : st.U;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int b = 32 * k + lane, x = n_first[k] * planes_per_b;
+    const unsigned hit = __ballot_sync(
+        0xffffffffu, b < prm.B && x > 0 && u0 >= before_first[k] && u0 < before_first[k] + x);
+    if (hit && st.sb == prm.B) {
+      const int src = __ffs(hit) - 1;
+      const int bef = __shfl_sync(0xffffffffu, before_first[k], src);
+      const int nn = __shfl_sync(0xffffffffu, n_first[k], src);
+      const int off = u0 - bef;
+      st.sb = 32 * k + src;
+      st.spib = off / nn;
+      st.ss = off % nn;
+      st.snsub = nn;
+    }
+  }
+  return st;
 }
 
 // Merges another (m, l, acc) state into this one for one row: returns the
@@ -454,19 +505,81 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
-  // While the previous grid finishes, warm L2 with the sequence lengths the
-  // prologue reads first (one prefetch per 128-byte line).
-  if (warp == 0)
-    for (int b = 32 * lane; b < prm.B; b += 32 * 32) prefetch_l2(prm.seqlens + b);
+  if (warp == kEpilogueWarp && lane == 0) {
+    for (int s = 0; s < NSTG; ++s) {
+      mbar_init(full + 8 * s, 1);
+      mbar_init(empty + 8 * s, kMmaWarps);
+    }
+    for (int e = 0; e < NSTG; ++e) mbar_init(ep_full + 8 * e, kMmaWarps);
+    fence_barrier_init();
+  }
+  // While the previous grid finishes (it may still be writing the inputs),
+  // warp 0 works out the CTA's start from a first read of the lengths (B <=
+  // 128) and prefetches the CTA's first two units of K and V into L2. The
+  // start stands only if a read after the dependency wait finds the same
+  // lengths; a prefetch never changes what is read.
+  const bool few_b = prm.B <= 128;
+  int spec_len[4];
+  Start spec{};
+  if (warp == 0) {
+    if (few_b) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int b = 32 * k + lane;
+        spec_len[k] = b < prm.B ? __ldcg(prm.seqlens_first + b) : 0;
+      }
+      spec = locate_start<kSub>(prm, spec_len, lane, c, planes_per_b);
+      if (lane == 0 && c < spec.G && spec.sb < prm.B) {
+        const int plane_kv = spec.sb * prm.H_kv + spec.spib / prm.nhg;
+        for (int s = spec.ss; s < spec.ss + 2 && s < spec.snsub; ++s) {
+#pragma unroll
+          for (int q = 0; q < (kByte ? 1 : D / 64); ++q) {
+            tma_prefetch_l2_3d(&tm_k, q * 64, s * kSub, plane_kv);
+            tma_prefetch_l2_3d(&tm_v, q * 64, s * kSub, plane_kv);
+          }
+        }
+      }
+    } else {
+      for (int b = 32 * lane; b < prm.B; b += 32 * 32) prefetch_l2(prm.seqlens + b);
+    }
+  }
   // Global reads (inputs, partials, counters) come after the previous grid
   // of the stream has completed; the next grid may start setting up.
   grid_dependency_wait();
   grid_launch_dependents();
-  // ---- warp 0: lengths (128 per pass, loads in flight together, the first
-  // kLenCache kept in shared memory), total units and this CTA's start
-  if (warp == 0) {
+  // ---- warp 0 (B <= 128): the lengths again, and the start unless they changed
+  if (warp == 0 && few_b) {
+    int len[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int b = 32 * k + lane;
+      len[k] = b < prm.B ? __ldcg(prm.seqlens + b) : 0;
+    }
+    const bool same = __all_sync(0xffffffffu, len[0] == spec_len[0] && len[1] == spec_len[1] &&
+                                                  len[2] == spec_len[2] && len[3] == spec_len[3]);
+    const Start st = same ? spec : locate_start<kSub>(prm, len, lane, c, planes_per_b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int b = 32 * k + lane;
+      if (b < prm.B && b < kLenCache) s_len[b] = len[k];
+      if (b < prm.B && (len[k] < 0 || len[k] > prm.max_len) && c == 0)
+        record_error(prm.err_word, kErrBadSeqlen);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      info[0] = st.U;
+      info[1] = st.sb;
+      info[2] = st.spib;
+      info[3] = st.ss;
+      info[5] = st.G;
+      info[6] = st.snsub;
+    }
+  }
+  // ---- warp 0 (B > 128): lengths (128 per pass, loads in flight together,
+  // the first kLenCache kept in shared memory), total units and this CTA's
+  // start
+  if (warp == 0 && !few_b) {
     int U = 0;
-    int n_first[4], before_first[4];  // units and units before, sequences 32k + lane < 128
     for (int b0 = 0; b0 < prm.B; b0 += 128) {
       int len[4];
 #pragma unroll
@@ -488,10 +601,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           const int y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        if (b0 == 0) {
-          n_first[k] = n;
-          before_first[k] = U + incl - x;
-        }
         U += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
@@ -512,15 +621,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       ss = off % nn;
       snsub = nn;
     };
-    if (prm.B <= 128) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int b = 32 * k + lane, x = n_first[k] * planes_per_b;
-        const unsigned hit = __ballot_sync(
-            0xffffffffu, b < prm.B && x > 0 && u0 >= before_first[k] && u0 < before_first[k] + x);
-        if (hit && sb == prm.B) found(hit, 32 * k, before_first[k], n_first[k]);
-      }
-    } else {
+    {
       int cum = 0;
       for (int b0 = 0; b0 < prm.B && sb == prm.B; b0 += 32) {
         const int b = b0 + lane;
@@ -546,12 +647,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       info[3] = ss;
       info[5] = G;
       info[6] = snsub;
-      for (int s = 0; s < NSTG; ++s) {
-        mbar_init(full + 8 * s, 1);
-        mbar_init(empty + 8 * s, kMmaWarps);
-      }
-      for (int e = 0; e < NSTG; ++e) mbar_init(ep_full + 8 * e, kMmaWarps);
-      fence_barrier_init();
     }
   }
   __syncthreads();
@@ -1206,7 +1301,8 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                             const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                             float *lse, float *partials, int *counters, int B, int H_q, int H_kv,
                             int max_len, float scale, int grid, int *err_word,
-                            const float *k_scale, const float *v_scale, cudaStream_t stream) {
+                            const float *k_scale, const float *v_scale, cudaStream_t stream,
+                            const int *seqlens_first = nullptr) {
   using L = DecodeSmem<D, NSTG, kByte>;
   static_assert(L::kAlloc <= 227 * 1024, "shared memory");
   static unsigned configured = 0;
@@ -1222,6 +1318,7 @@ cudaError_t launch_decode_d(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
   DecodeParams prm;
   prm.q = static_cast<const __nv_bfloat16 *>(q);
   prm.seqlens = seqlens;
+  prm.seqlens_first = seqlens_first != nullptr ? seqlens_first : seqlens;
   prm.o = static_cast<__nv_bfloat16 *>(o);
   prm.lse = lse;
   prm.part = partials;
@@ -1278,13 +1375,13 @@ cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                                float *lse, float *partials, int *counters, int B, int H_q,
                                int H_kv, int max_len, int d, float scale, int grid,
-                               int *err_word, cudaStream_t stream) {
+                               int *err_word, cudaStream_t stream, const int *seqlens_first) {
   if (grid <= 0 || !decode_units_fit(B, H_q, H_kv, max_len)) return cudaErrorInvalidValue;
   // head dims 32 and 96 run the 64- and 128-column kernels on zero-padded boxes
 #define GQA_DECODE_BF16(D_, NSTG_, OD_)                                                      \
   launch_decode_d<D_, NSTG_, false, OD_>(tm_q, tm_k, tm_v, q, seqlens, o, lse, partials,       \
                                          counters, B, H_q, H_kv, max_len, scale, grid, err_word, \
-                                         nullptr, nullptr, stream)
+                                         nullptr, nullptr, stream, seqlens_first)
   switch (d) {
     case 32: return GQA_DECODE_BF16(64, 8, 32);
     case 64: return GQA_DECODE_BF16(64, 8, 64);

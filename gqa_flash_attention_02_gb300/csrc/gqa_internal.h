@@ -292,12 +292,15 @@ int decode_grid(int B, int H_q, int H_kv, int max_len, int d, int num_sms, int c
 // 32-bit unit indices.
 bool decode_units_fit(int B, int H_q, int H_kv, int max_len);
 // tm_q views q as [1][B * H_q][d] with 16-row boxes; tm_k / tm_v view the
-// caches as [B * H_kv][max_len][d] with 64-row boxes.
+// caches as [B * H_kv][max_len][d] with 64-row boxes. seqlens_first: the
+// lengths read before the grid-dependency wait to start early (null: the
+// same array as seqlens; anything else only in the self-test).
 cudaError_t launch_decode_bf16(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const void *q, const int *seqlens, void *o,
                                float *lse, float *partials, int *counters, int B, int H_q,
                                int H_kv, int max_len, int d, float scale, int grid,
-                               int *err_word, cudaStream_t stream);
+                               int *err_word, cudaStream_t stream,
+                               const int *seqlens_first = nullptr);
 
 // The same decode over a one-byte cache, fp8 (e4m3) or int8 codes: tm_k /
 // tm_v view the caches as [B * H_kv][max_len][d] bytes with boxes of 64 (d

@@ -33,6 +33,7 @@ EXPORTED = [
     "gqa_attn_decode_noalloc", "gqa_attn_fwd_lse", "gqa_attn_decode_lse",
     "gqa_attn_fwd_varlen", "gqa_attn_fwd_varlen_lse", "gqa_attn_fwd_bshd", "gqa_attn_bwd",
     "gqa_attn_decode_fp8", "gqa_attn_fwd_strided", "gqa_attn_decode_int8",
+    "gqa_attn_selftest_decode_early_lengths",
 ]
 
 
@@ -104,6 +105,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.gqa_attn_prefill_plan.restype = _i
             lib.gqa_attn_selftest_wait_timeout.argtypes = [_i, _vp]
             lib.gqa_attn_selftest_wait_timeout.restype = _i
+            lib.gqa_attn_selftest_decode_early_lengths.argtypes = [_vp] * 7 + [_i] * 5 + [_f, _vp]
+            lib.gqa_attn_selftest_decode_early_lengths.restype = _i
             lib.gqa_attn_shutdown.argtypes = []
             lib.gqa_attn_shutdown.restype = None
             _lib = lib
@@ -425,6 +428,31 @@ def gqa_attn_prefill_plan(B, H_q, H_kv, N_q, N_kv, causal):
 
 def gqa_attn_selftest_wait_timeout(timeout_us: int = 1000, stream=None) -> int:
     return load().gqa_attn_selftest_wait_timeout(int(timeout_us), _stream(stream))
+
+
+def gqa_attn_selftest_decode_early_lengths(q, k_cache, v_cache, seqlens, seqlens_early,
+                                           scale=None, stream=None):
+    """gqa_attn_decode_lse with the kernel's pre-wait read of the lengths taken
+    from ``seqlens_early`` (int32 [B] on the device). Returns (o, lse)."""
+    B, H_q, d = q.shape
+    if tuple(seqlens_early.shape) != (B,):
+        raise ValueError("seqlens_early must be [B]")
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    early = _dev(seqlens_early, torch.int32, "seqlens_early", 1)
+    _, H_kv, max_len, _ = k_cache.shape
+    o = torch.empty_like(q)
+    if scale is None:
+        scale = d ** -0.5
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[0] != B or \
+            k_cache.shape[3] != d or tuple(seqlens.shape) != (B,):
+        raise ValueError("shape mismatch between q, caches, seqlens")
+    rc = load().gqa_attn_selftest_decode_early_lengths(
+        _dev(q, torch.bfloat16, "q", 3), _dev(k_cache, torch.bfloat16, "k_cache", 4),
+        _dev(v_cache, torch.bfloat16, "v_cache", 4), _dev(seqlens, torch.int32, "seqlens", 1),
+        early, _dev(o, torch.bfloat16, "o", 3), _dev(lse, torch.float32, "lse", 2), B, H_q, H_kv,
+        max_len, d, float(scale), _stream(stream))
+    _check(rc, "gqa_attn_selftest_decode_early_lengths")
+    return o, lse
 
 
 def gqa_attn_shutdown():

@@ -386,6 +386,24 @@ int gqa_attn_prefill_plan(int B, int H_q, int H_kv, int N_q, int N_kv,
  */
 int gqa_attn_selftest_wait_timeout(int timeout_us, cudaStream_t stream);
 
+/*
+ * Self-test of the decode's early start: gqa_attn_decode_lse, except that
+ * the lengths the kernel reads before its grid-dependency wait (to locate
+ * each CTA's first unit and prefetch it into L2 while the previous grid
+ * finishes) come from `seqlens_early` (device int32 [B], 4-byte aligned)
+ * instead of `seqlens`. In normal use both reads see the same array; a
+ * preceding kernel that is still writing the lengths makes them differ, and
+ * then the start is worked out again from `seqlens`. With a decoy here the
+ * outputs must equal gqa_attn_decode_lse's for `seqlens`, bit for bit.
+ * Errors as gqa_attn_decode_lse, plus GQA_ERR_INVALID_ARG for a null or
+ * misaligned `seqlens_early`.
+ */
+int gqa_attn_selftest_decode_early_lengths(const void *q, const void *k_cache,
+                                           const void *v_cache, const int *seqlens,
+                                           const int *seqlens_early, void *o, float *lse,
+                                           int B, int H_q, int H_kv, int max_len, int d,
+                                           float scale, cudaStream_t stream);
+
 /* Frees every library-owned workspace on every device (synchronising the
  * streams they belong to first). Safe to call more than once. */
 void gqa_attn_shutdown(void);

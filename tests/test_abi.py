@@ -279,6 +279,22 @@ def test_decode_int8_validation():
     assert call(max_len=(1 << 20) + 1) == 2
 
 
+def test_selftest_decode_early_lengths_validation():
+    f = ops.load().gqa_attn_selftest_decode_early_lengths
+    EARLY = ctypes.c_void_p(0x30000)
+    ok = dict(B=2, H_q=8, H_kv=2, max_len=256, d=128, scale=0.1)
+
+    def call(early=EARLY, **kw):
+        a = dict(ok, **kw)
+        return f(A, A, A, SEQ, early, A, None, a["B"], a["H_q"], a["H_kv"], a["max_len"], a["d"],
+                 a["scale"], None)
+
+    assert call(early=None) == 1
+    assert call(early=ctypes.c_void_p(0x30002)) == 1
+    assert call(H_q=6, H_kv=4) == 1
+    assert call(d=48) == 2
+
+
 def test_strided_validation():
     f = ops.load().gqa_attn_fwd_strided
     dims = dict(B=2, H_q=8, H_kv=2, N_q=300, N_kv=300, d=128, causal=1, scale=0.088)
