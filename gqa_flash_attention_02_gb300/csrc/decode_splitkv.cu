@@ -54,7 +54,7 @@ constexpr int kThreads = 32 * (kMmaWarps + 2);
 template <int D>
 constexpr int kDimSplitOf = D == 256 ? 2 : 1;
 // Cache rows per unit: 16 per row group of a bf16 cache (64 rows, or 32 at
-// d = 256), 32 per MMA warp of an fp8 cache (128 rows), so a unit is 16 KB
+// d = 256), 32 per MMA warp of a one-byte cache (128 rows), so a unit is 16 KB
 // of K and of V at d = 128 and 256 alike, and each MMA warp's share of a
 // stage's rows holds its accumulator fragments when it hands a run to the
 // epilogue warp.
@@ -75,7 +75,7 @@ __device__ __forceinline__ uint32_t swz(int row, int u, int rows) {
   return static_cast<uint32_t>((u >> 3) * rows * 128 + row * 128 + (((u & 7) ^ (row & 7)) << 4));
 }
 
-// Byte offset of 16-byte chunk c of row `row` in an fp8 tile of D-byte rows
+// Byte offset of 16-byte chunk c of row `row` in a one-byte tile of D-byte rows
 // as TMA writes it: the 128-byte swizzle (D = 128) XORs the chunk index with
 // row % 8, the 64-byte swizzle (D = 64) with (row / 2) % 4, so the 8 rows
 // of an ldmatrix read fall in different banks.
@@ -109,7 +109,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// The same with f16 operands (P.V over an fp8 cache: e4m3 widens to f16
+// The same with f16 operands (P.V over a one-byte cache: e4m3 and int8 widen to f16
 // exactly, and P <= 1 keeps 11 significant bits in f16).
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                         uint32_t b1) {
@@ -210,7 +210,7 @@ struct DecodeParams {
   float *part;     // [(grid + planes)] slots of O [16][D] (unnormalised), m [16], l [16]
   int *counters;   // [planes], zero between launches (the last merger re-arms it)
   int *err_word;
-  const float *k_scale, *v_scale;  // fp8 cache: per K/V head dequantisation scales
+  const float *k_scale, *v_scale;  // one-byte caches: per K/V head dequantisation scales
   int B, H_q, H_kv, max_len, nhg;  // nhg = query-head groups of 16 per K/V head
   float scale_log2;
 };
@@ -413,7 +413,7 @@ __device__ __forceinline__ void merge_parts(const float *pbase, int nparts, int 
 
 // Writes one head's row of O (times il, as bf16) from accumulator
 // fragments: entries e0, e0 + 1 of each n-tile are the lane's columns cc,
-// cc + 1 of the tile. With an fp8 cache n-tile 2ch holds the even dims of the
+// cc + 1 of the tile. With a one-byte cache n-tile 2ch holds the even dims of the
 // 16-dim chunk ch and n-tile 2ch + 1 its odd dims (the order P.V produces
 // them in), so the lane's four values are dims 16ch + 2cc .. 16ch + 2cc + 3.
 // (bf16 cache at d = 256: the NTW n-tiles of one warp's columns from col0.)
@@ -440,7 +440,7 @@ __device__ __forceinline__ void write_o_row(__nv_bfloat16 *dst, const float (&A)
 // the lane) when the warp hands a run to the epilogue warp: the K and V rows
 // of the stage that only warp w reads hold exactly its 32 lanes x D/8
 // float4, lane-contiguous per n-tile (no bank conflicts). bf16 cache: rows
-// [16w, 16w+16) of each 64-column panel of K then V; fp8 cache: rows
+// [16w, 16w+16) of each 64-column panel of K then V; one-byte cache: rows
 // [32w, 32w+32) of K (n-tiles 0 .. D/16-1), then of V. At d = 256 warp w
 // has row group r = w % 2 and column half h = w / 2: rows [16r, 16r+16) of
 // K panels 2h, 2h+1, then of the same V panels (its 16 n-tiles; the K rows
@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (warp == 0 && lane == 0 && i == n_units - 3 && i > seg_first_i && i + (nsub - s) >= n_units)
       counter_seen2 = ld_relaxed_gpu(prm.counters + b * planes_per_b + pib);  // a later look
     const int rows_here = min(kSub, len - s * kSub);  // valid rows in this unit
-    // fp8 cache: the K/V head's scales (K's folds into the exponent scale)
+    // one-byte caches: the K/V head's scales (K's folds into the exponent scale)
     const float sl2 = kByte ? prm.scale_log2 * __ldg(prm.k_scale + h_kv) : prm.scale_log2;
 #pragma unroll 1
     for (int grp = 0; grp < kRows / 16; ++grp) {
@@ -917,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint32_t qt = kt + 2 * L::kTile;
     const bool lo_ok = (lane >> 2) < Gh, hi_ok = (lane >> 2) + 8 < Gh;
     if constexpr (kByte) {
-      // The fp8 K rows are read as 8x8 matrices of 16-bit pairs: lane l gets
+      // The one-byte K rows are read as 8x8 matrices of 16-bit pairs: lane l gets
       // key row l/4 of a matrix and bytes 4(l%4)..+3, the dims 4t..4t+3 (t =
       // l%4) of a 16-dim chunk. Widened to two bf16 pairs they are the B
       // fragment of one k16 step under a permutation of the contraction
@@ -1011,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     // ---- O += P V (V rows = k, d = n): transposed ldmatrix of 8x8 blocks
     if constexpr (kByte) {
-      // P as f16 (16 heads x 16 keys). The fp8 V rows are read transposed
+      // P as f16 (16 heads x 16 keys). The one-byte V rows are read transposed
       // as 16-bit pairs: lane l gets keys 2t, 2t+1 of a matrix at bytes
       // 2c, 2c+1 (c = l/4), i.e. two dims of a 16-dim chunk for two keys;
       // one byte permute splits them into the key pairs of dim 2c and of dim
