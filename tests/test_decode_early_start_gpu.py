@@ -5,9 +5,11 @@ sequence lengths made before its grid-dependency wait (the previous grid may
 still be writing them) and prefetches that unit into L2; after the wait it
 reads the lengths again and works the start out afresh if any changed. The
 self-test entry feeds the first read from a decoy array, so these cases take
-the second path: the outputs must be bit for bit those of the plain call
-(whose first read sees the real lengths) and close to the oracle, with no
-device error from the decoy's out-of-range values. Split-sequence cached
+the second path (up to 128 sequences; a larger batch reads its lengths only
+after the wait, and the decoy must then have no effect at all): the outputs
+must be bit for bit those of the plain call (whose first read sees the real
+lengths) and close to the oracle, with no device error from the decoy's
+out-of-range values. Split-sequence cached
 attention: microLLM-rocm optimisation log, Experiments 282-284.
 """
 import numpy as np
