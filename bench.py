@@ -356,9 +356,12 @@ def backward_block(torch, ops, inputs, dev, stream, tc_peak, peak_src, out):
                   "d": shape.d, "causal": shape.causal},
         "flops": "2.5 x the forward's algorithmic FLOPs", "launches_per_call": 2,
         "calls_per_rep": chain, "reps": 21, "l2": f"{copies} rotating copies",
-        "roofline": roofline_obj("tensor", ach, tc_peak, "TFLOP/s",
-                                 f"{peak_src} bf16_tflops (burst)",
-                                 f"bwd_prep_kernel<{shape.d}, {shape.d}> + bwd_kernel<{shape.d}, {shape.d}>")}
+        "roofline": dict(roofline_obj("tensor", ach, tc_peak, "TFLOP/s",
+                                      f"{peak_src} bf16_tflops (burst)",
+                                      f"bwd_prep_kernel<{shape.d}, {shape.d}> + bwd_kernel<{shape.d}, {shape.d}>",
+                                      recorded_traffic("gqa_flash_attention_02_gb300/csrc/attn_bwd.cu",
+                                                       f"bwd_kernel<{shape.d}, {shape.d}>")),
+                         traffic_kernel=f"bwd_kernel<{shape.d}, {shape.d}> (the main launch)")}
     del bufs, grads, qd, kd, vd, o, lse
     torch.cuda.empty_cache()
 
@@ -388,7 +391,12 @@ def decode_blocks(torch, ops, inputs, dev, stream, hbm_peak, peak_src, out):
             "bytes_per_call": nbytes, "calls_per_rep": chain, "reps": 21,
             "l2": f"{copies} rotating copies",
             "roofline": roofline_obj("hbm", ach, hbm_peak, "GB/s", f"{peak_src} hbm_gbs",
-                                     "decode_kernel<128,5,0,128,0>")}
+                                     "decode_kernel<128,5,0,128,0>",
+                                     # the capture is of the B=64 workload; the
+                                     # smaller batches have none of their own
+                                     recorded_traffic("gqa_flash_attention_02_gb300/csrc/decode_splitkv.cu",
+                                                      "decode_kernel<128,5,0,128,0>")
+                                     if shape.name == "decode_b64" else None)}
         del bufs, o
         torch.cuda.empty_cache()
 
