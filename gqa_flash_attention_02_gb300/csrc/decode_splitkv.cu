@@ -61,6 +61,23 @@ constexpr int kDimSplitOf = D == 256 ? 2 : 1;
 template <int D, bool kByte>
 constexpr int kSubFor = kByte ? 128 : 64 / kDimSplitOf<D>;
 constexpr int kHeads = kDecodeHeads;  // query heads per plane (mma M)
+
+// A K/V cache box, read once per launch: loaded with an L2 evict-first
+// policy, so the stream does not push out of L2 what is read back later in
+// the launch (the query rows, the split partials the merges read).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_3d_stream(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                   int c0, int c1, int c2, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
+      : "memory");
+}
 // Fewest units a CTA takes: fewer, longer runs (each run ends in a merge
 // step and a plane spans at most nsub / kMinUnits + 2 CTAs); no CTA range
 // is ever empty.
@@ -676,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // owners take two divisions: off the MMA warps' path) and loads K, V and
     // the plane's 16 query rows with one completion barrier.
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
       Pos p{info[1], info[2], info[3], info[6]};
       int c_first = 0, c_last = 0;
       for (int i = 0; i < n_units; ++i) {
@@ -702,14 +720,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         mbar_arrive_expect_tx(full + 8 * st, L::kStage);
         if constexpr (kByte) {
           // one box of kSub rows x D bytes each (unswizzled)
-          tma_load_3d(dst, &tm_k, full + 8 * st, 0, p.s * kSub, plane_kv);
-          tma_load_3d(dst + L::kTile, &tm_v, full + 8 * st, 0, p.s * kSub, plane_kv);
+          tma_load_3d_stream(dst, &tm_k, full + 8 * st, 0, p.s * kSub, plane_kv, pol);
+          tma_load_3d_stream(dst + L::kTile, &tm_v, full + 8 * st, 0, p.s * kSub, plane_kv, pol);
         } else {
 #pragma unroll
           for (int q = 0; q < D / 64; ++q) {
-            tma_load_3d(dst + q * kSub * 128, &tm_k, full + 8 * st, q * 64, p.s * kSub, plane_kv);
-            tma_load_3d(dst + L::kTile + q * kSub * 128, &tm_v, full + 8 * st, q * 64, p.s * kSub,
-                        plane_kv);
+            tma_load_3d_stream(dst + q * kSub * 128, &tm_k, full + 8 * st, q * 64, p.s * kSub,
+                               plane_kv, pol);
+            tma_load_3d_stream(dst + L::kTile + q * kSub * 128, &tm_v, full + 8 * st, q * 64,
+                               p.s * kSub, plane_kv, pol);
           }
         }
         // the plane's 16 query rows come with every unit (an L2 hit after the
