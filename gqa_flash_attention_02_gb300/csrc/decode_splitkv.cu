@@ -532,9 +532,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   // While the previous grid finishes (it may still be writing the inputs),
   // warp 0 works out the CTA's start from a first read of the lengths (B <=
-  // 128) and prefetches the CTA's first two units of K and V into L2. The
-  // start stands only if a read after the dependency wait finds the same
-  // lengths; a prefetch never changes what is read.
+  // 128) and prefetches the CTA's first units of K and V into L2: four with
+  // a bf16 cache, two with a one-byte cache (where four measured slower).
+  // The walk over planes reads the first read's lengths, put in shared
+  // memory for it and rewritten after the wait. The start stands only if a
+  // read after the dependency wait finds the same lengths; a prefetch never
+  // changes what is read.
   const bool few_b = prm.B <= 128;
   int spec_len[4];
   Start spec{};
@@ -546,14 +549,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         spec_len[k] = b < prm.B ? __ldcg(prm.seqlens_first + b) : 0;
       }
       spec = locate_start<kSub>(prm, spec_len, lane, c, planes_per_b);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (32 * k + lane < prm.B) s_len[32 * k + lane] = spec_len[k];
+      __syncwarp();
       if (lane == 0 && c < spec.G && spec.sb < prm.B) {
-        const int plane_kv = spec.sb * prm.H_kv + spec.spib / prm.nhg;
-        for (int s = spec.ss; s < spec.ss + 2 && s < spec.snsub; ++s) {
+        const Split sp{spec.U / spec.G, spec.U % spec.G};
+        const int n = min(kByte ? 2 : 4, sp.q + (c < sp.r ? 1 : 0));
+        Pos p{spec.sb, spec.spib, spec.ss, spec.snsub};
+        for (int i = 0; i < n && p.b < prm.B; ++i) {
+          const int plane_kv = p.b * prm.H_kv + p.pib / prm.nhg;
 #pragma unroll
           for (int q = 0; q < (kByte ? 1 : D / 64); ++q) {
-            tma_prefetch_l2_3d(&tm_k, q * 64, s * kSub, plane_kv);
-            tma_prefetch_l2_3d(&tm_v, q * 64, s * kSub, plane_kv);
+            tma_prefetch_l2_3d(&tm_k, q * 64, p.s * kSub, plane_kv);
+            tma_prefetch_l2_3d(&tm_v, q * 64, p.s * kSub, plane_kv);
           }
+          advance<kSub>(prm, s_len, planes_per_b, p);
         }
       }
     } else {
